@@ -1,0 +1,201 @@
+"""Plain float64 CPU oracle for Prefix-Sliding attention.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this module; the library never does.
+
+It computes the definition of the method directly, from the full,
+never-evicted K/V history, one query row at a time, with no blocking, fusion
+or reordering.  Sources (page title, then the section or paragraph):
+
+[NJH]  njhaofan.com article on PrefixSliding, section
+       "PrefixSliding如何丢掉中间Token？" (fixed prefix + last-W window, the
+       4196-token cap, Continue PE, tile skipping in the Hopper kernel).
+[EXP]  "Prefix Sliding：面向高效 test-time scaling 的前缀滑动方法"
+       (papers.ananclaw.com), sections "核心方法" and "伪代码" (PREFIX and
+       WINDOW blocks; cache size is the constant prefix_len + W).
+[AGI]  "Prefix Sliding for efficient test-time scaling" (agihunt.info), the
+       paragraphs on the 100-token prefix + 4,096 window cap, on Continue PE,
+       and on the two-level tile filter of the FlashAttention kernel.
+
+Readings taken where the pages are silent (each is restated where it is used):
+  * the window includes the current token: query p sees key j iff
+    j <= p and (j < P or j > p - W), so at most P + W keys ([NJH], [AGI] cap
+    of 100 + 4096 = 4196);
+  * RoPE is the half-split ("NeoX") rotation with inv_freq_i = theta^(-2i/D),
+    applied at the absolute, ever-increasing position (Continue PE, [AGI]);
+  * rotated Q and K are rounded to bfloat16 (the cache stores bfloat16);
+    values V are used as given;
+  * softmax scale 1/sqrt(D), LSE is the natural log of sum(exp(score)),
+    query head h reads KV head h // (Hq / Hkv).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+SKIP, PARTIAL, FULL = 0, 1, 2
+
+
+# --------------------------------------------------------------------------
+# number formats
+# --------------------------------------------------------------------------
+def round_bf16(x) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 value (ties to even).
+
+    bfloat16 keeps 8 significant bits and float32's exponent range; below
+    2**-126 the spacing is fixed at 2**-133 (subnormals).  One rounding from
+    the exact float64 value.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)                       # x = m * 2**e, 0.5 <= |m| < 1
+    e = np.maximum(e, -125)                  # subnormal range keeps a fixed quantum
+    quantum = np.ldexp(1.0, e - 8)
+    r = np.rint(x / quantum) * quantum       # rint: round half to even
+    r = np.where(np.abs(r) > 3.3895313892515355e38, np.sign(r) * np.inf, r)
+    return np.where(x == 0.0, x, r)
+
+
+# --------------------------------------------------------------------------
+# RoPE with Continue PE ([AGI] paragraph on position encodings)
+# --------------------------------------------------------------------------
+def rope(x, pos, theta: float) -> np.ndarray:
+    """Rotate the last axis (length D, even) of ``x`` at absolute position(s) ``pos``.
+
+    Half-split pairing: element i rotates with element i + D/2 by the angle
+    pos * theta**(-2i/D).  ``pos`` broadcasts against the leading axes of ``x``
+    (a scalar, or one position per leading row).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    half = d // 2
+    i = np.arange(half, dtype=np.float64)
+    inv_freq = theta ** (-2.0 * i / d)
+    p = np.asarray(pos, dtype=np.float64)
+    p = p.reshape(p.shape + (1,) * (x.ndim - p.ndim))   # align to x's leading axes
+    ang = p * inv_freq                                   # broadcasts over the last axis
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+# --------------------------------------------------------------------------
+# the mask ([NJH] section "PrefixSliding如何丢掉中间Token？", [EXP] "核心方法")
+# --------------------------------------------------------------------------
+def allowed(p, j, P: int, W: int):
+    """True where query position p may attend key position j."""
+    p = np.asarray(p)
+    j = np.asarray(j)
+    return (j <= p) & ((j < P) | (j > p - W))
+
+
+def visible_positions(p: int, P: int, W: int) -> np.ndarray:
+    """All key positions query p sees, found by scanning the whole history [0, p]."""
+    j = np.arange(p + 1, dtype=np.int64)
+    return j[allowed(p, j, P, W)]
+
+
+# --------------------------------------------------------------------------
+# attention over an explicit key set
+# --------------------------------------------------------------------------
+def masked_attention(q_hat, k_hat, v, scale: float):
+    """Softmax attention of each query head over every given key (float64).
+
+    q_hat [Hq, D]; k_hat, v [n, Hkv, D].  Returns O [Hq, D] and the natural-log
+    LSE [Hq] of the scaled scores.
+    """
+    q_hat = np.asarray(q_hat, dtype=np.float64)
+    hq = q_hat.shape[0]
+    hkv = k_hat.shape[1]
+    group = hq // hkv
+    out = np.zeros((hq, v.shape[2]))
+    lse = np.zeros(hq)
+    for h in range(hq):
+        kh = h // group
+        s = (k_hat[:, kh, :] @ q_hat[h]) * scale
+        m = s.max()
+        e = np.exp(s - m)
+        l = e.sum()
+        lse[h] = m + math.log(l)
+        out[h] = (e / l) @ v[:, kh, :]
+    return out, lse
+
+
+def attend(q_raw, p: int, P: int, W: int, history, theta: float, scale: float | None = None):
+    """Prefix-Sliding attention output of one query at absolute position p.
+
+    ``q_raw`` [Hq, D] float64 (raw bfloat16 values, before RoPE).
+    ``history(positions)`` returns raw k, v [n, Hkv, D] float64 at those
+    absolute positions; the oracle asks only for the positions the mask admits,
+    after scanning every j in [0, p].
+    """
+    q_raw = np.asarray(q_raw, dtype=np.float64)
+    d = q_raw.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    js = visible_positions(p, P, W)
+    k_raw, v = history(js)
+    q_hat = round_bf16(rope(q_raw, p, theta))
+    k_hat = round_bf16(rope(k_raw, js, theta))
+    return masked_attention(q_hat, k_hat, v, scale)
+
+
+# --------------------------------------------------------------------------
+# the bounded cache ([EXP] "伪代码" invariant: size prefix_len + W)
+# --------------------------------------------------------------------------
+def ring_slot(pos: int, P: int, W: int) -> int:
+    """Slot of absolute position pos in a cache of P fixed + W rotating slots."""
+    return pos if pos < P else P + (pos - P) % W
+
+
+class RingSim:
+    """Position-level simulation of the P + W slot cache.
+
+    Each append stores the position in its slot.  ``check(p)`` asserts that
+    the positions held after appending 0..p are exactly the ones query p may
+    see by the mask definition.
+    """
+
+    def __init__(self, P: int, W: int):
+        self.P, self.W = P, W
+        self.slots = np.full(P + W, -1, dtype=np.int64)
+
+    def append(self, pos: int) -> int:
+        s = ring_slot(pos, self.P, self.W)
+        self.slots[s] = pos
+        return s
+
+    def live(self) -> np.ndarray:
+        return np.sort(self.slots[self.slots >= 0])
+
+    def check(self, p: int) -> None:
+        want = visible_positions(p, self.P, self.W)
+        got = self.live()
+        if not np.array_equal(got, want):
+            raise AssertionError(f"ring holds {got} but query {p} sees {want}")
+
+
+# --------------------------------------------------------------------------
+# tile classes ([NJH] / [AGI]: skip tiles wholly outside prefix and window,
+# mask elementwise inside tiles that straddle the boundary)
+# --------------------------------------------------------------------------
+def tile_classes(q_pos, k_pos, P: int, W: int, BM: int, BN: int) -> np.ndarray:
+    """Brute-force class of each (query tile, key tile): SKIP, PARTIAL or FULL.
+
+    ``q_pos`` / ``k_pos`` are the absolute positions of the query rows and of
+    the key rows in array order; tile (a, b) holds rows [a*BM, (a+1)*BM) and
+    keys [b*BN, (b+1)*BN), clipped to the arrays.  SKIP: no admitted pair;
+    FULL: every pair admitted; PARTIAL: otherwise.
+    """
+    q_pos = np.asarray(q_pos, dtype=np.int64)
+    k_pos = np.asarray(k_pos, dtype=np.int64)
+    nq = -(-len(q_pos) // BM)
+    nk = -(-len(k_pos) // BN)
+    out = np.zeros((nq, nk), dtype=np.uint8)
+    for a in range(nq):
+        qs = q_pos[a * BM:(a + 1) * BM]
+        m = allowed(qs[:, None], k_pos[None, :], P, W)
+        for b in range(nk):
+            blk = m[:, b * BN:(b + 1) * BN]
+            out[a, b] = FULL if blk.all() else (PARTIAL if blk.any() else SKIP)
+    return out

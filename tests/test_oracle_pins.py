@@ -1,0 +1,319 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+Each test ties one oracle function to a library routine, a closed form, a
+value printed on the pages, or an independent brute-force enumeration, so that
+a dropped term, a wrong sign, index or operand fails somewhere here.
+"""
+import cmath
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import (FULL, PARTIAL, SKIP, RingSim, allowed, attend, masked_attention,
+                    ring_slot, rope, round_bf16, tile_classes, visible_positions)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- bf16 ----
+def test_round_bf16_matches_torch_cast_on_float32_inputs():
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal(200000) * np.exp2(rng.integers(-140, 120, 200000))).astype(np.float32)
+    x = np.concatenate([x, np.array([1 + 2**-8, 1 + 3 * 2**-8, -(1 + 2**-8), 2**-130, 3e38], np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = round_bf16(x.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+def test_round_bf16_ties_to_even_by_hand():
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7: the even neighbour is 1.
+    assert round_bf16(1 + 2**-8) == 1.0
+    # 1 + 3*2^-8 lies halfway between 1 + 2^-7 and 1 + 2^-6: the even one is 1 + 2^-6.
+    assert round_bf16(1 + 3 * 2**-8) == 1 + 2**-6
+    # just above a tie rounds up (float64 input, single rounding)
+    assert round_bf16(1 + 2**-8 + 2**-30) == 1 + 2**-7
+    assert round_bf16(0.0) == 0.0
+
+
+def test_synth_bf16_cast_matches_torch():
+    x = np.random.default_rng(2).standard_normal(100000).astype(np.float32)
+    got = synth.bits_to_f64(synth.f32_to_bf16_bits(x))
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(got, want)
+
+
+def test_synth_is_standard_normal_and_coordinate_pure():
+    a = synth.bits_to_f64(synth.normal_bf16(3, synth.STREAM_K, 0, np.arange(4000), 4, 64))
+    assert abs(a.mean()) < 0.01 and abs(a.std() - 1.0) < 0.01
+    # any slice equals the same slice generated alone
+    b = synth.bits_to_f64(synth.normal_bf16(3, synth.STREAM_K, 0, [17, 3999], 4, 64))
+    assert np.array_equal(b, a[[17, 3999]])
+
+
+# ----------------------------------------------------------------- RoPE ----
+def test_rope_identity_at_position_zero():
+    x = np.random.default_rng(3).standard_normal((5, 128))
+    assert np.allclose(rope(x, 0, 10000.0), x, atol=0, rtol=0)
+
+
+def test_rope_hand_computed_d4():
+    # D = 4, theta = 100: pairs (0,2) at frequency 1 and (1,3) at 100^(-1/2) = 0.1.
+    p = 7
+    x = np.array([1.0, 2.0, 3.0, 4.0])
+    a0, a1 = p * 1.0, p * 0.1
+    want = np.array([1 * math.cos(a0) - 3 * math.sin(a0),
+                     2 * math.cos(a1) - 4 * math.sin(a1),
+                     3 * math.cos(a0) + 1 * math.sin(a0),
+                     4 * math.cos(a1) + 2 * math.sin(a1)])
+    assert np.allclose(rope(x, p, 100.0), want, rtol=1e-15, atol=1e-15)
+
+
+def test_rope_as_complex_rotation():
+    # Independent form: element pair (i, i+D/2) is the complex number x_i + i x_{i+D/2}
+    # multiplied by exp(i * pos * theta^(-2i/D)).
+    rng = np.random.default_rng(4)
+    d, theta = 16, 10000.0
+    for pos in (1, 1000, 262143):
+        x = rng.standard_normal(d)
+        got = rope(x, pos, theta)
+        for i in range(d // 2):
+            z = complex(x[i], x[i + d // 2]) * cmath.exp(1j * pos * theta ** (-2 * i / d))
+            assert abs(got[i] - z.real) < 1e-12 and abs(got[i + d // 2] - z.imag) < 1e-12
+
+
+def test_rope_norm_and_relative_position_invariance():
+    rng = np.random.default_rng(5)
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+    for p, j, shift in ((100, 40, 131072), (5000, 4999, 7), (262143, 0, 1)):
+        assert abs(np.linalg.norm(rope(q, p, 1e4)) - np.linalg.norm(q)) < 1e-12
+        a = rope(q, p, 1e4) @ rope(k, j, 1e4)
+        b = rope(q, p + shift, 1e4) @ rope(k, j + shift, 1e4)
+        assert abs(a - b) < 1e-9
+
+
+def test_rope_per_row_positions_broadcast():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((3, 2, 8))
+    pos = np.array([0, 5, 9])
+    got = rope(x, pos, 1e4)
+    for r in range(3):
+        assert np.allclose(got[r], rope(x[r], pos[r], 1e4))
+
+
+# ----------------------------------------------------------------- mask ----
+def test_key_count_closed_form_bruteforce():
+    for S in range(1, 17):
+        for P in range(0, S + 1):
+            for W in range(1, S + 2):
+                for p in range(S):
+                    n = len(visible_positions(p, P, W))
+                    assert n == min(p + 1, P + W), (S, P, W, p)
+
+
+def test_pages_cap_4196_keys():
+    g = json.load(open(os.path.join(GOLDEN, "pages_constants.json")))
+    c = g["cap_prefix100_window4096"]
+    for p in (4195, 4196, 100000, 262143):
+        assert len(visible_positions(p, c["P"], c["W"])) <= c["max_keys"]
+    assert len(visible_positions(100000, c["P"], c["W"])) == c["max_keys"]
+
+
+def test_mask_contains_prefix_and_current_token():
+    vis = visible_positions(100000, 100, 4096)
+    assert vis[0] == 0 and vis[99] == 99 and vis[100] == 100000 - 4095 and vis[-1] == 100000
+
+
+# ------------------------------------------------------- masked softmax ----
+def _sdpa_rows(qh, kh, vh, mask):
+    """torch SDPA in float64. qh [S,Hq,D], kh/vh [S,Hkv,D], mask [S,S] bool."""
+    hq, hkv = qh.shape[1], kh.shape[1]
+    g = hq // hkv
+    q = torch.from_numpy(qh).permute(1, 0, 2)
+    k = torch.from_numpy(kh).permute(1, 0, 2).repeat_interleave(g, 0)
+    v = torch.from_numpy(vh).permute(1, 0, 2).repeat_interleave(g, 0)
+    m = torch.from_numpy(mask)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=m)
+    sc = (q @ k.transpose(1, 2)) / math.sqrt(qh.shape[2])
+    lse = torch.logsumexp(sc.masked_fill(~m, -math.inf), dim=-1)
+    return o.permute(1, 0, 2).numpy(), lse.permute(1, 0).numpy()
+
+
+@pytest.mark.parametrize("S,P,W", [(40, 40, 64), (40, 0, 9), (40, 4, 9), (33, 7, 1), (50, 12, 16)])
+def test_attend_matches_sdpa_with_explicit_mask(S, P, W):
+    seed, hq, hkv, d, theta = 11, 4, 2, 32, 10000.0
+    hist = synth.History(seed, 0, hkv, d)
+    pos = np.arange(S)
+    q_raw = synth.bits_to_f64(synth.query_bits(seed, 0, pos, hq, d))
+    k_raw, v = hist.rows(pos)
+    qh = round_bf16(rope(q_raw, pos, theta))
+    kh = round_bf16(rope(k_raw, pos, theta))
+    jj, pp = np.meshgrid(pos, pos)
+    if W >= S:   # reduction 1: no sliding at all -> plain causal
+        mask = jj <= pp
+    elif P == 0:  # reduction 2: no prefix -> plain band (vanilla sliding window)
+        mask = (jj <= pp) & (jj > pp - W)
+    else:        # prefix rows OR band, built as the union of two textbook masks
+        mask = ((jj <= pp) & (jj < P)) | ((jj <= pp) & (jj > pp - W))
+    o_ref, lse_ref = _sdpa_rows(qh, kh, v, mask)
+    for p in range(S):
+        o, lse = attend(q_raw[p], p, P, W, hist.rows, theta)
+        assert np.allclose(o, o_ref[p], atol=1e-12, rtol=1e-10)
+        assert np.allclose(lse, lse_ref[p], atol=1e-12, rtol=1e-12)
+
+
+def test_masked_attention_one_key_and_uniform_keys():
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal((4, 16))
+    k = rng.standard_normal((1, 2, 16))
+    v = rng.standard_normal((1, 2, 16))
+    o, lse = masked_attention(q, k, v, 0.25)
+    for h in range(4):
+        assert np.allclose(o[h], v[0, h // 2], rtol=0, atol=0)
+        assert abs(lse[h] - 0.25 * (q[h] @ k[0, h // 2])) < 1e-14
+    n = 37
+    ku = np.repeat(k, n, axis=0)
+    vu = rng.standard_normal((n, 2, 16))
+    o, lse = masked_attention(q, ku, vu, 0.25)
+    for h in range(4):
+        assert np.allclose(o[h], vu[:, h // 2].mean(0), atol=1e-14)
+        assert abs(lse[h] - (math.log(n) + 0.25 * (q[h] @ k[0, h // 2]))) < 1e-12
+
+
+def test_attend_zero_keys_gives_mean_of_visible_values():
+    # raw k = 0 -> every score is 0 -> O = mean(V over visible keys), LSE = ln(count)
+    d, hkv = 16, 1
+    rng = np.random.default_rng(8)
+    vals = rng.standard_normal((300, hkv, d))
+
+    def hist(js):
+        return np.zeros((len(js), hkv, d)), vals[js]
+
+    for (p, P, W) in ((0, 5, 3), (10, 5, 3), (299, 16, 32), (299, 0, 7), (40, 100, 4)):
+        o, lse = attend(rng.standard_normal((2, d)), p, P, W, hist, 1e4)
+        js = [j for j in range(p + 1) if j < P or j > p - W]
+        assert np.allclose(o[0], vals[js, 0].mean(0), atol=1e-13)
+        assert abs(lse[0] - math.log(min(p + 1, P + W))) < 1e-13
+
+
+def _bruteforce_attend(q_raw, p, P, W, hist, theta):
+    """Scalar Python: key set as a union of two ranges, RoPE as a complex
+    rotation, bf16 by frexp, softmax without max subtraction."""
+    def bf16(x):
+        if x == 0.0:
+            return 0.0
+        m, e = math.frexp(x)
+        return math.ldexp(round(m * 256), e - 8)
+
+    def rot(vec, pos):
+        d = len(vec)
+        out = [0.0] * d
+        for i in range(d // 2):
+            z = complex(vec[i], vec[i + d // 2]) * cmath.exp(1j * pos * theta ** (-2 * i / d))
+            out[i], out[i + d // 2] = bf16(z.real), bf16(z.imag)
+        return out
+
+    keys = sorted(set(range(0, min(P, p + 1))) | set(range(max(0, p - W + 1), p + 1)))
+    k_raw, v = hist(np.array(keys))
+    hq, d = q_raw.shape
+    hkv = k_raw.shape[1]
+    outs, lses = [], []
+    for h in range(hq):
+        qv = rot(list(q_raw[h]), p)
+        ws, acc = [], [0.0] * d
+        for n, j in enumerate(keys):
+            kv = rot(list(k_raw[n, h * hkv // hq]), j)
+            ws.append(math.exp(sum(a * b for a, b in zip(qv, kv)) / math.sqrt(d)))
+        tot = sum(ws)
+        for n in range(len(keys)):
+            for t in range(d):
+                acc[t] += ws[n] / tot * v[n, h * hkv // hq, t]
+        outs.append(acc)
+        lses.append(math.log(tot))
+    return np.array(outs), np.array(lses)
+
+
+def test_attend_matches_pure_python_enumeration_on_tiny_inputs():
+    seed, hq, hkv, d, theta = 21, 2, 1, 8, 10000.0
+    hist = synth.History(seed, 1, hkv, d)
+    for S in (5, 12):
+        q_raw = synth.bits_to_f64(synth.query_bits(seed, 1, np.arange(S), hq, d))
+        for P in range(0, S + 1):
+            for W in range(1, S + 2):
+                for p in range(S):
+                    o, lse = attend(q_raw[p], p, P, W, hist.rows, theta)
+                    ob, lb = _bruteforce_attend(q_raw[p], p, P, W, hist.rows, theta)
+                    assert np.allclose(o, ob, atol=1e-12), (S, P, W, p)
+                    assert np.allclose(lse, lb, atol=1e-12), (S, P, W, p)
+
+
+# ----------------------------------------------------------------- ring ----
+@pytest.mark.parametrize("P,W,steps", [(16, 32, 4352), (0, 5, 300), (3, 1, 200), (100, 4096, 9000), (64, 8, 500)])
+def test_ring_live_set_equals_mask_after_every_append(P, W, steps):
+    ring = RingSim(P, W)
+    for p in range(steps):
+        s = ring.append(p)
+        assert 0 <= s < P + W
+        ring.check(p)
+
+
+def test_ring_slot_of_prefix_and_first_window_is_identity():
+    for P, W in ((16, 32), (0, 7), (100, 4096)):
+        for pos in range(P + W):
+            assert ring_slot(pos, P, W) == pos
+        # after wrap-around, pos and pos + W share a slot
+        assert ring_slot(P + W + 3, P, W) == ring_slot(P + 3, P, W)
+
+
+# ---------------------------------------------------------------- tiles ----
+def _classes_by_intervals(q_pos, k_pos, P, W, BM, BN):
+    """Independent classification: each query row admits keys in
+    [0, min(P, p+1)) U [max(0, p-W+1), p]; count admitted keys per tile by
+    interval arithmetic (key positions must be consecutive)."""
+    nq, nk = -(-len(q_pos) // BM), -(-len(k_pos) // BN)
+    out = np.zeros((nq, nk), dtype=np.uint8)
+    for a in range(nq):
+        rows = q_pos[a * BM:(a + 1) * BM]
+        for b in range(nk):
+            k0, k1 = k_pos[b * BN], k_pos[min((b + 1) * BN, len(k_pos)) - 1]
+            tot, n = 0, (k1 - k0 + 1)
+            for p in rows:
+                lo1, hi1 = 0, min(P, p + 1) - 1
+                lo2, hi2 = max(0, p - W + 1), p
+                c1 = max(0, min(hi1, k1) - max(lo1, k0) + 1)
+                c2 = max(0, min(hi2, k1) - max(lo2, k0) + 1)
+                ov = max(0, min(hi1, hi2, k1) - max(lo1, lo2, k0) + 1)
+                tot += c1 + c2 - ov
+            out[a, b] = SKIP if tot == 0 else (FULL if tot == n * len(rows) else PARTIAL)
+    return out
+
+
+@pytest.mark.parametrize("S,q0,P,W,BM,BN", [(70, 0, 9, 13, 16, 16), (70, 0, 0, 70, 16, 8), (97, 0, 30, 5, 8, 32),
+                                            (64, 0, 64, 1, 16, 16), (50, 0, 3, 200, 32, 32)])
+def test_tile_classes_match_interval_counting(S, q0, P, W, BM, BN):
+    pos = np.arange(q0, q0 + S)
+    assert np.array_equal(tile_classes(pos, pos, P, W, BM, BN), _classes_by_intervals(pos, pos, P, W, BM, BN))
+
+
+def test_tile_classes_causal_closed_form():
+    # W >= S, P = 0, square tiles: below the diagonal FULL, on it PARTIAL, above SKIP.
+    pos = np.arange(64)
+    c = tile_classes(pos, pos, 0, 64, 16, 16)
+    for a in range(4):
+        for b in range(4):
+            assert c[a, b] == (FULL if b < a else PARTIAL if b == a else SKIP)
+
+
+def test_tile_classes_golden_counts():
+    """Regression values for the two prefill workloads, written by
+    tests/golden/make_golden.py (oracle only) and also derived independently
+    when the hot-path scope was surveyed."""
+    g = json.load(open(os.path.join(GOLDEN, "tile_counts.json")))
+    for case in g["cases"]:
+        pos = np.arange(case["S"])
+        c = tile_classes(pos, pos, case["P"], case["W"], case["BM"], case["BN"])
+        assert [int((c == k).sum()) for k in (SKIP, PARTIAL, FULL)] == case["skip_partial_full"]
