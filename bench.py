@@ -1,0 +1,504 @@
+#!/usr/bin/env python
+"""Benchmark of the Prefix-Sliding attention hot path on one B300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+A step is one decode step of one attention layer for a batch of 64 sequences
+at position 131,072 (+ step), each with a 64..512-token prefix and a 4,096
+window, 16 query / 8 KV heads, head_dim 128: ps_kv_append of the new token's
+K/V, then ps_decode (split-KV partial kernel + LSE combine).  `value` is decode
+tokens/s for that layer over all ranks.  The same run also measures the
+prefill of a 32,768-token sequence (P = 100, W = 4,096) in TFLOP/s, a
+full-causal baseline of both from the same library, an end-to-end decode step
+through host buffers, and the CPU oracle on the host cores.
+
+Under torchrun (N > 1) every rank runs its own independent batch (replicas,
+no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefix-sliding decode tokens/s + HBM GB/s; prefill TFLOP/s vs bf16 peak"
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
+
+# ---- workloads ------------------------------------------------------------
+DEC = dict(nseq=64, pos0=131072, W=4096, Pmin=64, Pmax=512, hq=16, hkv=8, D=128, theta=10000.0, seed=3)
+PRE = dict(B=1, S=32768, P=100, W=4096, hq=16, hkv=8, D=128, theta=10000.0, seed=2)
+LAYERS = 28
+
+
+def decode_prefix_lens(seed, nseq):
+    import synth
+    return synth.uniform_int(seed, 10, nseq, DEC["Pmin"], DEC["Pmax"])
+
+
+def live_runs(p, P, W):
+    if p + 1 <= P + W:
+        return [(0, p + 1)]
+    return ([(0, P)] if P > 0 else []) + [(p - W + 1, W)]
+
+
+# ---- clocks ---------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        pmax = max(r[2] for r in rows)
+        load = [r for r in rows if r[2] >= 0.5 * pmax] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i, v in enumerate(r[3][1:5]) if "Active" in v
+                          and "Not" not in v})
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": pmax}
+
+
+# ---- helpers --------------------------------------------------------------
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("hbm_gbs", FALLBACK_HBM_GBS), d.get("bf16_tflops", FALLBACK_BF16_TFLOPS), \
+            d.get("bf16_tflops_sustained"), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1400.0, "fallback"
+
+
+def committed_traffic(name: str, source: str):
+    """ncu DRAM bytes per launch recorded under profiles/, if the kernel source
+    still matches the one the counters were taken on; else None."""
+    path = os.path.join(ROOT, "profiles", f"{name}.traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    sha = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()
+    if d.get("source_sha256") != sha:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def fill_random(cache, runs_per_seq, gen, torch, chunk_tokens=1 << 21):
+    """Append random raw K/V for each sequence's runs (batched per run index)."""
+    depth = max(len(r) for r in runs_per_seq.values())
+    dev = cache.k_pool.device
+    for i in range(depth):
+        items = [(s, r[i]) for s, r in runs_per_seq.items() if i < len(r) and r[i][1] > 0]
+        j = 0
+        while j < len(items):
+            group, tok = [], 0
+            while j < len(items) and (not group or tok + items[j][1][1] <= chunk_tokens):
+                group.append(items[j])
+                tok += items[j][1][1]
+                j += 1
+            seqs = torch.tensor([s for s, _ in group], dtype=torch.int32, device=dev)
+            pos0 = torch.tensor([r[0] for _, r in group], dtype=torch.int32, device=dev)
+            cu = torch.tensor(np.concatenate([[0], np.cumsum([r[1] for _, r in group])]),
+                              dtype=torch.int32, device=dev)
+            shape = (tok, cache.n_kv_heads, cache.head_dim)
+            k = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+            v = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+            cache.append(seqs, pos0, cu, k, v)
+            del k, v
+
+
+# ---- decode ---------------------------------------------------------------
+def decode_setup(ps, torch, seed, W, P, pos0, n_steps, full_causal=False):
+    d = DEC
+    nseq = d["nseq"]
+    if full_causal:
+        W = pos0 + n_steps + 1
+        P = np.zeros(nseq, dtype=np.int64)
+    cache = ps.RingCache(nseq, d["hkv"], d["D"], W, P, rope_theta=d["theta"],
+                         prefix_max=int(max(P.max(), d["Pmax"] if not full_causal else 0)), zero=False)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    runs = {s: live_runs(pos0 - 1, int(P[s]), W) for s in range(nseq)}
+    fill_random(cache, runs, gen, torch)
+    # per-step inputs, resident in HBM before timing
+    q = torch.randn(n_steps, nseq, d["hq"], d["D"], generator=gen, device="cuda").to(torch.bfloat16)
+    k = torch.randn(n_steps, nseq, d["hkv"], d["D"], generator=gen, device="cuda").to(torch.bfloat16)
+    v = torch.randn(n_steps, nseq, d["hkv"], d["D"], generator=gen, device="cuda").to(torch.bfloat16)
+    pos = (pos0 + torch.arange(n_steps, dtype=torch.int32, device="cuda"))[:, None].repeat(1, nseq).contiguous()
+    L = np.minimum(pos0 + 1, P + W)  # live slots per sequence once the step's token is in
+    return cache, q, k, v, pos, L
+
+
+def run_decode(ps, torch, cache, q, k, v, pos, steps, warmup, dist=None, per_kernel=True):
+    nseq, hq, D = q.shape[1], q.shape[2], q.shape[3]
+    out = torch.empty(nseq, hq, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(nseq, hq, dtype=torch.float32, device="cuda")
+    ws = cache.workspace(hq)
+    stream = torch.cuda.current_stream()
+
+    def step(i, evs=None):
+        cache.append_tokens(pos[i], k[i], v[i])
+        if evs is not None:
+            evs[0].record(stream)
+        cache.decode_partial(q[i], pos[i], workspace=ws)
+        if evs is not None:
+            evs[1].record(stream)
+        cache.decode_combine(out, lse, workspace=ws)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)] if per_kernel else None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(warmup + i, evs[i] if evs else None)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    total_ms = e0.elapsed_time(e1)
+    kern_ms = [a.elapsed_time(b) for a, b in evs] if evs else None
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, kern_ms, out, lse
+
+
+def run_decode_e2e(ps, torch, cache, steps, warmup, seed):
+    """Same decode step through host buffers: pinned host -> device copies of the
+    step's q, k, v, pos; append + decode; device -> host copy of O and LSE."""
+    d = DEC
+    nseq = d["nseq"]
+    gen = torch.Generator().manual_seed(seed)
+    n = steps + warmup
+    hq_ = torch.randn(n, nseq, d["hq"], d["D"], generator=gen).to(torch.bfloat16).pin_memory()
+    hk = torch.randn(n, nseq, d["hkv"], d["D"], generator=gen).to(torch.bfloat16).pin_memory()
+    hv = torch.randn(n, nseq, d["hkv"], d["D"], generator=gen).to(torch.bfloat16).pin_memory()
+    start = d["pos0"] + 100000  # positions after the device-resident run
+    hpos = (start + torch.arange(n, dtype=torch.int32))[:, None].repeat(1, nseq).contiguous().pin_memory()
+    dq = torch.empty(nseq, d["hq"], d["D"], dtype=torch.bfloat16, device="cuda")
+    dk = torch.empty(nseq, d["hkv"], d["D"], dtype=torch.bfloat16, device="cuda")
+    dv = torch.empty_like(dk)
+    dpos = torch.empty(nseq, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(dq)
+    lse = torch.empty(nseq, d["hq"], dtype=torch.float32, device="cuda")
+    ho = torch.empty(nseq, d["hq"], d["D"], dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty(nseq, d["hq"], dtype=torch.float32).pin_memory()
+    ws = cache.workspace(d["hq"])
+
+    def step(i):
+        dq.copy_(hq_[i], non_blocking=True)
+        dk.copy_(hk[i], non_blocking=True)
+        dv.copy_(hv[i], non_blocking=True)
+        dpos.copy_(hpos[i], non_blocking=True)
+        cache.append_tokens(dpos, dk, dv)
+        cache.decode(dq, dpos, out=out, lse=lse, workspace=ws)
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(warmup + i)
+    dt = time.perf_counter() - t0
+    h2d = (dq.numel() + dk.numel() + dv.numel()) * 2 + dpos.numel() * 4
+    d2h = out.numel() * 2 + lse.numel() * 4
+    return dt, h2d, d2h
+
+
+# ---- prefill --------------------------------------------------------------
+def prefill_flops(S, P, W, hq, D, bm=128, bn=128):
+    """Exact admitted (query, key) pairs and the pairs inside non-skipped tiles."""
+    p = np.arange(S, dtype=np.int64)
+    pairs = np.minimum(p + 1, P + W).sum()
+    return 4.0 * D * hq * float(pairs)
+
+
+def run_prefill(ps, torch, S, P, W, steps, warmup, seed, full_causal=False):
+    d = PRE
+    B, hq, hkv, D = d["B"], d["hq"], d["hkv"], d["D"]
+    if full_causal:
+        W = S
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    q = torch.randn(B, S, hq, D, generator=gen, device="cuda").to(torch.bfloat16)
+    k = torch.randn(B, S, hkv, D, generator=gen, device="cuda").to(torch.bfloat16)
+    v = torch.randn(B, S, hkv, D, generator=gen, device="cuda").to(torch.bfloat16)
+    qs = torch.zeros(B, dtype=torch.int32, device="cuda")
+    pl = torch.full((B,), P, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty(B, hq, S, dtype=torch.float32, device="cuda")
+    ws = torch.empty(ps.prefill_workspace_size(B, S, hq, hkv, D), dtype=torch.uint8, device="cuda")
+    for _ in range(warmup):
+        ps.prefill(q, k, v, qs, pl, W, rope_theta=d["theta"], out=out, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        ps.prefill(q, k, v, qs, pl, W, rope_theta=d["theta"], out=out, lse=lse, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    cls = ps.prefill_tile_classes(S, 0, P, W).cpu().numpy()
+    n_skip, n_part, n_full = [(cls == c).sum() for c in (0, 1, 2)]
+    return ms, dict(skip=int(n_skip), partial=int(n_part), full=int(n_full))
+
+
+# ---- CPU oracle -----------------------------------------------------------
+def _oracle_worker(args):
+    """Spawned worker: builds one sequence's visible history (untimed), then
+    times the oracle's attention for the query."""
+    seq, pos, P, W, hq, hkv, D, theta, seed = args
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    import numpy as np_  # noqa: F401
+    import synth
+    from oracle import attend, visible_positions
+    hist = synth.History(seed, seq, hkv, D)
+    js = visible_positions(pos, P, W)
+    k, v = hist.rows(js)
+    lut = {int(j): i for i, j in enumerate(js)}
+
+    def history(req):
+        idx = [lut[int(j)] for j in req]
+        return k[idx], v[idx]
+
+    q = synth.bits_to_f64(synth.query_bits(seed, seq, pos, hq, D))[0]
+    t0 = time.perf_counter()
+    attend(q, pos, P, W, history, theta)
+    return time.perf_counter() - t0
+
+
+def oracle_baseline(budget_s=20.0):
+    """Oracle decode throughput on this host's cores over a bounded sample of
+    the decode workload (tokens/s for one layer)."""
+    import multiprocessing as mp
+    d = DEC
+    P = decode_prefix_lens(d["seed"], d["nseq"])
+    cores = max(1, min(os.cpu_count() or 1, 32))
+    jobs = [(s % d["nseq"], d["pos0"], int(P[s % d["nseq"]]), d["W"], d["hq"], d["hkv"], d["D"],
+             d["theta"], d["seed"]) for s in range(d["nseq"])]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        t0 = time.perf_counter()
+        times = pool.map(_oracle_worker, jobs[:cores])   # calibrate
+        per_seq = statistics.median(times)
+        n = int(max(cores, min(len(jobs) * 8, budget_s * cores / max(per_seq, 1e-3))))
+        work = [jobs[i % len(jobs)] for i in range(n)]
+        t1 = time.perf_counter()
+        times = pool.map(_oracle_worker, work, chunksize=1)
+        wall = time.perf_counter() - t1
+    busy = sum(times)
+    # throughput of the attention compute: sequences done per second of the
+    # cores' attention time (history generation excluded)
+    value = n / (busy / cores)
+    return {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} decode queries (all 16 heads each) of the steady-decode workload, "
+                      f"float64 numpy oracle, {cores} spawned processes, attention time only "
+                      f"(history synthesis excluded); wall {wall:.1f} s",
+            "cpu_seconds": busy}
+
+
+# ---- main -----------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--no-baselines", action="store_true", help="skip full-causal and oracle legs")
+    ap.add_argument("--prefill-steps", type=int, default=20)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_
+        torch.cuda.set_device(local)
+        dist_.init_process_group("nccl")
+        dist = dist_
+    else:
+        torch.cuda.set_device(0)
+    import prefix_sliding_window_02_b300 as ps
+
+    hbm_peak, bf16_peak, bf16_sustained, peak_src = peaks()
+    d = DEC
+    seed = d["seed"] + 101 * rank
+    P = decode_prefix_lens(seed, d["nseq"])
+    n_steps = args.warmup + args.steps
+    cache, q, k, v, pos, L = decode_setup(ps, torch, seed, d["W"], P, d["pos0"], n_steps)
+    clocks = ClockSampler(local)
+    total_ms, kern_ms, out, lse = run_decode(ps, torch, cache, q, k, v, pos, args.steps, args.warmup, dist)
+    assert cache.check_status() == 0
+    assert torch.isfinite(out.float()).all()
+    ms_step = total_ms / args.steps
+    value = world * d["nseq"] * args.steps / (total_ms / 1e3)
+
+    kv_bytes = float(np.sum(2 * d["hkv"] * L * d["D"] * 2))  # K and V of the live slots
+    q_bytes = d["nseq"] * d["hq"] * d["D"] * 2
+    alg_bytes = kv_bytes + q_bytes
+    kern_avg_ms = statistics.mean(kern_ms)
+    achieved = alg_bytes / (kern_avg_ms / 1e3) / 1e9
+    step_gbs = alg_bytes / (ms_step / 1e3) / 1e9
+
+    e2e = None
+    full = None
+    pre = None
+    if rank == 0 or world == 1:
+        dt, h2d, d2h = run_decode_e2e(ps, torch, cache, min(args.steps, 200), 5, seed + 7)
+        e2e = {"value": d["nseq"] * min(args.steps, 200) / dt, "unit": "tok/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "how": "pinned host -> device copies of q, k, v, pos; ps_kv_append + ps_decode; "
+                      "device -> host O and LSE; stream sync each step; host wall clock"}
+    del cache, q, k, v
+    torch.cuda.empty_cache()
+
+    # prefill (one layer)
+    try:
+        pms, cls = run_prefill(ps, torch, PRE["S"], PRE["P"], PRE["W"], args.prefill_steps, 3, seed + 5)
+        flops = prefill_flops(PRE["S"], PRE["P"], PRE["W"], PRE["hq"], PRE["D"])
+        tile_flops = 4.0 * PRE["D"] * PRE["hq"] * 128 * 128 * (cls["partial"] + cls["full"])
+        pre = {"workload": "prefill 1 x 32768 tokens, P=100, W=4096, Hq 16 / Hkv 8, D 128, one layer",
+               "ms": pms, "tflops_algorithmic": flops / pms / 1e9,
+               "tflops_on_nonskipped_tiles": tile_flops / pms / 1e9,
+               "frac_of_measured_bf16_burst": tile_flops / pms / 1e9 / bf16_peak,
+               "tiles": cls, "skip_fraction_of_causal_tiles": cls["skip"] and
+               1 - (cls["partial"] + cls["full"]) / ((256 * 257) // 2)}
+    except Exception as e:  # noqa: BLE001
+        pre = {"unavailable": f"{type(e).__name__}: {e}"}
+
+    if not args.no_baselines and (rank == 0 or world == 1):
+        fsteps = min(args.steps, 30)
+        cfc, qf, kf, vf, posf, Lf = decode_setup(ps, torch, seed + 3, d["W"], P, d["pos0"],
+                                                 fsteps + 3, full_causal=True)
+        fms, _, _, _ = run_decode(ps, torch, cfc, qf, kf, vf, posf, fsteps, 3, None, per_kernel=False)
+        full = {"decode_tok_s": d["nseq"] * fsteps / (fms / 1e3), "decode_ms_per_step": fms / fsteps,
+                "kv_gb_per_step": float(np.sum(2 * d["hkv"] * Lf * d["D"] * 2)) / 1e9,
+                "how": "same library, W > position (no eviction), P = 0"}
+        del cfc, qf, kf, vf
+        torch.cuda.empty_cache()
+        if "ms" in pre:
+            try:
+                fpms, _ = run_prefill(ps, torch, PRE["S"], 0, PRE["W"], 5, 2, seed + 9, full_causal=True)
+                full["prefill_ms"] = fpms
+                pre["speedup_vs_full_causal"] = fpms / pre["ms"]
+            except Exception as e:  # noqa: BLE001
+                full["prefill_unavailable"] = str(e)
+        full["decode_speedup"] = value / world / full["decode_tok_s"]
+    clk = clocks.stop()
+
+    cpu = None
+    if not args.no_baselines and world == 1:
+        cpu = oracle_baseline()
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (N(0,1) bf16 K/V/Q, random-init)",
+        "config": {"workload": "steady decode: 64 sequences at position 131072+step, P uniform "
+                               "64..512, W 4096, Hq 16 / Hkv 8, D 128, one layer per step "
+                               "(append + split-KV partial + combine)",
+                   "layers_for_model_rate": LAYERS, "l2": "inputs larger than L2 "
+                   f"({kv_bytes / 1e9:.2f} GB of K/V read per step vs 126 MB L2)",
+                   "parallelism": f"replicas x{world} (independent batches, no collective)"},
+        "decode": {"tok_s_per_layer": value, "tok_s_28_layers": value / LAYERS,
+                   "step_hbm_gbs": step_gbs, "kv_bytes_per_step": kv_bytes,
+                   "partial_kernel_ms": kern_avg_ms, "step_ms": ms_step},
+        "roofline": {"kernel": "decode_partial_kernel<128,2,4,3>", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": f"{peak_src} hbm_gbs",
+                     "traffic": committed_traffic("decode_partial_steady",
+                                                  "prefix_sliding_window_02_b300/csrc/ps_decode.cu"),
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "frac_of_8tbs": achieved / 8000.0},
+        "prefill": pre, "full_causal": full, "e2e": e2e,
+        "gpu_launches": 3 * args.steps, "clocks": clk, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def reference_arm(args, world, rank):
+    """The oracle as the reference arm: timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    t0 = time.perf_counter()
+    runs = []
+    for _ in range(args.warmup + args.steps):
+        runs.append(oracle_baseline(budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup))))
+    timed = runs[args.warmup:]
+    value = statistics.mean(r["value"] for r in timed)
+    cpu = dict(timed[-1])
+    cpu["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * DEC["nseq"] / value, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "steady decode: 64 sequences at position 131072, P uniform 64..512, "
+                                   "W 4096, Hq 16 / Hkv 8, D 128, one layer (bounded sample per step)"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": time.perf_counter() - t0}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

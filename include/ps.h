@@ -1,0 +1,223 @@
+/*
+ * ps.h -- C ABI of libps.so: Prefix-Sliding attention for NVIDIA B300 (sm_103a).
+ *
+ * Prefix-Sliding attention: the query at absolute position p attends to key j
+ * iff  j <= p  and  (j < P  or  j > p - W): a fixed task prefix of P tokens
+ * plus the last W positions, the current token included.  Keys in between are
+ * evicted, so at most P + W keys are ever cached, and positions keep counting
+ * up ("Continue PE") so RoPE'd keys stay valid after eviction.
+ *   Sources: njhaofan.com article, section "PrefixSliding如何丢掉中间Token？";
+ *   "Prefix Sliding：面向高效 test-time scaling 的前缀滑动方法"
+ *   (papers.ananclaw.com), sections "核心方法" and "伪代码";
+ *   "Prefix Sliding for efficient test-time scaling" (agihunt.info), the
+ *   paragraphs on the 4,196-token cap, on Continue PE and on the two-level
+ *   tile filter of the FlashAttention kernel.
+ *
+ * Conventions for every call
+ *   - Pointers marked "device" are CUDA device pointers owned by the caller
+ *     (e.g. torch tensors).  The library never allocates, frees or keeps them.
+ *   - "bf16" is IEEE bfloat16 (__nv_bfloat16), stored row-major as documented.
+ *   - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and never synchronises.  The library is
+ *     stateless and thread-safe.
+ *   - Host-side checks run before any launch and return a ps_status_t.
+ *     Checks that need device data (per-sequence prefix lengths, positions,
+ *     pool bases) run inside the kernels: a failing sequence is skipped and
+ *     PS_DEV_* bits are OR-ed into the optional device status word, which
+ *     ps_check_device_status() reads back.  Kernels never trap.
+ *   - RoPE: half-split ("NeoX") rotation, element i with element i + D/2, by
+ *     the angle pos * theta^(-2i/D), at the absolute position.  The angle is
+ *     reduced modulo one turn in 64-bit fixed point, so positions up to 2^31
+ *     keep full precision.  Rotated Q and K are rounded to bf16.
+ *   - Softmax scale is the `scale` argument (normally 1/sqrt(D)); LSE is the
+ *     natural log of sum_j exp(scale * q.k_j).  Query head h reads KV head
+ *     h / (Hq / Hkv).
+ */
+#ifndef PS_H_
+#define PS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ps_status_t {
+  PS_OK = 0,
+  PS_ERR_INVALID_ARGUMENT = 1, /* null pointer, W < 1, P < 0, Hq % Hkv != 0, sizes */
+  PS_ERR_UNSUPPORTED = 2,      /* head_dim not in {64, 128}, group size, tile size */
+  PS_ERR_ALIGNMENT = 3,        /* a tensor pointer is not 16-byte aligned          */
+  PS_ERR_WORKSPACE = 4,        /* workspace missing or too small                   */
+  PS_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed             */
+  PS_ERR_DEVICE = 6            /* ps_check_device_status found flags set           */
+} ps_status_t;
+
+/* Bits a kernel ORs into the device status word. */
+#define PS_DEV_BAD_PREFIX 0x1  /* prefix_len < 0 or > prefix_max                  */
+#define PS_DEV_BAD_POS    0x2  /* a position < 0                                   */
+#define PS_DEV_BAD_SLOT   0x4  /* slot_base/capacity outside the pool              */
+#define PS_DEV_TIMEOUT    0x8  /* a bounded wait on an mbarrier gave up            */
+#define PS_DEV_BAD_RUN    0x10 /* cu_tokens not increasing / outside [0, n_tokens] */
+#define PS_DEV_BAD_SEQ    0x20 /* a sequence index outside [0, nseq)               */
+
+/* Human-readable name of a status code (static string). */
+const char* ps_status_string(ps_status_t status);
+
+/*
+ * The bounded KV cache ("伪代码" section: total cache size is the constant
+ * prefix_len + W).  Sequence s owns pool rows [slot_base[s], slot_base[s] +
+ * capacity).  Position pos of sequence s lives in row slot_base[s] + slot(pos):
+ *     slot(pos) = pos                       if pos < P_s
+ *               = P_s + (pos - P_s) mod W   otherwise,
+ * so prefix slots never move and each window slot is overwritten exactly
+ * when its previous occupant leaves the window.  After positions 0..p are
+ * appended, slots [0, min(p+1, P_s+W)) hold exactly the keys query p may see.
+ */
+typedef struct ps_cache_desc {
+  void* k_pool;              /* device bf16 [total_slots, n_kv_heads, head_dim], RoPE'd K */
+  void* v_pool;              /* device bf16 [total_slots, n_kv_heads, head_dim], V        */
+  const int64_t* slot_base;  /* device [nseq]: first pool row of each sequence            */
+  const int32_t* prefix_len; /* device [nseq]: P of each sequence, 0 <= P <= prefix_max   */
+  int32_t* status;           /* device int32 status word, or NULL                         */
+  int64_t total_slots;       /* rows in each pool                                          */
+  int32_t nseq;              /* sequences described                                        */
+  int32_t n_kv_heads;        /* Hkv >= 1                                                   */
+  int32_t head_dim;          /* D: 64 or 128                                               */
+  int32_t window;            /* W >= 1                                                     */
+  int32_t capacity;          /* rows reserved per sequence, >= prefix_max + window         */
+  int32_t prefix_max;        /* host bound on every prefix_len                             */
+  double rope_theta;         /* RoPE base, > 0                                             */
+} ps_cache_desc;
+
+/*
+ * ps_ring_slots: slot(pos) of the formula above for n independent entries.
+ *   pos, prefix_len : device int32 [n]; window >= 1; slot : device int32 [n].
+ * Entries with pos < 0 or prefix_len < 0 get slot -1.
+ */
+ps_status_t ps_ring_slots(const int32_t* pos, const int32_t* prefix_len, int32_t window,
+                          int32_t* slot, int64_t n, void* stream);
+
+/*
+ * ps_kv_append: rotate new keys at their absolute positions (Continue PE:
+ * agihunt.info paragraph on position encodings) and store K and V into the
+ * ring ("PrefixSliding如何丢掉中间Token？": older middle tokens leave the cache).
+ *   k, v      : device bf16 [n_tokens, n_kv_heads, head_dim], raw (un-rotated) K, V.
+ *   Tokens come in runs: run r covers tokens [cu_tokens[r], cu_tokens[r+1]) of
+ *   sequence seq_idx[r], at consecutive positions pos0[r], pos0[r]+1, ...
+ *   seq_idx, pos0 : device int32 [nrun]; cu_tokens : device int32 [nrun+1],
+ *   cu_tokens[0] = 0, non-decreasing, cu_tokens[nrun] = n_tokens.
+ *   A run longer than W writes only its survivors (prefix positions and the
+ *   last W positions), so the result equals appending one token at a time.
+ *   Two runs of one sequence in one call: undefined.
+ * Decode appends one token per sequence: nrun = nseq, cu_tokens = 0..nseq.
+ */
+ps_status_t ps_kv_append(const ps_cache_desc* cache, const int32_t* seq_idx,
+                         const int32_t* pos0, const int32_t* cu_tokens, int32_t nrun,
+                         const void* k, const void* v, int64_t n_tokens, void* stream);
+
+/*
+ * ps_decode_workspace_size: bytes of device workspace ps_decode needs for
+ * nseq sequences on the current device (split-KV partial results).
+ */
+ps_status_t ps_decode_workspace_size(int32_t nseq, int32_t n_q_heads, int32_t n_kv_heads,
+                                     int32_t head_dim, size_t* bytes);
+
+/*
+ * ps_decode: one query token per sequence against the prefix and window keys
+ * in the cache (the generation step of the "伪代码" section).
+ *   q   : device bf16 [nseq, n_q_heads, head_dim], raw (rotated here at pos[s]).
+ *   pos : device int32 [nseq], absolute position of each query; its own K/V
+ *         must already be appended.  Sequence s reads slots
+ *         [0, min(pos[s]+1, P_s+W)).
+ *   out : device bf16 [nseq, n_q_heads, head_dim]; lse : device fp32 [nseq, n_q_heads].
+ *   workspace : device, >= ps_decode_workspace_size bytes, 256-byte aligned.
+ * Work is split evenly over all SMs in 32-slot tiles regardless of per-sequence
+ * length (no host synchronisation), then a second kernel merges the partial
+ * softmax results by their log-sum-exp.  n_q_heads / n_kv_heads in {1,2,4,8}.
+ */
+ps_status_t ps_decode(const ps_cache_desc* cache, const void* q, const int32_t* pos,
+                      int32_t n_q_heads, float scale, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The two launches of ps_decode, callable on their own (same arguments and
+ * workspace): ps_decode_partial streams the K/V tiles and writes the partial
+ * softmax records into the workspace; ps_decode_combine merges them into out
+ * and lse.  Between the two calls the workspace must not be reused.
+ */
+ps_status_t ps_decode_partial(const ps_cache_desc* cache, const void* q, const int32_t* pos,
+                              int32_t n_q_heads, float scale, void* workspace,
+                              size_t workspace_bytes, void* stream);
+ps_status_t ps_decode_combine(const ps_cache_desc* cache, int32_t n_q_heads, void* out, float* lse,
+                              const void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * ps_prefill_workspace_size: device workspace for ps_prefill (rotated Q and K
+ * and, with a ring, the gathered cached keys and values).
+ *   ring_rows_max : 0 without a ring, else the ring's prefix_max + window.
+ */
+ps_status_t ps_prefill_workspace_size(int32_t batch, int32_t seqlen, int32_t n_q_heads,
+                                      int32_t n_kv_heads, int32_t head_dim,
+                                      int32_t ring_rows_max, size_t* bytes);
+
+/*
+ * ps_prefill: tiled forward of Prefix-Sliding attention for a chunk of
+ * `seqlen` tokens per batch row (prompt prefill, chunked extend, and the
+ * truncated-backprop training forward of the agihunt.info paragraph on RL).
+ * Tiles that hold no admitted (query, key) pair are skipped; tiles that hold
+ * some but not all are masked element by element; the rest run unmasked
+ * (agihunt.info paragraph on the two-level filter; njhaofan.com section
+ * "PrefixSliding如何丢掉中间Token？").
+ *   q : device bf16 [batch, seqlen, n_q_heads, head_dim]; k, v : device bf16
+ *       [batch, seqlen, n_kv_heads, head_dim]; raw, rotated here.
+ *   q_start : device int32 [batch]: absolute position of the chunk's first token.
+ *   prefix_len : device int32 [batch]: P of each row.
+ *   ring == NULL: the keys are the chunk's own tokens.
+ *   ring != NULL: the keys are the ring's live entries of sequence ring_seq[b]
+ *       (positions < q_start[b], as left by ps_kv_append) followed by the
+ *       chunk; ring_seq : device int32 [batch] (NULL = identity), and
+ *       prefix_len must equal the ring's prefix_len of that sequence.
+ *   out : device bf16 [batch, seqlen, n_q_heads, head_dim];
+ *   lse : device fp32 [batch, n_q_heads, seqlen] (natural log).
+ *   status : device int32 word or NULL.
+ * Uses tcgen05 tensor cores with TMEM accumulators.  head_dim 128 only.
+ */
+ps_status_t ps_prefill(const void* q, const void* k, const void* v, int32_t batch,
+                       int32_t seqlen, const int32_t* q_start, const int32_t* prefix_len,
+                       int32_t window, int32_t n_q_heads, int32_t n_kv_heads,
+                       int32_t head_dim, float scale, double rope_theta,
+                       const ps_cache_desc* ring, const int32_t* ring_seq, void* out,
+                       float* lse, void* workspace, size_t workspace_bytes,
+                       int32_t* status, void* stream);
+
+/*
+ * Tile geometry used by ps_prefill for one batch row: nq x nk tiles of
+ * bm x bn.  with_ring != 0 counts the ring rows a chunk starting at q_start
+ * would gather ((min(P, q_start) prefix keys plus the window keys before q_start).
+ */
+ps_status_t ps_prefill_tile_grid(int32_t seqlen, int32_t q_start, int32_t prefix_len,
+                                 int32_t window, int32_t with_ring, int32_t bm, int32_t bn,
+                                 int32_t* nq, int32_t* nk);
+
+/*
+ * ps_prefill_tile_classes: the class ps_prefill assigns to each (query tile,
+ * key tile) of one batch row: 0 = skip, 1 = partial (masked), 2 = full.
+ *   out : device uint8 [nq * nk] (row-major by query tile), sizes from
+ *   ps_prefill_tile_grid with the same arguments.  Any bm, bn >= 1.
+ */
+ps_status_t ps_prefill_tile_classes(int32_t seqlen, int32_t q_start, int32_t prefix_len,
+                                    int32_t window, int32_t with_ring, int32_t bm, int32_t bn,
+                                    uint8_t* out, void* stream);
+
+/*
+ * ps_check_device_status: synchronously copy the device status word to
+ * *host_flags.  Returns PS_ERR_DEVICE if any flag is set, PS_OK otherwise.
+ * Test and debugging use; it synchronises the device.
+ */
+ps_status_t ps_check_device_status(const int32_t* status, int32_t* host_flags);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PS_H_ */

@@ -52,7 +52,7 @@ def round_bf16(x) -> np.ndarray:
     e = np.maximum(e, -125)                  # subnormal range keeps a fixed quantum
     quantum = np.ldexp(1.0, e - 8)
     r = np.rint(x / quantum) * quantum       # rint: round half to even
-    r = np.where(np.abs(r) > 3.3895313892515355e38, np.sign(r) * np.inf, r)
+    r = np.where(np.abs(r) > 3.3895313892515355e38, np.copysign(np.inf, x), r)
     return np.where(x == 0.0, x, r)
 
 

@@ -1,0 +1,218 @@
+"""Prefix-Sliding attention on B300: Python binding of libps.so.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+torch supplies device memory and streams.  Names follow include/ps.h.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Sequence
+
+import torch
+
+from ._lib import (CacheDesc, PsError, check, lib, PS_DEV_BAD_POS, PS_DEV_BAD_PREFIX,  # noqa: F401
+                   PS_DEV_BAD_RUN, PS_DEV_BAD_SEQ, PS_DEV_BAD_SLOT, PS_DEV_TIMEOUT)
+
+__all__ = ["RingCache", "ring_slots", "decode_workspace_size", "prefill_workspace_size",
+           "prefill", "prefill_tile_grid", "prefill_tile_classes", "PsError", "lib"]
+
+BF16 = torch.bfloat16
+
+
+def _vp(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA tensor of {dtype}, got "
+                         f"{t.dtype} on {t.device} (contiguous={t.is_contiguous()})")
+
+
+class RingCache:
+    """Bounded per-sequence K/V cache of ``prefix_max + window`` slots.
+
+    Pools are torch tensors of shape [nseq * capacity, n_kv_heads, head_dim];
+    sequence s owns rows [s * capacity, (s + 1) * capacity).
+    """
+
+    def __init__(self, nseq: int, n_kv_heads: int, head_dim: int, window: int,
+                 prefix_len: Sequence[int] | torch.Tensor, rope_theta: float = 10000.0,
+                 prefix_max: Optional[int] = None, capacity: Optional[int] = None,
+                 device="cuda", zero: bool = True):
+        pl = torch.as_tensor(prefix_len, dtype=torch.int32).reshape(-1)
+        if pl.numel() != nseq:
+            raise ValueError("prefix_len must have nseq entries")
+        self.prefix_max = int(pl.max()) if prefix_max is None else int(prefix_max)
+        self.capacity = self.prefix_max + window if capacity is None else int(capacity)
+        self.nseq, self.n_kv_heads, self.head_dim, self.window = nseq, n_kv_heads, head_dim, window
+        self.rope_theta = float(rope_theta)
+        rows = nseq * self.capacity
+        alloc = torch.zeros if zero else torch.empty
+        self.k_pool = alloc(rows, n_kv_heads, head_dim, dtype=BF16, device=device)
+        self.v_pool = alloc(rows, n_kv_heads, head_dim, dtype=BF16, device=device)
+        self.slot_base = (torch.arange(nseq, dtype=torch.int64) * self.capacity).to(device)
+        self.prefix_len = pl.to(device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self._ws = None
+        self.desc = CacheDesc(
+            k_pool=self.k_pool.data_ptr(), v_pool=self.v_pool.data_ptr(),
+            slot_base=self.slot_base.data_ptr(), prefix_len=self.prefix_len.data_ptr(),
+            status=self.status.data_ptr(), total_slots=rows, nseq=nseq, n_kv_heads=n_kv_heads,
+            head_dim=head_dim, window=window, capacity=self.capacity, prefix_max=self.prefix_max,
+            rope_theta=self.rope_theta)
+
+    # ------------------------------------------------------------ append ----
+    def append(self, seq_idx: torch.Tensor, pos0: torch.Tensor, cu_tokens: torch.Tensor,
+               k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+        """ps_kv_append: runs r = tokens [cu[r], cu[r+1]) of sequence seq_idx[r]
+        at positions pos0[r], pos0[r] + 1, ...  k, v: [n_tokens, Hkv, D] bf16, raw."""
+        for t, n in ((seq_idx, "seq_idx"), (pos0, "pos0"), (cu_tokens, "cu_tokens")):
+            _need(t, torch.int32, n)
+        _need(k, BF16, "k")
+        _need(v, BF16, "v")
+        check(lib.ps_kv_append(ctypes.byref(self.desc), _vp(seq_idx), _vp(pos0), _vp(cu_tokens),
+                               seq_idx.numel(), _vp(k), _vp(v), k.shape[0], _stream(stream)),
+              "ps_kv_append")
+
+    def append_tokens(self, pos: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None,
+                      _cu: dict = {}) -> None:
+        """One token per sequence (the decode step): k, v [nseq, Hkv, D], pos [nseq]."""
+        key = (self.nseq, k.device)
+        if key not in _cu:
+            _cu[key] = (torch.arange(self.nseq, dtype=torch.int32, device=k.device),
+                        torch.arange(self.nseq + 1, dtype=torch.int32, device=k.device))
+        seq, cu = _cu[key]
+        self.append(seq, pos, cu, k, v, stream)
+
+    # ------------------------------------------------------------ decode ----
+    def workspace(self, n_q_heads: int) -> torch.Tensor:
+        need = decode_workspace_size(self.nseq, n_q_heads, self.n_kv_heads, self.head_dim)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.k_pool.device)
+        return self._ws
+
+    def decode(self, q: torch.Tensor, pos: torch.Tensor, scale: Optional[float] = None,
+               out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+               workspace: Optional[torch.Tensor] = None, stream=None):
+        """ps_decode: q [nseq, Hq, D] bf16 raw; pos [nseq] int32.  Returns (out, lse)."""
+        _need(q, BF16, "q")
+        _need(pos, torch.int32, "pos")
+        hq = q.shape[1]
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.head_dim)
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty(q.shape[0], hq, dtype=torch.float32, device=q.device)
+        ws = self.workspace(hq) if workspace is None else workspace
+        check(lib.ps_decode(ctypes.byref(self.desc), _vp(q), _vp(pos), hq, ctypes.c_float(scale),
+                            _vp(out), _vp(lse), _vp(ws), ws.numel(), _stream(stream)), "ps_decode")
+        return out, lse
+
+    def decode_partial(self, q: torch.Tensor, pos: torch.Tensor, scale: Optional[float] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+        """ps_decode_partial: the K/V-streaming launch of ps_decode."""
+        _need(q, BF16, "q")
+        _need(pos, torch.int32, "pos")
+        hq = q.shape[1]
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.head_dim)
+        ws = self.workspace(hq) if workspace is None else workspace
+        check(lib.ps_decode_partial(ctypes.byref(self.desc), _vp(q), _vp(pos), hq,
+                                    ctypes.c_float(scale), _vp(ws), ws.numel(), _stream(stream)),
+              "ps_decode_partial")
+
+    def decode_combine(self, out: torch.Tensor, lse: torch.Tensor,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+        """ps_decode_combine: merges the partial records into out [nseq,Hq,D] and lse [nseq,Hq]."""
+        _need(out, BF16, "out")
+        _need(lse, torch.float32, "lse")
+        hq = out.shape[1]
+        ws = self.workspace(hq) if workspace is None else workspace
+        check(lib.ps_decode_combine(ctypes.byref(self.desc), hq, _vp(out), _vp(lse), _vp(ws),
+                                    ws.numel(), _stream(stream)), "ps_decode_combine")
+
+    def check_status(self) -> int:
+        flags = ctypes.c_int32(0)
+        lib.ps_check_device_status(_vp(self.status), ctypes.byref(flags))
+        return flags.value
+
+
+def ring_slots(pos: torch.Tensor, prefix_len: torch.Tensor, window: int, stream=None) -> torch.Tensor:
+    _need(pos, torch.int32, "pos")
+    _need(prefix_len, torch.int32, "prefix_len")
+    out = torch.empty_like(pos)
+    check(lib.ps_ring_slots(_vp(pos), _vp(prefix_len), window, _vp(out), pos.numel(),
+                            _stream(stream)), "ps_ring_slots")
+    return out
+
+
+def decode_workspace_size(nseq: int, n_q_heads: int, n_kv_heads: int, head_dim: int) -> int:
+    b = ctypes.c_size_t(0)
+    check(lib.ps_decode_workspace_size(nseq, n_q_heads, n_kv_heads, head_dim, ctypes.byref(b)),
+          "ps_decode_workspace_size")
+    return b.value
+
+
+def prefill_workspace_size(batch: int, seqlen: int, n_q_heads: int, n_kv_heads: int,
+                           head_dim: int, ring_rows_max: int = 0) -> int:
+    b = ctypes.c_size_t(0)
+    check(lib.ps_prefill_workspace_size(batch, seqlen, n_q_heads, n_kv_heads, head_dim,
+                                        ring_rows_max, ctypes.byref(b)), "ps_prefill_workspace_size")
+    return b.value
+
+
+def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_start: torch.Tensor,
+            prefix_len: torch.Tensor, window: int, scale: Optional[float] = None,
+            rope_theta: float = 10000.0, ring: Optional[RingCache] = None,
+            ring_seq: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+            status: Optional[torch.Tensor] = None, stream=None):
+    """ps_prefill: q [B,S,Hq,D], k, v [B,S,Hkv,D] bf16 raw.  Returns (out, lse [B,Hq,S])."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, BF16, n)
+    _need(q_start, torch.int32, "q_start")
+    _need(prefix_len, torch.int32, "prefix_len")
+    B, S, hq, D = q.shape
+    hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, hq, S, dtype=torch.float32, device=q.device)
+    ring_rows = 0 if ring is None else ring.prefix_max + ring.window
+    if workspace is None:
+        workspace = torch.empty(prefill_workspace_size(B, S, hq, hkv, D, ring_rows),
+                                dtype=torch.uint8, device=q.device)
+    desc = None if ring is None else ctypes.byref(ring.desc)
+    check(lib.ps_prefill(_vp(q), _vp(k), _vp(v), B, S, _vp(q_start), _vp(prefix_len), window, hq,
+                         hkv, D, ctypes.c_float(scale), ctypes.c_double(rope_theta), desc,
+                         _vp(ring_seq), _vp(out), _vp(lse), _vp(workspace), workspace.numel(),
+                         _vp(status), _stream(stream)), "ps_prefill")
+    return out, lse
+
+
+def prefill_tile_grid(seqlen: int, q_start: int, prefix_len: int, window: int,
+                      with_ring: bool = False, bm: int = 128, bn: int = 128):
+    nq, nk = ctypes.c_int32(0), ctypes.c_int32(0)
+    check(lib.ps_prefill_tile_grid(seqlen, q_start, prefix_len, window, int(with_ring), bm, bn,
+                                   ctypes.byref(nq), ctypes.byref(nk)), "ps_prefill_tile_grid")
+    return nq.value, nk.value
+
+
+def prefill_tile_classes(seqlen: int, q_start: int, prefix_len: int, window: int,
+                         with_ring: bool = False, bm: int = 128, bn: int = 128,
+                         device="cuda", stream=None) -> torch.Tensor:
+    nq, nk = prefill_tile_grid(seqlen, q_start, prefix_len, window, with_ring, bm, bn)
+    out = torch.empty(nq, nk, dtype=torch.uint8, device=device)
+    check(lib.ps_prefill_tile_classes(seqlen, q_start, prefix_len, window, int(with_ring), bm, bn,
+                                      _vp(out), _stream(stream)), "ps_prefill_tile_classes")
+    return out

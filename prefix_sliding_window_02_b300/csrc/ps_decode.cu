@@ -1,0 +1,558 @@
+// ps_decode.cu -- split-KV decode over the prefix and window slots, then an
+// LSE-weighted combine.
+//
+// One generated token per sequence attends to its prefix and its last W
+// positions, which after eviction are exactly ring slots [0, min(p+1, P+W))
+// (njhaofan.com section "PrefixSliding如何丢掉中间Token？": once the window is
+// full the per-step cost no longer grows; papers.ananclaw.com "伪代码" step
+// decode).  The step is a memory-bound GEMV, so it runs on CUDA cores.
+//
+// Work split ("stream-K" over tiles): the (sequence, kv head) segments are laid
+// end to end as 32-slot tiles, N tiles in all; warp w of NW owns tiles
+// [w*N/NW, (w+1)*N/NW), whatever the sequence lengths.  Each warp streams its
+// tiles through a private STAGES-deep TMA ring in shared memory and writes
+// one partial (unnormalised O, running max, running sum) per segment piece
+// it touches.  Piece (warp w, segment sg) goes to record w + sg, which is
+// unique because both indices only grow along the tile line; so NW + #segments
+// records suffice.  The combine kernel finds the warps covering a segment
+// from the same arithmetic.
+#include "ps_internal.h"
+
+namespace ps {
+
+constexpr int kDecTile = 32;  // slots per tile (one per lane after the reduction)
+
+struct DecodeParams {
+  CUtensorMap tmk;  // 3D {D, Hkv, total_slots}, box {D, 1, 32}
+  CUtensorMap tmv;
+  const __nv_bfloat16* q;  // [nseq, Hq, D]
+  const int32_t* pos;
+  const int64_t* slot_base;
+  const int32_t* prefix_len;
+  int32_t* status;
+  int32_t* seg_tiles;  // workspace: [nseq + 1] exclusive prefix of tiles per sequence
+  float* rec;          // workspace: [NW + nseq*Hkv][rec_floats]
+  int64_t total_slots;
+  int32_t nseq, hq, hkv, window, capacity, prefix_max;
+  int32_t nwarps_total;
+  float scale_log2;  // softmax scale * log2(e)
+  RopeTurns turns;
+};
+
+template <int D, int G>
+struct DecShape {
+  static constexpr int EPL = D / 32;                       // elements per lane
+  static constexpr int TILE_BYTES = kDecTile * D * 2;      // one K or V tile
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int REC = ((G * D + 2 * G) + 3) & ~3;   // floats per record
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Largest s in [0, nseq] with pfx[s] * hkv <= g (pfx non-decreasing, pfx[0] = 0).
+__device__ __forceinline__ int find_seq(const int32_t* pfx, int nseq, int hkv, int64_t g) {
+  int lo = 0, hi = nseq;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)pfx[mid] * hkv <= g) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Warp owning global tile t when N tiles are split over NW warps.
+__device__ __forceinline__ int owner_warp(int64_t t, int64_t N, int64_t NW) {
+  return (int)(((t + 1) * NW + N - 1) / N - 1);
+}
+
+template <int D, int G, int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32, 1)
+    decode_partial_kernel(const __grid_constant__ DecodeParams p) {
+  using S = DecShape<D, G>;
+  constexpr int EPL = S::EPL;
+  constexpr int HP = G >= 2 ? 2 : 1;  // heads per QK pass
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* tiles = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WARPS * STAGES * S::STAGE_BYTES);
+  float* pbuf_all = reinterpret_cast<float*>(bars + WARPS * STAGES);  // [WARPS][32][G]
+  int32_t* pfx = reinterpret_cast<int32_t*>(pbuf_all + WARPS * 32 * G);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // 1) tiles per sequence and their exclusive prefix (warp 0, 32 sequences at a time)
+  if (warp == 0) {
+    int32_t run = 0;
+    for (int b0 = 0; b0 < p.nseq; b0 += 32) {
+      const int s = b0 + lane;
+      int32_t n = 0;
+      if (s < p.nseq) {
+        const int32_t P = p.prefix_len[s], ps_ = p.pos[s];
+        const int64_t sb = p.slot_base[s];
+        int32_t bad = 0;
+        if (P < 0 || P > p.prefix_max) bad |= PS_DEV_BAD_PREFIX;
+        if (ps_ < 0) bad |= PS_DEV_BAD_POS;
+        if (sb < 0 || sb + p.capacity > p.total_slots) bad |= PS_DEV_BAD_SLOT;
+        if (bad) {
+          if (blockIdx.x == 0) set_flag(p.status, bad);
+        } else {
+          const int64_t L = min((int64_t)ps_ + 1, (int64_t)P + p.window);
+          n = (int32_t)((L + kDecTile - 1) / kDecTile);
+        }
+      }
+      int32_t x = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (s < p.nseq) pfx[s] = run + x - n;
+      run += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) pfx[p.nseq] = run;
+  }
+  if (lane == 0) {
+    for (int st = 0; st < STAGES; ++st) mbar_init(&bars[warp * STAGES + st], 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&p.tmk);
+    prefetch_tmap(&p.tmv);
+  }
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= p.nseq; i += blockDim.x) p.seg_tiles[i] = pfx[i];
+
+  const int64_t N = (int64_t)pfx[p.nseq] * p.hkv;
+  const int64_t NW = p.nwarps_total;
+  const int w = blockIdx.x * WARPS + warp;
+  const int64_t lo = N * w / NW, hi = N * (w + 1) / NW;
+  if (lo >= hi) return;  // no block-wide barrier follows
+
+  uint8_t* my_tiles = tiles + warp * STAGES * S::STAGE_BYTES;
+  uint64_t* my_bars = bars + warp * STAGES;
+  float* pbuf = pbuf_all + warp * 32 * G;
+
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](int64_t g, int st) {
+    const int s = find_seq(pfx, p.nseq, p.hkv, g);
+    const int32_t nt = pfx[s + 1] - pfx[s];
+    const int64_t r = g - (int64_t)pfx[s] * p.hkv;
+    const int h = (int)(r / nt), t = (int)(r % nt);
+    const int32_t row0 = (int32_t)(p.slot_base[s] + (int64_t)t * kDecTile);
+    uint64_t* bar = &my_bars[st];
+    uint8_t* dst = my_tiles + st * S::STAGE_BYTES;
+    mbar_arrive_expect_tx(bar, S::STAGE_BYTES);
+    tma_load_3d(dst, &p.tmk, bar, 0, h, row0, pol);
+    tma_load_3d(dst + S::TILE_BYTES, &p.tmv, bar, 0, h, row0, pol);
+  };
+
+  if (lane == 0)
+    for (int k = 0; k < STAGES && lo + k < hi; ++k) issue(lo + k, k);
+
+  uint32_t parity = 0;  // bit st = parity expected next on stage st
+  float qf[G][EPL], acc[G][EPL], m[G], lsum[G];
+  int cur_L = 0;
+  bool ok = true;
+  int64_t consumed = lo;
+
+  for (int64_t g = lo; g < hi; ++g) {
+    const int st = (int)((g - lo) % STAGES);
+    const int s = find_seq(pfx, p.nseq, p.hkv, g);
+    const int32_t nt = pfx[s + 1] - pfx[s];
+    const int64_t r = g - (int64_t)pfx[s] * p.hkv;
+    const int h = (int)(r / nt), t = (int)(r % nt);
+
+    if (g == lo || t == 0) {
+      // new segment piece: rotate the group's queries at position pos[s]
+      const int32_t ppos = p.pos[s];
+      cur_L = (int)min((int64_t)ppos + 1, (int64_t)p.prefix_len[s] + p.window);
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        const __nv_bfloat16* qrow = p.q + ((int64_t)s * p.hq + h * G + gg) * D + lane * EPL;
+        float x[EPL];
+        if constexpr (EPL == 4) {
+          uint2 w2 = *reinterpret_cast<const uint2*>(qrow);
+          x[0] = bf16lo(w2.x); x[1] = bf16hi(w2.x); x[2] = bf16lo(w2.y); x[3] = bf16hi(w2.y);
+        } else {
+          uint32_t w1 = *reinterpret_cast<const uint32_t*>(qrow);
+          x[0] = bf16lo(w1); x[1] = bf16hi(w1);
+        }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          // half-split RoPE: element i pairs with i + D/2, held by lane ^ 16
+          const float partner = __shfl_xor_sync(0xffffffffu, x[e], 16);
+          const int i = (lane & 15) * EPL + e;
+          float c, sn;
+          rope_cos_sin(ppos, p.turns.f[i], c, sn);
+          const float y = (lane < 16) ? (x[e] * c - partner * sn) : (x[e] * c + partner * sn);
+          // rotated Q is rounded to bf16, as the tensor-core path stores it
+          qf[gg][e] = __bfloat162float(__float2bfloat16_rn(y)) * p.scale_log2;
+          acc[gg][e] = 0.f;
+        }
+        m[gg] = -INFINITY;
+        lsum[gg] = 0.f;
+      }
+    }
+
+    if (!mbar_wait(&my_bars[st], (parity >> st) & 1u)) {
+      ok = false;
+      break;
+    }
+    parity ^= 1u << st;
+    consumed = g + 1;
+
+    const uint8_t* kt = my_tiles + st * S::STAGE_BYTES;
+    const uint8_t* vt = kt + S::TILE_BYTES;
+    const int nvalid = min(kDecTile, cur_L - t * kDecTile);
+
+    // ---- scores: lane j ends with the dot product of slot row j
+    float sc[G];
+#pragma unroll
+    for (int hp = 0; hp < G; hp += HP) {
+      float part[HP][32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const uint8_t* rowp = kt + j * (D * 2) + lane * (EPL * 2);
+        float k4[EPL];
+        if constexpr (EPL == 4) {
+          uint2 w2 = *reinterpret_cast<const uint2*>(rowp);
+          k4[0] = bf16lo(w2.x); k4[1] = bf16hi(w2.x); k4[2] = bf16lo(w2.y); k4[3] = bf16hi(w2.y);
+        } else {
+          uint32_t w1 = *reinterpret_cast<const uint32_t*>(rowp);
+          k4[0] = bf16lo(w1); k4[1] = bf16hi(w1);
+        }
+#pragma unroll
+        for (int hh = 0; hh < HP; ++hh) {
+          float a = qf[hp + hh][0] * k4[0];
+#pragma unroll
+          for (int e = 1; e < EPL; ++e) a = fmaf(qf[hp + hh][e], k4[e], a);
+          part[hh][j] = a;
+        }
+      }
+      // transpose-reduce: after the step at offset o, a lane keeps the half
+      // of its partials whose row index has bit o equal to its lane bit o.
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+#pragma unroll
+          for (int hh = 0; hh < HP; ++hh) {
+            const float send = up ? part[hh][i] : part[hh][i + o];
+            const float keep = up ? part[hh][i + o] : part[hh][i];
+            part[hh][i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < HP; ++hh) sc[hp + hh] = part[hh][0];
+    }
+
+    // ---- online softmax (log2 domain; scores already carry scale*log2 e)
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+      const float x = (lane < nvalid) ? sc[gg] : -INFINITY;
+      const float mn = fmaxf(m[gg], warp_max(x));
+      const float alpha = fast_exp2(m[gg] - mn);
+      const float pr = fast_exp2(x - mn);
+      lsum[gg] = lsum[gg] * alpha + pr;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[gg][e] *= alpha;
+      m[gg] = mn;
+      pbuf[lane * G + gg] = pr;
+    }
+    __syncwarp();
+
+    // ---- O += P V over the valid rows
+    auto pv_row = [&](int j) {
+      const uint8_t* rowp = vt + j * (D * 2) + lane * (EPL * 2);
+      float v4[EPL];
+      if constexpr (EPL == 4) {
+        uint2 w2 = *reinterpret_cast<const uint2*>(rowp);
+        v4[0] = bf16lo(w2.x); v4[1] = bf16hi(w2.x); v4[2] = bf16lo(w2.y); v4[3] = bf16hi(w2.y);
+      } else {
+        uint32_t w1 = *reinterpret_cast<const uint32_t*>(rowp);
+        v4[0] = bf16lo(w1); v4[1] = bf16hi(w1);
+      }
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        const float pj = pbuf[j * G + gg];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[gg][e] = fmaf(pj, v4[e], acc[gg][e]);
+      }
+    };
+    if (nvalid == kDecTile) {
+#pragma unroll
+      for (int j = 0; j < kDecTile; ++j) pv_row(j);
+    } else {
+      for (int j = 0; j < nvalid; ++j) pv_row(j);
+    }
+
+    // ---- end of this warp's piece of the segment: write the partial record
+    if (t == nt - 1 || g == hi - 1) {
+      float* rec = p.rec + (size_t)(w + (int64_t)s * p.hkv + h) * S::REC;
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        float* o = rec + gg * D + lane * EPL;
+        if constexpr (EPL == 4) {
+          *reinterpret_cast<float4*>(o) = make_float4(acc[gg][0], acc[gg][1], acc[gg][2], acc[gg][3]);
+        } else {
+          *reinterpret_cast<float2*>(o) = make_float2(acc[gg][0], acc[gg][1]);
+        }
+        const float tot = warp_sum(lsum[gg]);
+        if (lane == 0) {
+          rec[G * D + gg] = m[gg];
+          rec[G * D + G + gg] = tot;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && g + STAGES < hi) {
+      fence_proxy_async_smem();
+      issue(g + STAGES, st);
+    }
+  }
+
+  if (!ok) {
+    // a wait gave up: report, then let the copies already issued land (bounded)
+    if (lane == 0) set_flag(p.status, PS_DEV_TIMEOUT);
+    const int64_t issued_end = min(hi, consumed + STAGES);
+    for (int64_t g = consumed + 1; g < issued_end; ++g) {
+      const int st = (int)((g - lo) % STAGES);
+      if (!mbar_wait(&my_bars[st], (parity >> st) & 1u)) break;
+      parity ^= 1u << st;
+    }
+  }
+}
+
+struct CombineParams {
+  const float* rec;
+  const int32_t* seg_tiles;
+  __nv_bfloat16* out;  // [nseq, Hq, D]
+  float* lse;          // [nseq, Hq]
+  int32_t nseq, hq, hkv, nwarps_total;
+};
+
+// One warp per (sequence, query head): merge the partial softmax records of the
+// warps that covered its segment.
+template <int D, int G>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ CombineParams p) {
+  using S = DecShape<D, G>;
+  constexpr int EPL = S::EPL;
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (gw >= (int64_t)p.nseq * p.hq) return;
+  const int s = (int)(gw / p.hq), hq = (int)(gw % p.hq);
+  const int h = hq / G, gg = hq % G;
+  const int32_t nt = p.seg_tiles[s + 1] - p.seg_tiles[s];
+  __nv_bfloat16* o = p.out + gw * D + lane * EPL;
+  if (nt == 0) {  // sequence rejected by the device checks
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] = __float2bfloat16_rn(0.f);
+    if (lane == 0) p.lse[gw] = -INFINITY;
+    return;
+  }
+  const int64_t N = (int64_t)p.seg_tiles[p.nseq] * p.hkv;
+  const int64_t start = (int64_t)p.seg_tiles[s] * p.hkv + (int64_t)h * nt;
+  const int w0 = owner_warp(start, N, p.nwarps_total);
+  const int w1 = owner_warp(start + nt - 1, N, p.nwarps_total);
+  const int64_t sg = (int64_t)s * p.hkv + h;
+  const int64_t NW = p.nwarps_total;
+  // warps between w0 and w1 that own no tile at all (possible when N < NW)
+  // wrote no record
+  auto owns_tiles = [&](int w) { return N * w / NW < N * (w + 1) / NW; };
+  float M = -INFINITY;
+  for (int w = w0; w <= w1; ++w)
+    if (owns_tiles(w)) M = fmaxf(M, p.rec[(size_t)(w + sg) * S::REC + G * D + gg]);
+  float a[EPL] = {};
+  float l = 0.f;
+  for (int w = w0; w <= w1; ++w) {
+    if (!owns_tiles(w)) continue;
+    const float* r = p.rec + (size_t)(w + sg) * S::REC;
+    const float f = fast_exp2(r[G * D + gg] - M);
+    l = fmaf(f, r[G * D + G + gg], l);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) a[e] = fmaf(f, r[gg * D + lane * EPL + e], a[e]);
+  }
+  const float inv = 1.f / l;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) o[e] = __float2bfloat16_rn(a[e] * inv);
+  if (lane == 0) p.lse[gw] = (M + log2f(l)) * 0.69314718055994530942f;
+}
+
+// ----------------------------------------------------------------- host ----
+constexpr int kDecWarps = 4;
+constexpr int kDecStages = 3;
+
+template <int D, int G>
+static size_t dec_smem_bytes(int nseq) {
+  using S = DecShape<D, G>;
+  return (size_t)kDecWarps * kDecStages * S::STAGE_BYTES + kDecWarps * kDecStages * 8 +
+         kDecWarps * 32 * G * 4 + (size_t)(nseq + 1) * 4;
+}
+
+struct DecPlan {
+  int grid = 0, nwarps = 0;
+  size_t smem = 0, rec_floats = 0;
+  void (*partial)(DecodeParams) = nullptr;
+  void (*combine)(CombineParams) = nullptr;
+};
+
+template <int D, int G>
+static bool plan_for(int nseq, DecPlan* pl) {
+  auto kp = decode_partial_kernel<D, G, kDecWarps, kDecStages>;
+  pl->smem = dec_smem_bytes<D, G>(nseq);
+  if (pl->smem > 227 * 1024) return false;
+  if (cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl->smem) !=
+      cudaSuccess)
+    return false;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kp, kDecWarps * 32, pl->smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    return false;
+  const int sms = device_sm_count();
+  if (sms < 1) return false;
+  pl->grid = sms * per_sm;
+  pl->nwarps = pl->grid * kDecWarps;
+  pl->rec_floats = DecShape<D, G>::REC;
+  pl->partial = reinterpret_cast<void (*)(DecodeParams)>(kp);
+  pl->combine = reinterpret_cast<void (*)(CombineParams)>(decode_combine_kernel<D, G>);
+  return true;
+}
+
+static bool make_plan(int D, int G, int nseq, DecPlan* pl) {
+#define PS_DEC_CASE(DD, GG) \
+  if (D == DD && G == GG) return plan_for<DD, GG>(nseq, pl);
+  PS_DEC_CASE(128, 1) PS_DEC_CASE(128, 2) PS_DEC_CASE(128, 4) PS_DEC_CASE(128, 8)
+  PS_DEC_CASE(64, 1) PS_DEC_CASE(64, 2) PS_DEC_CASE(64, 4) PS_DEC_CASE(64, 8)
+#undef PS_DEC_CASE
+  return false;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static size_t dec_ws_bytes(const DecPlan& pl, int nseq, int hkv) {
+  return align256((size_t)(nseq + 1) * 4) +
+         (size_t)(pl.nwarps + (size_t)nseq * hkv) * pl.rec_floats * 4;
+}
+
+static ps_status_t check_heads(int hq, int hkv, int D) {
+  if (hq < 1 || hkv < 1 || hq % hkv) return PS_ERR_INVALID_ARGUMENT;
+  const int G = hq / hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return PS_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return PS_ERR_UNSUPPORTED;
+  return PS_OK;
+}
+
+}  // namespace ps
+
+using namespace ps;
+
+static constexpr int kMaxDecodeSeqs = 4096;
+
+extern "C" ps_status_t ps_decode_workspace_size(int32_t nseq, int32_t n_q_heads, int32_t n_kv_heads,
+                                                int32_t head_dim, size_t* bytes) {
+  if (!bytes || nseq < 1) return PS_ERR_INVALID_ARGUMENT;
+  if (nseq > kMaxDecodeSeqs) return PS_ERR_UNSUPPORTED;
+  ps_status_t st = check_heads(n_q_heads, n_kv_heads, head_dim);
+  if (st != PS_OK) return st;
+  DecPlan pl;
+  if (!make_plan(head_dim, n_q_heads / n_kv_heads, nseq, &pl)) return PS_ERR_CUDA;
+  *bytes = dec_ws_bytes(pl, nseq, n_kv_heads);
+  return PS_OK;
+}
+
+// Validates the decode arguments and fills the launch parameters of both kernels.
+static ps_status_t prepare_decode(const ps_cache_desc* cache, int32_t n_q_heads, const void* ws,
+                                  size_t ws_bytes, DecPlan* pl) {
+  ps_status_t st = check_cache(cache);
+  if (st != PS_OK) return st;
+  st = check_heads(n_q_heads, cache->n_kv_heads, cache->head_dim);
+  if (st != PS_OK) return st;
+  if (cache->nseq > kMaxDecodeSeqs) return PS_ERR_UNSUPPORTED;
+  if (!make_plan(cache->head_dim, n_q_heads / cache->n_kv_heads, cache->nseq, pl)) return PS_ERR_CUDA;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return PS_ERR_WORKSPACE;
+  if (ws_bytes < dec_ws_bytes(*pl, cache->nseq, cache->n_kv_heads)) return PS_ERR_WORKSPACE;
+  return PS_OK;
+}
+
+static float* records_of(void* ws, int nseq) {
+  return reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256((size_t)(nseq + 1) * 4));
+}
+
+extern "C" ps_status_t ps_decode_partial(const ps_cache_desc* cache, const void* q,
+                                         const int32_t* pos, int32_t n_q_heads, float scale,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !pos || !(scale > 0.f)) return PS_ERR_INVALID_ARGUMENT;
+  DecPlan pl;
+  ps_status_t st = prepare_decode(cache, n_q_heads, workspace, workspace_bytes, &pl);
+  if (st != PS_OK) return st;
+  if (!aligned16(q)) return PS_ERR_ALIGNMENT;
+  const int D = cache->head_dim, hkv = cache->n_kv_heads, nseq = cache->nseq;
+  DecodeParams p;
+  const uint64_t dims[3] = {(uint64_t)D, (uint64_t)hkv, (uint64_t)cache->total_slots};
+  const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)hkv * D * 2};
+  const uint32_t box[3] = {(uint32_t)D, 1u, (uint32_t)kDecTile};
+  if (!encode_tmap(&p.tmk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, cache->k_pool, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tmap(&p.tmv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, cache->v_pool, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    return PS_ERR_CUDA;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.pos = pos;
+  p.slot_base = cache->slot_base;
+  p.prefix_len = cache->prefix_len;
+  p.status = cache->status;
+  p.seg_tiles = static_cast<int32_t*>(workspace);
+  p.rec = records_of(workspace, nseq);
+  p.total_slots = cache->total_slots;
+  p.nseq = nseq;
+  p.hq = n_q_heads;
+  p.hkv = hkv;
+  p.window = cache->window;
+  p.capacity = cache->capacity;
+  p.prefix_max = cache->prefix_max;
+  p.nwarps_total = pl.nwarps;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  make_rope_turns(cache->rope_theta, D, &p.turns);
+  pl.partial<<<pl.grid, kDecWarps * 32, pl.smem, (cudaStream_t)stream>>>(p);
+  return launch_status();
+}
+
+extern "C" ps_status_t ps_decode_combine(const ps_cache_desc* cache, int32_t n_q_heads, void* out,
+                                         float* lse, const void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  if (!out || !lse) return PS_ERR_INVALID_ARGUMENT;
+  DecPlan pl;
+  ps_status_t st = prepare_decode(cache, n_q_heads, workspace, workspace_bytes, &pl);
+  if (st != PS_OK) return st;
+  if (!aligned16(out)) return PS_ERR_ALIGNMENT;
+  const int nseq = cache->nseq;
+  CombineParams c;
+  c.rec = records_of(const_cast<void*>(workspace), nseq);
+  c.seg_tiles = static_cast<const int32_t*>(workspace);
+  c.out = static_cast<__nv_bfloat16*>(out);
+  c.lse = lse;
+  c.nseq = nseq;
+  c.hq = n_q_heads;
+  c.hkv = cache->n_kv_heads;
+  c.nwarps_total = pl.nwarps;
+  const int64_t warps = (int64_t)nseq * n_q_heads;
+  pl.combine<<<(unsigned)((warps + 3) / 4), 128, 0, (cudaStream_t)stream>>>(c);
+  return launch_status();
+}
+
+extern "C" ps_status_t ps_decode(const ps_cache_desc* cache, const void* q, const int32_t* pos,
+                                 int32_t n_q_heads, float scale, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (!out || !lse) return PS_ERR_INVALID_ARGUMENT;
+  ps_status_t st = ps_decode_partial(cache, q, pos, n_q_heads, scale, workspace, workspace_bytes,
+                                     stream);
+  if (st != PS_OK) return st;
+  return ps_decode_combine(cache, n_q_heads, out, lse, workspace, workspace_bytes, stream);
+}

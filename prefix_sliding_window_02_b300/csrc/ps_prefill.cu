@@ -1,0 +1,607 @@
+// ps_prefill.cu -- Prefix-Sliding prefill / extend / training forward.
+//
+// Two kernels per call:
+//  1. rope_gather_kernel rotates Q and the chunk's K at their absolute
+//     positions (Continue PE) into the workspace; with a ring it first copies
+//     the ring's live keys and values (already rotated when appended) in
+//     position order, so the key array is [cached prefix][cached window][chunk].
+//  2. prefill_kernel: one CTA per (128-query tile, query head, batch row).  It
+//     visits only the key tiles that can hold an admitted pair -- the prefix
+//     tiles and the band of tiles around the diagonal -- and classifies each:
+//     FULL tiles run unmasked, PARTIAL tiles get the element mask ("Prefix
+//     Sliding for efficient test-time scaling", agihunt.info, paragraph on the
+//     kernel's two-level filter).  S = Q K^T and O += P V run on tcgen05 tensor
+//     cores with fp32 accumulators in TMEM; softmax runs one thread per query
+//     row straight out of TMEM.
+#include "ps_internal.h"
+#include "ps_tc.cuh"
+#include "ps_tiles.cuh"
+
+namespace ps {
+
+// ---------------------------------------------------------------------------
+// tile export
+// ---------------------------------------------------------------------------
+__global__ void tile_classes_kernel(KeyMap m, int32_t seqlen, int32_t q_start, int32_t P,
+                                    int32_t W, int32_t bm, int32_t bn, int32_t nq, int32_t nk,
+                                    uint8_t* __restrict__ out) {
+  const int64_t n = (int64_t)nq * nk;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int a = (int)(i / nk), b = (int)(i % nk);
+    const int32_t qa = a * bm, qb = min(seqlen, (a + 1) * bm) - 1;
+    const int32_t ka = b * bn, kb = min(m.n_keys, (b + 1) * bn) - 1;
+    out[i] = tile_class(m, q_start, qa, qb, ka, kb, P, W);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 1. RoPE + gather
+// ---------------------------------------------------------------------------
+struct GatherParams {
+  const uint4* q;  // [B, S, Hq, D]
+  const uint4* k;  // [B, S, Hkv, D]
+  const uint4* v;
+  uint4* qh;       // [B, S, Hq, D]       rotated
+  uint4* kh;       // [B, Skv, Hkv, D]    rotated (ring part gathered)
+  uint4* vg;       // [B, Skv, Hkv, D]    gathered values (ring only) or null
+  const int32_t* q_start;
+  const int32_t* prefix_len;
+  int32_t* status;
+  // ring (null k_pool = no ring)
+  const uint4* k_pool;
+  const uint4* v_pool;
+  const int64_t* slot_base;
+  const int32_t* ring_prefix;
+  const int32_t* ring_seq;
+  int64_t total_slots;
+  int32_t nseq, capacity;
+  int32_t B, S, Skv, hq, hkv, W;
+  RopeTurns turns;
+};
+
+__device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, int32_t pos,
+                                        const unsigned long long* f, uint4& ra, uint4& rb) {
+  const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
+  const uint32_t* bw = reinterpret_cast<const uint32_t*>(&b);
+  uint32_t* raw = reinterpret_cast<uint32_t*>(&ra);
+  uint32_t* rbw = reinterpret_cast<uint32_t*>(&rb);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float c0, s0, c1, s1;
+    rope_cos_sin(pos, f[2 * e], c0, s0);
+    rope_cos_sin(pos, f[2 * e + 1], c1, s1);
+    const float x0 = bf16lo(aw[e]), x1 = bf16hi(aw[e]);
+    const float y0 = bf16lo(bw[e]), y1 = bf16hi(bw[e]);
+    raw[e] = pack_bf16(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
+    rbw[e] = pack_bf16(y0 * c0 + x0 * s0, y1 * c1 + x1 * s1);
+  }
+}
+
+// One thread per (row, head, group of 8 rotation pairs); D = 128 (16 vectors a row).
+__global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant__ GatherParams p) {
+  constexpr int VEC = 16, HALFV = 8, GROUPS = 8;
+  const int64_t nq_items = (int64_t)p.B * p.S * p.hq * GROUPS;
+  const int64_t nk_items = (int64_t)p.B * p.Skv * p.hkv * GROUPS;
+  const bool ring = p.k_pool != nullptr;
+  for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < nq_items + nk_items;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    if (it < nq_items) {
+      const int g = (int)(it % GROUPS);
+      int64_t r = it / GROUPS;
+      const int h = (int)(r % p.hq);
+      r /= p.hq;                       // r = b * S + row
+      const int b = (int)(r / p.S);
+      const int32_t pos = p.q_start[b] + (int32_t)(r % p.S);
+      const int64_t base = (r * p.hq + h) * VEC;
+      uint4 ra, rb;
+      rotate8(p.q[base + g], p.q[base + HALFV + g], pos, &p.turns.f[8 * g], ra, rb);
+      p.qh[base + g] = ra;
+      p.qh[base + HALFV + g] = rb;
+      continue;
+    }
+    const int64_t kt = it - nq_items;
+    const int g = (int)(kt % GROUPS);
+    int64_t r = kt / GROUPS;
+    const int h = (int)(r % p.hkv);
+    r /= p.hkv;                        // r = b * Skv + key index
+    const int b = (int)(r / p.Skv);
+    const int32_t kidx = (int32_t)(r % p.Skv);
+    const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
+    const KeyMap km = make_keymap(p.S, c0, P, p.W, ring);
+    const int64_t dst = (r * p.hkv + h) * VEC;
+    const int32_t n_ring = km.n_keys - p.S;
+    if (kidx >= km.n_keys) {  // padding rows up to the workspace stride: zeros
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      p.kh[dst + g] = z;
+      p.kh[dst + HALFV + g] = z;
+      if (p.vg) {
+        p.vg[dst + g] = z;
+        p.vg[dst + HALFV + g] = z;
+      }
+      continue;
+    }
+    if (kidx < n_ring) {  // cached key: copy the rotated row out of the ring
+      const int32_t s = p.ring_seq ? p.ring_seq[b] : b;
+      bool bad = s < 0 || s >= p.nseq;
+      int32_t rp = 0;
+      int64_t sb = 0;
+      if (!bad) {
+        rp = p.ring_prefix[s];
+        sb = p.slot_base[s];
+        if (rp != P) { set_flag(p.status, PS_DEV_BAD_PREFIX); bad = true; }
+        if (sb < 0 || sb + p.capacity > p.total_slots) { set_flag(p.status, PS_DEV_BAD_SLOT); bad = true; }
+      } else {
+        set_flag(p.status, PS_DEV_BAD_SEQ);
+      }
+      uint4 k0 = make_uint4(0, 0, 0, 0), k1 = k0, v0 = k0, v1 = k0;
+      if (!bad) {
+        const int32_t pos = key_pos(km, kidx);
+        const int64_t src = ((sb + ring_slot(pos, P, p.W)) * p.hkv + h) * VEC;
+        k0 = p.k_pool[src + g];
+        k1 = p.k_pool[src + HALFV + g];
+        v0 = p.v_pool[src + g];
+        v1 = p.v_pool[src + HALFV + g];
+      }
+      p.kh[dst + g] = k0;
+      p.kh[dst + HALFV + g] = k1;
+      p.vg[dst + g] = v0;
+      p.vg[dst + HALFV + g] = v1;
+      continue;
+    }
+    // chunk key
+    const int32_t t = kidx - n_ring;
+    const int64_t src = (((int64_t)b * p.S + t) * p.hkv + h) * VEC;
+    uint4 ra, rb;
+    rotate8(p.k[src + g], p.k[src + HALFV + g], c0 + t, &p.turns.f[8 * g], ra, rb);
+    p.kh[dst + g] = ra;
+    p.kh[dst + HALFV + g] = rb;
+    if (p.vg) {
+      p.vg[dst + g] = p.v[src + g];
+      p.vg[dst + HALFV + g] = p.v[src + HALFV + g];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. tile kernel
+// ---------------------------------------------------------------------------
+constexpr int kBM = 128, kBN = 128, kHD = 128;
+constexpr int kHalf = kBM * 64 * 2;  // one 64-column swizzled half block: 16 KB
+constexpr int kTile = 2 * kHalf;     // 128 x 128 bf16: 32 KB
+constexpr uint32_t kIdescQK = tc::idesc_bf16(kBM, kBN, false);
+constexpr uint32_t kIdescPV = tc::idesc_bf16(kBM, kHD, true);
+constexpr int kSmemPrefill = kTile * 6 + 1024 /*barriers*/ + 1024 /*alignment*/;
+
+struct PrefillParams {
+  CUtensorMap tmq;  // rotated Q  {D, Hq, S, B}
+  CUtensorMap tmk;  // rotated K  {D, Hkv, Skv, B}
+  CUtensorMap tmv;  // values     {D, Hkv, S or Skv, B}
+  __nv_bfloat16* out;
+  float* lse;
+  const int32_t* q_start;
+  const int32_t* prefix_len;
+  int32_t* status;
+  int32_t S, hq, hkv, W, with_ring, nq;
+  float scale_log2;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint8_t* sQ = smem;
+  uint8_t* sK0 = smem + kTile;
+  uint8_t* sV0 = smem + 3 * kTile;
+  uint8_t* sP = smem + 5 * kTile;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * kTile);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;  // [2]
+  uint64_t* s_done = bars + 3;
+  uint64_t* o_done = bars + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int qt = p.nq - 1 - (int)blockIdx.x;  // longest rows first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / (p.hq / p.hkv);
+  const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
+  const KeyMap km = make_keymap(p.S, c0, P, p.W, p.with_ring != 0);
+  const int32_t q0r = qt * kBM, q1r = min(p.S, q0r + kBM) - 1;
+  const int64_t q0 = (int64_t)c0 + q0r, q1 = (int64_t)c0 + q1r;
+
+  // key tiles that can hold an admitted pair: the prefix tiles, then the band
+  const int32_t kc = keys_below(km, q1 + 1);  // keys at or before the last query
+  const int32_t kP = keys_below(km, P);       // prefix keys
+  const int t1_end = (min(kP, kc) + kBN - 1) / kBN;
+  const int32_t kw = keys_below(km, q0 - p.W + 1);
+  const int t2_begin = max(t1_end, kw / kBN);
+  const int t2_end = (kc + kBN - 1) / kBN;
+  const int n_tiles = t1_end + max(0, t2_end - t2_begin);
+  auto tile_at = [&](int it) { return it < t1_end ? it : t2_begin + (it - t1_end); };
+
+  if (warp == 0) {
+    tc::alloc(smem_u32(tmem_slot), 256);
+    tc::relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    prefetch_tmap(&p.tmq);
+    prefetch_tmap(&p.tmk);
+    prefetch_tmap(&p.tmv);
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 128;
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+
+  const uint64_t pol_q = policy_evict_first();
+  const uint64_t pol_kv = policy_evict_last();
+  auto load_kv = [&](int stage, int kt) {
+    uint8_t* dk = sK0 + stage * kTile;
+    uint8_t* dv = sV0 + stage * kTile;
+    mbar_arrive_expect_tx(&kv_full[stage], 2 * kTile);
+    tma_load_4d(dk, &p.tmk, &kv_full[stage], 0, hk, kt * kBN, b, pol_kv);
+    tma_load_4d(dk + kHalf, &p.tmk, &kv_full[stage], 64, hk, kt * kBN, b, pol_kv);
+    tma_load_4d(dv, &p.tmv, &kv_full[stage], 0, hk, kt * kBN, b, pol_kv);
+    tma_load_4d(dv + kHalf, &p.tmv, &kv_full[stage], 64, hk, kt * kBN, b, pol_kv);
+  };
+  int issued = 0;  // key tiles whose loads were issued (thread 0)
+  if (tid == 0 && n_tiles > 0) {
+    mbar_arrive_expect_tx(q_full, kTile);
+    tma_load_4d(sQ, &p.tmq, q_full, 0, h, q0r, b, pol_q);
+    tma_load_4d(sQ + kHalf, &p.tmq, q_full, 64, h, q0r, b, pol_q);
+    for (; issued < 2 && issued < n_tiles; ++issued) load_kv(issued, tile_at(issued));
+  }
+
+  const int row = tid;
+  const int64_t qpos = q0 + row;
+  float m_ref = -INFINITY, l = 0.f;
+  bool ok = true;
+  int committed_pv = 0;
+  int it = 0;
+  for (; it < n_tiles; ++it) {
+    const int st = it & 1;
+    const int kt = tile_at(it);
+    const int32_t ka = kt * kBN;
+    const int32_t kb = min(km.n_keys, ka + kBN) - 1;
+    const uint8_t cls = tile_class(km, c0, q0r, q1r, ka, kb, P, p.W);
+    const bool masked = cls != kFull || ka + kBN > km.n_keys;
+
+    if (tid == 0) {
+      bool w = true;
+      if (it == 0) w = mbar_wait(q_full, 0);
+      w = w && mbar_wait(&kv_full[st], (it >> 1) & 1);
+      if (w) {
+        tc::fence_after();
+        const uint32_t aq = smem_u32(sQ), ak = smem_u32(sK0 + st * kTile);
+#pragma unroll
+        for (int kk = 0; kk < kHD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          tc::mma_bf16(tS, tc::sdesc_sw128(aq + off, 16, 1024), tc::sdesc_sw128(ak + off, 16, 1024),
+                       kIdescQK, kk > 0);
+        }
+      } else {
+        ok = false;
+      }
+      tc::commit(smem_u32(s_done));  // arrives at once if nothing was issued
+    }
+    if (!mbar_wait(s_done, it & 1)) ok = false;
+    tc::fence_after();
+
+    // ---- scores of this thread's query row
+    float s[kBN];
+#pragma unroll
+    for (int c = 0; c < kBN / 32; ++c) {
+      uint32_t r[32];
+      tc::ld32(tS + lane_off + c * 32, r);
+      tc::wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) s[c * 32 + j] = __uint_as_float(r[j]) * p.scale_log2;
+    }
+    if (masked) {
+#pragma unroll
+      for (int j = 0; j < kBN; ++j) {
+        const int32_t kidx = ka + j;
+        const bool keep = kidx < km.n_keys && admitted(qpos, key_pos(km, kidx), P, p.W);
+        s[j] = keep ? s[j] : -INFINITY;
+      }
+    }
+    float mt = s[0];
+#pragma unroll
+    for (int j = 1; j < kBN; ++j) mt = fmaxf(mt, s[j]);
+    const float m_new = fmaxf(m_ref, mt);
+    float alpha = 1.f;
+    bool rescale = false;
+    if (it == 0) {
+      m_ref = m_new;  // the first P V overwrites O
+    } else if (m_new > m_ref + 8.f) {  // lazy rescale: keep the stale max while within 2^8
+      alpha = ex2(m_ref - m_new);
+      m_ref = m_new;
+      rescale = true;
+    }
+    const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+
+    // ---- the previous P V must be done before P and O are touched
+    if (it > 0) {
+      if (!mbar_wait(o_done, (it - 1) & 1)) ok = false;
+      tc::fence_after();
+      if (tid == 0 && ok && issued < n_tiles) {  // its K/V stage is free: prefetch
+        fence_proxy_async_smem();
+        load_kv(issued & 1, tile_at(issued));
+        ++issued;
+      }
+    }
+    if (rescale) {
+#pragma unroll
+      for (int c = 0; c < kHD / 32; ++c) {
+        uint32_t r[32];
+        tc::ld32(tO + lane_off + c * 32, r);
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+        tc::st32(tO + lane_off + c * 32, r);
+      }
+      tc::wait_st();
+    }
+    // ---- P = exp2(s - m) as bf16 into shared memory, K-major 128-byte
+    // swizzle (the A operand of P V), 8 keys (one 16-byte chunk) at a time
+    float rs = 0.f;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int j = hh * 64 + c * 8;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = ex2(s[j + 2 * e] - mu), bb = ex2(s[j + 2 * e + 1] - mu);
+          rs += a + bb;
+          w[e] = pack_bf16(a, bb);
+        }
+        const uint32_t addr = smem_u32(sP) + hh * kHalf + (row >> 3) * 1024 + (row & 7) * 128 +
+                              ((c ^ (row & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3])
+                     : "memory");
+      }
+    }
+    l = l * alpha + rs;
+    fence_proxy_async_smem();
+    tc::fence_before();
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok) break;
+    if (tid == 0) {
+      tc::fence_after();
+      const uint32_t ap = smem_u32(sP), av = smem_u32(sV0 + st * kTile);
+#pragma unroll
+      for (int kk = 0; kk < kBN / 16; ++kk) {
+        const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
+        // V is MN-major: 64-column atoms 16 KB apart (LBO), 8-key groups 1 KB apart (SBO)
+        tc::mma_bf16(tO, tc::sdesc_sw128(ap + aoff, 16, 1024),
+                     tc::sdesc_sw128(av + kk * 2048, kHalf, 1024), kIdescPV, (it > 0) || (kk > 0));
+      }
+      tc::commit(smem_u32(o_done));
+    }
+    committed_pv = it + 1;
+  }
+
+  if (ok && n_tiles > 0) {
+    if (!mbar_wait(o_done, (n_tiles - 1) & 1)) ok = false;
+    tc::fence_after();
+  }
+  if (ok && n_tiles > 0) {
+    const float inv = 1.f / l;
+    const int32_t qrow = q0r + row;
+    __nv_bfloat16* orow = p.out + (((int64_t)b * p.S + qrow) * p.hq + h) * kHD;
+#pragma unroll
+    for (int c = 0; c < kHD / 32; ++c) {
+      uint32_t r[32];
+      tc::ld32(tO + lane_off + c * 32, r);
+      tc::wait_ld();
+      if (qrow <= q1r) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          uint4 v;
+          v.x = pack_bf16(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv);
+          v.y = pack_bf16(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
+          v.z = pack_bf16(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv);
+          v.w = pack_bf16(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
+          *reinterpret_cast<uint4*>(orow + c * 32 + j) = v;
+        }
+      }
+    }
+    if (qrow <= q1r)
+      p.lse[((int64_t)b * p.hq + h) * p.S + qrow] = (m_ref + __log2f(l)) * 0.69314718055994530942f;
+  }
+  if (!ok && tid == 0) {
+    set_flag(p.status, PS_DEV_TIMEOUT);
+    // let what was issued land before the CTA's shared memory goes away (bounded)
+    for (int t = it; t < issued; ++t) mbar_wait(&kv_full[t & 1], (t >> 1) & 1);
+    if (committed_pv > 0) mbar_wait(o_done, (committed_pv - 1) & 1);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tmem, 256);
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct PrefillLayout {
+  size_t q_off, k_off, v_off, total;
+  int32_t skv;
+};
+
+static PrefillLayout prefill_layout(int B, int S, int hq, int hkv, int D, int ring_rows) {
+  PrefillLayout L;
+  L.skv = S + ring_rows;
+  L.q_off = 0;
+  L.k_off = align256((size_t)B * S * hq * D * 2);
+  L.v_off = L.k_off + align256((size_t)B * L.skv * hkv * D * 2);
+  L.total = L.v_off + (ring_rows > 0 ? align256((size_t)B * L.skv * hkv * D * 2) : 0);
+  return L;
+}
+
+}  // namespace ps
+
+using namespace ps;
+
+extern "C" ps_status_t ps_prefill_tile_grid(int32_t seqlen, int32_t q_start, int32_t prefix_len,
+                                            int32_t window, int32_t with_ring, int32_t bm,
+                                            int32_t bn, int32_t* nq, int32_t* nk) {
+  if (!nq || !nk || seqlen < 1 || q_start < 0 || prefix_len < 0 || window < 1 || bm < 1 || bn < 1)
+    return PS_ERR_INVALID_ARGUMENT;
+  if ((int64_t)q_start + seqlen > 0x7fffffffLL) return PS_ERR_INVALID_ARGUMENT;
+  const KeyMap m = make_keymap(seqlen, q_start, prefix_len, window, with_ring != 0);
+  *nq = (seqlen + bm - 1) / bm;
+  *nk = (m.n_keys + bn - 1) / bn;
+  return PS_OK;
+}
+
+extern "C" ps_status_t ps_prefill_tile_classes(int32_t seqlen, int32_t q_start,
+                                               int32_t prefix_len, int32_t window,
+                                               int32_t with_ring, int32_t bm, int32_t bn,
+                                               uint8_t* out, void* stream) {
+  int32_t nq = 0, nk = 0;
+  ps_status_t st = ps_prefill_tile_grid(seqlen, q_start, prefix_len, window, with_ring, bm, bn,
+                                        &nq, &nk);
+  if (st != PS_OK) return st;
+  if (!out) return PS_ERR_INVALID_ARGUMENT;
+  const KeyMap m = make_keymap(seqlen, q_start, prefix_len, window, with_ring != 0);
+  const int64_t n = (int64_t)nq * nk;
+  const int threads = 256;
+  int64_t blocks = (n + threads - 1) / threads;
+  if (blocks > 4096) blocks = 4096;
+  tile_classes_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+      m, seqlen, q_start, prefix_len, window, bm, bn, nq, nk, out);
+  return launch_status();
+}
+
+extern "C" ps_status_t ps_prefill_workspace_size(int32_t batch, int32_t seqlen, int32_t n_q_heads,
+                                                 int32_t n_kv_heads, int32_t head_dim,
+                                                 int32_t ring_rows_max, size_t* bytes) {
+  if (!bytes || batch < 1 || seqlen < 1 || n_q_heads < 1 || n_kv_heads < 1 || ring_rows_max < 0 ||
+      n_q_heads % n_kv_heads)
+    return PS_ERR_INVALID_ARGUMENT;
+  if (head_dim != 128) return PS_ERR_UNSUPPORTED;
+  *bytes = prefill_layout(batch, seqlen, n_q_heads, n_kv_heads, head_dim, ring_rows_max).total;
+  return PS_OK;
+}
+
+extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, int32_t batch,
+                                  int32_t seqlen, const int32_t* q_start,
+                                  const int32_t* prefix_len, int32_t window, int32_t n_q_heads,
+                                  int32_t n_kv_heads, int32_t head_dim, float scale,
+                                  double rope_theta, const ps_cache_desc* ring,
+                                  const int32_t* ring_seq, void* out, float* lse, void* workspace,
+                                  size_t workspace_bytes, int32_t* status, void* stream) {
+  if (!q || !k || !v || !q_start || !prefix_len || !out || !lse) return PS_ERR_INVALID_ARGUMENT;
+  if (batch < 1 || seqlen < 1 || window < 1 || n_q_heads < 1 || n_kv_heads < 1 ||
+      n_q_heads % n_kv_heads || !(scale > 0.f) || !(rope_theta > 0.0))
+    return PS_ERR_INVALID_ARGUMENT;
+  if (head_dim != kHD) return PS_ERR_UNSUPPORTED;
+  if (batch > 65535 || n_q_heads > 65535) return PS_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return PS_ERR_ALIGNMENT;
+  int ring_rows = 0;
+  if (ring) {
+    ps_status_t st = check_cache(ring);
+    if (st != PS_OK) return st;
+    if (ring->head_dim != head_dim || ring->n_kv_heads != n_kv_heads || ring->window != window)
+      return PS_ERR_INVALID_ARGUMENT;
+    ring_rows = ring->prefix_max + ring->window;
+  }
+  const PrefillLayout L = prefill_layout(batch, seqlen, n_q_heads, n_kv_heads, head_dim, ring_rows);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PS_ERR_WORKSPACE;
+  if (workspace_bytes < L.total) return PS_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = (cudaStream_t)stream;
+
+  GatherParams g;
+  g.q = static_cast<const uint4*>(q);
+  g.k = static_cast<const uint4*>(k);
+  g.v = static_cast<const uint4*>(v);
+  g.qh = reinterpret_cast<uint4*>(ws + L.q_off);
+  g.kh = reinterpret_cast<uint4*>(ws + L.k_off);
+  g.vg = ring ? reinterpret_cast<uint4*>(ws + L.v_off) : nullptr;
+  g.q_start = q_start;
+  g.prefix_len = prefix_len;
+  g.status = status;
+  g.k_pool = ring ? static_cast<const uint4*>(ring->k_pool) : nullptr;
+  g.v_pool = ring ? static_cast<const uint4*>(ring->v_pool) : nullptr;
+  g.slot_base = ring ? ring->slot_base : nullptr;
+  g.ring_prefix = ring ? ring->prefix_len : nullptr;
+  g.ring_seq = ring_seq;
+  g.total_slots = ring ? ring->total_slots : 0;
+  g.nseq = ring ? ring->nseq : 0;
+  g.capacity = ring ? ring->capacity : 0;
+  g.B = batch;
+  g.S = seqlen;
+  g.Skv = L.skv;
+  g.hq = n_q_heads;
+  g.hkv = n_kv_heads;
+  g.W = window;
+  make_rope_turns(rope_theta, head_dim, &g.turns);
+  {
+    const int64_t items = ((int64_t)batch * seqlen * n_q_heads + (int64_t)batch * L.skv * n_kv_heads) * 8;
+    int64_t blocks = (items + 255) / 256;
+    const int sms = device_sm_count();
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;
+    if (blocks > cap) blocks = cap;
+    rope_gather_kernel<<<(unsigned)blocks, 256, 0, s>>>(g);
+    if (cudaGetLastError() != cudaSuccess) return PS_ERR_CUDA;
+  }
+
+  PrefillParams p;
+  const uint64_t qd[4] = {(uint64_t)head_dim, (uint64_t)n_q_heads, (uint64_t)seqlen, (uint64_t)batch};
+  const uint64_t qs[3] = {(uint64_t)head_dim * 2, (uint64_t)n_q_heads * head_dim * 2,
+                          (uint64_t)seqlen * n_q_heads * head_dim * 2};
+  const uint64_t kd[4] = {(uint64_t)head_dim, (uint64_t)n_kv_heads, (uint64_t)L.skv, (uint64_t)batch};
+  const uint64_t ks[3] = {(uint64_t)head_dim * 2, (uint64_t)n_kv_heads * head_dim * 2,
+                          (uint64_t)L.skv * n_kv_heads * head_dim * 2};
+  const uint64_t vd[4] = {(uint64_t)head_dim, (uint64_t)n_kv_heads, (uint64_t)seqlen, (uint64_t)batch};
+  const uint64_t vs[3] = {(uint64_t)head_dim * 2, (uint64_t)n_kv_heads * head_dim * 2,
+                          (uint64_t)seqlen * n_kv_heads * head_dim * 2};
+  const uint32_t box[4] = {64u, 1u, (uint32_t)kBM, 1u};
+  bool okm = encode_tmap(&p.tmq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ws + L.q_off, qd, qs, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B) &&
+             encode_tmap(&p.tmk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ws + L.k_off, kd, ks, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+  if (ring)
+    okm = okm && encode_tmap(&p.tmv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ws + L.v_off, kd, ks, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    okm = okm && encode_tmap(&p.tmv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, vd, vs, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!okm) return PS_ERR_CUDA;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.q_start = q_start;
+  p.prefix_len = prefix_len;
+  p.status = status;
+  p.S = seqlen;
+  p.hq = n_q_heads;
+  p.hkv = n_kv_heads;
+  p.W = window;
+  p.with_ring = ring ? 1 : 0;
+  p.nq = (seqlen + kBM - 1) / kBM;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemPrefill) != cudaSuccess)
+      return PS_ERR_CUDA;
+    attr_set = true;
+  }
+  dim3 grid((unsigned)p.nq, (unsigned)n_q_heads, (unsigned)batch);
+  prefill_kernel<<<grid, 128, kSmemPrefill, s>>>(p);
+  return launch_status();
+}

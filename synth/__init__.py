@@ -69,6 +69,11 @@ def normal_bf16(seed: int, stream: int, seq, pos, heads: int, dim: int) -> np.nd
         raise ValueError("pos out of range [0, 2**20)")
     if not (0 < heads <= 64 and 0 < dim <= 256):
         raise ValueError("heads/dim out of range")
+    rows_per_chunk = max(1, (1 << 22) // (heads * dim))
+    if seq.size > rows_per_chunk:  # bound the temporaries of large requests
+        return np.concatenate([normal_bf16(seed, stream, seq[i:i + rows_per_chunk],
+                                           pos[i:i + rows_per_chunk], heads, dim)
+                               for i in range(0, seq.size, rows_per_chunk)])
     key = _splitmix64(np.uint64(seed * 256 + stream))
     row = (seq.astype(np.uint64) << np.uint64(20)) + pos.astype(np.uint64)
     h = np.arange(heads, dtype=np.uint64)

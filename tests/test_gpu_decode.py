@@ -1,0 +1,155 @@
+"""ps_kv_append + ps_decode against the float64 oracle, which attends from the
+full, never-evicted history (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import attend
+
+from _util import (append_runs, assert_attention_close, bf16_tensor_to_f64, bits_to_bf16_tensor,
+                   live_runs, random_source, synth_source)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ps():
+    import prefix_sliding_window_02_b300 as ps
+    return ps
+
+
+def _oracle_rows(seed, seqs, pos, P, W, hq, hkv, D, theta, qscale_log2=0):
+    out = {}
+    for s in seqs:
+        q = synth.bits_to_f64(synth.query_bits(seed, s, pos[s], hq, D, qscale_log2))[0]
+        out[s] = attend(q, int(pos[s]), int(P[s]), W, synth.History(seed, s, hkv, D).rows, theta)
+    return out
+
+
+def _queries(seed, nseq, pos, hq, D, qscale_log2=0):
+    bits = np.concatenate([synth.query_bits(seed, s, pos[s], hq, D, qscale_log2) for s in range(nseq)])
+    return bits_to_bf16_tensor(bits)
+
+
+def _step_decode(ps, cache, seed, p, hq, hkv, D):
+    """Decode step of one sequence: append token p, then attend with q at p."""
+    k, v = synth.History(seed, 0, hkv, D).rows_bits([p])
+    pos = torch.tensor([p], dtype=torch.int32, device="cuda")
+    cache.append_tokens(pos, bits_to_bf16_tensor(k), bits_to_bf16_tensor(v))
+    q = bits_to_bf16_tensor(synth.query_bits(seed, 0, p, hq, D))
+    return cache.decode(q, pos)
+
+
+def test_tiny_decode_240_steps_with_evictions(ps):
+    """Batch 1, 2 query heads / 1 KV head, D=64, P=16, W=32; the 16-token
+    prefix goes in as one chunk, then 240 decode steps (positions 16..255,
+    208 evictions), each checked against the full-history oracle."""
+    seed, hq, hkv, D, P, W, theta = 1, 2, 1, 64, 16, 32, 10000.0
+    cache = ps.RingCache(1, hkv, D, W, [P], rope_theta=theta)
+    append_runs(cache, {0: [(0, P)]}, synth_source(seed, hkv, D))
+    hist = synth.History(seed, 0, hkv, D)
+    for p in range(P, 256):
+        o, lse = _step_decode(ps, cache, seed, p, hq, hkv, D)
+        q = synth.bits_to_f64(synth.query_bits(seed, 0, p, hq, D))[0]
+        o_ref, lse_ref = attend(q, p, P, W, hist.rows, theta)
+        assert_attention_close(bf16_tensor_to_f64(o[0]), lse[0].cpu().numpy(), o_ref, lse_ref, f"p={p}")
+    assert cache.check_status() == 0
+
+
+def test_decode_soak_4352_steps(ps):
+    """Same shape for 4,352 steps (4,320 evictions); every step checked."""
+    seed, hq, hkv, D, P, W, theta = 2, 2, 1, 64, 16, 32, 10000.0
+    cache = ps.RingCache(1, hkv, D, W, [P], rope_theta=theta)
+    hist = synth.History(seed, 0, hkv, D)
+    for p in range(0, 4352):
+        o, lse = _step_decode(ps, cache, seed, p, hq, hkv, D)
+        q = synth.bits_to_f64(synth.query_bits(seed, 0, p, hq, D))[0]
+        o_ref, lse_ref = attend(q, p, P, W, hist.rows, theta)
+        assert_attention_close(bf16_tensor_to_f64(o[0]), lse[0].cpu().numpy(), o_ref, lse_ref, f"p={p}")
+    assert cache.check_status() == 0
+
+
+CASES = [
+    # nseq, Hq, Hkv, D, P per seq, W, pos per seq, q scale (log2)
+    (3, 16, 8, 128, [100, 0, 7], 64, [50, 1000, 170], 0),
+    (2, 4, 4, 128, [5, 300], 16, [4, 299], 0),          # G=1; p < P; p+1 = P
+    (2, 8, 2, 64, [0, 33], 1, [0, 5000], 0),             # G=4; W=1; p = 0
+    (2, 8, 1, 128, [64, 64], 200, [263, 264], 0),        # G=8; L = P+W-? around the fill point
+    (4, 16, 8, 128, [512, 64, 300, 1], 4096, [131072, 4159, 4395, 262143], 0),
+    (2, 16, 8, 128, [100, 100], 4096, [10000, 4196], 2),  # q x 4: sharper softmax
+    (1, 2, 1, 64, [16], 32, [16], 0),
+]
+
+
+@pytest.mark.parametrize("nseq,hq,hkv,D,P,W,pos,qs", CASES)
+def test_decode_shapes_and_edges(ps, nseq, hq, hkv, D, P, W, pos, qs):
+    seed, theta = 7, 10000.0
+    cache = ps.RingCache(nseq, hkv, D, W, P, rope_theta=theta)
+    runs = {s: live_runs(pos[s], P[s], W) for s in range(nseq)}
+    append_runs(cache, runs, synth_source(seed, hkv, D))
+    q = _queries(seed, nseq, pos, hq, D, qs)
+    o, lse = cache.decode(q, torch.tensor(pos, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert cache.check_status() == 0
+    ref = _oracle_rows(seed, range(nseq), pos, P, W, hq, hkv, D, theta, qs)
+    for s in range(nseq):
+        assert_attention_close(bf16_tensor_to_f64(o[s]), lse[s].cpu().numpy(), *ref[s], f"seq {s}")
+
+
+def _full_size_case(ps, seed, nseq, pos, P, W, sampled):
+    hq, hkv, D, theta = 16, 8, 128, 10000.0
+    cache = ps.RingCache(nseq, hkv, D, W, P, rope_theta=theta, prefix_max=512)
+    syn = synth_source(seed, hkv, D)
+    rnd = random_source(seed + 1000, hkv, D)
+    runs = {s: live_runs(int(pos[s]), int(P[s]), W) for s in range(nseq)}
+    append_runs(cache, {s: r for s, r in runs.items() if s in sampled}, syn)
+    append_runs(cache, {s: r for s, r in runs.items() if s not in sampled}, rnd)
+    qbits = np.concatenate([synth.query_bits(seed, s, int(pos[s]), hq, D) for s in range(nseq)])
+    q = bits_to_bf16_tensor(qbits)
+    o, lse = cache.decode(q, torch.tensor(pos, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert cache.check_status() == 0
+    ref = _oracle_rows(seed, sampled, pos, P, W, hq, hkv, D, theta)
+    for s in sampled:
+        assert_attention_close(bf16_tensor_to_f64(o[s]), lse[s].cpu().numpy(), *ref[s], f"seq {s}")
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    return cache
+
+
+def test_steady_decode_full_size_sampled(ps):
+    """64 sequences at position 131,072, P uniform in 64..512, W = 4,096,
+    16/8 heads, D = 128, in the launch configuration the benchmark times;
+    4 sequences checked against the oracle."""
+    seed, nseq, W = 3, 64, 4096
+    P = synth.uniform_int(seed, 10, nseq, 64, 512)
+    pos = np.full(nseq, 131072)
+    _full_size_case(ps, seed, nseq, pos, P, W, sampled=[0, 17, 42, 63])
+
+
+def test_ragged_decode_full_size_sampled(ps):
+    """256 sequences, positions uniform in [1024, 262144], P in 64..512,
+    W = 8,192; the sample includes sequences still in the causal regime."""
+    seed, nseq, W = 4, 256, 8192
+    P = synth.uniform_int(seed, 10, nseq, 64, 512)
+    pos = synth.uniform_int(seed, 11, nseq, 1024, 262143)
+    causal = [int(s) for s in np.nonzero(pos + 1 < P + W)[0]][:3]
+    sampled = sorted(set(causal + [0, 100, 255]))
+    assert causal, "the recipe should put a few sequences below P + W"
+    _full_size_case(ps, seed, nseq, pos, P, W, sampled)
+
+
+def test_decode_flags_bad_prefix_and_keeps_others(ps):
+    seed, hq, hkv, D, W = 8, 4, 2, 128, 16
+    P = [3, 3]
+    cache = ps.RingCache(2, hkv, D, W, P, rope_theta=1e4)
+    pos = [40, 41]
+    append_runs(cache, {s: live_runs(pos[s], P[s], W) for s in range(2)}, synth_source(seed, hkv, D))
+    cache.prefix_len[1] = 99  # above prefix_max: the kernel must refuse sequence 1
+    q = _queries(seed, 2, pos, hq, D)
+    o, lse = cache.decode(q, torch.tensor(pos, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert cache.check_status() & ps.PS_DEV_BAD_PREFIX
+    assert torch.all(o[1].float() == 0) and torch.all(torch.isinf(lse[1]))
+    ref = _oracle_rows(seed, [0], pos, P, W, hq, hkv, D, 1e4)
+    assert_attention_close(bf16_tensor_to_f64(o[0]), lse[0].cpu().numpy(), *ref[0], "seq 0")

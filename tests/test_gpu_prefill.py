@@ -1,0 +1,165 @@
+"""ps_prefill (RoPE pre-pass + tcgen05 tile kernel) and its tile classes
+against the oracle (GPU)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import (FULL, PARTIAL, SKIP, attend, masked_attention, rope, round_bf16, tile_classes,
+                    visible_positions)
+
+from _util import (append_runs, assert_attention_close, bf16_tensor_to_f64, bits_to_bf16_tensor,
+                   synth_source)
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def ps():
+    import prefix_sliding_window_02_b300 as ps
+    return ps
+
+
+# ------------------------------------------------------------ tile classes --
+def _ring_key_positions(S, q0, P, W):
+    n_pre = min(P, q0)
+    wlo = max(P, q0 - W)
+    return np.array(list(range(n_pre)) + list(range(wlo, q0)) + list(range(q0, q0 + S)))
+
+
+@pytest.mark.parametrize("S,q0,P,W,ring,bm,bn", [
+    (1000, 0, 37, 300, False, 128, 128), (70, 0, 9, 13, False, 16, 8), (97, 0, 30, 5, False, 8, 32),
+    (64, 0, 64, 1, False, 16, 16), (300, 700, 20, 64, False, 32, 32), (150, 300, 20, 64, True, 16, 16),
+    (150, 50, 20, 64, True, 16, 16), (40, 10, 20, 64, True, 8, 8), (1, 5000, 100, 4096, True, 128, 128),
+    (513, 9000, 100, 4096, True, 128, 128), (77, 0, 0, 3, False, 7, 5)])
+def test_tile_classes_bit_exact(ps, S, q0, P, W, ring, bm, bn):
+    got = ps.prefill_tile_classes(S, q0, P, W, ring, bm, bn).cpu().numpy()
+    kpos = _ring_key_positions(S, q0, P, W) if ring else np.arange(q0, q0 + S)
+    want = tile_classes(np.arange(q0, q0 + S), kpos, P, W, bm, bn)
+    assert np.array_equal(got, want)
+
+
+def test_tile_classes_full_size_counts(ps):
+    g = json.load(open(os.path.join(GOLDEN, "tile_counts.json")))
+    for case in g["cases"]:
+        got = ps.prefill_tile_classes(case["S"], 0, case["P"], case["W"], False, case["BM"],
+                                      case["BN"]).cpu().numpy()
+        assert [int((got == k).sum()) for k in (SKIP, PARTIAL, FULL)] == case["skip_partial_full"]
+    # and element for element at the prefill workload's size
+    pos = np.arange(32768)
+    want = tile_classes(pos, pos, 100, 4096, 128, 128)
+    assert np.array_equal(ps.prefill_tile_classes(32768, 0, 100, 4096).cpu().numpy(), want)
+
+
+# ------------------------------------------------------------------ prefill --
+def _inputs(seed, B, S, q_start, hq, hkv, D, qscale=0):
+    q = np.stack([synth.query_bits(seed, b, np.arange(q_start[b], q_start[b] + S), hq, D, qscale)
+                  for b in range(B)])
+    kv = [synth.History(seed, b, hkv, D).rows_bits(np.arange(q_start[b], q_start[b] + S))
+          for b in range(B)]
+    k = np.stack([x[0] for x in kv])
+    v = np.stack([x[1] for x in kv])
+    return q, k, v
+
+
+def _run(ps, q, k, v, q_start, P, W, theta, ring=None):
+    i32 = dict(dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, **i32)
+    out, lse = ps.prefill(bits_to_bf16_tensor(q), bits_to_bf16_tensor(k), bits_to_bf16_tensor(v),
+                          torch.tensor(q_start, **i32), torch.tensor(P, **i32), W,
+                          rope_theta=theta, ring=ring, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out, lse
+
+
+def _check_rows(seed, out, lse, q, q_start, P, W, theta, rows_per_b, hkv, what=""):
+    B = out.shape[0]
+    D = out.shape[3]
+    for b in range(B):
+        hist = synth.History(seed, b, hkv, D)
+        ob = out[b]
+        for r in rows_per_b[b]:
+            p = q_start[b] + r
+            o_ref, l_ref = attend(synth.bits_to_f64(q[b, r]), p, P[b], W, hist.rows, theta)
+            assert_attention_close(bf16_tensor_to_f64(ob[r]), lse[b, :, r].cpu().numpy(), o_ref,
+                                   l_ref, f"{what} b={b} row={r}")
+
+
+@pytest.mark.parametrize("B,S,hq,hkv,P,W,qs", [
+    (2, 300, 4, 2, [37, 0], 100, 0),     # ragged tail (300 = 2*128 + 44), prefix and band
+    (1, 257, 2, 1, [5], 1000, 0),        # W >= S: plain causal
+    (1, 384, 2, 2, [0], 128, 0),         # P = 0: vanilla sliding window, tile-aligned W
+    (1, 200, 8, 1, [300], 16, 0),        # P >= S: causal through the prefix
+    (1, 260, 4, 2, [4], 1, 0),           # W = 1, StreamingLLM-like sink of 4
+    (2, 200, 4, 2, [17, 130], 70, 2),    # q x 4: sharper softmax, stale-max rescaling
+])
+def test_prefill_all_rows(ps, B, S, hq, hkv, P, W, qs):
+    seed, D, theta = 31, 128, 10000.0
+    q_start = [0] * B
+    q, k, v = _inputs(seed, B, S, q_start, hq, hkv, D, qs)
+    out, lse = _run(ps, q, k, v, q_start, P, W, theta)
+    _check_rows(seed, out, lse, q, q_start, P, W, theta, [range(S)] * B, hkv)
+
+
+def test_prefill_chunk_without_ring_sees_only_the_chunk(ps):
+    """q_start > 0 and no ring: keys are the chunk's own tokens (positions
+    q_start..q_start+S-1); the mask is still the absolute-position rule."""
+    seed, B, S, hq, hkv, D, P, W, theta = 32, 1, 200, 4, 2, 128, 16, 64, 10000.0
+    c0 = 1000
+    q, k, v = _inputs(seed, B, S, [c0], hq, hkv, D)
+    out, lse = _run(ps, q, k, v, [c0], [P], W, theta)
+    hist = synth.History(seed, 0, hkv, D)
+    for r in range(S):
+        p = c0 + r
+        js = visible_positions(p, P, W)
+        js = js[js >= c0]
+        kr, vv = hist.rows(js)
+        qh = round_bf16(rope(synth.bits_to_f64(q[0, r]), p, theta))
+        kh = round_bf16(rope(kr, js, theta))
+        o_ref, l_ref = masked_attention(qh, kh, vv, 1 / math.sqrt(D))
+        assert_attention_close(bf16_tensor_to_f64(out[0, r]), lse[0, :, r].cpu().numpy(), o_ref, l_ref,
+                               f"row {r}")
+
+
+@pytest.mark.parametrize("c0,S", [(300, 150), (50, 150), (10, 40), (5000, 1), (84, 64), (20, 300)])
+def test_prefill_extend_from_ring(ps, c0, S):
+    """Chunked extend: the cache holds positions < c0 (after eviction); the
+    chunk [c0, c0+S) attends to the ring's live keys plus itself."""
+    seed, B, hq, hkv, D, P, W, theta = 33, 2, 4, 2, 128, 20, 64, 10000.0
+    cache = ps.RingCache(B, hkv, D, W, [P] * B, rope_theta=theta)
+    append_runs(cache, {b: [(0, c0)] for b in range(B)}, synth_source(seed, hkv, D))
+    q, k, v = _inputs(seed, B, S, [c0] * B, hq, hkv, D)
+    out, lse = _run(ps, q, k, v, [c0] * B, [P] * B, W, theta, ring=cache)
+    _check_rows(seed, out, lse, q, [c0] * B, [P] * B, W, theta, [range(S)] * B, hkv, "extend")
+    assert cache.check_status() == 0
+
+
+def test_prefill_32k_sampled_rows(ps):
+    """One Qwen3-1.7B-shaped layer: 32,768 tokens, P = 100, W = 4,096, 16/8
+    heads; rows at every boundary of the mask plus random ones."""
+    seed, B, S, hq, hkv, D, P, W, theta = 2, 1, 32768, 16, 8, 128, 100, 4096, 10000.0
+    q, k, v = _inputs(seed, B, S, [0], hq, hkv, D)
+    out, lse = _run(ps, q, k, v, [0], [P], W, theta)
+    rng = np.random.default_rng(0)
+    rows = sorted(set([0, 1, 99, 100, 127, 128, 4095, 4096, 4196, 4197, 8191, 32767]
+                      + list(rng.integers(0, S, 12))))
+    _check_rows(seed, out, lse, q, [0], [P], W, theta, [rows], hkv, "32k")
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+def test_training_forward_sampled_rows(ps):
+    """Truncated-backprop forward: 8 x 8,192 tokens, P = 256, W = 2,048."""
+    seed, B, S, hq, hkv, D, P, W, theta = 5, 8, 8192, 16, 8, 128, 256, 2048, 10000.0
+    q, k, v = _inputs(seed, B, S, [0] * B, hq, hkv, D)
+    out, lse = _run(ps, q, k, v, [0] * B, [P] * B, W, theta)
+    rng = np.random.default_rng(1)
+    rows = [sorted(set([0, 255, 256, 2047, 2048, 2303, 8191] + list(rng.integers(0, S, 4))))
+            for _ in range(B)]
+    _check_rows(seed, out, lse, q, [0] * B, [P] * B, W, theta, rows, hkv, "train")
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()

@@ -1,0 +1,97 @@
+"""C-ABI library checks that need no GPU: it loads, it exports every symbol
+include/ps.h declares, and host-side validation rejects bad arguments before
+any CUDA call."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_symbols():
+    text = open(os.path.join(ROOT, "include", "ps.h")).read()
+    return sorted(set(re.findall(r"\b(ps_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def ps():
+    import prefix_sliding_window_02_b300 as ps
+    return ps
+
+
+def test_library_exports_every_declared_symbol(ps):
+    syms = _header_symbols()
+    assert "ps_decode" in syms and "ps_kv_append" in syms and "ps_prefill" in syms
+    raw = ctypes.CDLL(ps._lib.LIB_PATH)
+    for s in syms:
+        assert hasattr(raw, s), s
+    assert set(syms) <= set(ps._lib.EXPORTS) | set()
+
+
+def test_library_is_built_for_sm_103a(ps):
+    # the fatbin section names the target architecture (text scan of the ELF)
+    blob = open(ps._lib.LIB_PATH, "rb").read()
+    assert b"sm_103a" in blob
+
+
+def test_status_strings(ps):
+    for code, name in enumerate(["PS_OK", "PS_ERR_INVALID_ARGUMENT", "PS_ERR_UNSUPPORTED",
+                                 "PS_ERR_ALIGNMENT", "PS_ERR_WORKSPACE", "PS_ERR_CUDA",
+                                 "PS_ERR_DEVICE"]):
+        assert ps.lib.ps_status_string(code).decode() == name
+
+
+def test_host_validation_rejects_before_launch(ps):
+    lib = ps.lib
+    nq, nk = ctypes.c_int32(), ctypes.c_int32()
+    assert lib.ps_prefill_tile_grid(0, 0, 1, 1, 0, 128, 128, ctypes.byref(nq), ctypes.byref(nk)) == 1
+    assert lib.ps_prefill_tile_grid(10, 0, -1, 1, 0, 128, 128, ctypes.byref(nq), ctypes.byref(nk)) == 1
+    assert lib.ps_prefill_tile_grid(10, 0, 1, 0, 0, 128, 128, ctypes.byref(nq), ctypes.byref(nk)) == 1
+    assert lib.ps_ring_slots(None, None, 0, None, 5, None) == 1           # W < 1
+    assert lib.ps_ring_slots(None, None, 4, None, 0, None) == 0           # nothing to do
+    assert lib.ps_kv_append(None, None, None, None, 0, None, None, 1, None) == 1
+    b = ctypes.c_size_t()
+    assert lib.ps_decode_workspace_size(4, 3, 2, 128, ctypes.byref(b)) == 1   # Hq % Hkv
+    assert lib.ps_decode_workspace_size(4, 32, 2, 128, ctypes.byref(b)) == 2  # group 16
+    assert lib.ps_decode_workspace_size(4, 16, 8, 96, ctypes.byref(b)) == 2   # head_dim
+    assert lib.ps_decode_workspace_size(0, 16, 8, 128, ctypes.byref(b)) == 1
+    desc = ps.CacheDesc()
+    assert lib.ps_decode(ctypes.byref(desc), None, None, 16, ctypes.c_float(0.1), None, None,
+                         None, 0, None) == 1
+    flags = ctypes.c_int32()
+    assert lib.ps_check_device_status(None, ctypes.byref(flags)) == 1
+
+
+def _bad_desc(ps, **kw):
+    d = dict(k_pool=4096, v_pool=8192, slot_base=256, prefix_len=512, status=0, total_slots=100,
+             nseq=1, n_kv_heads=1, head_dim=128, window=4, capacity=10, prefix_max=6,
+             rope_theta=1e4)
+    d.update(kw)
+    return ps.CacheDesc(**d)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(window=0), 1), (dict(capacity=9), 1), (dict(head_dim=96), 2), (dict(k_pool=4100), 3),
+    (dict(rope_theta=0.0), 1), (dict(nseq=0), 1), (dict(total_slots=2**31), 1)])
+def test_cache_descriptor_validation(ps, kw, code):
+    d = _bad_desc(ps, **kw)
+    r = ps.lib.ps_kv_append(ctypes.byref(d), 16, 16, 16, 1, 4096, 4096, 1, None)
+    assert r == code
+
+
+def test_tile_grid_matches_oracle_shapes(ps):
+    from oracle import tile_classes
+    for S, q0, P, W, ring, bm, bn in [(1000, 0, 37, 300, 0, 128, 128), (70, 5, 9, 13, 0, 16, 8),
+                                      (50, 600, 40, 100, 1, 16, 16), (50, 30, 40, 100, 1, 8, 8)]:
+        nq, nk = ps.prefill_tile_grid(S, q0, P, W, bool(ring), bm, bn)
+        if ring:
+            n_pre = min(P, q0)
+            wlo = max(P, q0 - W)
+            kpos = list(range(n_pre)) + list(range(wlo, q0)) + list(range(q0, q0 + S))
+        else:
+            kpos = list(range(q0, q0 + S))
+        c = tile_classes(np.arange(q0, q0 + S), np.array(kpos), P, W, bm, bn)
+        assert (nq, nk) == c.shape
