@@ -112,17 +112,23 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1400.0, "fallback"
 
 
-def committed_traffic(name: str, source: str):
-    """ncu DRAM bytes per launch recorded under profiles/, if the kernel source
-    still matches the one the counters were taken on; else None."""
-    path = os.path.join(ROOT, "profiles", f"{name}.traffic.json")
+def committed_traffic(profile: str, source: str):
+    """ncu DRAM bytes per launch recorded in a profiles/ summary ("traffic_record:"
+    line), if the kernel source still matches the one the counters were taken
+    on; else None."""
+    path = os.path.join(ROOT, "profiles", profile)
     if not os.path.exists(path):
         return None
-    d = json.load(open(path))
-    sha = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()
-    if d.get("source_sha256") != sha:
+    rec = {}
+    for line in open(path):
+        if line.startswith("traffic_record:"):
+            rec = dict(kv.split("=", 1) for kv in line.split(":", 1)[1].split())
+    if not rec or rec.get("source") != source:
         return None
-    return d.get("dram_bytes_per_launch")
+    sha = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()
+    if rec.get("source_sha256") != sha:
+        return None
+    return float(rec["dram_bytes_per_launch"])
 
 
 def fill_random(cache, runs_per_seq, gen, torch, chunk_tokens=1 << 21):
@@ -355,6 +361,7 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-baselines", action="store_true", help="skip full-causal and oracle legs")
     ap.add_argument("--prefill-steps", type=int, default=20)
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill leg")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -410,6 +417,8 @@ def main():
 
     # prefill (one layer)
     try:
+        if args.no_prefill:
+            raise RuntimeError("prefill leg skipped (--no-prefill)")
         pms, cls = run_prefill(ps, torch, PRE["S"], PRE["P"], PRE["W"], args.prefill_steps, 3, seed + 5)
         flops = prefill_flops(PRE["S"], PRE["P"], PRE["W"], PRE["hq"], PRE["D"])
         tile_flops = 4.0 * PRE["D"] * PRE["hq"] * 128 * 128 * (cls["partial"] + cls["full"])
@@ -432,7 +441,7 @@ def main():
                 "how": "same library, W > position (no eviction), P = 0"}
         del cfc, qf, kf, vf
         torch.cuda.empty_cache()
-        if "ms" in pre:
+        if pre and "ms" in pre:
             try:
                 fpms, _ = run_prefill(ps, torch, PRE["S"], 0, PRE["W"], 5, 2, seed + 9, full_causal=True)
                 full["prefill_ms"] = fpms
@@ -464,7 +473,7 @@ def main():
         "roofline": {"kernel": "decode_partial_kernel<128,2,4,3>", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_src} hbm_gbs",
-                     "traffic": committed_traffic("decode_partial_steady",
+                     "traffic": committed_traffic("decode_partial_steady_64x131072.md",
                                                   "prefix_sliding_window_02_b300/csrc/ps_decode.cu"),
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "frac_of_8tbs": achieved / 8000.0},

@@ -5,7 +5,9 @@
 //     positions (Continue PE) into the workspace; with a ring it first copies
 //     the ring's live keys and values (already rotated when appended) in
 //     position order, so the key array is [cached prefix][cached window][chunk].
-//  2. prefill_kernel: one CTA per (128-query tile, query head, batch row).  It
+//  2. the tile kernel: prefill_pair_kernel (warp-specialised, two query heads
+//     of one KV head per CTA) when the GQA group size is even, else
+//     prefill_kernel: one CTA per (128-query tile, query head, batch row).  It
 //     visits only the key tiles that can hold an admitted pair -- the prefix
 //     tiles and the band of tiles around the diagonal -- and classifies each:
 //     FULL tiles run unmasked, PARTIAL tiles get the element mask ("Prefix
@@ -296,6 +298,9 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
       tc::commit(smem_u32(s_done));  // arrives at once if nothing was issued
     }
     if (!mbar_wait(s_done, it & 1)) ok = false;
+    // tcgen05.ld / st are warp-collective (.sync.aligned): reconverge after the
+    // per-thread spin above before touching tensor memory
+    __syncwarp();
     tc::fence_after();
 
     // ---- scores of this thread's query row
@@ -341,7 +346,8 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
         ++issued;
       }
     }
-    if (rescale) {
+    __syncwarp();
+    if (__any_sync(0xffffffffu, rescale)) {  // warp-uniform: alpha is 1 on the other rows
 #pragma unroll
       for (int c = 0; c < kHD / 32; ++c) {
         uint32_t r[32];
@@ -399,6 +405,7 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
     if (!mbar_wait(o_done, (n_tiles - 1) & 1)) ok = false;
     tc::fence_after();
   }
+  ok = __all_sync(0xffffffffu, ok);
   if (ok && n_tiles > 0) {
     const float inv = 1.f / l;
     const int32_t qrow = q0r + row;
@@ -432,6 +439,384 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
   tc::fence_before();
   __syncthreads();
   if (warp == 0) tc::dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------
+// 3. warp-specialised tile kernel for a pair of query heads that share one KV
+//    head (the GQA group size is even).
+//
+// One CTA = one 128-row query tile of two query heads.  Both heads admit the
+// same (query, key) pairs, so they walk the same key tiles and every K/V tile
+// staged in shared memory feeds two 128x128 products.  Roles:
+//   warps 0-3  softmax, rescale and epilogue of head 0 (one thread per row)
+//   warps 4-7  the same for head 1
+//   warp 8     TMA producer (Q once, then K / V tiles through two rings)
+//   warp 9     tcgen05 issuer
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each.  Each softmax
+// thread writes its row of probabilities as bf16 over the first 64 columns of
+// its S, and P V reads them from there (tensor-memory A operand), so P never
+// touches shared memory.  The issuer interleaves the heads: P_0 V, S_0 = Q_0 K,
+// P_1 V, S_1 = Q_1 K, so one head's softmax overlaps the other head's MMAs.
+// Tensor-core instructions of one thread run in issue order, which is what
+// lets S_i(j+1) overwrite the columns P_i(j) V has just read.
+// ---------------------------------------------------------------------------
+namespace ws {
+
+constexpr int kThreads = 320;
+constexpr int kStK = 2, kStV = 2;
+constexpr int kSmem = (2 + kStK + kStV) * kTile + 1024 /*barriers*/ + 1024 /*alignment*/;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[kStK], k_empty[kStK];
+  uint64_t v_full[kStV], v_empty[kStV];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint32_t tmem_slot;
+  int32_t abort;
+};
+
+// Bounded wait that also gives up as soon as another role has given up.
+__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+}  // namespace ws
+
+// 2^x on the FMA pipe, for x <= 0, to take part of the exponentials off the
+// MUFU unit.  Cody-Waite style split x = n + f with n = round(x) (the 1.5 * 2^23
+// addition rounds to an integer), f in [-1/2, 1/2]; 2^f by a cubic fitted here
+// for least relative error on that interval (max relative error 7.5e-5, far
+// below the bf16 rounding P gets next); 2^n added into the exponent field.
+// Inputs below -126 are clamped there, so masked (-inf) scores give about
+// 1e-38 rather than 0, which no sum or bf16 product can notice.
+__device__ __forceinline__ float exp2_fma(float x) {
+  x = fmaxf(x, -126.f);
+  const float t = x + 12582912.f;  // 1.5 * 2^23
+  const float f = x - (t - 12582912.f);
+  float q = fmaf(0.05517168715596199f, f, 0.2426111400127411f);
+  q = fmaf(q, f, 0.6932609677314758f);
+  q = fmaf(q, f, 0.9999280571937561f);
+  return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
+}
+
+// Columns whose exponential goes through exp2_fma instead of ex2.approx: every
+// kPolyEvery-th pair of columns (0 = none).
+constexpr int kPolyEvery = 0;
+
+// c is a constant after unrolling, so the choice folds away.
+__device__ __forceinline__ float exp2_col(int c, float x) {
+  if (kPolyEvery > 0 && (c / 2) % kPolyEvery == kPolyEvery - 1) return exp2_fma(x);
+  return ex2(x);
+}
+
+// One query row's share of a 128-key tile: S from TMEM, optional element mask
+// (keep column c iff c < A1 or B0 <= c < B1), online-softmax bookkeeping with a
+// lazy rescale, and P = exp2(S * scale - m) stored back over the first 64
+// columns as bf16 pairs.  Returns the factor O must be scaled by (1 = none).
+// The masked and unmasked variants are whole functions so that the 128 scores
+// are never live across a branch.
+template <bool MASK>
+__device__ __forceinline__ float softmax_tile(uint32_t tS, int j, float scale_log2, int32_t A1,
+                                              int32_t B0, int32_t B1, float& m_used, float& l) {
+  float s[kBN];
+  {
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    tc::ld32(tS, r0);
+    tc::ld32(tS + 32, r1);
+    tc::ld32(tS + 64, r2);
+    tc::ld32(tS + 96, r3);
+    tc::wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      s[e] = __uint_as_float(r0[e]);
+      s[32 + e] = __uint_as_float(r1[e]);
+      s[64 + e] = __uint_as_float(r2[e]);
+      s[96 + e] = __uint_as_float(r3[e]);
+    }
+  }
+  if (MASK) {
+#pragma unroll
+    for (int c = 0; c < kBN; ++c) {
+      const bool keep = (c < A1) || (c >= B0 && c < B1);
+      s[c] = keep ? s[c] : -INFINITY;
+    }
+  }
+  float mx = s[0];
+#pragma unroll
+  for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+  const float m_new = fmaxf(m_used, mx * scale_log2);
+  float alpha = 1.f;
+  if (j == 0) {
+    m_used = m_new;
+  } else if (m_new > m_used + 8.f) {  // keep a stale max while within a factor 2^8
+    alpha = ex2(m_used - m_new);
+    m_used = m_new;
+  }
+  const float mu = m_used == -INFINITY ? 0.f : m_used;
+  float rs = 0.f;
+  uint32_t p0[32], p1[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const float x = exp2_col(2 * c, fmaf(s[2 * c], scale_log2, -mu));
+    const float y = exp2_col(2 * c + 1, fmaf(s[2 * c + 1], scale_log2, -mu));
+    rs += x + y;
+    p0[c] = pack_bf16(x, y);
+  }
+  tc::st32(tS, p0);
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const float x = exp2_col(64 + 2 * c, fmaf(s[64 + 2 * c], scale_log2, -mu));
+    const float y = exp2_col(64 + 2 * c + 1, fmaf(s[64 + 2 * c + 1], scale_log2, -mu));
+    rs += x + y;
+    p1[c] = pack_bf16(x, y);
+  }
+  tc::st32(tS + 32, p1);
+  l = fmaf(l, alpha, rs);
+  return alpha;
+}
+
+__global__ void __launch_bounds__(ws::kThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ PrefillParams p) {
+  using namespace ws;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint8_t* sQ = smem;                   // [2] heads
+  uint8_t* sK = smem + 2 * kTile;       // [kStK]
+  uint8_t* sV = sK + kStK * kTile;      // [kStV]
+  Bars* bar = reinterpret_cast<Bars*>(sV + kStV * kTile);
+  volatile int32_t* abort = &bar->abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qt = p.nq - 1 - (int)blockIdx.x;  // longest rows first
+  const int h0 = 2 * blockIdx.y, b = blockIdx.z;
+  const int hk = h0 / (p.hq / p.hkv);
+  const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
+  const KeyMap km = make_keymap(p.S, c0, P, p.W, p.with_ring != 0);
+  const int32_t q0r = qt * kBM, q1r = min(p.S, q0r + kBM) - 1;
+  const int64_t q0 = (int64_t)c0 + q0r, q1 = (int64_t)c0 + q1r;
+
+  // key tiles that can hold an admitted pair: the prefix tiles, then the band
+  const int32_t kc = keys_below(km, q1 + 1);
+  const int32_t kP = keys_below(km, P);
+  const int t1_end = (min(kP, kc) + kBN - 1) / kBN;
+  const int32_t kw = keys_below(km, q0 - p.W + 1);
+  const int t2_begin = max(t1_end, kw / kBN);
+  const int t2_end = (kc + kBN - 1) / kBN;
+  const int n_tiles = t1_end + max(0, t2_end - t2_begin);
+  auto tile_at = [&](int it) { return it < t1_end ? it : t2_begin + (it - t1_end); };
+
+  if (warp == 0) {
+    tc::alloc(smem_u32(&bar->tmem_slot), 512);
+    tc::relinquish();
+  }
+  if (tid == 32) {
+    mbar_init(&bar->q_full, 1);
+    for (int s = 0; s < kStK; ++s) {
+      mbar_init(&bar->k_full[s], 1);
+      mbar_init(&bar->k_empty[s], 1);
+    }
+    for (int s = 0; s < kStV; ++s) {
+      mbar_init(&bar->v_full[s], 1);
+      mbar_init(&bar->v_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar->s_full[i], 1);
+      mbar_init(&bar->p_full[i], 128);
+      mbar_init(&bar->o_done[i], 1);
+    }
+    bar->abort = 0;
+    fence_mbar_init();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = bar->tmem_slot;
+
+  if (n_tiles > 0 && warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tmq);
+      prefetch_tmap(&p.tmk);
+      prefetch_tmap(&p.tmv);
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      mbar_arrive_expect_tx(&bar->q_full, 2 * kTile);
+      for (int i = 0; i < 2; ++i) {
+        tma_load_4d(sQ + i * kTile, &p.tmq, &bar->q_full, 0, h0 + i, q0r, b, pol_q);
+        tma_load_4d(sQ + i * kTile + kHalf, &p.tmq, &bar->q_full, 64, h0 + i, q0r, b, pol_q);
+      }
+      for (int j = 0; j < n_tiles; ++j) {
+        const int kt = tile_at(j);
+        const int sk = j % kStK, sv = j % kStV;
+        if (!wait(&bar->k_empty[sk], ((j / kStK) & 1) ^ 1, abort)) break;
+        uint8_t* dk = sK + sk * kTile;
+        mbar_arrive_expect_tx(&bar->k_full[sk], kTile);
+        tma_load_4d(dk, &p.tmk, &bar->k_full[sk], 0, hk, kt * kBN, b, pol_kv);
+        tma_load_4d(dk + kHalf, &p.tmk, &bar->k_full[sk], 64, hk, kt * kBN, b, pol_kv);
+        if (!wait(&bar->v_empty[sv], ((j / kStV) & 1) ^ 1, abort)) break;
+        uint8_t* dv = sV + sv * kTile;
+        mbar_arrive_expect_tx(&bar->v_full[sv], kTile);
+        tma_load_4d(dv, &p.tmv, &bar->v_full[sv], 0, hk, kt * kBN, b, pol_kv);
+        tma_load_4d(dv + kHalf, &p.tmv, &bar->v_full[sv], 64, hk, kt * kBN, b, pol_kv);
+      }
+    }
+    __syncwarp();
+  } else if (n_tiles > 0 && warp == kMmaWarp) {
+    // -------------------------------------------------------------- issuer
+    if (lane == 0) {
+      const uint32_t aq = smem_u32(sQ);
+      auto qk = [&](int i, int sk) {
+        const uint32_t a = aq + i * kTile, k = smem_u32(sK + sk * kTile);
+#pragma unroll
+        for (int kk = 0; kk < kHD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          tc::mma_bf16(tmem + i * 128, tc::sdesc_sw128(a + off, 16, 1024),
+                       tc::sdesc_sw128(k + off, 16, 1024), kIdescQK, kk > 0);
+        }
+        tc::commit(smem_u32(&bar->s_full[i]));
+      };
+      auto pv = [&](int i, int sv, bool acc) {
+        const uint32_t av = smem_u32(sV + sv * kTile);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          tc::mma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
+                          tc::sdesc_sw128(av + kk * 2048, kHalf, 1024), kIdescPV, acc || kk > 0);
+      };
+      bool ok = wait(&bar->q_full, 0, abort);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int sk = j % kStK;
+        if (!(ok = wait(&bar->k_full[sk], (j / kStK) & 1, abort))) break;
+        tc::fence_after();
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (j > 0) {
+            const int sv = (j - 1) % kStV;
+            if (!(ok = wait(&bar->p_full[i], (j - 1) & 1, abort))) break;
+            if (i == 0 && !(ok = wait(&bar->v_full[sv], ((j - 1) / kStV) & 1, abort))) break;
+            tc::fence_after();
+            pv(i, sv, j > 1);
+            if (i == 1) tc::commit(smem_u32(&bar->v_empty[sv]));
+          }
+          qk(i, sk);
+        }
+        if (ok) tc::commit(smem_u32(&bar->k_empty[sk]));
+      }
+      if (ok) {
+        const int j = n_tiles;
+        const int sv = (j - 1) % kStV;
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (!(ok = wait(&bar->p_full[i], (j - 1) & 1, abort))) break;
+          if (i == 0 && !(ok = wait(&bar->v_full[sv], ((j - 1) / kStV) & 1, abort))) break;
+          tc::fence_after();
+          pv(i, sv, j > 1);
+          tc::commit(smem_u32(&bar->o_done[i]));
+        }
+      }
+    }
+    __syncwarp();
+  } else if (n_tiles > 0 && warp < 8) {
+    // ------------------------------------------------------------- softmax
+    const int i = warp >> 2;                 // head of the pair
+    const int row = tid & 127;               // TMEM lane = query row in the tile
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + i * 128 + lane_off, tO = tmem + 256 + i * 128 + lane_off;
+    const int64_t qpos = q0 + row;
+    // admitted key positions of this row: [0, min(P, qpos+1)) and [max(0, qpos-W+1), qpos]
+    const int32_t a1 = keys_below(km, min((int64_t)P, qpos + 1));
+    const int32_t b0 = keys_below(km, max((int64_t)0, qpos - p.W + 1));
+    const int32_t b1 = keys_below(km, qpos + 1);
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = wait(&bar->s_full[i], j & 1, abort);
+      // tcgen05.ld / st are warp-collective (.sync.aligned): the warp decides
+      // together and reconverges here after the per-thread spin
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+      const int kt = tile_at(j);
+      const int32_t ka = kt * kBN;
+      const int32_t kb = min(km.n_keys, ka + kBN) - 1;
+      const uint8_t cls = tile_class(km, c0, q0r, q1r, ka, kb, P, p.W);
+      float alpha;
+      if (cls != kFull || ka + kBN > km.n_keys)
+        alpha = softmax_tile<true>(tS, j, p.scale_log2, a1 - ka, b0 - ka, b1 - ka, m_used, l);
+      else
+        alpha = softmax_tile<false>(tS, j, p.scale_log2, 0, 0, 0, m_used, l);
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {  // alpha is 1 on the other rows
+        // O_i already holds every P V issued before S_i(j), which has completed,
+        // and P_i(j) V is not issued before this thread arrives below
+#pragma unroll 1
+        for (int c = 0; c < kHD / 32; ++c) {
+          uint32_t o[32];
+          tc::ld32(tO + c * 32, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tc::st32(tO + c * 32, o);
+        }
+      }
+      tc::wait_st();
+      tc::fence_before();
+      mbar_arrive(&bar->p_full[i]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok) ok = wait(&bar->o_done[i], 0, abort);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc::fence_after();
+      const int32_t qrow = q0r + row;
+      const float inv = 1.f / l;
+      __nv_bfloat16* orow = p.out + (((int64_t)b * p.S + qrow) * p.hq + h0 + i) * kHD;
+#pragma unroll
+      for (int c = 0; c < kHD / 32; ++c) {
+        uint32_t o[32];
+        tc::ld32(tO + c * 32, o);
+        tc::wait_ld();
+        if (qrow <= q1r) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
+          }
+        }
+      }
+      if (qrow <= q1r)
+        p.lse[((int64_t)b * p.hq + h0 + i) * p.S + qrow] =
+            (m_used + __log2f(l)) * 0.69314718055994530942f;
+    }
+  }
+
+  tc::fence_before();
+  __syncthreads();
+  if (*abort) {
+    if (tid == 0) set_flag(p.status, PS_DEV_TIMEOUT);
+    // copies and products already issued finish on their own within microseconds;
+    // give them time before the CTA's shared and tensor memory are released
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 100000ull) {
+    }
+    __syncthreads();
+  }
+  tc::fence_after();
+  if (warp == 0) tc::dealloc(tmem, 512);
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -594,14 +979,21 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
   p.with_ring = ring ? 1 : 0;
   p.nq = (seqlen + kBM - 1) / kBM;
   p.scale_log2 = scale * 1.4426950408889634f;
-  static bool attr_set = false;
-  if (!attr_set) {
+  // cudaFuncSetAttribute is cheap and per device; call it every time rather
+  // than caching a flag that would be wrong on a second device
+  const int group = n_q_heads / n_kv_heads;
+  if (group % 2 == 0) {
+    if (cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             ws::kSmem) != cudaSuccess)
+      return PS_ERR_CUDA;
+    dim3 grid((unsigned)p.nq, (unsigned)(n_q_heads / 2), (unsigned)batch);
+    prefill_pair_kernel<<<grid, ws::kThreads, ws::kSmem, s>>>(p);
+  } else {
     if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemPrefill) != cudaSuccess)
       return PS_ERR_CUDA;
-    attr_set = true;
+    dim3 grid((unsigned)p.nq, (unsigned)n_q_heads, (unsigned)batch);
+    prefill_kernel<<<grid, 128, kSmemPrefill, s>>>(p);
   }
-  dim3 grid((unsigned)p.nq, (unsigned)n_q_heads, (unsigned)batch);
-  prefill_kernel<<<grid, 128, kSmemPrefill, s>>>(p);
   return launch_status();
 }

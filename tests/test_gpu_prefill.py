@@ -127,11 +127,13 @@ def test_prefill_chunk_without_ring_sees_only_the_chunk(ps):
                                f"row {r}")
 
 
-@pytest.mark.parametrize("c0,S", [(300, 150), (50, 150), (10, 40), (5000, 1), (84, 64), (20, 300)])
-def test_prefill_extend_from_ring(ps, c0, S):
+@pytest.mark.parametrize("c0,S,hq", [(300, 150, 4), (50, 150, 4), (10, 40, 4), (5000, 1, 4),
+                                     (84, 64, 4), (20, 300, 4), (300, 150, 2), (84, 200, 2)])
+def test_prefill_extend_from_ring(ps, c0, S, hq):
     """Chunked extend: the cache holds positions < c0 (after eviction); the
-    chunk [c0, c0+S) attends to the ring's live keys plus itself."""
-    seed, B, hq, hkv, D, P, W, theta = 33, 2, 4, 2, 128, 20, 64, 10000.0
+    chunk [c0, c0+S) attends to the ring's live keys plus itself.  hq = 4
+    (GQA pairs) and hq = 2 (one query head per KV head) take the two kernels."""
+    seed, B, hkv, D, P, W, theta = 33, 2, 2, 128, 20, 64, 10000.0
     cache = ps.RingCache(B, hkv, D, W, [P] * B, rope_theta=theta)
     append_runs(cache, {b: [(0, c0)] for b in range(B)}, synth_source(seed, hkv, D))
     q, k, v = _inputs(seed, B, S, [c0] * B, hq, hkv, D)
