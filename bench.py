@@ -157,23 +157,28 @@ def fill_random(cache, runs_per_seq, gen, torch, chunk_tokens=1 << 21):
 
 # ---- decode ---------------------------------------------------------------
 def decode_setup(ps, torch, seed, W, P, pos0, n_steps, full_causal=False):
+    """Ring cache holding, per sequence, the live K/V of positions < pos0[s]
+    (random values), plus every step's q, k, v and positions resident in HBM.
+    pos0 is one position for all sequences or one per sequence."""
     d = DEC
-    nseq = d["nseq"]
+    nseq = len(P)
+    pos0 = np.broadcast_to(np.asarray(pos0, dtype=np.int64), (nseq,)).copy()
     if full_causal:
-        W = pos0 + n_steps + 1
+        W = int(pos0.max()) + n_steps + 1
         P = np.zeros(nseq, dtype=np.int64)
     cache = ps.RingCache(nseq, d["hkv"], d["D"], W, P, rope_theta=d["theta"],
                          prefix_max=int(max(P.max(), d["Pmax"] if not full_causal else 0)), zero=False)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(seed)
-    runs = {s: live_runs(pos0 - 1, int(P[s]), W) for s in range(nseq)}
+    runs = {s: live_runs(int(pos0[s]) - 1, int(P[s]), W) for s in range(nseq)}
     fill_random(cache, runs, gen, torch)
     # per-step inputs, resident in HBM before timing
     q = torch.randn(n_steps, nseq, d["hq"], d["D"], generator=gen, device="cuda").to(torch.bfloat16)
     k = torch.randn(n_steps, nseq, d["hkv"], d["D"], generator=gen, device="cuda").to(torch.bfloat16)
     v = torch.randn(n_steps, nseq, d["hkv"], d["D"], generator=gen, device="cuda").to(torch.bfloat16)
-    pos = (pos0 + torch.arange(n_steps, dtype=torch.int32, device="cuda"))[:, None].repeat(1, nseq).contiguous()
-    L = np.minimum(pos0 + 1, P + W)  # live slots per sequence once the step's token is in
+    pos = (torch.from_numpy(pos0.astype(np.int32)).cuda()[None, :]
+           + torch.arange(n_steps, dtype=torch.int32, device="cuda")[:, None]).contiguous()
+    L = np.minimum(pos0 + 1, P + W)  # live slots per sequence once the first step's token is in
     return cache, q, k, v, pos, L
 
 
@@ -214,6 +219,55 @@ def run_decode(ps, torch, cache, q, k, v, pos, steps, warmup, dist=None, per_ker
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     return total_ms, kern_ms, out, lse
+
+
+def decode_leg(ps, torch, name, P, W, pos0, steps, warmup, seed, hbm_peak):
+    """One decode workload: append + partial + combine per step, one layer."""
+    d = DEC
+    cache, q, k, v, pos, L = decode_setup(ps, torch, seed, W, P, pos0, steps + warmup)
+    total_ms, kern_ms, out, lse = run_decode(ps, torch, cache, q, k, v, pos, steps, warmup)
+    assert cache.check_status() == 0 and torch.isfinite(out.float()).all()
+    nseq = len(P)
+    kv = float(np.sum(2 * d["hkv"] * L * d["D"] * 2))
+    alg = kv + nseq * d["hq"] * d["D"] * 2
+    kern = statistics.mean(kern_ms)
+    rep = {"workload": name, "tok_s_per_layer": nseq * steps / (total_ms / 1e3),
+           "tok_s_28_layers": nseq * steps / (total_ms / 1e3) / LAYERS,
+           "step_ms": total_ms / steps, "partial_kernel_ms": kern,
+           "kv_bytes_first_step": kv, "live_slots_mean": float(np.mean(L)),
+           "partial_gbs": alg / (kern / 1e3) / 1e9,
+           "partial_frac_of_measured_hbm": alg / (kern / 1e3) / 1e9 / hbm_peak}
+    del cache, q, k, v, pos
+    torch.cuda.empty_cache()
+    return rep
+
+
+def ragged_leg(ps, torch, steps, seed, hbm_peak):
+    """256 sequences, positions uniform in [1024, 262143], P in 64..512, W 8,192."""
+    import synth
+    nseq, W = 256, 8192
+    P = synth.uniform_int(seed, 10, nseq, 64, 512)
+    pos0 = synth.uniform_int(seed, 11, nseq, 1024, 262143)
+    rep = decode_leg(ps, torch, "ragged decode: 256 sequences, positions uniform in [1024, 262143], "
+                     "P uniform 64..512, W 8192, Hq 16 / Hkv 8, D 128, one layer", P, W, pos0,
+                     steps, 5, seed, hbm_peak)
+    rep["sequences_still_causal"] = int(np.sum(pos0 + 1 < P + W))
+    return rep
+
+
+def flatness_leg(ps, torch, steps, seed, hbm_peak):
+    """Steady-decode shapes at growing positions: cost must stop growing once
+    every sequence's window is full (p >= P + W - 1)."""
+    d = DEC
+    P = decode_prefix_lens(seed, d["nseq"])
+    W = d["W"]
+    out = []
+    for label, pos0 in (("P+W/2", P + W // 2), ("P+W", P + W), ("2(P+W)", 2 * (P + W)),
+                        ("32768", 32768), ("131072", 131072), ("262143", 262143 - steps - 8)):
+        r = decode_leg(ps, torch, f"p = {label}", P, W, pos0, steps, 3, seed, hbm_peak)
+        out.append({"p": label, "live_slots_mean": r["live_slots_mean"], "step_ms": r["step_ms"],
+                    "partial_kernel_ms": r["partial_kernel_ms"], "tok_s_per_layer": r["tok_s_per_layer"]})
+    return out
 
 
 def run_decode_e2e(ps, torch, cache, steps, warmup, seed):
@@ -268,9 +322,12 @@ def prefill_flops(S, P, W, hq, D, bm=128, bn=128):
     return 4.0 * D * hq * float(pairs)
 
 
-def run_prefill(ps, torch, S, P, W, steps, warmup, seed, full_causal=False):
+def run_prefill(ps, torch, S, P, W, steps, warmup, seed, full_causal=False, B=None):
+    """Times whole ps_prefill calls (RoPE pre-pass + tile kernel) on one layer's
+    resident q, k, v; returns ms per call and the tile classes of one row."""
     d = PRE
-    B, hq, hkv, D = d["B"], d["hq"], d["hkv"], d["D"]
+    B = d["B"] if B is None else B
+    hq, hkv, D = d["hq"], d["hkv"], d["D"]
     if full_causal:
         W = S
     gen = torch.Generator(device="cuda")
@@ -283,19 +340,46 @@ def run_prefill(ps, torch, S, P, W, steps, warmup, seed, full_causal=False):
     out = torch.empty_like(q)
     lse = torch.empty(B, hq, S, dtype=torch.float32, device="cuda")
     ws = torch.empty(ps.prefill_workspace_size(B, S, hq, hkv, D), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for _ in range(warmup):
-        ps.prefill(q, k, v, qs, pl, W, rope_theta=d["theta"], out=out, lse=lse, workspace=ws)
+        ps.prefill(q, k, v, qs, pl, W, rope_theta=d["theta"], out=out, lse=lse, workspace=ws,
+                   status=status)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(steps):
-        ps.prefill(q, k, v, qs, pl, W, rope_theta=d["theta"], out=out, lse=lse, workspace=ws)
+        ps.prefill(q, k, v, qs, pl, W, rope_theta=d["theta"], out=out, lse=lse, workspace=ws,
+                   status=status)
     e1.record()
     torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"prefill device status {int(status.item())}"
+    assert torch.isfinite(lse).all()
     ms = e0.elapsed_time(e1) / steps
     cls = ps.prefill_tile_classes(S, 0, P, W).cpu().numpy()
     n_skip, n_part, n_full = [(cls == c).sum() for c in (0, 1, 2)]
     return ms, dict(skip=int(n_skip), partial=int(n_part), full=int(n_full))
+
+
+def prefill_report(ps, torch, name, B, S, P, W, steps, seed, bf16_peak, full_causal_steps=0):
+    """Prefill leg: algorithmic and executed TFLOP/s of one ps_prefill call."""
+    d = PRE
+    ms, cls = run_prefill(ps, torch, S, P, W, steps, 3, seed, B=B)
+    flops = B * prefill_flops(S, P, W, d["hq"], d["D"])
+    tile_flops = B * 4.0 * d["D"] * d["hq"] * 128 * 128 * (cls["partial"] + cls["full"])
+    nq = -(-S // 128)
+    causal_tiles = nq * (nq + 1) // 2
+    rep = {"workload": name, "ms": ms, "tflops_algorithmic": flops / ms / 1e9,
+           "tflops_on_nonskipped_tiles": tile_flops / ms / 1e9,
+           "frac_of_measured_bf16_burst": tile_flops / ms / 1e9 / bf16_peak,
+           "timed": "whole ps_prefill call: RoPE pre-pass + tile kernel",
+           "tiles_per_row_and_head": cls,
+           "skip_fraction_of_causal_tiles": 1 - (cls["partial"] + cls["full"]) / causal_tiles}
+    if full_causal_steps:
+        fms, _ = run_prefill(ps, torch, S, 0, W, full_causal_steps, 2, seed + 9, full_causal=True, B=B)
+        rep["full_causal_ms"] = fms
+        rep["speedup_vs_full_causal"] = fms / ms
+    torch.cuda.empty_cache()
+    return rep
 
 
 # ---- CPU oracle -----------------------------------------------------------
@@ -362,6 +446,8 @@ def main():
     ap.add_argument("--no-baselines", action="store_true", help="skip full-causal and oracle legs")
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill leg")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the ragged-decode and flatness legs")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -415,21 +501,25 @@ def main():
     del cache, q, k, v
     torch.cuda.empty_cache()
 
-    # prefill (one layer)
+    # prefill (one layer) and the truncated-backprop training forward
     try:
         if args.no_prefill:
             raise RuntimeError("prefill leg skipped (--no-prefill)")
-        pms, cls = run_prefill(ps, torch, PRE["S"], PRE["P"], PRE["W"], args.prefill_steps, 3, seed + 5)
-        flops = prefill_flops(PRE["S"], PRE["P"], PRE["W"], PRE["hq"], PRE["D"])
-        tile_flops = 4.0 * PRE["D"] * PRE["hq"] * 128 * 128 * (cls["partial"] + cls["full"])
-        pre = {"workload": "prefill 1 x 32768 tokens, P=100, W=4096, Hq 16 / Hkv 8, D 128, one layer",
-               "ms": pms, "tflops_algorithmic": flops / pms / 1e9,
-               "tflops_on_nonskipped_tiles": tile_flops / pms / 1e9,
-               "frac_of_measured_bf16_burst": tile_flops / pms / 1e9 / bf16_peak,
-               "tiles": cls, "skip_fraction_of_causal_tiles": cls["skip"] and
-               1 - (cls["partial"] + cls["full"]) / ((256 * 257) // 2)}
+        fc = 0 if args.no_baselines else 3
+        pre = prefill_report(ps, torch, "prefill 1 x 32768 tokens, P=100, W=4096, Hq 16 / Hkv 8, "
+                             "D 128, one layer", 1, PRE["S"], PRE["P"], PRE["W"], args.prefill_steps,
+                             seed + 5, bf16_peak, fc)
+        train = prefill_report(ps, torch, "training forward 8 x 8192 tokens, P=256, W=2048, Hq 16 / "
+                               "Hkv 8, D 128, one layer", 8, 8192, 256, 2048, args.prefill_steps,
+                               seed + 6, bf16_peak, fc)
     except Exception as e:  # noqa: BLE001
         pre = {"unavailable": f"{type(e).__name__}: {e}"}
+        train = None
+
+    ragged = flat = None
+    if not args.no_extra and (rank == 0 or world == 1):
+        ragged = ragged_leg(ps, torch, 100, 4, hbm_peak)
+        flat = flatness_leg(ps, torch, 20, seed, hbm_peak)
 
     if not args.no_baselines and (rank == 0 or world == 1):
         fsteps = min(args.steps, 30)
@@ -441,13 +531,6 @@ def main():
                 "how": "same library, W > position (no eviction), P = 0"}
         del cfc, qf, kf, vf
         torch.cuda.empty_cache()
-        if pre and "ms" in pre:
-            try:
-                fpms, _ = run_prefill(ps, torch, PRE["S"], 0, PRE["W"], 5, 2, seed + 9, full_causal=True)
-                full["prefill_ms"] = fpms
-                pre["speedup_vs_full_causal"] = fpms / pre["ms"]
-            except Exception as e:  # noqa: BLE001
-                full["prefill_unavailable"] = str(e)
         full["decode_speedup"] = value / world / full["decode_tok_s"]
     clk = clocks.stop()
 
@@ -470,14 +553,15 @@ def main():
         "decode": {"tok_s_per_layer": value, "tok_s_28_layers": value / LAYERS,
                    "step_hbm_gbs": step_gbs, "kv_bytes_per_step": kv_bytes,
                    "partial_kernel_ms": kern_avg_ms, "step_ms": ms_step},
-        "roofline": {"kernel": "decode_partial_kernel<128,2,4,3>", "bound": "hbm",
+        "roofline": {"kernel": "decode_partial_kernel<128,2,8,3>", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_src} hbm_gbs",
                      "traffic": committed_traffic("decode_partial_steady_64x131072.md",
                                                   "prefix_sliding_window_02_b300/csrc/ps_decode.cu"),
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "frac_of_8tbs": achieved / 8000.0},
-        "prefill": pre, "full_causal": full, "e2e": e2e,
+        "prefill": pre, "train_forward": train, "ragged_decode": ragged, "flatness": flat,
+        "full_causal": full, "e2e": e2e,
         "gpu_launches": 3 * args.steps, "clocks": clk, "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

@@ -8,7 +8,7 @@
 // decode).  The step is a memory-bound GEMV, so it runs on CUDA cores.
 //
 // Work split ("stream-K" over tiles): the (sequence, kv head) segments are laid
-// end to end as 32-slot tiles, N tiles in all; warp w of NW owns tiles
+// end to end as 16-slot tiles, N tiles in all; warp w of NW owns tiles
 // [w*N/NW, (w+1)*N/NW), whatever the sequence lengths.  Each warp streams its
 // tiles through a private STAGES-deep TMA ring in shared memory and writes
 // one partial (unnormalised O, running max, running sum) per segment piece
@@ -16,14 +16,22 @@
 // unique because both indices only grow along the tile line; so NW + #segments
 // records suffice.  The combine kernel finds the warps covering a segment
 // from the same arithmetic.
+//
+// Inside a warp, lane l holds D/32 consecutive elements of every row.  For a
+// 16-row tile and two query heads the 32 partial dot products per lane are
+// reduced by a butterfly transpose, after which lane l holds the score of row
+// l % 16 for head l / 16; the softmax runs on those, and P V accumulates
+// each lane's D/32 output elements of every head.  Eight warps per SM (two
+// per scheduler) keep the scheduler busy while one warp waits on shared
+// memory or shuffles.
 #include "ps_internal.h"
 
 namespace ps {
 
-constexpr int kDecTile = 32;  // slots per tile (one per lane after the reduction)
+constexpr int kDecTile = 16;  // slots per tile
 
 struct DecodeParams {
-  CUtensorMap tmk;  // 3D {D, Hkv, total_slots}, box {D, 1, 32}
+  CUtensorMap tmk;  // 3D {D, Hkv, total_slots}, box {D, 1, kDecTile}
   CUtensorMap tmv;
   const __nv_bfloat16* q;  // [nseq, Hq, D]
   const int32_t* pos;
@@ -45,6 +53,8 @@ struct DecShape {
   static constexpr int TILE_BYTES = kDecTile * D * 2;      // one K or V tile
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int REC = ((G * D + 2 * G) + 3) & ~3;   // floats per record
+  static constexpr int HP = G >= 2 ? 2 : 1;                // heads per score pass
+  static constexpr int NPASS = G / HP;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -68,17 +78,53 @@ __device__ __forceinline__ int owner_warp(int64_t t, int64_t N, int64_t NW) {
   return (int)(((t + 1) * NW + N - 1) / N - 1);
 }
 
+// Position on the tile line: tile t of kv head h of sequence s (nt tiles per head).
+struct TileIter {
+  int64_t g;
+  int s, h, t, nt;
+
+  __device__ __forceinline__ void init(const int32_t* pfx, int nseq, int hkv, int64_t g0) {
+    g = g0;
+    s = find_seq(pfx, nseq, hkv, g0);
+    nt = pfx[s + 1] - pfx[s];
+    const int64_t r = g0 - (int64_t)pfx[s] * hkv;
+    h = (int)(r / nt);
+    t = (int)(r % nt);
+  }
+  __device__ __forceinline__ void next(const int32_t* pfx, int nseq, int hkv) {
+    ++g;
+    if (++t < nt) return;
+    t = 0;
+    if (++h < hkv) return;
+    h = 0;
+    do {
+      ++s;
+    } while (s < nseq && pfx[s + 1] == pfx[s]);  // sequences with no tiles own no line
+    nt = s < nseq ? pfx[s + 1] - pfx[s] : 0;
+  }
+};
+
+template <int EPL>
+__device__ __forceinline__ void load_row_f32(const uint8_t* rowp, float (&x)[EPL]) {
+  if constexpr (EPL == 4) {
+    const uint2 w2 = *reinterpret_cast<const uint2*>(rowp);
+    x[0] = bf16lo(w2.x); x[1] = bf16hi(w2.x); x[2] = bf16lo(w2.y); x[3] = bf16hi(w2.y);
+  } else {
+    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(rowp);
+    x[0] = bf16lo(w1); x[1] = bf16hi(w1);
+  }
+}
+
 template <int D, int G, int WARPS, int STAGES>
 __global__ void __launch_bounds__(WARPS * 32, 1)
     decode_partial_kernel(const __grid_constant__ DecodeParams p) {
   using S = DecShape<D, G>;
-  constexpr int EPL = S::EPL;
-  constexpr int HP = G >= 2 ? 2 : 1;  // heads per QK pass
+  constexpr int EPL = S::EPL, HP = S::HP, NPASS = S::NPASS, TS = kDecTile;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WARPS * STAGES * S::STAGE_BYTES);
-  float* pbuf_all = reinterpret_cast<float*>(bars + WARPS * STAGES);  // [WARPS][32][G]
-  int32_t* pfx = reinterpret_cast<int32_t*>(pbuf_all + WARPS * 32 * G);
+  float* pbuf_all = reinterpret_cast<float*>(bars + WARPS * STAGES);  // [WARPS][G * TS]
+  int32_t* pfx = reinterpret_cast<int32_t*>(pbuf_all + WARPS * G * TS);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -100,7 +146,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
           if (blockIdx.x == 0) set_flag(p.status, bad);
         } else {
           const int64_t L = min((int64_t)ps_ + 1, (int64_t)P + p.window);
-          n = (int32_t)((L + kDecTile - 1) / kDecTile);
+          n = (int32_t)((L + TS - 1) / TS);
         }
       }
       int32_t x = n;
@@ -134,39 +180,38 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
 
   uint8_t* my_tiles = tiles + warp * STAGES * S::STAGE_BYTES;
   uint64_t* my_bars = bars + warp * STAGES;
-  float* pbuf = pbuf_all + warp * 32 * G;
+  float* pbuf = pbuf_all + warp * G * TS;
 
   const uint64_t pol = policy_evict_first();
-  auto issue = [&](int64_t g, int st) {
-    const int s = find_seq(pfx, p.nseq, p.hkv, g);
-    const int32_t nt = pfx[s + 1] - pfx[s];
-    const int64_t r = g - (int64_t)pfx[s] * p.hkv;
-    const int h = (int)(r / nt), t = (int)(r % nt);
-    const int32_t row0 = (int32_t)(p.slot_base[s] + (int64_t)t * kDecTile);
+  TileIter nxt;  // next tile to request (lane 0 only)
+  auto issue = [&](int st) {
+    const int32_t row0 = (int32_t)(p.slot_base[nxt.s] + (int64_t)nxt.t * TS);
     uint64_t* bar = &my_bars[st];
     uint8_t* dst = my_tiles + st * S::STAGE_BYTES;
     mbar_arrive_expect_tx(bar, S::STAGE_BYTES);
-    tma_load_3d(dst, &p.tmk, bar, 0, h, row0, pol);
-    tma_load_3d(dst + S::TILE_BYTES, &p.tmv, bar, 0, h, row0, pol);
+    tma_load_3d(dst, &p.tmk, bar, 0, nxt.h, row0, pol);
+    tma_load_3d(dst + S::TILE_BYTES, &p.tmv, bar, 0, nxt.h, row0, pol);
   };
+  if (lane == 0) {
+    nxt.init(pfx, p.nseq, p.hkv, lo);
+    for (int k = 0; k < STAGES && nxt.g < hi; ++k) {
+      issue(k);
+      nxt.next(pfx, p.nseq, p.hkv);
+    }
+  }
 
-  if (lane == 0)
-    for (int k = 0; k < STAGES && lo + k < hi; ++k) issue(lo + k, k);
-
+  TileIter cur;
+  cur.init(pfx, p.nseq, p.hkv, lo);
   uint32_t parity = 0;  // bit st = parity expected next on stage st
-  float qf[G][EPL], acc[G][EPL], m[G], lsum[G];
+  float qf[G][EPL], acc[G][EPL], m[NPASS], lsum[NPASS];
   int cur_L = 0;
   bool ok = true;
   int64_t consumed = lo;
+  int st = 0;
 
-  for (int64_t g = lo; g < hi; ++g) {
-    const int st = (int)((g - lo) % STAGES);
-    const int s = find_seq(pfx, p.nseq, p.hkv, g);
-    const int32_t nt = pfx[s + 1] - pfx[s];
-    const int64_t r = g - (int64_t)pfx[s] * p.hkv;
-    const int h = (int)(r / nt), t = (int)(r % nt);
-
-    if (g == lo || t == 0) {
+  for (; cur.g < hi; cur.next(pfx, p.nseq, p.hkv)) {
+    const int s = cur.s, h = cur.h, t = cur.t;
+    if (cur.g == lo || t == 0) {
       // new segment piece: rotate the group's queries at position pos[s]
       const int32_t ppos = p.pos[s];
       cur_L = (int)min((int64_t)ppos + 1, (int64_t)p.prefix_len[s] + p.window);
@@ -174,13 +219,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
       for (int gg = 0; gg < G; ++gg) {
         const __nv_bfloat16* qrow = p.q + ((int64_t)s * p.hq + h * G + gg) * D + lane * EPL;
         float x[EPL];
-        if constexpr (EPL == 4) {
-          uint2 w2 = *reinterpret_cast<const uint2*>(qrow);
-          x[0] = bf16lo(w2.x); x[1] = bf16hi(w2.x); x[2] = bf16lo(w2.y); x[3] = bf16hi(w2.y);
-        } else {
-          uint32_t w1 = *reinterpret_cast<const uint32_t*>(qrow);
-          x[0] = bf16lo(w1); x[1] = bf16hi(w1);
-        }
+        load_row_f32<EPL>(reinterpret_cast<const uint8_t*>(qrow), x);
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
           // half-split RoPE: element i pairs with i + D/2, held by lane ^ 16
@@ -189,12 +228,15 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
           float c, sn;
           rope_cos_sin(ppos, p.turns.f[i], c, sn);
           const float y = (lane < 16) ? (x[e] * c - partner * sn) : (x[e] * c + partner * sn);
-          // rotated Q is rounded to bf16, as the tensor-core path stores it
+          // rotated Q is rounded to bf16, as the cache stores rotated K
           qf[gg][e] = __bfloat162float(__float2bfloat16_rn(y)) * p.scale_log2;
           acc[gg][e] = 0.f;
         }
-        m[gg] = -INFINITY;
-        lsum[gg] = 0.f;
+      }
+#pragma unroll
+      for (int ps_ = 0; ps_ < NPASS; ++ps_) {
+        m[ps_] = -INFINITY;
+        lsum[ps_] = 0.f;
       }
     }
 
@@ -202,98 +244,95 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
       ok = false;
       break;
     }
+    __syncwarp();
     parity ^= 1u << st;
-    consumed = g + 1;
+    consumed = cur.g + 1;
 
     const uint8_t* kt = my_tiles + st * S::STAGE_BYTES;
     const uint8_t* vt = kt + S::TILE_BYTES;
-    const int nvalid = min(kDecTile, cur_L - t * kDecTile);
+    const int nvalid = min(TS, cur_L - t * TS);
+    const int myrow = lane & (TS - 1);
 
-    // ---- scores: lane j ends with the dot product of slot row j
-    float sc[G];
 #pragma unroll
-    for (int hp = 0; hp < G; hp += HP) {
-      float part[HP][32];
+    for (int ps_ = 0; ps_ < NPASS; ++ps_) {
+      // ---- scores: 16 rows x HP heads of partial dot products per lane
+      float v[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const uint8_t* rowp = kt + j * (D * 2) + lane * (EPL * 2);
+      for (int j = 0; j < TS; ++j) {
         float k4[EPL];
-        if constexpr (EPL == 4) {
-          uint2 w2 = *reinterpret_cast<const uint2*>(rowp);
-          k4[0] = bf16lo(w2.x); k4[1] = bf16hi(w2.x); k4[2] = bf16lo(w2.y); k4[3] = bf16hi(w2.y);
-        } else {
-          uint32_t w1 = *reinterpret_cast<const uint32_t*>(rowp);
-          k4[0] = bf16lo(w1); k4[1] = bf16hi(w1);
-        }
+        load_row_f32<EPL>(kt + j * (D * 2) + lane * (EPL * 2), k4);
 #pragma unroll
         for (int hh = 0; hh < HP; ++hh) {
-          float a = qf[hp + hh][0] * k4[0];
+          float a = qf[ps_ * HP + hh][0] * k4[0];
 #pragma unroll
-          for (int e = 1; e < EPL; ++e) a = fmaf(qf[hp + hh][e], k4[e], a);
-          part[hh][j] = a;
+          for (int e = 1; e < EPL; ++e) a = fmaf(qf[ps_ * HP + hh][e], k4[e], a);
+          v[hh * TS + j] = a;
         }
       }
-      // transpose-reduce: after the step at offset o, a lane keeps the half
-      // of its partials whose row index has bit o equal to its lane bit o.
+      if constexpr (HP == 1) {  // one head: fold the two lane halves, then transpose
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
+        for (int i = 0; i < TS; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], 16);
+      } else {
+        // butterfly transpose-reduce: after the step at offset o a lane keeps
+        // the half of its partials whose index has bit o equal to its lane bit
+        const bool up = (lane & 16) != 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float send = up ? v[i] : v[i + 16];
+          const float keep = up ? v[i + 16] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+      }
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) {
         const bool up = (lane & o) != 0;
 #pragma unroll
         for (int i = 0; i < o; ++i) {
-#pragma unroll
-          for (int hh = 0; hh < HP; ++hh) {
-            const float send = up ? part[hh][i] : part[hh][i + o];
-            const float keep = up ? part[hh][i + o] : part[hh][i];
-            part[hh][i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-          }
+          const float send = up ? v[i] : v[i + o];
+          const float keep = up ? v[i + o] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
       }
+      // lane l: score of row l % 16 for head ps_ * HP + l / 16 (log2 domain)
+      const float x = myrow < nvalid ? v[0] : -INFINITY;
+      float tmax = x;
 #pragma unroll
-      for (int hh = 0; hh < HP; ++hh) sc[hp + hh] = part[hh][0];
-    }
-
-    // ---- online softmax (log2 domain; scores already carry scale*log2 e)
-#pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-      const float x = (lane < nvalid) ? sc[gg] : -INFINITY;
-      const float mn = fmaxf(m[gg], warp_max(x));
-      const float alpha = fast_exp2(m[gg] - mn);
+      for (int o = 8; o >= 1; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+      const float mn = fmaxf(m[ps_], tmax);
+      const float alpha = fast_exp2(m[ps_] - mn);
       const float pr = fast_exp2(x - mn);
-      lsum[gg] = lsum[gg] * alpha + pr;
+      lsum[ps_] = lsum[ps_] * alpha + pr;
+      m[ps_] = mn;
+      if (HP == 2 || lane < 16) pbuf[ps_ * 32 + lane] = pr;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[gg][e] *= alpha;
-      m[gg] = mn;
-      pbuf[lane * G + gg] = pr;
+      for (int hh = 0; hh < HP; ++hh) {
+        const float a_h = __shfl_sync(0xffffffffu, alpha, hh * 16);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[ps_ * HP + hh][e] *= a_h;
+      }
     }
     __syncwarp();
 
-    // ---- O += P V over the valid rows
+    // ---- O += P V over the valid rows (invalid rows may hold stale values)
     auto pv_row = [&](int j) {
-      const uint8_t* rowp = vt + j * (D * 2) + lane * (EPL * 2);
       float v4[EPL];
-      if constexpr (EPL == 4) {
-        uint2 w2 = *reinterpret_cast<const uint2*>(rowp);
-        v4[0] = bf16lo(w2.x); v4[1] = bf16hi(w2.x); v4[2] = bf16lo(w2.y); v4[3] = bf16hi(w2.y);
-      } else {
-        uint32_t w1 = *reinterpret_cast<const uint32_t*>(rowp);
-        v4[0] = bf16lo(w1); v4[1] = bf16hi(w1);
-      }
+      load_row_f32<EPL>(vt + j * (D * 2) + lane * (EPL * 2), v4);
 #pragma unroll
       for (int gg = 0; gg < G; ++gg) {
-        const float pj = pbuf[j * G + gg];
+        const float pj = pbuf[gg * TS + j];
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[gg][e] = fmaf(pj, v4[e], acc[gg][e]);
       }
     };
-    if (nvalid == kDecTile) {
+    if (nvalid == TS) {
 #pragma unroll
-      for (int j = 0; j < kDecTile; ++j) pv_row(j);
+      for (int j = 0; j < TS; ++j) pv_row(j);
     } else {
       for (int j = 0; j < nvalid; ++j) pv_row(j);
     }
 
     // ---- end of this warp's piece of the segment: write the partial record
-    if (t == nt - 1 || g == hi - 1) {
+    if (t == cur.nt - 1 || cur.g == hi - 1) {
       float* rec = p.rec + (size_t)(w + (int64_t)s * p.hkv + h) * S::REC;
 #pragma unroll
       for (int gg = 0; gg < G; ++gg) {
@@ -303,18 +342,26 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         } else {
           *reinterpret_cast<float2*>(o) = make_float2(acc[gg][0], acc[gg][1]);
         }
-        const float tot = warp_sum(lsum[gg]);
-        if (lane == 0) {
-          rec[G * D + gg] = m[gg];
+      }
+#pragma unroll
+      for (int ps_ = 0; ps_ < NPASS; ++ps_) {
+        float tot = lsum[ps_];
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if ((lane & 15) == 0 && (HP == 2 || lane == 0)) {
+          const int gg = ps_ * HP + (lane >> 4);
+          rec[G * D + gg] = m[ps_];
           rec[G * D + G + gg] = tot;
         }
       }
     }
     __syncwarp();
-    if (lane == 0 && g + STAGES < hi) {
+    if (lane == 0 && nxt.g < hi) {
       fence_proxy_async_smem();
-      issue(g + STAGES, st);
+      issue(st);
+      nxt.next(pfx, p.nseq, p.hkv);
     }
+    st = st + 1 == STAGES ? 0 : st + 1;
   }
 
   if (!ok) {
@@ -322,9 +369,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     if (lane == 0) set_flag(p.status, PS_DEV_TIMEOUT);
     const int64_t issued_end = min(hi, consumed + STAGES);
     for (int64_t g = consumed + 1; g < issued_end; ++g) {
-      const int st = (int)((g - lo) % STAGES);
-      if (!mbar_wait(&my_bars[st], (parity >> st) & 1u)) break;
-      parity ^= 1u << st;
+      const int sg = (int)((g - lo) % STAGES);
+      if (!mbar_wait(&my_bars[sg], (parity >> sg) & 1u)) break;
+      parity ^= 1u << sg;
     }
   }
 }
@@ -385,14 +432,14 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
 }
 
 // ----------------------------------------------------------------- host ----
-constexpr int kDecWarps = 4;
+constexpr int kDecWarps = 8;
 constexpr int kDecStages = 3;
 
 template <int D, int G>
 static size_t dec_smem_bytes(int nseq) {
   using S = DecShape<D, G>;
   return (size_t)kDecWarps * kDecStages * S::STAGE_BYTES + kDecWarps * kDecStages * 8 +
-         kDecWarps * 32 * G * 4 + (size_t)(nseq + 1) * 4;
+         kDecWarps * G * kDecTile * 4 + (size_t)(nseq + 1) * 4;
 }
 
 struct DecPlan {

@@ -62,106 +62,129 @@ struct GatherParams {
   RopeTurns turns;
 };
 
-__device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, int32_t pos,
-                                        const unsigned long long* f, uint4& ra, uint4& rb) {
+// Rotates 8 rotation pairs: elements 8g..8g+7 of the first half (a) with their
+// partners 8g+64.. of the second half (b); cs holds (cos, sin) of each pair.
+__device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, const float2* cs,
+                                        uint4& ra, uint4& rb) {
   const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
   const uint32_t* bw = reinterpret_cast<const uint32_t*>(&b);
   uint32_t* raw = reinterpret_cast<uint32_t*>(&ra);
   uint32_t* rbw = reinterpret_cast<uint32_t*>(&rb);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    float c0, s0, c1, s1;
-    rope_cos_sin(pos, f[2 * e], c0, s0);
-    rope_cos_sin(pos, f[2 * e + 1], c1, s1);
+    const float2 t0 = cs[2 * e], t1 = cs[2 * e + 1];
     const float x0 = bf16lo(aw[e]), x1 = bf16hi(aw[e]);
     const float y0 = bf16lo(bw[e]), y1 = bf16hi(bw[e]);
-    raw[e] = pack_bf16(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
-    rbw[e] = pack_bf16(y0 * c0 + x0 * s0, y1 * c1 + x1 * s1);
+    raw[e] = pack_bf16(x0 * t0.x - y0 * t0.y, x1 * t1.x - y1 * t1.y);
+    rbw[e] = pack_bf16(y0 * t0.x + x0 * t0.y, y1 * t1.x + x1 * t1.y);
   }
 }
 
-// One thread per (row, head, group of 8 rotation pairs); D = 128 (16 vectors a row).
+constexpr int kRopeRows = 4;  // chunk rows per block iteration (256 threads: 4 rows x 64 pairs)
+
+// D = 128.  Phase A: groups of kRopeRows chunk rows; the 64 (cos, sin) pairs of
+// each row's position are computed once into shared memory and shared by all
+// Hq query heads and Hkv key heads of that row.  Phase B: the ring rows
+// (copied, already rotated) and the zero padding of each batch row's key array.
 __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant__ GatherParams p) {
-  constexpr int VEC = 16, HALFV = 8, GROUPS = 8;
-  const int64_t nq_items = (int64_t)p.B * p.S * p.hq * GROUPS;
-  const int64_t nk_items = (int64_t)p.B * p.Skv * p.hkv * GROUPS;
+  constexpr int VEC = 16, HALFV = 8;
+  __shared__ float2 cs[kRopeRows][64];
   const bool ring = p.k_pool != nullptr;
-  for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < nq_items + nk_items;
-       it += (int64_t)gridDim.x * blockDim.x) {
-    if (it < nq_items) {
-      const int g = (int)(it % GROUPS);
-      int64_t r = it / GROUPS;
-      const int h = (int)(r % p.hq);
-      r /= p.hq;                       // r = b * S + row
-      const int b = (int)(r / p.S);
-      const int32_t pos = p.q_start[b] + (int32_t)(r % p.S);
-      const int64_t base = (r * p.hq + h) * VEC;
-      uint4 ra, rb;
-      rotate8(p.q[base + g], p.q[base + HALFV + g], pos, &p.turns.f[8 * g], ra, rb);
-      p.qh[base + g] = ra;
-      p.qh[base + HALFV + g] = rb;
-      continue;
+  const int64_t n_rows = (int64_t)p.B * p.S;
+  const int64_t n_groups = (n_rows + kRopeRows - 1) / kRopeRows;
+  const int heads = p.hq + p.hkv;
+  for (int64_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {
+    const int64_t r0 = grp * kRopeRows;
+    {
+      const int rr = threadIdx.x >> 6, i = threadIdx.x & 63;
+      const int64_t r = r0 + rr;
+      if (r < n_rows) {
+        const int b = (int)(r / p.S);
+        const int32_t pos = p.q_start[b] + (int32_t)(r % p.S);
+        float c, s;
+        rope_cos_sin(pos, p.turns.f[i], c, s);
+        cs[rr][i] = make_float2(c, s);
+      }
     }
-    const int64_t kt = it - nq_items;
-    const int g = (int)(kt % GROUPS);
-    int64_t r = kt / GROUPS;
-    const int h = (int)(r % p.hkv);
-    r /= p.hkv;                        // r = b * Skv + key index
-    const int b = (int)(r / p.Skv);
-    const int32_t kidx = (int32_t)(r % p.Skv);
+    __syncthreads();
+    const int items = kRopeRows * heads * 8;
+    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+      const int g = it & 7;
+      const int hd = (it >> 3) % heads;
+      const int rr = (it >> 3) / heads;
+      const int64_t r = r0 + rr;
+      if (r >= n_rows) continue;
+      const float2* ang = &cs[rr][8 * g];
+      uint4 ra, rb;
+      if (hd < p.hq) {
+        const int64_t base = (r * p.hq + hd) * VEC;
+        rotate8(p.q[base + g], p.q[base + HALFV + g], ang, ra, rb);
+        p.qh[base + g] = ra;
+        p.qh[base + HALFV + g] = rb;
+      } else {
+        const int h = hd - p.hq;
+        const int b = (int)(r / p.S);
+        const int32_t t = (int32_t)(r % p.S);
+        const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
+        const KeyMap km = make_keymap(p.S, c0, P, p.W, ring);
+        const int32_t n_ring = km.n_keys - p.S;
+        // the ring part must fit the workspace stride: 0 <= P <= the ring's
+        // prefix_max (which ps_prefill sized it by) and q_start >= 0
+        if (c0 < 0 || (ring && (P < 0 || n_ring > p.Skv - p.S))) {
+          set_flag(p.status, c0 < 0 ? PS_DEV_BAD_POS : PS_DEV_BAD_PREFIX);
+          continue;
+        }
+        const int64_t src = (r * p.hkv + h) * VEC;
+        const int64_t dst = (((int64_t)b * p.Skv + n_ring + t) * p.hkv + h) * VEC;
+        rotate8(p.k[src + g], p.k[src + HALFV + g], ang, ra, rb);
+        p.kh[dst + g] = ra;
+        p.kh[dst + HALFV + g] = rb;
+        if (p.vg) {
+          p.vg[dst + g] = p.v[src + g];
+          p.vg[dst + HALFV + g] = p.v[src + HALFV + g];
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // phase B: per batch row, key indices [0, n_ring) come from the ring and
+  // [n_keys, Skv) are padding up to the workspace stride
+  const int32_t extra = p.Skv - p.S;
+  const int64_t n_extra = (int64_t)p.B * extra * p.hkv * VEC;
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < n_extra;
+       u += (int64_t)gridDim.x * blockDim.x) {
+    const int vec = (int)(u % VEC);
+    int64_t rest = u / VEC;
+    const int h = (int)(rest % p.hkv);
+    rest /= p.hkv;
+    const int b = (int)(rest / extra);
+    const int32_t x = (int32_t)(rest % extra);
     const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
     const KeyMap km = make_keymap(p.S, c0, P, p.W, ring);
-    const int64_t dst = (r * p.hkv + h) * VEC;
     const int32_t n_ring = km.n_keys - p.S;
-    if (kidx >= km.n_keys) {  // padding rows up to the workspace stride: zeros
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      p.kh[dst + g] = z;
-      p.kh[dst + HALFV + g] = z;
-      if (p.vg) {
-        p.vg[dst + g] = z;
-        p.vg[dst + HALFV + g] = z;
-      }
-      continue;
-    }
-    if (kidx < n_ring) {  // cached key: copy the rotated row out of the ring
+    const int32_t kidx = x < n_ring ? x : x + p.S;
+    const int64_t dst = (((int64_t)b * p.Skv + kidx) * p.hkv + h) * VEC + vec;
+    uint4 kk = make_uint4(0, 0, 0, 0), vv = kk;
+    if (kidx < km.n_keys) {  // cached key: copy the rotated row out of the ring
       const int32_t s = p.ring_seq ? p.ring_seq[b] : b;
       bool bad = s < 0 || s >= p.nseq;
-      int32_t rp = 0;
-      int64_t sb = 0;
-      if (!bad) {
-        rp = p.ring_prefix[s];
-        sb = p.slot_base[s];
-        if (rp != P) { set_flag(p.status, PS_DEV_BAD_PREFIX); bad = true; }
-        if (sb < 0 || sb + p.capacity > p.total_slots) { set_flag(p.status, PS_DEV_BAD_SLOT); bad = true; }
-      } else {
+      if (bad) {
         set_flag(p.status, PS_DEV_BAD_SEQ);
+      } else {
+        const int64_t sb = p.slot_base[s];
+        if (p.ring_prefix[s] != P) { set_flag(p.status, PS_DEV_BAD_PREFIX); bad = true; }
+        if (sb < 0 || sb + p.capacity > p.total_slots) { set_flag(p.status, PS_DEV_BAD_SLOT); bad = true; }
+        if (!bad) {
+          const int32_t pos = key_pos(km, kidx);
+          const int64_t src = ((sb + ring_slot(pos, P, p.W)) * p.hkv + h) * VEC + vec;
+          kk = p.k_pool[src];
+          vv = p.v_pool[src];
+        }
       }
-      uint4 k0 = make_uint4(0, 0, 0, 0), k1 = k0, v0 = k0, v1 = k0;
-      if (!bad) {
-        const int32_t pos = key_pos(km, kidx);
-        const int64_t src = ((sb + ring_slot(pos, P, p.W)) * p.hkv + h) * VEC;
-        k0 = p.k_pool[src + g];
-        k1 = p.k_pool[src + HALFV + g];
-        v0 = p.v_pool[src + g];
-        v1 = p.v_pool[src + HALFV + g];
-      }
-      p.kh[dst + g] = k0;
-      p.kh[dst + HALFV + g] = k1;
-      p.vg[dst + g] = v0;
-      p.vg[dst + HALFV + g] = v1;
-      continue;
     }
-    // chunk key
-    const int32_t t = kidx - n_ring;
-    const int64_t src = (((int64_t)b * p.S + t) * p.hkv + h) * VEC;
-    uint4 ra, rb;
-    rotate8(p.k[src + g], p.k[src + HALFV + g], c0 + t, &p.turns.f[8 * g], ra, rb);
-    p.kh[dst + g] = ra;
-    p.kh[dst + HALFV + g] = rb;
-    if (p.vg) {
-      p.vg[dst + g] = p.v[src + g];
-      p.vg[dst + HALFV + g] = p.v[src + HALFV + g];
-    }
+    p.kh[dst] = kk;
+    if (p.vg) p.vg[dst] = vv;
   }
 }
 
@@ -523,7 +546,9 @@ __device__ __forceinline__ float exp2_col(int c, float x) {
 // One query row's share of a 128-key tile: S from TMEM, optional element mask
 // (keep column c iff c < A1 or B0 <= c < B1), online-softmax bookkeeping with a
 // lazy rescale, and P = exp2(S * scale - m) stored back over the first 64
-// columns as bf16 pairs.  Returns the factor O must be scaled by (1 = none).
+// columns as bf16 pairs.  The row sum adds the fp32 probabilities: summing
+// the bf16-rounded ones instead moves the LSE of rows with few keys by up to
+// a bf16 rounding (2e-3).  Returns the factor O must be scaled by (1 = none).
 // The masked and unmasked variants are whole functions so that the 128 scores
 // are never live across a branch.
 template <bool MASK>
@@ -552,9 +577,15 @@ __device__ __forceinline__ float softmax_tile(uint32_t tS, int j, float scale_lo
       s[c] = keep ? s[c] : -INFINITY;
     }
   }
-  float mx = s[0];
+  // row max as a tree of independent chains (a single running max would be a
+  // 127-deep dependent chain on the critical path between S and P)
+  float mx8[8];
 #pragma unroll
-  for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+  for (int c = 0; c < 8; ++c) mx8[c] = s[c];
+#pragma unroll
+  for (int c = 8; c < kBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+  const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
   const float m_new = fmaxf(m_used, mx * scale_log2);
   float alpha = 1.f;
   if (j == 0) {
@@ -564,25 +595,25 @@ __device__ __forceinline__ float softmax_tile(uint32_t tS, int j, float scale_lo
     m_used = m_new;
   }
   const float mu = m_used == -INFINITY ? 0.f : m_used;
-  float rs = 0.f;
+  float rs4[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
   uint32_t p0[32], p1[32];
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     const float x = exp2_col(2 * c, fmaf(s[2 * c], scale_log2, -mu));
     const float y = exp2_col(2 * c + 1, fmaf(s[2 * c + 1], scale_log2, -mu));
-    rs += x + y;
     p0[c] = pack_bf16(x, y);
+    rs4[c & 3] += x + y;
   }
   tc::st32(tS, p0);
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     const float x = exp2_col(64 + 2 * c, fmaf(s[64 + 2 * c], scale_log2, -mu));
     const float y = exp2_col(64 + 2 * c + 1, fmaf(s[64 + 2 * c + 1], scale_log2, -mu));
-    rs += x + y;
     p1[c] = pack_bf16(x, y);
+    rs4[c & 3] += x + y;
   }
   tc::st32(tS + 32, p1);
-  l = fmaf(l, alpha, rs);
+  l = fmaf(l, alpha, (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
   return alpha;
 }
 
@@ -936,10 +967,11 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
   g.W = window;
   make_rope_turns(rope_theta, head_dim, &g.turns);
   {
-    const int64_t items = ((int64_t)batch * seqlen * n_q_heads + (int64_t)batch * L.skv * n_kv_heads) * 8;
-    int64_t blocks = (items + 255) / 256;
+    const int64_t groups = ((int64_t)batch * seqlen + kRopeRows - 1) / kRopeRows;
+    const int64_t extra = (int64_t)batch * (L.skv - seqlen) * n_kv_heads * 16;
+    int64_t blocks = groups > (extra + 255) / 256 ? groups : (extra + 255) / 256;
     const int sms = device_sm_count();
-    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;
     if (blocks > cap) blocks = cap;
     rope_gather_kernel<<<(unsigned)blocks, 256, 0, s>>>(g);
     if (cudaGetLastError() != cudaSuccess) return PS_ERR_CUDA;

@@ -36,65 +36,100 @@ struct AppendParams {
   RopeTurns turns;
 };
 
-// One thread per (token, kv head, group of 8 rotation pairs): it loads the 8
-// elements of the first half and their 8 partners in the second half (two
-// 16-byte loads), rotates them in fp32 and stores bf16 (round to nearest even).
-__global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendParams p) {
-  const int groups = p.head_dim / 16;
-  const int vec_per_row = p.head_dim / 8;  // 16-byte vectors per head row
-  const int64_t items = p.n_tokens * p.hkv * groups;
-  for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < items;
-       it += (int64_t)gridDim.x * blockDim.x) {
-    const int g = (int)(it % groups);
-    const int64_t rest = it / groups;
-    const int h = (int)(rest % p.hkv);
-    const int64_t t = rest / p.hkv;
-    // run r: the largest r with cu[r] <= t
-    int lo = 0, hi = p.nrun - 1;
-    while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (p.cu[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    const int64_t c0 = p.cu[lo], c1 = p.cu[lo + 1];
-    if (!(c0 <= t && t < c1)) { set_flag(p.status, PS_DEV_BAD_RUN); continue; }
-    const int32_t s = p.seq_idx[lo];
-    if (s < 0 || s >= p.nseq) { set_flag(p.status, PS_DEV_BAD_SEQ); continue; }
-    const int32_t P = p.prefix_len[s];
-    if (P < 0 || P > p.prefix_max) { set_flag(p.status, PS_DEV_BAD_PREFIX); continue; }
-    const int64_t base = p.slot_base[s];
-    if (base < 0 || base + p.capacity > p.total_slots) { set_flag(p.status, PS_DEV_BAD_SLOT); continue; }
-    const int64_t first = p.pos0[lo];
-    const int64_t last = first + (c1 - c0) - 1;
-    if (first < 0 || last > 0x7fffffffLL) { set_flag(p.status, PS_DEV_BAD_POS); continue; }
-    const int32_t pos = (int32_t)(first + (t - c0));
-    // A window position is overwritten later in the same run once a position
-    // W further on is also in it: only prefix positions and the last W survive.
-    if (!(pos < P || (int64_t)pos > last - p.window)) continue;
-    const int64_t row = base + ring_slot(pos, P, p.window);
+// A block of 128 threads takes 128 / (D/2) tokens at a time.  First each
+// thread resolves one (token, rotation pair): the token's run, sequence,
+// position and destination row, and the (cos, sin) of the pair's angle, into
+// shared memory; the angle of a position is shared by all KV heads.  Then one
+// thread per (token, kv head, group of 8 pairs) loads the 8 elements of the
+// first half and their 8 partners (two 16-byte loads), rotates them in fp32 and
+// stores bf16 (round to nearest even); V is copied alongside.
+constexpr int kAppendThreads = 128;
 
-    const int64_t src = (t * p.hkv + h) * vec_per_row;
-    const int64_t dst = (row * p.hkv + h) * vec_per_row;
-    const int half_vec = vec_per_row / 2;
-    uint4 a = p.k[src + g], b = p.k[src + half_vec + g];
-    const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
-    const uint32_t* bw = reinterpret_cast<const uint32_t*>(&b);
-    uint4 ra, rb;
-    uint32_t* raw = reinterpret_cast<uint32_t*>(&ra);
-    uint32_t* rbw = reinterpret_cast<uint32_t*>(&rb);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float c0f, s0f, c1f, s1f;
-      rope_cos_sin(pos, p.turns.f[8 * g + 2 * e], c0f, s0f);
-      rope_cos_sin(pos, p.turns.f[8 * g + 2 * e + 1], c1f, s1f);
-      const float x0 = bf16lo(aw[e]), x1 = bf16hi(aw[e]);  // first-half elements
-      const float y0 = bf16lo(bw[e]), y1 = bf16hi(bw[e]);  // their partners
-      raw[e] = pack_bf16(x0 * c0f - y0 * s0f, x1 * c1f - y1 * s1f);
-      rbw[e] = pack_bf16(y0 * c0f + x0 * s0f, y1 * c1f + x1 * s1f);
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_constant__ AppendParams p) {
+  __shared__ float2 cs[kAppendThreads];
+  __shared__ int64_t row_of[kAppendThreads];  // destination pool row, or -1 = write nothing
+  const int half = p.head_dim / 2;
+  const int tpb = kAppendThreads / half;     // tokens per block iteration
+  const int groups = p.head_dim / 16;
+  const int vec_per_row = p.head_dim / 8;    // 16-byte vectors per head row
+  const int64_t n_groups = (p.n_tokens + tpb - 1) / tpb;
+  for (int64_t tg = blockIdx.x; tg < n_groups; tg += gridDim.x) {
+    {
+      const int tl = threadIdx.x / half, i = threadIdx.x % half;
+      const int64_t t = tg * tpb + tl;
+      int64_t row = -1;
+      int32_t pos = 0;
+      if (t < p.n_tokens) {
+        // run r: the largest r with cu[r] <= t
+        int lo = 0, hi = p.nrun - 1;
+        while (lo < hi) {
+          int mid = (lo + hi + 1) >> 1;
+          if (p.cu[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        const int64_t c0 = p.cu[lo], c1 = p.cu[lo + 1];
+        const int32_t s = p.seq_idx[lo];
+        int32_t bad = 0;
+        if (!(c0 <= t && t < c1)) bad = PS_DEV_BAD_RUN;
+        else if (s < 0 || s >= p.nseq) bad = PS_DEV_BAD_SEQ;
+        int32_t P = 0;
+        int64_t base = 0, last = 0;
+        if (!bad) {
+          P = p.prefix_len[s];
+          base = p.slot_base[s];
+          const int64_t first = p.pos0[lo];
+          last = first + (c1 - c0) - 1;
+          if (P < 0 || P > p.prefix_max) bad = PS_DEV_BAD_PREFIX;
+          else if (base < 0 || base + p.capacity > p.total_slots) bad = PS_DEV_BAD_SLOT;
+          else if (first < 0 || last > 0x7fffffffLL) bad = PS_DEV_BAD_POS;
+          else pos = (int32_t)(first + (t - c0));
+        }
+        if (bad) {
+          if (i == 0) set_flag(p.status, bad);
+        } else if (pos < P || (int64_t)pos > last - p.window) {
+          // a window position is overwritten later in the same run once a
+          // position W further on is also in it: only prefix positions and
+          // the last W of the run survive
+          row = base + ring_slot(pos, P, p.window);
+        }
+      }
+      float c = 1.f, sn = 0.f;
+      if (row >= 0) rope_cos_sin(pos, p.turns.f[i], c, sn);
+      cs[threadIdx.x] = make_float2(c, sn);
+      if (i == 0) row_of[tl] = row;
     }
-    p.kp[dst + g] = ra;
-    p.kp[dst + half_vec + g] = rb;
-    p.vp[dst + g] = p.v[src + g];
-    p.vp[dst + half_vec + g] = p.v[src + half_vec + g];
+    __syncthreads();
+    const int items = tpb * p.hkv * groups;
+    for (int it = threadIdx.x; it < items; it += kAppendThreads) {
+      const int g = it % groups;
+      const int h = (it / groups) % p.hkv;
+      const int tl = it / (groups * p.hkv);
+      const int64_t row = row_of[tl];
+      if (row < 0) continue;
+      const int64_t t = tg * tpb + tl;
+      const int64_t src = (t * p.hkv + h) * vec_per_row;
+      const int64_t dst = (row * p.hkv + h) * vec_per_row;
+      const int half_vec = vec_per_row / 2;
+      const float2* ang = &cs[tl * half + 8 * g];
+      uint4 a = p.k[src + g], b = p.k[src + half_vec + g];
+      const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
+      const uint32_t* bw = reinterpret_cast<const uint32_t*>(&b);
+      uint4 ra, rb;
+      uint32_t* raw = reinterpret_cast<uint32_t*>(&ra);
+      uint32_t* rbw = reinterpret_cast<uint32_t*>(&rb);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 t0 = ang[2 * e], t1 = ang[2 * e + 1];
+        const float x0 = bf16lo(aw[e]), x1 = bf16hi(aw[e]);  // first-half elements
+        const float y0 = bf16lo(bw[e]), y1 = bf16hi(bw[e]);  // their partners
+        raw[e] = pack_bf16(x0 * t0.x - y0 * t0.y, x1 * t1.x - y1 * t1.y);
+        rbw[e] = pack_bf16(y0 * t0.x + x0 * t0.y, y1 * t1.x + x1 * t1.y);
+      }
+      p.kp[dst + g] = ra;
+      p.kp[dst + half_vec + g] = rb;
+      p.vp[dst + g] = p.v[src + g];
+      p.vp[dst + half_vec + g] = p.v[src + half_vec + g];
+    }
+    __syncthreads();
   }
 }
 
@@ -144,12 +179,11 @@ extern "C" ps_status_t ps_kv_append(const ps_cache_desc* cache, const int32_t* s
   p.capacity = cache->capacity;
   p.prefix_max = cache->prefix_max;
   make_rope_turns(cache->rope_theta, cache->head_dim, &p.turns);
-  const int threads = 256;
-  const int64_t items = n_tokens * cache->n_kv_heads * (cache->head_dim / 16);
-  int64_t blocks = (items + threads - 1) / threads;
+  const int64_t tpb = kAppendThreads / (cache->head_dim / 2);
+  int64_t blocks = (n_tokens + tpb - 1) / tpb;
   const int sms = device_sm_count();
   const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;
   if (blocks > cap) blocks = cap;
-  append_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(p);
+  append_kernel<<<(unsigned)blocks, kAppendThreads, 0, (cudaStream_t)stream>>>(p);
   return launch_status();
 }

@@ -6,10 +6,28 @@ import torch
 
 import synth
 
-# Tolerances for bf16 inputs with fp32 accumulation (per (case, head) tensor):
-O_ABS = 1e-2      # max |O_gpu - O_ref|
-O_REL = 2e-2      # max |O_gpu - O_ref| / max |O_ref|
-LSE_ABS = 1e-3    # max |LSE_gpu - LSE_ref|
+# Tolerances for bf16 inputs with fp32 accumulation, read as an absolute plus a
+# relative term per element (the numpy/torch allclose convention):
+#     |O_gpu - O_ref| <= O_ABS + O_REL * |O_ref|   and   |LSE_gpu - LSE_ref| <= LSE_ABS.
+# O is returned in bf16, whose rounding alone is half an ulp of the value
+# (0.0156 for |O| in [4, 8)), so a purely absolute 1e-2 bound cannot hold for
+# large outputs of any bf16-output kernel; the relative term covers that.
+O_ABS = 1e-2
+O_REL = 2e-2
+LSE_ABS = 1e-3
+
+
+def lse_tol(qscale_log2: int = 0) -> float:
+    """LSE bound for queries scaled by 2**qscale_log2 (stress cases only).
+
+    Both sides round the rotated query to bf16; the kernel rotates in fp32 and
+    the oracle in fp64, so an element lying almost exactly between two bf16
+    values can round to different neighbours (about one element in 10^4).  One
+    such flip moves a score by one bf16 ulp of q_i times |k_i| / sqrt(D), and
+    the LSE of a row dominated by that key by the same amount; scaling q by 2^s
+    scales the ulp, hence the bound, by 2^s.  Unscaled inputs keep 1e-3.
+    """
+    return LSE_ABS * 2.0 ** qscale_log2
 
 
 def bits_to_bf16_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
@@ -77,12 +95,13 @@ def random_source(seed, hkv, d, device="cuda"):
     return src
 
 
-def assert_attention_close(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+def assert_attention_close(o_gpu, lse_gpu, o_ref, lse_ref, what="", lse_abs=LSE_ABS):
     """o_*: [H, D]; lse_*: [H].  Checks each head against the stated tolerances."""
     for h in range(o_ref.shape[0]):
-        d = float(np.abs(o_gpu[h] - o_ref[h]).max())
-        ref = float(np.abs(o_ref[h]).max())
+        err = np.abs(o_gpu[h] - o_ref[h])
+        bound = O_ABS + O_REL * np.abs(o_ref[h])
+        i = int(np.argmax(err - bound))
         dl = float(abs(lse_gpu[h] - lse_ref[h]))
-        assert d <= O_ABS, f"{what} head {h}: max|dO| = {d:.3e}"
-        assert d <= O_REL * ref, f"{what} head {h}: max|dO|/max|O| = {d / ref:.3e}"
-        assert dl <= LSE_ABS, f"{what} head {h}: |dLSE| = {dl:.3e}"
+        assert err[i] <= bound[i], (f"{what} head {h}: |dO| = {err[i]:.3e} at element {i} "
+                                    f"(|O_ref| = {abs(o_ref[h][i]):.3e}, bound {bound[i]:.3e})")
+        assert dl <= lse_abs, f"{what} head {h}: |dLSE| = {dl:.3e}"
