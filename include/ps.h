@@ -153,6 +153,30 @@ ps_status_t ps_decode_combine(const ps_cache_desc* cache, int32_t n_q_heads, voi
                               const void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * ps_decode_noalloc: ps_decode without a caller-supplied workspace, for
+ * callers that cannot allocate device memory when they decode -- a host that
+ * has no allocator of its own (plain C linking this library), code that runs
+ * while a caching allocator is locked or shutting down, or a server that
+ * reserves all its memory at start-up and forbids allocation during
+ * generation.  The pages have no counterpart to this call; it is a packaging
+ * choice.
+ *   Arguments, outputs and numerics are those of ps_decode.  The scratch is a
+ *   fixed 4 MiB device array inside this library (every GPU that loads the
+ *   library holds it until the process exits); the call allocates and frees
+ *   nothing.  It returns PS_ERR_WORKSPACE when ps_decode_workspace_size for
+ *   these shapes exceeds 4 MiB; 4 MiB holds, on a 148-SM B300, 256 sequences
+ *   at Hkv = 8, head_dim 128 and two query heads per KV head.
+ *   The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ *   All calls share the one array and nothing in it needs to start at zero;
+ *   calls whose kernels overlap on the GPU (several streams, or threads on
+ *   one device) race on it, so serialise them.
+ */
+ps_status_t ps_decode_noalloc(const ps_cache_desc* cache, const void* q, const int32_t* pos,
+                              int32_t n_q_heads, float scale, void* out, float* lse,
+                              void* stream);
+
+/*
  * ps_prefill_workspace_size: device workspace for ps_prefill (rotated Q and K
  * and, with a ring, the gathered cached keys and values).
  *   ring_rows_max : 0 without a ring, else the ring's prefix_max + window.
