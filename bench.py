@@ -183,6 +183,12 @@ def decode_setup(ps, torch, seed, W, P, pos0, n_steps, full_causal=False):
 
 
 def run_decode(ps, torch, cache, q, k, v, pos, steps, warmup, dist=None, per_kernel=True):
+    """Times `steps` decode steps (append + partial + combine) after `warmup`.
+
+    The headline loop records no event between the kernels of a step, so
+    programmatic dependent launch can overlap their launches; a second pass over
+    the same inputs brackets each partial kernel with events for its own time.
+    Needs warmup + steps rows of per-step inputs."""
     nseq, hq, D = q.shape[1], q.shape[2], q.shape[3]
     out = torch.empty(nseq, hq, D, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(nseq, hq, dtype=torch.float32, device="cuda")
@@ -204,20 +210,27 @@ def run_decode(ps, torch, cache, q, k, v, pos, steps, warmup, dist=None, per_ker
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)] if per_kernel else None
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(steps):
-        step(warmup + i, evs[i] if evs else None)
+        step(warmup + i)
     e1.record(stream)
     torch.cuda.synchronize()
     total_ms = e0.elapsed_time(e1)
-    kern_ms = [a.elapsed_time(b) for a, b in evs] if evs else None
     if dist is not None:
         t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
+    kern_ms = None
+    if per_kernel:
+        # the same steps again (the ring's later slots are simply overwritten again):
+        # events around each partial kernel, on the stream it runs on
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            step(warmup + i, evs[i])
+        torch.cuda.synchronize()
+        kern_ms = [a.elapsed_time(b) for a, b in evs]
     return total_ms, kern_ms, out, lse
 
 
@@ -267,6 +280,27 @@ def flatness_leg(ps, torch, steps, seed, hbm_peak):
         r = decode_leg(ps, torch, f"p = {label}", P, W, pos0, steps, 3, seed, hbm_peak)
         out.append({"p": label, "live_slots_mean": r["live_slots_mean"], "step_ms": r["step_ms"],
                     "partial_kernel_ms": r["partial_kernel_ms"], "tok_s_per_layer": r["tok_s_per_layer"]})
+    return out
+
+
+def comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak):
+    """The same library on the same shapes with a plain sliding window (P = 0)
+    and a StreamingLLM-style 4-token sink (P = 4): decode at the steady-decode
+    shapes, prefill at the 32K prefill shape."""
+    d = DEC
+    out = {}
+    for name, pval in (("sliding_window_P0", 0), ("streaming_sink_P4", 4)):
+        P = np.full(d["nseq"], pval, dtype=np.int64)
+        r = decode_leg(ps, torch, f"decode, 64 x 131072, W 4096, P = {pval}", P, d["W"], d["pos0"],
+                       100, 5, seed + 11, hbm_peak)
+        rep = {"decode_tok_s_per_layer": r["tok_s_per_layer"], "decode_step_ms": r["step_ms"],
+               "decode_partial_ms": r["partial_kernel_ms"], "decode_partial_gbs": r["partial_gbs"]}
+        if not args.no_prefill:
+            pr = prefill_report(ps, torch, f"prefill 32768, W 4096, P = {pval}", 1, PRE["S"], pval,
+                                PRE["W"], args.prefill_steps, seed + 12, bf16_peak)
+            rep.update({"prefill_ms": pr["ms"], "prefill_tflops_algorithmic": pr["tflops_algorithmic"],
+                        "prefill_frac_of_measured_bf16": pr["frac_of_measured_bf16_burst"]})
+        out[name] = rep
     return out
 
 
@@ -516,10 +550,11 @@ def main():
         pre = {"unavailable": f"{type(e).__name__}: {e}"}
         train = None
 
-    ragged = flat = None
+    ragged = flat = comparators = None
     if not args.no_extra and (rank == 0 or world == 1):
         ragged = ragged_leg(ps, torch, 100, 4, hbm_peak)
         flat = flatness_leg(ps, torch, 20, seed, hbm_peak)
+        comparators = comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak)
 
     if not args.no_baselines and (rank == 0 or world == 1):
         fsteps = min(args.steps, 30)
@@ -561,6 +596,7 @@ def main():
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "frac_of_8tbs": achieved / 8000.0},
         "prefill": pre, "train_forward": train, "ragged_decode": ragged, "flatness": flat,
+        "comparators": comparators,
         "full_causal": full, "e2e": e2e,
         "gpu_launches": 3 * args.steps, "clocks": clk, "cpu_baseline": cpu,
     }

@@ -66,18 +66,28 @@ const char* ps_status_string(ps_status_t status);
 
 /*
  * The bounded KV cache ("伪代码" section: total cache size is the constant
- * prefix_len + W).  Sequence s owns pool rows [slot_base[s], slot_base[s] +
- * capacity).  Position pos of sequence s lives in row slot_base[s] + slot(pos):
+ * prefix_len + W).  Position pos of sequence s lives in its logical slot
  *     slot(pos) = pos                       if pos < P_s
  *               = P_s + (pos - P_s) mod W   otherwise,
  * so prefix slots never move and each window slot is overwritten exactly
  * when its previous occupant leaves the window.  After positions 0..p are
  * appended, slots [0, min(p+1, P_s+W)) hold exactly the keys query p may see.
+ * Logical slot -> pool row:
+ *   block_table == NULL: contiguous, row = slot_base[s] + slot; sequence s
+ *     owns rows [slot_base[s], slot_base[s] + capacity).
+ *   block_table != NULL: paged, as in paged-attention serving engines (the
+ *     papers.ananclaw.com explainer, section "对工程落地的启发", calls the
+ *     method orthogonal to paged KV memory management); row =
+ *     block_table[s * blocks_per_seq + slot / block_size] * block_size
+ *     + slot % block_size.  slot_base is not read and may be NULL.  Only the
+ *     blocks covering slots [0, P_s + W) are read or written.  A block id
+ *     outside the pool sets PS_DEV_BAD_SLOT; the access goes to block 0 or is
+ *     skipped, never outside the pool.
  */
 typedef struct ps_cache_desc {
   void* k_pool;              /* device bf16 [total_slots, n_kv_heads, head_dim], RoPE'd K */
   void* v_pool;              /* device bf16 [total_slots, n_kv_heads, head_dim], V        */
-  const int64_t* slot_base;  /* device [nseq]: first pool row of each sequence            */
+  const int64_t* slot_base;  /* device [nseq]: first pool row of each sequence (contiguous) */
   const int32_t* prefix_len; /* device [nseq]: P of each sequence, 0 <= P <= prefix_max   */
   int32_t* status;           /* device int32 status word, or NULL                         */
   int64_t total_slots;       /* rows in each pool                                          */
@@ -88,6 +98,9 @@ typedef struct ps_cache_desc {
   int32_t capacity;          /* rows reserved per sequence, >= prefix_max + window         */
   int32_t prefix_max;        /* host bound on every prefix_len                             */
   double rope_theta;         /* RoPE base, > 0                                             */
+  const int32_t* block_table; /* device int32 [nseq, blocks_per_seq], or NULL (contiguous) */
+  int32_t block_size;        /* paged: slots per block, a multiple of 16                   */
+  int32_t blocks_per_seq;    /* paged: >= ceil(capacity / block_size)                      */
 } ps_cache_desc;
 
 /*

@@ -38,14 +38,20 @@ def _need(t: torch.Tensor, dtype, name: str):
 class RingCache:
     """Bounded per-sequence K/V cache of ``prefix_max + window`` slots.
 
-    Pools are torch tensors of shape [nseq * capacity, n_kv_heads, head_dim];
+    Contiguous (default): pools of shape [nseq * capacity, n_kv_heads, head_dim];
     sequence s owns rows [s * capacity, (s + 1) * capacity).
+    Paged (``block_size`` given, a multiple of 16): the pools hold
+    ``nseq * blocks_per_seq`` blocks of ``block_size`` rows, and
+    ``block_table[s, i]`` names the block of the sequence's logical slots
+    [i * block_size, (i + 1) * block_size); ``block_order`` (a permutation of the
+    block ids, default identity) sets that assignment.
     """
 
     def __init__(self, nseq: int, n_kv_heads: int, head_dim: int, window: int,
                  prefix_len: Sequence[int] | torch.Tensor, rope_theta: float = 10000.0,
                  prefix_max: Optional[int] = None, capacity: Optional[int] = None,
-                 device="cuda", zero: bool = True):
+                 device="cuda", zero: bool = True, block_size: Optional[int] = None,
+                 block_order: Optional[Sequence[int]] = None):
         pl = torch.as_tensor(prefix_len, dtype=torch.int32).reshape(-1)
         if pl.numel() != nseq:
             raise ValueError("prefix_len must have nseq entries")
@@ -53,7 +59,20 @@ class RingCache:
         self.capacity = self.prefix_max + window if capacity is None else int(capacity)
         self.nseq, self.n_kv_heads, self.head_dim, self.window = nseq, n_kv_heads, head_dim, window
         self.rope_theta = float(rope_theta)
-        rows = nseq * self.capacity
+        self.block_size = block_size
+        if block_size is None:
+            rows = nseq * self.capacity
+            self.block_table = None
+            self.blocks_per_seq = 0
+        else:
+            self.blocks_per_seq = -(-self.capacity // block_size)
+            nblocks = nseq * self.blocks_per_seq
+            rows = nblocks * block_size
+            order = torch.arange(nblocks, dtype=torch.int32) if block_order is None else \
+                torch.as_tensor(block_order, dtype=torch.int32)
+            if sorted(order.tolist()) != list(range(nblocks)):
+                raise ValueError("block_order must be a permutation of the block ids")
+            self.block_table = order.reshape(nseq, self.blocks_per_seq).contiguous().to(device)
         alloc = torch.zeros if zero else torch.empty
         self.k_pool = alloc(rows, n_kv_heads, head_dim, dtype=BF16, device=device)
         self.v_pool = alloc(rows, n_kv_heads, head_dim, dtype=BF16, device=device)
@@ -66,7 +85,17 @@ class RingCache:
             slot_base=self.slot_base.data_ptr(), prefix_len=self.prefix_len.data_ptr(),
             status=self.status.data_ptr(), total_slots=rows, nseq=nseq, n_kv_heads=n_kv_heads,
             head_dim=head_dim, window=window, capacity=self.capacity, prefix_max=self.prefix_max,
-            rope_theta=self.rope_theta)
+            rope_theta=self.rope_theta,
+            block_table=None if self.block_table is None else self.block_table.data_ptr(),
+            block_size=block_size or 0, blocks_per_seq=self.blocks_per_seq)
+
+    def rows_of(self, seq: int) -> torch.Tensor:
+        """Pool rows of the sequence's logical slots 0..capacity-1, in slot order."""
+        slots = torch.arange(self.capacity, dtype=torch.int64)
+        if self.block_table is None:
+            return seq * self.capacity + slots
+        bt = self.block_table[seq].cpu().to(torch.int64)
+        return bt[slots // self.block_size] * self.block_size + slots % self.block_size
 
     # ------------------------------------------------------------ append ----
     def append(self, seq_idx: torch.Tensor, pos0: torch.Tensor, cu_tokens: torch.Tensor,

@@ -43,6 +43,9 @@ class CacheDesc(ctypes.Structure):
         ("capacity", ctypes.c_int32),
         ("prefix_max", ctypes.c_int32),
         ("rope_theta", ctypes.c_double),
+        ("block_table", ctypes.c_void_p),
+        ("block_size", ctypes.c_int32),
+        ("blocks_per_seq", ctypes.c_int32),
     ]
 
 

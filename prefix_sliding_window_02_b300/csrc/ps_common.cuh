@@ -30,6 +30,20 @@ __device__ __forceinline__ void rope_cos_sin(int32_t pos, unsigned long long F, 
   sincospif(x, &s, &c);
 }
 
+// Programmatic dependent launch.  The kernels of one call sequence are launched
+// so that a kernel may be scheduled while the previous kernel in the stream is
+// still running; each calls grid_dependency_wait() before it reads or writes
+// any memory that earlier stream work touches (the wait returns once every
+// earlier kernel has completed and its writes are visible; without the launch
+// attribute it returns at once), and allow_dependents() to let the next kernel
+// be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_flag(int32_t* status, int32_t bits) {
   if (status) atomicOr(status, bits);
 }
@@ -154,6 +168,29 @@ __device__ __forceinline__ float warp_sum(float x) {
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
 }
+
+// Pool row of a sequence's logical slot: contiguous from slot_base[s], or
+// through a block table (paged cache).
+struct SlotMap {
+  const int64_t* slot_base;    // contiguous layout (block_table == nullptr)
+  const int32_t* block_table;  // [nseq][blocks_per_seq] or nullptr
+  int64_t total_slots;
+  int32_t capacity, block_size, blocks_per_seq;
+
+  // contiguous layout: the sequence's rows lie inside the pool
+  __device__ __forceinline__ bool seq_ok(int s) const {
+    if (block_table) return true;
+    const int64_t sb = slot_base[s];
+    return sb >= 0 && sb + capacity <= total_slots;
+  }
+  // row of logical slot `slot`, or -1 if its block lies outside the pool
+  __device__ __forceinline__ int64_t row(int s, int32_t slot) const {
+    if (!block_table) return slot_base[s] + slot;
+    const int32_t blk = block_table[(int64_t)s * blocks_per_seq + slot / block_size];
+    if (blk < 0 || (int64_t)(blk + 1) * block_size > total_slots) return -1;
+    return (int64_t)blk * block_size + slot % block_size;
+  }
+};
 
 // Ring slot of an absolute position (prefix slots fixed, window slots rotate).
 __device__ __forceinline__ int32_t ring_slot(int32_t pos, int32_t P, int32_t W) {

@@ -14,8 +14,8 @@
 // one partial (unnormalised O, running max, running sum) per segment piece
 // it touches.  Piece (warp w, segment sg) goes to record w + sg, which is
 // unique because both indices only grow along the tile line; so NW + #segments
-// records suffice.  The combine kernel finds the warps covering a segment
-// from the same arithmetic.
+// records suffice.  The warps that take a segment's first and last tiles
+// record themselves, and the combine kernel merges the records in between.
 //
 // Inside a warp, lane l holds D/32 consecutive elements of every row.  For a
 // 16-row tile and two query heads the 32 partial dot products per lane are
@@ -35,13 +35,13 @@ struct DecodeParams {
   CUtensorMap tmv;
   const __nv_bfloat16* q;  // [nseq, Hq, D]
   const int32_t* pos;
-  const int64_t* slot_base;
   const int32_t* prefix_len;
   int32_t* status;
   int32_t* seg_tiles;  // workspace: [nseq + 1] exclusive prefix of tiles per sequence
+  int32_t* seg_warps;  // workspace: [nseq*Hkv][2] first and last warp of each segment
   float* rec;          // workspace: [NW + nseq*Hkv][rec_floats]
-  int64_t total_slots;
-  int32_t nseq, hq, hkv, window, capacity, prefix_max;
+  SlotMap map;
+  int32_t nseq, hq, hkv, window, prefix_max;
   int32_t nwarps_total;
   float scale_log2;  // softmax scale * log2(e)
   RopeTurns turns;
@@ -71,11 +71,6 @@ __device__ __forceinline__ int find_seq(const int32_t* pfx, int nseq, int hkv, i
     if ((int64_t)pfx[mid] * hkv <= g) lo = mid; else hi = mid - 1;
   }
   return lo;
-}
-
-// Warp owning global tile t when N tiles are split over NW warps.
-__device__ __forceinline__ int owner_warp(int64_t t, int64_t N, int64_t NW) {
-  return (int)(((t + 1) * NW + N - 1) / N - 1);
 }
 
 // Position on the tile line: tile t of kv head h of sequence s (nt tiles per head).
@@ -129,6 +124,17 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  if (lane == 0) {
+    for (int st = 0; st < STAGES; ++st) mbar_init(&bars[warp * STAGES + st], 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&p.tmk);
+    prefetch_tmap(&p.tmv);
+  }
+  grid_dependency_wait();  // the appended tokens and the workspace come from earlier work
+  allow_dependents();
+
   // 1) tiles per sequence and their exclusive prefix (warp 0, 32 sequences at a time)
   if (warp == 0) {
     int32_t run = 0;
@@ -137,11 +143,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
       int32_t n = 0;
       if (s < p.nseq) {
         const int32_t P = p.prefix_len[s], ps_ = p.pos[s];
-        const int64_t sb = p.slot_base[s];
         int32_t bad = 0;
         if (P < 0 || P > p.prefix_max) bad |= PS_DEV_BAD_PREFIX;
         if (ps_ < 0) bad |= PS_DEV_BAD_POS;
-        if (sb < 0 || sb + p.capacity > p.total_slots) bad |= PS_DEV_BAD_SLOT;
+        if (!p.map.seq_ok(s)) bad |= PS_DEV_BAD_SLOT;
         if (bad) {
           if (blockIdx.x == 0) set_flag(p.status, bad);
         } else {
@@ -160,14 +165,6 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     }
     if (lane == 0) pfx[p.nseq] = run;
   }
-  if (lane == 0) {
-    for (int st = 0; st < STAGES; ++st) mbar_init(&bars[warp * STAGES + st], 1);
-    fence_mbar_init();
-  }
-  if (threadIdx.x == 0) {
-    prefetch_tmap(&p.tmk);
-    prefetch_tmap(&p.tmv);
-  }
   __syncthreads();
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i <= p.nseq; i += blockDim.x) p.seg_tiles[i] = pfx[i];
@@ -185,7 +182,12 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
   const uint64_t pol = policy_evict_first();
   TileIter nxt;  // next tile to request (lane 0 only)
   auto issue = [&](int st) {
-    const int32_t row0 = (int32_t)(p.slot_base[nxt.s] + (int64_t)nxt.t * TS);
+    int64_t r = p.map.row(nxt.s, nxt.t * TS);  // a tile never straddles a block
+    if (r < 0) {  // block outside the pool: flag it and read block 0 instead
+      set_flag(p.status, PS_DEV_BAD_SLOT);
+      r = 0;
+    }
+    const int32_t row0 = (int32_t)r;
     uint64_t* bar = &my_bars[st];
     uint8_t* dst = my_tiles + st * S::STAGE_BYTES;
     mbar_arrive_expect_tx(bar, S::STAGE_BYTES);
@@ -211,6 +213,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
 
   for (; cur.g < hi; cur.next(pfx, p.nseq, p.hkv)) {
     const int s = cur.s, h = cur.h, t = cur.t;
+    if (lane == 0) {  // segment ends: the combine reads its warps from here
+      if (t == 0) p.seg_warps[2 * ((int64_t)s * p.hkv + h)] = w;
+      if (t == cur.nt - 1) p.seg_warps[2 * ((int64_t)s * p.hkv + h) + 1] = w;
+    }
     if (cur.g == lo || t == 0) {
       // new segment piece: rotate the group's queries at position pos[s]
       const int32_t ppos = p.pos[s];
@@ -379,18 +385,22 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
 struct CombineParams {
   const float* rec;
   const int32_t* seg_tiles;
+  const int32_t* seg_warps;
   __nv_bfloat16* out;  // [nseq, Hq, D]
   float* lse;          // [nseq, Hq]
   int32_t nseq, hq, hkv, nwarps_total;
 };
 
 // One warp per (sequence, query head): merge the partial softmax records of the
-// warps that covered its segment.
+// warps that covered its segment, first to last as the partial kernel
+// recorded them, in one pass with a running maximum (all loads independent).
 template <int D, int G>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ CombineParams p) {
   using S = DecShape<D, G>;
   constexpr int EPL = S::EPL;
   const int lane = threadIdx.x & 31;
+  grid_dependency_wait();  // the partial records come from the previous kernel
+  allow_dependents();
   const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
   if (gw >= (int64_t)p.nseq * p.hq) return;
   const int s = (int)(gw / p.hq), hq = (int)(gw % p.hq);
@@ -403,27 +413,27 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
     if (lane == 0) p.lse[gw] = -INFINITY;
     return;
   }
-  const int64_t N = (int64_t)p.seg_tiles[p.nseq] * p.hkv;
-  const int64_t start = (int64_t)p.seg_tiles[s] * p.hkv + (int64_t)h * nt;
-  const int w0 = owner_warp(start, N, p.nwarps_total);
-  const int w1 = owner_warp(start + nt - 1, N, p.nwarps_total);
   const int64_t sg = (int64_t)s * p.hkv + h;
+  const int w0 = p.seg_warps[2 * sg], w1 = p.seg_warps[2 * sg + 1];
+  const int64_t N = (int64_t)p.seg_tiles[p.nseq] * p.hkv;
   const int64_t NW = p.nwarps_total;
-  // warps between w0 and w1 that own no tile at all (possible when N < NW)
-  // wrote no record
-  auto owns_tiles = [&](int w) { return N * w / NW < N * (w + 1) / NW; };
-  float M = -INFINITY;
-  for (int w = w0; w <= w1; ++w)
-    if (owns_tiles(w)) M = fmaxf(M, p.rec[(size_t)(w + sg) * S::REC + G * D + gg]);
-  float a[EPL] = {};
-  float l = 0.f;
+  // with fewer tiles than warps, warps between w0 and w1 may own no tile and
+  // wrote no record; otherwise every warp owns at least one
+  const bool dense = N >= NW;
+  float M = -INFINITY, l = 0.f, a[EPL] = {};
   for (int w = w0; w <= w1; ++w) {
-    if (!owns_tiles(w)) continue;
+    if (!dense && N * w / NW == N * (w + 1) / NW) continue;
     const float* r = p.rec + (size_t)(w + sg) * S::REC;
-    const float f = fast_exp2(r[G * D + gg] - M);
-    l = fmaf(f, r[G * D + G + gg], l);
+    const float mw = r[G * D + gg], lw = r[G * D + G + gg];
+    float aw[EPL];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) a[e] = fmaf(f, r[gg * D + lane * EPL + e], a[e]);
+    for (int e = 0; e < EPL; ++e) aw[e] = r[gg * D + lane * EPL + e];
+    const float mn = fmaxf(M, mw);
+    const float f_old = fast_exp2(M - mn), f_new = fast_exp2(mw - mn);
+    l = l * f_old + lw * f_new;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) a[e] = a[e] * f_old + aw[e] * f_new;
+    M = mn;
   }
   const float inv = 1.f / l;
 #pragma unroll
@@ -484,7 +494,7 @@ static bool make_plan(int D, int G, int nseq, DecPlan* pl) {
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 static size_t dec_ws_bytes(const DecPlan& pl, int nseq, int hkv) {
-  return align256((size_t)(nseq + 1) * 4) +
+  return align256((size_t)(nseq + 1) * 4) + align256((size_t)nseq * hkv * 2 * 4) +
          (size_t)(pl.nwarps + (size_t)nseq * hkv) * pl.rec_floats * 4;
 }
 
@@ -528,8 +538,13 @@ static ps_status_t prepare_decode(const ps_cache_desc* cache, int32_t n_q_heads,
   return PS_OK;
 }
 
-static float* records_of(void* ws, int nseq) {
-  return reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256((size_t)(nseq + 1) * 4));
+static int32_t* seg_warps_of(void* ws, int nseq) {
+  return reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + align256((size_t)(nseq + 1) * 4));
+}
+
+static float* records_of(void* ws, int nseq, int hkv) {
+  return reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256((size_t)(nseq + 1) * 4) +
+                                  align256((size_t)nseq * hkv * 2 * 4));
 }
 
 extern "C" ps_status_t ps_decode_partial(const ps_cache_desc* cache, const void* q,
@@ -552,22 +567,23 @@ extern "C" ps_status_t ps_decode_partial(const ps_cache_desc* cache, const void*
     return PS_ERR_CUDA;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.pos = pos;
-  p.slot_base = cache->slot_base;
   p.prefix_len = cache->prefix_len;
   p.status = cache->status;
   p.seg_tiles = static_cast<int32_t*>(workspace);
-  p.rec = records_of(workspace, nseq);
-  p.total_slots = cache->total_slots;
+  p.seg_warps = seg_warps_of(workspace, nseq);
+  p.rec = records_of(workspace, nseq, hkv);
+  p.map = slot_map(cache);
   p.nseq = nseq;
   p.hq = n_q_heads;
   p.hkv = hkv;
   p.window = cache->window;
-  p.capacity = cache->capacity;
   p.prefix_max = cache->prefix_max;
   p.nwarps_total = pl.nwarps;
   p.scale_log2 = scale * 1.4426950408889634f;
   make_rope_turns(cache->rope_theta, D, &p.turns);
-  pl.partial<<<pl.grid, kDecWarps * 32, pl.smem, (cudaStream_t)stream>>>(p);
+  if (launch_dependent(pl.partial, dim3(pl.grid), dim3(kDecWarps * 32), pl.smem,
+                       (cudaStream_t)stream, p) != cudaSuccess)
+    return PS_ERR_CUDA;
   return launch_status();
 }
 
@@ -581,8 +597,9 @@ extern "C" ps_status_t ps_decode_combine(const ps_cache_desc* cache, int32_t n_q
   if (!aligned16(out)) return PS_ERR_ALIGNMENT;
   const int nseq = cache->nseq;
   CombineParams c;
-  c.rec = records_of(const_cast<void*>(workspace), nseq);
+  c.rec = records_of(const_cast<void*>(workspace), nseq, cache->n_kv_heads);
   c.seg_tiles = static_cast<const int32_t*>(workspace);
+  c.seg_warps = seg_warps_of(const_cast<void*>(workspace), nseq);
   c.out = static_cast<__nv_bfloat16*>(out);
   c.lse = lse;
   c.nseq = nseq;
@@ -590,7 +607,9 @@ extern "C" ps_status_t ps_decode_combine(const ps_cache_desc* cache, int32_t n_q
   c.hkv = cache->n_kv_heads;
   c.nwarps_total = pl.nwarps;
   const int64_t warps = (int64_t)nseq * n_q_heads;
-  pl.combine<<<(unsigned)((warps + 3) / 4), 128, 0, (cudaStream_t)stream>>>(c);
+  if (launch_dependent(pl.combine, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0,
+                       (cudaStream_t)stream, c) != cudaSuccess)
+    return PS_ERR_CUDA;
   return launch_status();
 }
 

@@ -54,6 +54,17 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
   return r == CUDA_SUCCESS;
 }
 
+SlotMap slot_map(const ps_cache_desc* c) {
+  SlotMap m;
+  m.slot_base = c->slot_base;
+  m.block_table = c->block_table;
+  m.total_slots = c->total_slots;
+  m.capacity = c->capacity;
+  m.block_size = c->block_table ? c->block_size : 0;
+  m.blocks_per_seq = c->block_table ? c->blocks_per_seq : 0;
+  return m;
+}
+
 int device_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -62,8 +73,14 @@ int device_sm_count() {
 }
 
 ps_status_t check_cache(const ps_cache_desc* c) {
-  if (!c || !c->k_pool || !c->v_pool || !c->slot_base || !c->prefix_len)
+  if (!c || !c->k_pool || !c->v_pool || !c->prefix_len) return PS_ERR_INVALID_ARGUMENT;
+  if (c->block_table) {
+    if (c->block_size < 16 || c->block_size % 16 || c->blocks_per_seq < 1 ||
+        (int64_t)c->blocks_per_seq * c->block_size < (int64_t)c->capacity)
+      return PS_ERR_INVALID_ARGUMENT;
+  } else if (!c->slot_base) {
     return PS_ERR_INVALID_ARGUMENT;
+  }
   if (c->nseq < 1 || c->n_kv_heads < 1 || c->window < 1 || c->prefix_max < 0 ||
       c->total_slots < 1 || c->total_slots > 0x7fffffffLL || !(c->rope_theta > 0.0))
     return PS_ERR_INVALID_ARGUMENT;

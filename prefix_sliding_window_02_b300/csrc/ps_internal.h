@@ -20,11 +20,32 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
 
 int device_sm_count();  // SM count of the current device (0 on failure)
 
+// Launches `kernel` with programmatic stream serialisation: it may be scheduled
+// before the previous kernel in `stream` completes (see grid_dependency_wait).
+template <typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline ps_status_t launch_status() {
   return cudaGetLastError() == cudaSuccess ? PS_OK : PS_ERR_CUDA;
 }
+
+// Logical-slot -> pool-row map of a cache descriptor (contiguous or paged).
+SlotMap slot_map(const ps_cache_desc* c);
 
 // Validates the host-visible fields of a cache descriptor.
 ps_status_t check_cache(const ps_cache_desc* c);

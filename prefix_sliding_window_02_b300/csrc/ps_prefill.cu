@@ -53,11 +53,10 @@ struct GatherParams {
   // ring (null k_pool = no ring)
   const uint4* k_pool;
   const uint4* v_pool;
-  const int64_t* slot_base;
   const int32_t* ring_prefix;
   const int32_t* ring_seq;
-  int64_t total_slots;
-  int32_t nseq, capacity;
+  SlotMap map;
+  int32_t nseq;
   int32_t B, S, Skv, hq, hkv, W;
   RopeTurns turns;
 };
@@ -89,6 +88,8 @@ constexpr int kRopeRows = 4;  // chunk rows per block iteration (256 threads: 4 
 __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant__ GatherParams p) {
   constexpr int VEC = 16, HALFV = 8;
   __shared__ float2 cs[kRopeRows][64];
+  grid_dependency_wait();  // inputs and workspace may be in use by earlier stream work
+  allow_dependents();      // the tile kernel may set up meanwhile; it waits for this one
   const bool ring = p.k_pool != nullptr;
   const int64_t n_rows = (int64_t)p.B * p.S;
   const int64_t n_groups = (n_rows + kRopeRows - 1) / kRopeRows;
@@ -172,14 +173,18 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
       if (bad) {
         set_flag(p.status, PS_DEV_BAD_SEQ);
       } else {
-        const int64_t sb = p.slot_base[s];
         if (p.ring_prefix[s] != P) { set_flag(p.status, PS_DEV_BAD_PREFIX); bad = true; }
-        if (sb < 0 || sb + p.capacity > p.total_slots) { set_flag(p.status, PS_DEV_BAD_SLOT); bad = true; }
+        if (!p.map.seq_ok(s)) { set_flag(p.status, PS_DEV_BAD_SLOT); bad = true; }
         if (!bad) {
           const int32_t pos = key_pos(km, kidx);
-          const int64_t src = ((sb + ring_slot(pos, P, p.W)) * p.hkv + h) * VEC + vec;
-          kk = p.k_pool[src];
-          vv = p.v_pool[src];
+          const int64_t r = p.map.row(s, ring_slot(pos, P, p.W));
+          if (r < 0) {
+            set_flag(p.status, PS_DEV_BAD_SLOT);
+          } else {
+            const int64_t src = (r * p.hkv + h) * VEC + vec;
+            kk = p.k_pool[src];
+            vv = p.v_pool[src];
+          }
         }
       }
     }
@@ -207,7 +212,7 @@ struct PrefillParams {
   const int32_t* q_start;
   const int32_t* prefix_len;
   int32_t* status;
-  int32_t S, hq, hkv, W, with_ring, nq;
+  int32_t S, hq, hkv, W, with_ring, nq, B;
   float scale_log2;
 };
 
@@ -267,6 +272,7 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem, tO = tmem + 128;
+  grid_dependency_wait();  // rotated Q / K come from the pre-pass
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 
   const uint64_t pol_q = policy_evict_first();
@@ -465,15 +471,17 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------
-// 3. warp-specialised tile kernel for a pair of query heads that share one KV
-//    head (the GQA group size is even).
+// 3. warp-specialised, persistent tile kernel for pairs of query heads that
+//    share one KV head (the GQA group size is even).
 //
-// One CTA = one 128-row query tile of two query heads.  Both heads admit the
-// same (query, key) pairs, so they walk the same key tiles and every K/V tile
-// staged in shared memory feeds two 128x128 products.  Roles:
+// A work item is one 128-row query tile of two query heads of one batch row.
+// Both heads admit the same (query, key) pairs, so they walk the same key
+// tiles and every K/V tile staged in shared memory feeds two 128x128
+// products.  One CTA per SM walks the items longest-first in a static
+// round-robin.  Roles:
 //   warps 0-3  softmax, rescale and epilogue of head 0 (one thread per row)
 //   warps 4-7  the same for head 1
-//   warp 8     TMA producer (Q once, then K / V tiles through two rings)
+//   warp 8     TMA producer (Q per item, then K / V tiles through two rings)
 //   warp 9     tcgen05 issuer
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each.  Each softmax
 // thread writes its row of probabilities as bf16 over the first 64 columns of
@@ -481,7 +489,11 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
 // touches shared memory.  The issuer interleaves the heads: P_0 V, S_0 = Q_0 K,
 // P_1 V, S_1 = Q_1 K, so one head's softmax overlaps the other head's MMAs.
 // Tensor-core instructions of one thread run in issue order, which is what
-// lets S_i(j+1) overwrite the columns P_i(j) V has just read.
+// lets S_i(j+1) overwrite the columns P_i(j) V has just read.  Across items,
+// the next Q is loaded once the last Q K of the current item completes
+// (q_empty), and the next item's first P V waits until the epilogue has read
+// O out of tensor memory (o_free), so the next item's loads and first Q K
+// overlap the current epilogue.  Barrier phases run on across items.
 // ---------------------------------------------------------------------------
 namespace ws {
 
@@ -491,10 +503,10 @@ constexpr int kSmem = (2 + kStK + kStV) * kTile + 1024 /*barriers*/ + 1024 /*ali
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint64_t k_full[kStK], k_empty[kStK];
   uint64_t v_full[kStV], v_empty[kStV];
-  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint32_t tmem_slot;
   int32_t abort;
 };
@@ -514,33 +526,68 @@ __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile in
   }
 }
 
-}  // namespace ws
+// One work item and the key tiles it visits: the prefix tiles, then the band
+// of tiles that can hold window keys of some row of the item.
+struct Item {
+  int qt, h0, hk, b;
+  int32_t c0, P, q0r, q1r;
+  int64_t q0, q1;
+  KeyMap km;
+  int t1_end, t2_begin, n_tiles;
+  __device__ __forceinline__ int tile_at(int j) const {
+    return j < t1_end ? j : t2_begin + (j - t1_end);
+  }
+};
 
-// 2^x on the FMA pipe, for x <= 0, to take part of the exponentials off the
-// MUFU unit.  Cody-Waite style split x = n + f with n = round(x) (the 1.5 * 2^23
-// addition rounds to an integer), f in [-1/2, 1/2]; 2^f by a cubic fitted here
-// for least relative error on that interval (max relative error 7.5e-5, far
-// below the bf16 rounding P gets next); 2^n added into the exponent field.
-// Inputs below -126 are clamped there, so masked (-inf) scores give about
-// 1e-38 rather than 0, which no sum or bf16 product can notice.
-__device__ __forceinline__ float exp2_fma(float x) {
-  x = fmaxf(x, -126.f);
-  const float t = x + 12582912.f;  // 1.5 * 2^23
-  const float f = x - (t - 12582912.f);
-  float q = fmaf(0.05517168715596199f, f, 0.2426111400127411f);
-  q = fmaf(q, f, 0.6932609677314758f);
-  q = fmaf(q, f, 0.9999280571937561f);
-  return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
+__device__ __forceinline__ Item make_item(const PrefillParams& p, int u) {
+  Item it;
+  const int npairs = p.hq / 2;
+  const int per_qt = npairs * p.B;
+  it.qt = p.nq - 1 - u / per_qt;  // longest rows first
+  const int rem = u % per_qt;
+  it.h0 = 2 * (rem % npairs);
+  it.b = rem / npairs;
+  it.hk = it.h0 / (p.hq / p.hkv);
+  it.c0 = p.q_start[it.b];
+  it.P = p.prefix_len[it.b];
+  it.km = make_keymap(p.S, it.c0, it.P, p.W, p.with_ring != 0);
+  it.q0r = it.qt * kBM;
+  it.q1r = min(p.S, it.q0r + kBM) - 1;
+  it.q0 = (int64_t)it.c0 + it.q0r;
+  it.q1 = (int64_t)it.c0 + it.q1r;
+  const int32_t kc = keys_below(it.km, it.q1 + 1);
+  const int32_t kP = keys_below(it.km, it.P);
+  it.t1_end = (min(kP, kc) + kBN - 1) / kBN;
+  const int32_t kw = keys_below(it.km, it.q0 - p.W + 1);
+  it.t2_begin = max(it.t1_end, kw / kBN);
+  const int t2_end = (kc + kBN - 1) / kBN;
+  it.n_tiles = it.t1_end + max(0, t2_end - it.t2_begin);
+  return it;
 }
 
-// Columns whose exponential goes through exp2_fma instead of ex2.approx: every
-// kPolyEvery-th pair of columns (0 = none).
-constexpr int kPolyEvery = 0;
+}  // namespace ws
 
-// c is a constant after unrolling, so the choice folds away.
-__device__ __forceinline__ float exp2_col(int c, float x) {
-  if (kPolyEvery > 0 && (c / 2) % kPolyEvery == kPolyEvery - 1) return exp2_fma(x);
-  return ex2(x);
+// Packed fp32x2 arithmetic and the three-input max of sm_100+: two elements
+// (or two new candidates) per instruction on the softmax critical path.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                      float c0, float c1) {
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // One query row's share of a 128-key tile: S from TMEM, optional element mask
@@ -550,7 +597,9 @@ __device__ __forceinline__ float exp2_col(int c, float x) {
 // the bf16-rounded ones instead moves the LSE of rows with few keys by up to
 // a bf16 rounding (2e-3).  Returns the factor O must be scaled by (1 = none).
 // The masked and unmasked variants are whole functions so that the 128 scores
-// are never live across a branch.
+// are never live across a branch.  Max, scale and sum use independent chains
+// of three-input and packed instructions: this per-row chain, S -> P, is what
+// the other head's MMAs have to cover.
 template <bool MASK>
 __device__ __forceinline__ float softmax_tile(uint32_t tS, int j, float scale_log2, int32_t A1,
                                               int32_t B0, int32_t B1, float& m_used, float& l) {
@@ -577,15 +626,13 @@ __device__ __forceinline__ float softmax_tile(uint32_t tS, int j, float scale_lo
       s[c] = keep ? s[c] : -INFINITY;
     }
   }
-  // row max as a tree of independent chains (a single running max would be a
-  // 127-deep dependent chain on the critical path between S and P)
   float mx8[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) mx8[c] = s[c];
 #pragma unroll
-  for (int c = 8; c < kBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-  const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+  for (int c = 8; c < kBN; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], s[c], s[c + 1]);
+  const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                         fmaxf(mx8[6], mx8[7]));
   const float m_new = fmaxf(m_used, mx * scale_log2);
   float alpha = 1.f;
   if (j == 0) {
@@ -594,26 +641,30 @@ __device__ __forceinline__ float softmax_tile(uint32_t tS, int j, float scale_lo
     alpha = ex2(m_used - m_new);
     m_used = m_new;
   }
-  const float mu = m_used == -INFINITY ? 0.f : m_used;
-  float rs4[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+  const float nmu = m_used == -INFINITY ? 0.f : -m_used;
+  float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // four packed partial sums
   uint32_t p0[32], p1[32];
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
-    const float x = exp2_col(2 * c, fmaf(s[2 * c], scale_log2, -mu));
-    const float y = exp2_col(2 * c + 1, fmaf(s[2 * c + 1], scale_log2, -mu));
+    float x, y;
+    ffma2(x, y, s[2 * c], s[2 * c + 1], scale_log2, scale_log2, nmu, nmu);
+    x = ex2(x);
+    y = ex2(y);
     p0[c] = pack_bf16(x, y);
-    rs4[c & 3] += x + y;
+    fadd2(rs[2 * (c & 3)], rs[2 * (c & 3) + 1], rs[2 * (c & 3)], rs[2 * (c & 3) + 1], x, y);
   }
   tc::st32(tS, p0);
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
-    const float x = exp2_col(64 + 2 * c, fmaf(s[64 + 2 * c], scale_log2, -mu));
-    const float y = exp2_col(64 + 2 * c + 1, fmaf(s[64 + 2 * c + 1], scale_log2, -mu));
+    float x, y;
+    ffma2(x, y, s[64 + 2 * c], s[64 + 2 * c + 1], scale_log2, scale_log2, nmu, nmu);
+    x = ex2(x);
+    y = ex2(y);
     p1[c] = pack_bf16(x, y);
-    rs4[c & 3] += x + y;
+    fadd2(rs[2 * (c & 3)], rs[2 * (c & 3) + 1], rs[2 * (c & 3)], rs[2 * (c & 3) + 1], x, y);
   }
   tc::st32(tS + 32, p1);
-  l = fmaf(l, alpha, (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+  l = fmaf(l, alpha, ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
   return alpha;
 }
 
@@ -630,23 +681,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
   volatile int32_t* abort = &bar->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qt = p.nq - 1 - (int)blockIdx.x;  // longest rows first
-  const int h0 = 2 * blockIdx.y, b = blockIdx.z;
-  const int hk = h0 / (p.hq / p.hkv);
-  const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
-  const KeyMap km = make_keymap(p.S, c0, P, p.W, p.with_ring != 0);
-  const int32_t q0r = qt * kBM, q1r = min(p.S, q0r + kBM) - 1;
-  const int64_t q0 = (int64_t)c0 + q0r, q1 = (int64_t)c0 + q1r;
-
-  // key tiles that can hold an admitted pair: the prefix tiles, then the band
-  const int32_t kc = keys_below(km, q1 + 1);
-  const int32_t kP = keys_below(km, P);
-  const int t1_end = (min(kP, kc) + kBN - 1) / kBN;
-  const int32_t kw = keys_below(km, q0 - p.W + 1);
-  const int t2_begin = max(t1_end, kw / kBN);
-  const int t2_end = (kc + kBN - 1) / kBN;
-  const int n_tiles = t1_end + max(0, t2_end - t2_begin);
-  auto tile_at = [&](int it) { return it < t1_end ? it : t2_begin + (it - t1_end); };
+  const int n_items = p.nq * (p.hq / 2) * p.B;
 
   if (warp == 0) {
     tc::alloc(smem_u32(&bar->tmem_slot), 512);
@@ -654,6 +689,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
   }
   if (tid == 32) {
     mbar_init(&bar->q_full, 1);
+    mbar_init(&bar->q_empty, 1);
     for (int s = 0; s < kStK; ++s) {
       mbar_init(&bar->k_full[s], 1);
       mbar_init(&bar->k_empty[s], 1);
@@ -664,8 +700,9 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
-      mbar_init(&bar->p_full[i], 128);
+      mbar_init(&bar->p_full[i], 4);  // one arrival per softmax warp
       mbar_init(&bar->o_done[i], 1);
+      mbar_init(&bar->o_free[i], 4);
     }
     bar->abort = 0;
     fence_mbar_init();
@@ -674,8 +711,12 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = bar->tmem_slot;
+  grid_dependency_wait();  // rotated Q / K come from the pre-pass
 
-  if (n_tiles > 0 && warp == kProducerWarp) {
+  // Every role walks the same item sequence; items without tiles (only
+  // possible for invalid inputs) are skipped by all of them alike.
+  // g counts key tiles and k items processed so far: barrier phases follow them.
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&p.tmq);
@@ -683,141 +724,183 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       prefetch_tmap(&p.tmv);
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      mbar_arrive_expect_tx(&bar->q_full, 2 * kTile);
-      for (int i = 0; i < 2; ++i) {
-        tma_load_4d(sQ + i * kTile, &p.tmq, &bar->q_full, 0, h0 + i, q0r, b, pol_q);
-        tma_load_4d(sQ + i * kTile + kHalf, &p.tmq, &bar->q_full, 64, h0 + i, q0r, b, pol_q);
-      }
-      for (int j = 0; j < n_tiles; ++j) {
-        const int kt = tile_at(j);
-        const int sk = j % kStK, sv = j % kStV;
-        if (!wait(&bar->k_empty[sk], ((j / kStK) & 1) ^ 1, abort)) break;
-        uint8_t* dk = sK + sk * kTile;
-        mbar_arrive_expect_tx(&bar->k_full[sk], kTile);
-        tma_load_4d(dk, &p.tmk, &bar->k_full[sk], 0, hk, kt * kBN, b, pol_kv);
-        tma_load_4d(dk + kHalf, &p.tmk, &bar->k_full[sk], 64, hk, kt * kBN, b, pol_kv);
-        if (!wait(&bar->v_empty[sv], ((j / kStV) & 1) ^ 1, abort)) break;
-        uint8_t* dv = sV + sv * kTile;
-        mbar_arrive_expect_tx(&bar->v_full[sv], kTile);
-        tma_load_4d(dv, &p.tmv, &bar->v_full[sv], 0, hk, kt * kBN, b, pol_kv);
-        tma_load_4d(dv + kHalf, &p.tmv, &bar->v_full[sv], 64, hk, kt * kBN, b, pol_kv);
+      int g = 0, k = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < n_items; u += gridDim.x) {
+        const Item it = make_item(p, u);
+        if (it.n_tiles <= 0) continue;
+        if (!(ok = wait(&bar->q_empty, (k & 1) ^ 1, abort))) break;  // previous item's Q K done
+        mbar_arrive_expect_tx(&bar->q_full, 2 * kTile);
+        for (int i = 0; i < 2; ++i) {
+          tma_load_4d(sQ + i * kTile, &p.tmq, &bar->q_full, 0, it.h0 + i, it.q0r, it.b, pol_q);
+          tma_load_4d(sQ + i * kTile + kHalf, &p.tmq, &bar->q_full, 64, it.h0 + i, it.q0r, it.b,
+                      pol_q);
+        }
+        for (int j = 0; j < it.n_tiles; ++j) {
+          const int gj = g + j, kt = it.tile_at(j);
+          const int sk = gj % kStK, sv = gj % kStV;
+          if (!(ok = wait(&bar->k_empty[sk], ((gj / kStK) & 1) ^ 1, abort))) break;
+          uint8_t* dk = sK + sk * kTile;
+          mbar_arrive_expect_tx(&bar->k_full[sk], kTile);
+          tma_load_4d(dk, &p.tmk, &bar->k_full[sk], 0, it.hk, kt * kBN, it.b, pol_kv);
+          tma_load_4d(dk + kHalf, &p.tmk, &bar->k_full[sk], 64, it.hk, kt * kBN, it.b, pol_kv);
+          if (!(ok = wait(&bar->v_empty[sv], ((gj / kStV) & 1) ^ 1, abort))) break;
+          uint8_t* dv = sV + sv * kTile;
+          mbar_arrive_expect_tx(&bar->v_full[sv], kTile);
+          tma_load_4d(dv, &p.tmv, &bar->v_full[sv], 0, it.hk, kt * kBN, it.b, pol_kv);
+          tma_load_4d(dv + kHalf, &p.tmv, &bar->v_full[sv], 64, it.hk, kt * kBN, it.b, pol_kv);
+        }
+        g += it.n_tiles;
+        ++k;
       }
     }
     __syncwarp();
-  } else if (n_tiles > 0 && warp == kMmaWarp) {
+  } else if (warp == kMmaWarp) {
     // -------------------------------------------------------------- issuer
     if (lane == 0) {
       const uint32_t aq = smem_u32(sQ);
+      // Descriptors are built once: moving a descriptor by `off` bytes adds
+      // off / 16 to its start-address field (shared addresses stay below 256 KB,
+      // so the 14-bit field never carries), which keeps the issue of the 16
+      // products of a step off the critical path.
+      const uint64_t dq = tc::sdesc_sw128(aq, 16, 1024);
+      const uint64_t dk = tc::sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dv = tc::sdesc_sw128(smem_u32(sV), kHalf, 1024);
       auto qk = [&](int i, int sk) {
-        const uint32_t a = aq + i * kTile, k = smem_u32(sK + sk * kTile);
+        const uint64_t a = dq + (uint64_t)((i * kTile) >> 4), b = dk + (uint64_t)((sk * kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc::mma_bf16(tmem + i * 128, tc::sdesc_sw128(a + off, 16, 1024),
-                       tc::sdesc_sw128(k + off, 16, 1024), kIdescQK, kk > 0);
+          const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+          tc::mma_bf16(tmem + i * 128, a + off, b + off, kIdescQK, kk > 0);
         }
         tc::commit(smem_u32(&bar->s_full[i]));
       };
       auto pv = [&](int i, int sv, bool acc) {
-        const uint32_t av = smem_u32(sV + sv * kTile);
+        const uint64_t b = dv + (uint64_t)((sv * kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          tc::mma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
-                          tc::sdesc_sw128(av + kk * 2048, kHalf, 1024), kIdescPV, acc || kk > 0);
+          tc::mma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, b + ((kk * 2048) >> 4),
+                          kIdescPV, acc || kk > 0);
       };
-      bool ok = wait(&bar->q_full, 0, abort);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int sk = j % kStK;
-        if (!(ok = wait(&bar->k_full[sk], (j / kStK) & 1, abort))) break;
+      // P_i V of tile gt (the item's jt-th); its first one overwrites O_i, which
+      // must wait until the previous item's epilogue has read O_i out
+      auto pv_step = [&](int i, int gt, int jt, int k) -> bool {
+        const int sv = gt % kStV;
+        if (!wait(&bar->p_full[i], gt & 1, abort)) return false;
+        if (i == 0 && !wait(&bar->v_full[sv], (gt / kStV) & 1, abort)) return false;
+        if (jt == 0 && !wait(&bar->o_free[i], (k & 1) ^ 1, abort)) return false;
         tc::fence_after();
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (j > 0) {
-            const int sv = (j - 1) % kStV;
-            if (!(ok = wait(&bar->p_full[i], (j - 1) & 1, abort))) break;
-            if (i == 0 && !(ok = wait(&bar->v_full[sv], ((j - 1) / kStV) & 1, abort))) break;
-            tc::fence_after();
-            pv(i, sv, j > 1);
-            if (i == 1) tc::commit(smem_u32(&bar->v_empty[sv]));
-          }
-          qk(i, sk);
-        }
-        if (ok) tc::commit(smem_u32(&bar->k_empty[sk]));
-      }
-      if (ok) {
-        const int j = n_tiles;
-        const int sv = (j - 1) % kStV;
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (!(ok = wait(&bar->p_full[i], (j - 1) & 1, abort))) break;
-          if (i == 0 && !(ok = wait(&bar->v_full[sv], ((j - 1) / kStV) & 1, abort))) break;
+        pv(i, sv, jt > 0);
+        if (i == 1) tc::commit(smem_u32(&bar->v_empty[sv]));
+        return true;
+      };
+      int g = 0, k = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < n_items; u += gridDim.x) {
+        const Item it = make_item(p, u);
+        const int n = it.n_tiles;
+        if (n <= 0) continue;
+        if (!(ok = wait(&bar->q_full, k & 1, abort))) break;
+        for (int j = 0; ok && j < n; ++j) {
+          const int gj = g + j, sk = gj % kStK;
+          if (!(ok = wait(&bar->k_full[sk], (gj / kStK) & 1, abort))) break;
           tc::fence_after();
-          pv(i, sv, j > 1);
+          for (int i = 0; i < 2 && ok; ++i) {
+            if (j > 0 && !(ok = pv_step(i, gj - 1, j - 1, k))) break;
+            qk(i, sk);
+          }
+          if (!ok) break;
+          tc::commit(smem_u32(&bar->k_empty[sk]));
+        }
+        if (!ok) break;
+        tc::commit(smem_u32(&bar->q_empty));  // every Q K of this item is issued
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (!(ok = pv_step(i, g + n - 1, n - 1, k))) break;
           tc::commit(smem_u32(&bar->o_done[i]));
         }
+        g += n;
+        ++k;
       }
     }
     __syncwarp();
-  } else if (n_tiles > 0 && warp < 8) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------- softmax
     const int i = warp >> 2;                 // head of the pair
     const int row = tid & 127;               // TMEM lane = query row in the tile
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + i * 128 + lane_off, tO = tmem + 256 + i * 128 + lane_off;
-    const int64_t qpos = q0 + row;
-    // admitted key positions of this row: [0, min(P, qpos+1)) and [max(0, qpos-W+1), qpos]
-    const int32_t a1 = keys_below(km, min((int64_t)P, qpos + 1));
-    const int32_t b0 = keys_below(km, max((int64_t)0, qpos - p.W + 1));
-    const int32_t b1 = keys_below(km, qpos + 1);
-    float m_used = -INFINITY, l = 0.f;
+    int g = 0, k = 0;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      ok = wait(&bar->s_full[i], j & 1, abort);
-      // tcgen05.ld / st are warp-collective (.sync.aligned): the warp decides
-      // together and reconverges here after the per-thread spin
+    for (int u = blockIdx.x; ok && u < n_items; u += gridDim.x) {
+      const Item it = make_item(p, u);
+      if (it.n_tiles <= 0) continue;
+      const int64_t qpos = it.q0 + row;
+      // admitted key positions of this row: [0, min(P, qpos+1)) and [max(0, qpos-W+1), qpos]
+      const int32_t a1 = keys_below(it.km, min((int64_t)it.P, qpos + 1));
+      const int32_t b0 = keys_below(it.km, max((int64_t)0, qpos - p.W + 1));
+      const int32_t b1 = keys_below(it.km, qpos + 1);
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < it.n_tiles; ++j) {
+        // the tile's class and mask bounds are worked out before the wait, off
+        // the S -> P critical path
+        const int kt = it.tile_at(j);
+        const int32_t ka = kt * kBN;
+        const int32_t kb = min(it.km.n_keys, ka + kBN) - 1;
+        const bool masked = tile_class(it.km, it.c0, it.q0r, it.q1r, ka, kb, it.P, p.W) != kFull ||
+                            ka + kBN > it.km.n_keys;
+        ok = wait(&bar->s_full[i], (g + j) & 1, abort);
+        // tcgen05.ld / st are warp-collective (.sync.aligned): the warp decides
+        // together and reconverges here after the per-thread spin
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+        float alpha;
+        if (masked)
+          alpha = softmax_tile<true>(tS, j, p.scale_log2, a1 - ka, b0 - ka, b1 - ka, m_used, l);
+        else
+          alpha = softmax_tile<false>(tS, j, p.scale_log2, 0, 0, 0, m_used, l);
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {  // alpha is 1 on the other rows
+          // O_i already holds every P V issued before S_i(j), which has completed,
+          // and P_i(j) V is not issued before this thread arrives below
+#pragma unroll 1
+          for (int c = 0; c < kHD / 32; ++c) {
+            uint32_t o[32];
+            tc::ld32(tO + c * 32, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tc::st32(tO + c * 32, o);
+          }
+        }
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar->p_full[i]);
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      ok = wait(&bar->o_done[i], k & 1, abort);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc::fence_after();
-      const int kt = tile_at(j);
-      const int32_t ka = kt * kBN;
-      const int32_t kb = min(km.n_keys, ka + kBN) - 1;
-      const uint8_t cls = tile_class(km, c0, q0r, q1r, ka, kb, P, p.W);
-      float alpha;
-      if (cls != kFull || ka + kBN > km.n_keys)
-        alpha = softmax_tile<true>(tS, j, p.scale_log2, a1 - ka, b0 - ka, b1 - ka, m_used, l);
-      else
-        alpha = softmax_tile<false>(tS, j, p.scale_log2, 0, 0, 0, m_used, l);
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {  // alpha is 1 on the other rows
-        // O_i already holds every P V issued before S_i(j), which has completed,
-        // and P_i(j) V is not issued before this thread arrives below
-#pragma unroll 1
-        for (int c = 0; c < kHD / 32; ++c) {
-          uint32_t o[32];
-          tc::ld32(tO + c * 32, o);
-          tc::wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tc::st32(tO + c * 32, o);
-        }
-      }
-      tc::wait_st();
-      tc::fence_before();
-      mbar_arrive(&bar->p_full[i]);
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok) ok = wait(&bar->o_done[i], 0, abort);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      tc::fence_after();
-      const int32_t qrow = q0r + row;
+      const int32_t qrow = it.q0r + row;
       const float inv = 1.f / l;
-      __nv_bfloat16* orow = p.out + (((int64_t)b * p.S + qrow) * p.hq + h0 + i) * kHD;
+      __nv_bfloat16* orow = p.out + (((int64_t)it.b * p.S + qrow) * p.hq + it.h0 + i) * kHD;
 #pragma unroll
       for (int c = 0; c < kHD / 32; ++c) {
         uint32_t o[32];
         tc::ld32(tO + c * 32, o);
         tc::wait_ld();
-        if (qrow <= q1r) {
+        if (c == kHD / 32 - 1) {  // O_i is read out: the next item may overwrite it
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar->o_free[i]);
+        }
+        if (qrow <= it.q1r) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 v;
@@ -829,9 +912,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           }
         }
       }
-      if (qrow <= q1r)
-        p.lse[((int64_t)b * p.hq + h0 + i) * p.S + qrow] =
+      if (qrow <= it.q1r)
+        p.lse[((int64_t)it.b * p.hq + it.h0 + i) * p.S + qrow] =
             (m_used + __log2f(l)) * 0.69314718055994530942f;
+      g += it.n_tiles;
+      ++k;
     }
   }
 
@@ -953,12 +1038,10 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
   g.status = status;
   g.k_pool = ring ? static_cast<const uint4*>(ring->k_pool) : nullptr;
   g.v_pool = ring ? static_cast<const uint4*>(ring->v_pool) : nullptr;
-  g.slot_base = ring ? ring->slot_base : nullptr;
   g.ring_prefix = ring ? ring->prefix_len : nullptr;
   g.ring_seq = ring_seq;
-  g.total_slots = ring ? ring->total_slots : 0;
+  g.map = ring ? slot_map(ring) : SlotMap{};
   g.nseq = ring ? ring->nseq : 0;
-  g.capacity = ring ? ring->capacity : 0;
   g.B = batch;
   g.S = seqlen;
   g.Skv = L.skv;
@@ -973,7 +1056,9 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
     const int sms = device_sm_count();
     const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;
     if (blocks > cap) blocks = cap;
-    rope_gather_kernel<<<(unsigned)blocks, 256, 0, s>>>(g);
+    if (launch_dependent(rope_gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s, g) !=
+        cudaSuccess)
+      return PS_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return PS_ERR_CUDA;
   }
 
@@ -1010,6 +1095,7 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
   p.W = window;
   p.with_ring = ring ? 1 : 0;
   p.nq = (seqlen + kBM - 1) / kBM;
+  p.B = batch;
   p.scale_log2 = scale * 1.4426950408889634f;
   // cudaFuncSetAttribute is cheap and per device; call it every time rather
   // than caching a flag that would be wrong on a second device
@@ -1018,14 +1104,21 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
     if (cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              ws::kSmem) != cudaSuccess)
       return PS_ERR_CUDA;
-    dim3 grid((unsigned)p.nq, (unsigned)(n_q_heads / 2), (unsigned)batch);
-    prefill_pair_kernel<<<grid, ws::kThreads, ws::kSmem, s>>>(p);
+    const int64_t n_items = (int64_t)p.nq * (n_q_heads / 2) * batch;
+    if (n_items > 0x7fffffffLL) return PS_ERR_UNSUPPORTED;
+    const int sms = device_sm_count();
+    const int64_t grid = n_items < (sms > 0 ? sms : 148) ? n_items : (sms > 0 ? sms : 148);
+    if (launch_dependent(prefill_pair_kernel, dim3((unsigned)grid), dim3(ws::kThreads),
+                         (size_t)ws::kSmem, s, p) != cudaSuccess)
+      return PS_ERR_CUDA;
   } else {
     if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemPrefill) != cudaSuccess)
       return PS_ERR_CUDA;
     dim3 grid((unsigned)p.nq, (unsigned)n_q_heads, (unsigned)batch);
-    prefill_kernel<<<grid, 128, kSmemPrefill, s>>>(p);
+    if (launch_dependent(prefill_kernel, grid, dim3(128), (size_t)kSmemPrefill, s, p) !=
+        cudaSuccess)
+      return PS_ERR_CUDA;
   }
   return launch_status();
 }

@@ -27,12 +27,11 @@ struct AppendParams {
   const int32_t* seq_idx;
   const int32_t* pos0;
   const int32_t* cu;
-  const int64_t* slot_base;
   const int32_t* prefix_len;
   int32_t* status;
+  SlotMap map;
   int64_t n_tokens;
-  int64_t total_slots;
-  int32_t nrun, nseq, hkv, head_dim, window, capacity, prefix_max;
+  int32_t nrun, nseq, hkv, head_dim, window, prefix_max;
   RopeTurns turns;
 };
 
@@ -45,9 +44,22 @@ struct AppendParams {
 // stores bf16 (round to nearest even); V is copied alongside.
 constexpr int kAppendThreads = 128;
 
+constexpr int kAppendCuSmem = 2048;  // run offsets staged in shared memory up to this many
+
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_constant__ AppendParams p) {
   __shared__ float2 cs[kAppendThreads];
   __shared__ int64_t row_of[kAppendThreads];  // destination pool row, or -1 = write nothing
+  __shared__ int32_t s_cu[kAppendCuSmem];
+  grid_dependency_wait();  // inputs and the pool may be in use by earlier stream work
+  allow_dependents();
+  // the run lookup below is a binary search over cu: in shared memory it costs a
+  // few cycles per step instead of a dependent global load per step
+  const bool cu_in_smem = p.nrun + 1 <= kAppendCuSmem;
+  if (cu_in_smem) {
+    for (int i = threadIdx.x; i <= p.nrun; i += kAppendThreads) s_cu[i] = p.cu[i];
+    __syncthreads();
+  }
+  const int32_t* cu = cu_in_smem ? s_cu : p.cu;
   const int half = p.head_dim / 2;
   const int tpb = kAppendThreads / half;     // tokens per block iteration
   const int groups = p.head_dim / 16;
@@ -64,33 +76,32 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_con
         int lo = 0, hi = p.nrun - 1;
         while (lo < hi) {
           int mid = (lo + hi + 1) >> 1;
-          if (p.cu[mid] <= t) lo = mid; else hi = mid - 1;
+          if (cu[mid] <= t) lo = mid; else hi = mid - 1;
         }
-        const int64_t c0 = p.cu[lo], c1 = p.cu[lo + 1];
+        const int64_t c0 = cu[lo], c1 = cu[lo + 1];
         const int32_t s = p.seq_idx[lo];
         int32_t bad = 0;
         if (!(c0 <= t && t < c1)) bad = PS_DEV_BAD_RUN;
         else if (s < 0 || s >= p.nseq) bad = PS_DEV_BAD_SEQ;
         int32_t P = 0;
-        int64_t base = 0, last = 0;
+        int64_t last = 0;
         if (!bad) {
           P = p.prefix_len[s];
-          base = p.slot_base[s];
           const int64_t first = p.pos0[lo];
           last = first + (c1 - c0) - 1;
           if (P < 0 || P > p.prefix_max) bad = PS_DEV_BAD_PREFIX;
-          else if (base < 0 || base + p.capacity > p.total_slots) bad = PS_DEV_BAD_SLOT;
+          else if (!p.map.seq_ok(s)) bad = PS_DEV_BAD_SLOT;
           else if (first < 0 || last > 0x7fffffffLL) bad = PS_DEV_BAD_POS;
           else pos = (int32_t)(first + (t - c0));
         }
-        if (bad) {
-          if (i == 0) set_flag(p.status, bad);
-        } else if (pos < P || (int64_t)pos > last - p.window) {
+        if (!bad && (pos < P || (int64_t)pos > last - p.window)) {
           // a window position is overwritten later in the same run once a
           // position W further on is also in it: only prefix positions and
           // the last W of the run survive
-          row = base + ring_slot(pos, P, p.window);
+          row = p.map.row(s, ring_slot(pos, P, p.window));
+          if (row < 0) bad = PS_DEV_BAD_SLOT;
         }
+        if (bad && i == 0) set_flag(p.status, bad);
       }
       float c = 1.f, sn = 0.f;
       if (row >= 0) rope_cos_sin(pos, p.turns.f[i], c, sn);
@@ -166,17 +177,15 @@ extern "C" ps_status_t ps_kv_append(const ps_cache_desc* cache, const int32_t* s
   p.seq_idx = seq_idx;
   p.pos0 = pos0;
   p.cu = cu_tokens;
-  p.slot_base = cache->slot_base;
   p.prefix_len = cache->prefix_len;
   p.status = cache->status;
+  p.map = slot_map(cache);
   p.n_tokens = n_tokens;
-  p.total_slots = cache->total_slots;
   p.nrun = nrun;
   p.nseq = cache->nseq;
   p.hkv = cache->n_kv_heads;
   p.head_dim = cache->head_dim;
   p.window = cache->window;
-  p.capacity = cache->capacity;
   p.prefix_max = cache->prefix_max;
   make_rope_turns(cache->rope_theta, cache->head_dim, &p.turns);
   const int64_t tpb = kAppendThreads / (cache->head_dim / 2);
@@ -184,6 +193,8 @@ extern "C" ps_status_t ps_kv_append(const ps_cache_desc* cache, const int32_t* s
   const int sms = device_sm_count();
   const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;
   if (blocks > cap) blocks = cap;
-  append_kernel<<<(unsigned)blocks, kAppendThreads, 0, (cudaStream_t)stream>>>(p);
+  if (launch_dependent(append_kernel, dim3((unsigned)blocks), dim3(kAppendThreads), 0,
+                       (cudaStream_t)stream, p) != cudaSuccess)
+    return PS_ERR_CUDA;
   return launch_status();
 }

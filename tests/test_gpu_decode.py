@@ -98,6 +98,46 @@ def test_decode_shapes_and_edges(ps, nseq, hq, hkv, D, P, W, pos, qs):
                                lse_abs=lse_tol(qs))
 
 
+PAGED_CASES = [
+    # nseq, Hq, Hkv, D, P per seq, W, pos per seq, block size
+    (3, 16, 8, 128, [100, 0, 7], 64, [50, 1000, 170], 16),
+    (4, 16, 8, 128, [512, 64, 300, 1], 4096, [131072, 4159, 4395, 262143], 64),
+    (2, 8, 2, 64, [0, 33], 1, [0, 5000], 32),
+]
+
+
+@pytest.mark.parametrize("nseq,hq,hkv,D,P,W,pos,bs", PAGED_CASES)
+def test_decode_paged_cache(ps, nseq, hq, hkv, D, P, W, pos, bs):
+    """Paged cache behind a shuffled block table: same results as the oracle."""
+    seed, theta = 12, 10000.0
+    probe = ps.RingCache(nseq, hkv, D, W, P, rope_theta=theta, block_size=bs, device="cpu")
+    order = np.random.default_rng(3).permutation(nseq * probe.blocks_per_seq)
+    cache = ps.RingCache(nseq, hkv, D, W, P, rope_theta=theta, block_size=bs, block_order=order)
+    append_runs(cache, {s: live_runs(pos[s], P[s], W) for s in range(nseq)},
+                synth_source(seed, hkv, D))
+    q = _queries(seed, nseq, pos, hq, D)
+    o, lse = cache.decode(q, torch.tensor(pos, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert cache.check_status() == 0
+    ref = _oracle_rows(seed, range(nseq), pos, P, W, hq, hkv, D, theta)
+    for s in range(nseq):
+        assert_attention_close(bf16_tensor_to_f64(o[s]), lse[s].cpu().numpy(), *ref[s], f"seq {s}")
+
+
+def test_decode_paged_block_outside_pool_is_flagged(ps):
+    """A block id outside the pool is reported, and nothing outside the pool is read."""
+    seed, hq, hkv, D, W = 13, 4, 2, 128, 32
+    cache = ps.RingCache(2, hkv, D, W, [4, 4], rope_theta=1e4, block_size=16)
+    append_runs(cache, {s: live_runs(40, 4, W) for s in range(2)}, synth_source(seed, hkv, D))
+    cache.block_table[1, 1] = 10 ** 6
+    q = _queries(seed, 2, [40, 40], hq, D)
+    o, lse = cache.decode(q, torch.tensor([40, 40], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert cache.check_status() & ps.PS_DEV_BAD_SLOT
+    ref = _oracle_rows(seed, [0], [40, 40], [4, 4], W, hq, hkv, D, 1e4)
+    assert_attention_close(bf16_tensor_to_f64(o[0]), lse[0].cpu().numpy(), *ref[0], "seq 0")
+
+
 def _full_size_case(ps, seed, nseq, pos, P, W, sampled):
     hq, hkv, D, theta = 16, 8, 128, 10000.0
     cache = ps.RingCache(nseq, hkv, D, W, P, rope_theta=theta, prefix_max=512)

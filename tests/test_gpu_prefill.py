@@ -142,6 +142,19 @@ def test_prefill_extend_from_ring(ps, c0, S, hq):
     assert cache.check_status() == 0
 
 
+def test_prefill_extend_from_paged_ring(ps):
+    """Chunked extend whose cached keys sit in a paged ring (shuffled blocks of 32)."""
+    seed, B, hq, hkv, D, P, W, theta, c0, S = 34, 2, 4, 2, 128, 20, 64, 10000.0, 300, 150
+    probe = ps.RingCache(B, hkv, D, W, [P] * B, rope_theta=theta, block_size=32, device="cpu")
+    order = np.random.default_rng(5).permutation(B * probe.blocks_per_seq)
+    cache = ps.RingCache(B, hkv, D, W, [P] * B, rope_theta=theta, block_size=32, block_order=order)
+    append_runs(cache, {b: [(0, c0)] for b in range(B)}, synth_source(seed, hkv, D))
+    q, k, v = _inputs(seed, B, S, [c0] * B, hq, hkv, D)
+    out, lse = _run(ps, q, k, v, [c0] * B, [P] * B, W, theta, ring=cache)
+    _check_rows(seed, out, lse, q, [c0] * B, [P] * B, W, theta, [range(S)] * B, hkv, "paged extend")
+    assert cache.check_status() == 0
+
+
 def test_prefill_32k_sampled_rows(ps):
     """One Qwen3-1.7B-shaped layer: 32,768 tokens, P = 100, W = 4,096, 16/8
     heads; rows at every boundary of the mask plus random ones."""

@@ -36,9 +36,9 @@ def test_ring_slots_bit_exact(ps):
 def _check_ring_contents(cache, seq, sim, hist, theta, D):
     """Pool rows of `seq` vs the oracle's ring simulation: V exact, K within
     one bf16 ulp of the oracle's rotated-and-rounded key, flips rare."""
-    cap = cache.capacity
-    kp = bf16_tensor_to_f64(cache.k_pool[seq * cap:(seq + 1) * cap])
-    vp = bf16_tensor_to_f64(cache.v_pool[seq * cap:(seq + 1) * cap])
+    rows = cache.rows_of(seq).to(cache.k_pool.device)
+    kp = bf16_tensor_to_f64(cache.k_pool[rows])
+    vp = bf16_tensor_to_f64(cache.v_pool[rows])
     held = sim.slots
     slots = np.nonzero(held >= 0)[0]
     kraw, vraw = hist.rows(held[slots])
@@ -79,6 +79,30 @@ def test_append_matches_ring_simulation(ps, P, W, D, steps, chunk):
     torch.cuda.synchronize()
     assert cache.check_status() == 0
     _check_ring_contents(cache, 0, sim, hist, theta, D)
+
+
+@pytest.mark.parametrize("block_size", [16, 48])
+def test_append_paged_matches_ring_simulation(ps, block_size):
+    """Paged cache: the same appends land in the blocks a shuffled block table
+    names; read back through the table they equal the ring simulation."""
+    seed, hkv, D, W, theta = 6, 2, 128, 100, 10000.0
+    P = [7, 30, 0]
+    ends = [900, 64, 350]
+    nseq = len(P)
+    probe = ps.RingCache(nseq, hkv, D, W, P, rope_theta=theta, block_size=block_size, device="cpu")
+    nblocks = nseq * probe.blocks_per_seq
+    order = np.random.default_rng(1).permutation(nblocks)
+    cache = ps.RingCache(nseq, hkv, D, W, P, rope_theta=theta, block_size=block_size,
+                         block_order=order)
+    runs = {s: [(0, ends[s] // 2), (ends[s] // 2, ends[s] - ends[s] // 2)] for s in range(nseq)}
+    append_runs(cache, runs, synth_source(seed, hkv, D))
+    torch.cuda.synchronize()
+    assert cache.check_status() == 0
+    for s in range(nseq):
+        sim = RingSim(P[s], W)
+        for x in range(ends[s]):
+            sim.append(x)
+        _check_ring_contents(cache, s, sim, synth.History(seed, s, hkv, D), theta, D)
 
 
 def test_append_many_sequences_one_call(ps):

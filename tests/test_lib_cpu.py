@@ -82,6 +82,18 @@ def test_cache_descriptor_validation(ps, kw, code):
     assert r == code
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(block_table=1024, block_size=8, blocks_per_seq=2), 1),    # block not a multiple of 16
+    (dict(block_table=1024, block_size=16, blocks_per_seq=0), 1),   # too few blocks per sequence
+    (dict(block_table=1024, block_size=32, blocks_per_seq=1, capacity=40), 1),  # 32 < capacity
+    (dict(slot_base=0), 1),                                          # contiguous needs slot_base
+])
+def test_paged_descriptor_validation(ps, kw, code):
+    d = _bad_desc(ps, **kw)
+    r = ps.lib.ps_kv_append(ctypes.byref(d), 16, 16, 16, 1, 4096, 4096, 1, None)
+    assert r == code
+
+
 def test_tile_grid_matches_oracle_shapes(ps):
     from oracle import tile_classes
     for S, q0, P, W, ring, bm, bn in [(1000, 0, 37, 300, 0, 128, 128), (70, 5, 9, 13, 0, 16, 8),
