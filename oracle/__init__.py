@@ -21,8 +21,12 @@ something other than itself):
                     (thousands of evictions), slot range [0, P+W)
   tile_classes      sum of admitted pairs equals the closed-form total; the
                     pages' skip rule (no admitted element) checked per tile
+  reset_positions / attend_reset_pe
+                    pure-Python enumeration that rotates every key at its
+                    renumbered position; equals attend while nothing has been
+                    evicted; window-only keys (P = 0) are a uniform shift
 """
 from .prefix_sliding import (  # noqa: F401
-    FULL, PARTIAL, SKIP, RingSim, allowed, attend, masked_attention, ring_slot,
-    rope, round_bf16, tile_classes, visible_positions,
+    FULL, PARTIAL, SKIP, RingSim, allowed, attend, attend_reset_pe, masked_attention,
+    reset_positions, ring_slot, rope, round_bf16, tile_classes, visible_positions,
 )

@@ -140,6 +140,56 @@ def attend(q_raw, p: int, P: int, W: int, history, theta: float, scale: float | 
     return masked_attention(q_hat, k_hat, v, scale)
 
 
+def reset_positions(p: int, P: int, W: int) -> tuple[np.ndarray, np.ndarray, int]:
+    """Reset PE renumbering for query p ([AGI] paragraph on position encodings:
+    Reset PE reassigns the cached entries' positions; the pages do not give the
+    rule).  Reading taken: the cache is renumbered in order, the P prefix keys
+    keep 0..P-1 and the window keys, oldest first, take P, P+1, ...; the query
+    is the newest window entry.  Returns (key positions js, their reset
+    positions, the query's reset position)."""
+    js = visible_positions(p, P, W)
+    reset = np.where(js < P, js, 0)
+    win = js >= P
+    reset[win] = P + np.arange(int(win.sum()))
+    return js, reset, int(reset[-1])
+
+
+def attend_reset_pe(q_raw, p: int, P: int, W: int, history, theta: float,
+                    scale: float | None = None):
+    """Prefix-Sliding attention of query p under Reset PE.
+
+    The scores depend only on the rotation between query and key, so a key
+    kept rotated at its absolute position j (the cache is never rewritten) and
+    a query rotated at r_q - (r_j - j), with r the reset positions, give the
+    reset-position score exactly.  Window keys are contiguous, so r_q - r_j =
+    p - j for them: their query rotation is the absolute one, p.  Prefix keys
+    keep r_j = j: their query rotation is r_q.  Rounding contract as in
+    ``attend``: the stored key and each rotated query are bf16.
+    """
+    q_raw = np.asarray(q_raw, dtype=np.float64)
+    d = q_raw.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    js, reset, rq = reset_positions(p, P, W)
+    k_raw, v = history(js)
+    k_hat = round_bf16(rope(k_raw, js, theta))
+    q_win = round_bf16(rope(q_raw, p, theta))
+    q_pre = round_bf16(rope(q_raw, rq, theta))
+    pre = js < P
+    hq = q_raw.shape[0]
+    group = hq // k_hat.shape[1]
+    out = np.zeros((hq, d))
+    lse = np.zeros(hq)
+    for h in range(hq):
+        kh = h // group
+        s = np.where(pre, k_hat[:, kh, :] @ q_pre[h], k_hat[:, kh, :] @ q_win[h]) * scale
+        m = s.max()
+        e = np.exp(s - m)
+        lse[h] = m + math.log(e.sum())
+        out[h] = (e / e.sum()) @ v[:, kh, :]
+    return out, lse
+
+
 # --------------------------------------------------------------------------
 # the bounded cache ([EXP] "伪代码" invariant: size prefix_len + W)
 # --------------------------------------------------------------------------

@@ -317,3 +317,88 @@ def test_tile_classes_golden_counts():
         pos = np.arange(case["S"])
         c = tile_classes(pos, pos, case["P"], case["W"], case["BM"], case["BN"])
         assert [int((c == k).sum()) for k in (SKIP, PARTIAL, FULL)] == case["skip_partial_full"]
+
+
+# ------------------------------------------------------------- Reset PE ----
+from oracle import attend_reset_pe, reset_positions  # noqa: E402
+import oracle.prefix_sliding as _ops  # noqa: E402
+
+
+def test_reset_positions_renumber_the_cache_in_order():
+    for P, W in ((4, 8), (0, 5), (16, 32), (3, 1)):
+        for p in range(0, 120):
+            js, reset, rq = reset_positions(p, P, W)
+            L = min(p + 1, P + W)
+            assert len(js) == L
+            assert np.array_equal(reset, np.arange(L))      # 0..L-1, cache order
+            assert np.array_equal(reset[js < P], js[js < P])  # prefix keeps its positions
+            assert rq == L - 1
+
+
+def test_reset_pe_equals_continue_pe_before_any_eviction():
+    seed, hq, hkv, d, theta = 23, 4, 2, 16, 1e4
+    hist = synth.History(seed, 0, hkv, d)
+    q = synth.bits_to_f64(synth.query_bits(seed, 0, np.arange(60), hq, d))
+    for P, W in ((8, 32), (0, 60), (40, 10)):
+        for p in range(0, 60):
+            if p + 1 > P + W:
+                continue
+            o1, l1 = attend(q[p], p, P, W, hist.rows, theta)
+            o2, l2 = attend_reset_pe(q[p], p, P, W, hist.rows, theta)
+            assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def _bruteforce_reset(q_raw, p, P, W, hist, theta):
+    """Scalar Python, no rounding: every key rotated at its renumbered
+    position (prefix 0..P-1, then the window oldest first), the query at the
+    newest window entry's position; keys found by listing the two ranges."""
+    keys = sorted(set(range(0, min(P, p + 1))) | set(range(max(0, p - W + 1), p + 1)))
+    newpos = {j: r for r, j in enumerate(keys)}
+    k_raw, v = hist(np.array(keys))
+    hq, d = q_raw.shape
+    hkv = k_raw.shape[1]
+
+    def rot(vec, pos):
+        out = [0.0] * d
+        for i in range(d // 2):
+            z = complex(vec[i], vec[i + d // 2]) * cmath.exp(1j * pos * theta ** (-2 * i / d))
+            out[i], out[i + d // 2] = z.real, z.imag
+        return out
+
+    outs, lses = [], []
+    for h in range(hq):
+        qv = rot(list(q_raw[h]), newpos[p])
+        ws = [math.exp(sum(a * b for a, b in zip(qv, rot(list(k_raw[n, h * hkv // hq]), newpos[j])))
+                       / math.sqrt(d)) for n, j in enumerate(keys)]
+        tot = sum(ws)
+        outs.append([sum(ws[n] / tot * v[n, h * hkv // hq, t] for n in range(len(keys)))
+                     for t in range(d)])
+        lses.append(math.log(tot))
+    return np.array(outs), np.array(lses)
+
+
+def test_reset_pe_matches_explicit_renumbering_without_rounding(monkeypatch):
+    """With the bf16 contract rounding switched off, the oracle's query-side
+    rotation equals rotating every key at its renumbered position."""
+    monkeypatch.setattr(_ops, "round_bf16", lambda x: np.asarray(x, dtype=np.float64))
+    seed, hq, hkv, d, theta = 24, 2, 1, 8, 1e4
+    hist = synth.History(seed, 2, hkv, d)
+    q = synth.bits_to_f64(synth.query_bits(seed, 2, np.arange(40), hq, d))
+    for P, W in ((3, 5), (0, 4), (6, 1), (10, 30)):
+        for p in range(0, 40, 3):
+            o, l = _ops.attend_reset_pe(q[p], p, P, W, hist.rows, theta)
+            ob, lb = _bruteforce_reset(q[p], p, P, W, hist.rows, theta)
+            assert np.allclose(o, ob, atol=1e-12) and np.allclose(l, lb, atol=1e-12), (P, W, p)
+
+
+def test_reset_pe_without_prefix_is_a_uniform_shift(monkeypatch):
+    """P = 0: every key is a window key, renumbering shifts all positions by
+    the same amount, so (without rounding) Reset PE equals Continue PE."""
+    monkeypatch.setattr(_ops, "round_bf16", lambda x: np.asarray(x, dtype=np.float64))
+    seed, hq, hkv, d, theta = 25, 2, 1, 16, 1e4
+    hist = synth.History(seed, 3, hkv, d)
+    q = synth.bits_to_f64(synth.query_bits(seed, 3, np.arange(200), hq, d))
+    for p in (50, 120, 199):
+        o1, l1 = _ops.attend(q[p], p, 0, 17, hist.rows, theta)
+        o2, l2 = _ops.attend_reset_pe(q[p], p, 0, 17, hist.rows, theta)
+        assert np.allclose(o1, o2, atol=1e-12) and np.allclose(l1, l2, atol=1e-12)
