@@ -25,8 +25,11 @@ something other than itself):
                     pure-Python enumeration that rotates every key at its
                     renumbered position; equals attend while nothing has been
                     evicted; window-only keys (P = 0) are a uniform shift
+  attend_backward   torch autograd of scaled_dot_product_attention in float64
+                    (explicit mask, GQA by repeat); central finite differences
+                    of the forward through RoPE; its forward equals attend
 """
 from .prefix_sliding import (  # noqa: F401
-    FULL, PARTIAL, SKIP, RingSim, allowed, attend, attend_reset_pe, masked_attention,
+    FULL, PARTIAL, SKIP, RingSim, allowed, attend, attend_backward, attend_reset_pe, masked_attention,
     reset_positions, ring_slot, rope, round_bf16, tile_classes, visible_positions,
 )

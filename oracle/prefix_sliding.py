@@ -191,6 +191,65 @@ def attend_reset_pe(q_raw, p: int, P: int, W: int, history, theta: float,
 
 
 # --------------------------------------------------------------------------
+# backward of the training forward ([AGI] paragraph on truncated backprop:
+# the trainer back-propagates through the last 4W tokens under the mask)
+# --------------------------------------------------------------------------
+def attend_backward(q_raw, k_raw, v, d_out, P: int, W: int, theta: float,
+                    scale: float | None = None, positions=None):
+    """Gradients of Prefix-Sliding attention over one sequence (float64).
+
+    q_raw [S, Hq, D], k_raw / v [S, Hkv, D] (raw values), d_out [S, Hq, D]
+    (gradient of the loss w.r.t. O); positions default to 0..S-1.  Forward as
+    in ``attend``: q_hat = bf16(rope(q)), k_hat = bf16(rope(k)), softmax of
+    scale * q_hat . k_hat over the admitted keys.  Backward, per query row i
+    and admitted key j:
+        P_ij = exp(s_ij - LSE_i),   dV_j += P_ij dO_i,
+        dP_ij = dO_i . v_j,   D_i = sum_j P_ij dP_ij = dO_i . O_i,
+        dS_ij = P_ij (dP_ij - D_i),
+        dQhat_i = scale sum_j dS_ij k_hat_j,   dKhat_j += scale dS_ij q_hat_i,
+    then back through the rotation (its transpose is the rotation by the
+    negative angle); the bf16 rounding passes gradients straight through.
+    Query head h reads KV head h // (Hq / Hkv), so dK and dV sum over the
+    group.  Returns (dq_raw, dk_raw, dv, O, LSE [S, Hq]).
+    """
+    q_raw = np.asarray(q_raw, dtype=np.float64)
+    k_raw = np.asarray(k_raw, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    d_out = np.asarray(d_out, dtype=np.float64)
+    S, hq, d = q_raw.shape
+    hkv = k_raw.shape[1]
+    group = hq // hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pos = np.arange(S) if positions is None else np.asarray(positions)
+    q_hat = round_bf16(rope(q_raw, pos, theta))
+    k_hat = round_bf16(rope(k_raw, pos, theta))
+    dq_hat = np.zeros_like(q_hat)
+    dk_hat = np.zeros_like(k_hat)
+    dv = np.zeros_like(v)
+    out = np.zeros_like(q_raw)
+    lse = np.zeros((S, hq))
+    for i in range(S):
+        js = np.nonzero(allowed(pos[i], pos, P, W))[0]
+        for h in range(hq):
+            kh = h // group
+            s = (k_hat[js, kh, :] @ q_hat[i, h]) * scale
+            m = s.max()
+            e = np.exp(s - m)
+            lse[i, h] = m + math.log(e.sum())
+            pr = np.exp(s - lse[i, h])
+            out[i, h] = pr @ v[js, kh, :]
+            dv[js, kh, :] += np.outer(pr, d_out[i, h])
+            dp = v[js, kh, :] @ d_out[i, h]
+            ds = pr * (dp - pr @ dp)
+            dq_hat[i, h] = scale * (ds @ k_hat[js, kh, :])
+            dk_hat[js, kh, :] += scale * np.outer(ds, q_hat[i, h])
+    dq_raw = rope(dq_hat, -pos, theta)
+    dk_raw = rope(dk_hat, -pos, theta)
+    return dq_raw, dk_raw, dv, out, lse
+
+
+# --------------------------------------------------------------------------
 # the bounded cache ([EXP] "伪代码" invariant: size prefix_len + W)
 # --------------------------------------------------------------------------
 def ring_slot(pos: int, P: int, W: int) -> int:

@@ -402,3 +402,85 @@ def test_reset_pe_without_prefix_is_a_uniform_shift(monkeypatch):
         o1, l1 = _ops.attend(q[p], p, 0, 17, hist.rows, theta)
         o2, l2 = _ops.attend_reset_pe(q[p], p, 0, 17, hist.rows, theta)
         assert np.allclose(o1, o2, atol=1e-12) and np.allclose(l1, l2, atol=1e-12)
+
+
+# ------------------------------------------------------------- backward ----
+from oracle import attend_backward  # noqa: E402
+
+
+def _bwd_inputs(seed, S, hq, hkv, d):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((S, hq, d))
+    k = rng.standard_normal((S, hkv, d))
+    v = rng.standard_normal((S, hkv, d))
+    do = rng.standard_normal((S, hq, d))
+    return q, k, v, do
+
+
+@pytest.mark.parametrize("S,P,W", [(24, 5, 7), (20, 0, 4), (16, 16, 3), (19, 3, 40)])
+def test_backward_matches_torch_autograd_of_sdpa(monkeypatch, S, P, W):
+    """Rounding off: the hand-written gradients equal torch autograd through
+    scaled_dot_product_attention with the explicit mask (float64), pulled back
+    through the rotation by autograd as well."""
+    monkeypatch.setattr(_ops, "round_bf16", lambda x: np.asarray(x, dtype=np.float64))
+    hq, hkv, d, theta = 4, 2, 8, 100.0
+    q, k, v, do = _bwd_inputs(S * 7 + P, S, hq, hkv, d)
+    dq, dk, dv, o, lse = _ops.attend_backward(q, k, v, do, P, W, theta)
+    pos = torch.arange(S, dtype=torch.float64)
+    inv = theta ** (-2.0 * torch.arange(d // 2, dtype=torch.float64) / d)
+    ang = pos[:, None] * inv[None, :]
+    c, s_ = torch.cos(ang)[:, None, :], torch.sin(ang)[:, None, :]
+
+    def rot(x):  # half-split rotation written with torch ops, differentiable
+        x1, x2 = x[..., : d // 2], x[..., d // 2:]
+        return torch.cat([x1 * c - x2 * s_, x2 * c + x1 * s_], dim=-1)
+
+    tq = torch.tensor(q, requires_grad=True)
+    tk = torch.tensor(k, requires_grad=True)
+    tv = torch.tensor(v, requires_grad=True)
+    qh = rot(tq).permute(1, 0, 2)
+    kh = rot(tk).permute(1, 0, 2).repeat_interleave(hq // hkv, 0)
+    vh = tv.permute(1, 0, 2).repeat_interleave(hq // hkv, 0)
+    jj, pp = torch.meshgrid(torch.arange(S), torch.arange(S), indexing="xy")
+    mask = (jj <= pp) & ((jj < P) | (jj > pp - W))
+    out = torch.nn.functional.scaled_dot_product_attention(qh, kh, vh, attn_mask=mask)
+    out.backward(torch.tensor(do).permute(1, 0, 2))
+    assert np.allclose(o, out.detach().permute(1, 0, 2).numpy(), atol=1e-12)
+    assert np.allclose(dq, tq.grad.numpy(), atol=1e-10)
+    assert np.allclose(dk, tk.grad.numpy(), atol=1e-10)
+    assert np.allclose(dv, tv.grad.numpy(), atol=1e-10)
+
+
+def test_backward_matches_finite_differences(monkeypatch):
+    """Rounding off: d(sum(dO * O))/dq, dk, dv by central differences."""
+    monkeypatch.setattr(_ops, "round_bf16", lambda x: np.asarray(x, dtype=np.float64))
+    S, hq, hkv, d, P, W, theta = 9, 2, 1, 4, 2, 3, 50.0
+    q, k, v, do = _bwd_inputs(3, S, hq, hkv, d)
+    dq, dk, dv, _, _ = _ops.attend_backward(q, k, v, do, P, W, theta)
+
+    def loss(qq, kk, vv):
+        return float((_ops.attend_backward(qq, kk, vv, do, P, W, theta)[3] * do).sum())
+
+    eps = 1e-6
+    for arr, grad, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            plus = [q.copy(), k.copy(), v.copy()]
+            minus = [q.copy(), k.copy(), v.copy()]
+            plus[which][idx] += eps
+            minus[which][idx] -= eps
+            fd = (loss(*plus) - loss(*minus)) / (2 * eps)
+            assert abs(fd - grad[idx]) < 1e-6, (which, idx, fd, grad[idx])
+
+
+def test_backward_forward_equals_attend():
+    seed, S, hq, hkv, d, P, W, theta = 26, 30, 4, 2, 16, 6, 9, 1e4
+    hist = synth.History(seed, 0, hkv, d)
+    pos = np.arange(S)
+    q = synth.bits_to_f64(synth.query_bits(seed, 0, pos, hq, d))
+    k, v = hist.rows(pos)
+    _, _, _, o, lse = attend_backward(q, k, v, np.zeros_like(q), P, W, theta)
+    for p in range(S):
+        o_ref, l_ref = attend(q[p], p, P, W, hist.rows, theta)
+        assert np.allclose(o[p], o_ref, atol=1e-13) and np.allclose(lse[p], l_ref, atol=1e-13)
