@@ -416,6 +416,44 @@ def prefill_report(ps, torch, name, B, S, P, W, steps, seed, bf16_peak, full_cau
     return rep
 
 
+def backward_report(ps, torch, B, S, P, W, steps, seed, bf16_peak):
+    """Training backward (dq, dk, dv) of the truncated-backprop step, one layer."""
+    d = PRE
+    hq, hkv, D = d["hq"], d["hkv"], d["D"]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    q = torch.randn(B, S, hq, D, generator=gen, device="cuda").to(torch.bfloat16)
+    k = torch.randn(B, S, hkv, D, generator=gen, device="cuda").to(torch.bfloat16)
+    v = torch.randn(B, S, hkv, D, generator=gen, device="cuda").to(torch.bfloat16)
+    do = torch.randn(B, S, hq, D, generator=gen, device="cuda").to(torch.bfloat16)
+    qs = torch.zeros(B, dtype=torch.int32, device="cuda")
+    pl = torch.full((B,), P, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = ps.prefill(q, k, v, qs, pl, W, rope_theta=d["theta"], status=status)
+    for _ in range(2):
+        ps.prefill_backward(q, k, v, out, lse, do, qs, pl, W, rope_theta=d["theta"], status=status)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        ps.prefill_backward(q, k, v, out, lse, do, qs, pl, W, rope_theta=d["theta"], status=status)
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ms = e0.elapsed_time(e1) / steps
+    cls = ps.prefill_tile_classes(S, 0, P, W).cpu().numpy()
+    tiles = int((cls > 0).sum())
+    fwd_alg = B * prefill_flops(S, P, W, hq, D)
+    tile_flops = B * 4.0 * D * hq * 128 * 128 * tiles
+    torch.cuda.empty_cache()
+    return {"workload": f"training backward {B} x {S}, P={P}, W={W}, Hq 16 / Hkv 8, D 128, one layer",
+            "ms": ms, "tflops_algorithmic": 2.5 * fwd_alg / ms / 1e9,
+            "tflops_executed": 3.5 * tile_flops / ms / 1e9,
+            "frac_of_measured_bf16_burst": 3.5 * tile_flops / ms / 1e9 / bf16_peak,
+            "timed": "whole ps_prefill_backward call: pre-pass + dQ kernel + dK/dV kernel; "
+                     "algorithmic = 2.5 x forward FLOPs, executed = 7 tile products of 128^3"}
+
+
 # ---- CPU oracle -----------------------------------------------------------
 def _oracle_worker(args):
     """Spawned worker: builds one sequence's visible history (untimed), then
@@ -546,6 +584,8 @@ def main():
         train = prefill_report(ps, torch, "training forward 8 x 8192 tokens, P=256, W=2048, Hq 16 / "
                                "Hkv 8, D 128, one layer", 8, 8192, 256, 2048, args.prefill_steps,
                                seed + 6, bf16_peak, fc)
+        train["backward"] = backward_report(ps, torch, 8, 8192, 256, 2048, max(3, args.prefill_steps // 2),
+                                            seed + 8, bf16_peak)
     except Exception as e:  # noqa: BLE001
         pre = {"unavailable": f"{type(e).__name__}: {e}"}
         train = None
@@ -588,7 +628,7 @@ def main():
         "decode": {"tok_s_per_layer": value, "tok_s_28_layers": value / LAYERS,
                    "step_hbm_gbs": step_gbs, "kv_bytes_per_step": kv_bytes,
                    "partial_kernel_ms": kern_avg_ms, "step_ms": ms_step},
-        "roofline": {"kernel": "decode_partial_kernel<128,2,8,3>", "bound": "hbm",
+        "roofline": {"kernel": "decode_partial_kernel<128,2,8,3,false>", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_src} hbm_gbs",
                      "traffic": committed_traffic("decode_partial_steady_64x131072.md",

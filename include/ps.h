@@ -101,7 +101,25 @@ typedef struct ps_cache_desc {
   const int32_t* block_table; /* device int32 [nseq, blocks_per_seq], or NULL (contiguous) */
   int32_t block_size;        /* paged: slots per block, a multiple of 16                   */
   int32_t blocks_per_seq;    /* paged: >= ceil(capacity / block_size)                      */
+  int32_t pe_mode;           /* PS_PE_CONTINUE (0) or PS_PE_RESET (1); see below           */
 } ps_cache_desc;
+
+/*
+ * Position encoding of the cached keys (agihunt.info paragraph on position
+ * encodings; njhaofan.com section "PrefixSliding如何丢掉中间Token？").
+ *   PS_PE_CONTINUE: positions keep climbing; a query at p sees every cached
+ *     key at its absolute position (the pages' default).
+ *   PS_PE_RESET: the cache is renumbered in order for each query: prefix keys
+ *     0..P-1, then the window keys, oldest first, and the query as the newest
+ *     entry (L - 1, with L the keys it sees).  The pages do not give the rule;
+ *     this is the plainest one.  Keys stay stored rotated at their absolute
+ *     positions; window keys keep their distance to the query, so only the
+ *     prefix keys see a different query rotation (at L - 1).  ps_decode
+ *     honours it.  ps_kv_append stores keys the same way in both modes;
+ *     ps_prefill computes Continue PE only.
+ */
+#define PS_PE_CONTINUE 0
+#define PS_PE_RESET 1
 
 /*
  * ps_ring_slots: slot(pos) of the formula above for n independent entries.
@@ -227,6 +245,37 @@ ps_status_t ps_prefill(const void* q, const void* k, const void* v, int32_t batc
                        const ps_cache_desc* ring, const int32_t* ring_seq, void* out,
                        float* lse, void* workspace, size_t workspace_bytes,
                        int32_t* status, void* stream);
+
+/*
+ * ps_prefill_backward_workspace_size: device workspace for ps_prefill_backward
+ * (rotated Q and K, and D = rowsum(dO * O)).
+ */
+ps_status_t ps_prefill_backward_workspace_size(int32_t batch, int32_t seqlen, int32_t n_q_heads,
+                                               int32_t n_kv_heads, int32_t head_dim,
+                                               size_t* bytes);
+
+/*
+ * ps_prefill_backward: gradients of ps_prefill without a ring (the
+ * truncated-backprop training step: "Prefix Sliding for efficient test-time
+ * scaling", agihunt.info, paragraph on RL, back-propagates through the last
+ * 4W tokens under the same mask).
+ *   q, k, v, q_start, prefix_len, window, heads, scale, rope_theta: as given
+ *     to ps_prefill; out (bf16 [batch, seqlen, n_q_heads, head_dim]) and lse
+ *     (fp32 [batch, n_q_heads, seqlen]) are its results; d_out: bf16 like out.
+ *   dq : device fp32 [batch, seqlen, n_q_heads, head_dim], gradient of raw q;
+ *   dk, dv : device fp32 [batch, seqlen, n_kv_heads, head_dim] (summed over the
+ *     query heads of each group).  The rotation is differentiated exactly; the
+ *     bf16 rounding of the rotated q and k passes gradients straight through.
+ *   Probabilities and dS enter the tensor-core products as bf16.
+ *   head_dim 128 only.
+ */
+ps_status_t ps_prefill_backward(const void* q, const void* k, const void* v, const void* out,
+                                const float* lse, const void* d_out, int32_t batch,
+                                int32_t seqlen, const int32_t* q_start, const int32_t* prefix_len,
+                                int32_t window, int32_t n_q_heads, int32_t n_kv_heads,
+                                int32_t head_dim, float scale, double rope_theta, float* dq,
+                                float* dk, float* dv, void* workspace, size_t workspace_bytes,
+                                int32_t* status, void* stream);
 
 /*
  * Tile geometry used by ps_prefill for one batch row: nq x nk tiles of

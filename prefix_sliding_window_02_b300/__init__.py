@@ -12,10 +12,12 @@ from typing import Optional, Sequence
 import torch
 
 from ._lib import (CacheDesc, PsError, check, lib, PS_DEV_BAD_POS, PS_DEV_BAD_PREFIX,  # noqa: F401
-                   PS_DEV_BAD_RUN, PS_DEV_BAD_SEQ, PS_DEV_BAD_SLOT, PS_DEV_TIMEOUT)
+                   PS_DEV_BAD_RUN, PS_DEV_BAD_SEQ, PS_DEV_BAD_SLOT, PS_DEV_TIMEOUT, PS_PE_CONTINUE,
+                   PS_PE_RESET)
 
 __all__ = ["RingCache", "ring_slots", "decode_workspace_size", "prefill_workspace_size",
-           "prefill", "prefill_tile_grid", "prefill_tile_classes", "PsError", "lib"]
+           "prefill", "prefill_backward", "prefill_tile_grid", "prefill_tile_classes", "PsError",
+           "lib"]
 
 BF16 = torch.bfloat16
 
@@ -40,6 +42,8 @@ class RingCache:
 
     Contiguous (default): pools of shape [nseq * capacity, n_kv_heads, head_dim];
     sequence s owns rows [s * capacity, (s + 1) * capacity).
+    ``pe_mode``: PS_PE_CONTINUE (0, the default) or PS_PE_RESET (1), the
+    position encoding ps_decode applies (see include/ps.h).
     Paged (``block_size`` given, a multiple of 16): the pools hold
     ``nseq * blocks_per_seq`` blocks of ``block_size`` rows, and
     ``block_table[s, i]`` names the block of the sequence's logical slots
@@ -51,7 +55,7 @@ class RingCache:
                  prefix_len: Sequence[int] | torch.Tensor, rope_theta: float = 10000.0,
                  prefix_max: Optional[int] = None, capacity: Optional[int] = None,
                  device="cuda", zero: bool = True, block_size: Optional[int] = None,
-                 block_order: Optional[Sequence[int]] = None):
+                 block_order: Optional[Sequence[int]] = None, pe_mode: int = 0):
         pl = torch.as_tensor(prefix_len, dtype=torch.int32).reshape(-1)
         if pl.numel() != nseq:
             raise ValueError("prefix_len must have nseq entries")
@@ -87,7 +91,8 @@ class RingCache:
             head_dim=head_dim, window=window, capacity=self.capacity, prefix_max=self.prefix_max,
             rope_theta=self.rope_theta,
             block_table=None if self.block_table is None else self.block_table.data_ptr(),
-            block_size=block_size or 0, blocks_per_seq=self.blocks_per_seq)
+            block_size=block_size or 0, blocks_per_seq=self.blocks_per_seq, pe_mode=pe_mode)
+        self.pe_mode = pe_mode
 
     def rows_of(self, seq: int) -> torch.Tensor:
         """Pool rows of the sequence's logical slots 0..capacity-1, in slot order."""
@@ -227,6 +232,36 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_start: torch.Te
                          _vp(ring_seq), _vp(out), _vp(lse), _vp(workspace), workspace.numel(),
                          _vp(status), _stream(stream)), "ps_prefill")
     return out, lse
+
+
+def prefill_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+                     lse: torch.Tensor, d_out: torch.Tensor, q_start: torch.Tensor,
+                     prefix_len: torch.Tensor, window: int, scale: Optional[float] = None,
+                     rope_theta: float = 10000.0, status: Optional[torch.Tensor] = None,
+                     stream=None):
+    """ps_prefill_backward: returns fp32 (dq [B,S,Hq,D], dk, dv [B,S,Hkv,D])."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (d_out, "d_out")):
+        _need(t, BF16, n)
+    _need(lse, torch.float32, "lse")
+    _need(q_start, torch.int32, "q_start")
+    _need(prefix_len, torch.int32, "prefix_len")
+    B, S, hq, D = q.shape
+    hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    dv = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    b = ctypes.c_size_t(0)
+    check(lib.ps_prefill_backward_workspace_size(B, S, hq, hkv, D, ctypes.byref(b)),
+          "ps_prefill_backward_workspace_size")
+    ws = torch.empty(b.value, dtype=torch.uint8, device=q.device)
+    check(lib.ps_prefill_backward(_vp(q), _vp(k), _vp(v), _vp(out), _vp(lse), _vp(d_out), B, S,
+                                  _vp(q_start), _vp(prefix_len), window, hq, hkv, D,
+                                  ctypes.c_float(scale), ctypes.c_double(rope_theta), _vp(dq),
+                                  _vp(dk), _vp(dv), _vp(ws), ws.numel(), _vp(status),
+                                  _stream(stream)), "ps_prefill_backward")
+    return dq, dk, dv
 
 
 def prefill_tile_grid(seqlen: int, q_start: int, prefix_len: int, window: int,

@@ -12,6 +12,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libps.so")
 
 PS_OK = 0
+PS_PE_CONTINUE = 0
+PS_PE_RESET = 1
 PS_DEV_BAD_PREFIX = 0x1
 PS_DEV_BAD_POS = 0x2
 PS_DEV_BAD_SLOT = 0x4
@@ -23,6 +25,7 @@ EXPORTS = (
     "ps_status_string", "ps_ring_slots", "ps_kv_append", "ps_decode_workspace_size",
     "ps_decode", "ps_decode_partial", "ps_decode_combine", "ps_decode_noalloc",
     "ps_prefill_workspace_size", "ps_prefill", "ps_prefill_tile_grid", "ps_prefill_tile_classes",
+    "ps_prefill_backward_workspace_size", "ps_prefill_backward",
     "ps_check_device_status",
 )
 
@@ -46,6 +49,7 @@ class CacheDesc(ctypes.Structure):
         ("block_table", ctypes.c_void_p),
         ("block_size", ctypes.c_int32),
         ("blocks_per_seq", ctypes.c_int32),
+        ("pe_mode", ctypes.c_int32),
     ]
 
 
@@ -72,6 +76,10 @@ def _load():
                                                 ctypes.POINTER(i32), ctypes.POINTER(i32)]),
         "ps_prefill_tile_classes": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, i32, vp, vp]),
         "ps_check_device_status": (ctypes.c_int, [vp, ctypes.POINTER(i32)]),
+        "ps_prefill_backward_workspace_size": (ctypes.c_int, [i32, i32, i32, i32, i32,
+                                                              ctypes.POINTER(sz)]),
+        "ps_prefill_backward": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32,
+                                               i32, i32, f32, f64, vp, vp, vp, vp, sz, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -110,7 +110,7 @@ __device__ __forceinline__ void load_row_f32(const uint8_t* rowp, float (&x)[EPL
   }
 }
 
-template <int D, int G, int WARPS, int STAGES>
+template <int D, int G, int WARPS, int STAGES, bool RESET>
 __global__ void __launch_bounds__(WARPS * 32, 1)
     decode_partial_kernel(const __grid_constant__ DecodeParams p) {
   using S = DecShape<D, G>;
@@ -205,8 +205,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
   TileIter cur;
   cur.init(pfx, p.nseq, p.hkv, lo);
   uint32_t parity = 0;  // bit st = parity expected next on stage st
-  float qf[G][EPL], acc[G][EPL], m[NPASS], lsum[NPASS];
+  float qf[G][EPL], qr[G][EPL], acc[G][EPL], m[NPASS], lsum[NPASS];
   int cur_L = 0;
+  int32_t seg_P = 0;      // prefix length of the current sequence
+  bool seg_reset = false; // Reset PE changes this sequence's prefix scores
   bool ok = true;
   int64_t consumed = lo;
   int st = 0;
@@ -220,7 +222,12 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     if (cur.g == lo || t == 0) {
       // new segment piece: rotate the group's queries at position pos[s]
       const int32_t ppos = p.pos[s];
-      cur_L = (int)min((int64_t)ppos + 1, (int64_t)p.prefix_len[s] + p.window);
+      seg_P = p.prefix_len[s];
+      cur_L = (int)min((int64_t)ppos + 1, (int64_t)seg_P + p.window);
+      // Reset PE renumbers the cache 0..L-1 and the query as L-1: window keys
+      // keep their distance to the query, prefix keys see it rotated at L-1
+      const int32_t rpos = cur_L - 1;
+      seg_reset = RESET && rpos != ppos;
 #pragma unroll
       for (int gg = 0; gg < G; ++gg) {
         const __nv_bfloat16* qrow = p.q + ((int64_t)s * p.hq + h * G + gg) * D + lane * EPL;
@@ -236,6 +243,12 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
           const float y = (lane < 16) ? (x[e] * c - partner * sn) : (x[e] * c + partner * sn);
           // rotated Q is rounded to bf16, as the cache stores rotated K
           qf[gg][e] = __bfloat162float(__float2bfloat16_rn(y)) * p.scale_log2;
+          qr[gg][e] = qf[gg][e];
+          if (RESET && seg_reset) {
+            rope_cos_sin(rpos, p.turns.f[i], c, sn);
+            const float yr = (lane < 16) ? (x[e] * c - partner * sn) : (x[e] * c + partner * sn);
+            qr[gg][e] = __bfloat162float(__float2bfloat16_rn(yr)) * p.scale_log2;
+          }
           acc[gg][e] = 0.f;
         }
       }
@@ -259,19 +272,22 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     const int nvalid = min(TS, cur_L - t * TS);
     const int myrow = lane & (TS - 1);
 
-#pragma unroll
-    for (int ps_ = 0; ps_ < NPASS; ++ps_) {
-      // ---- scores: 16 rows x HP heads of partial dot products per lane
+    // ---- scores of pass ps_: 16 rows x HP heads of partial dot products per
+    // lane, reduced so that lane l holds row l % 16 of head ps_ * HP + l / 16
+    // rows j < npre (the Reset PE prefix rows of the tile) use qr, the rest qf
+    auto tile_scores = [&](int npre, int ps_) -> float {
       float v[32];
 #pragma unroll
       for (int j = 0; j < TS; ++j) {
         float k4[EPL];
         load_row_f32<EPL>(kt + j * (D * 2) + lane * (EPL * 2), k4);
+        const bool r = j < npre;
 #pragma unroll
         for (int hh = 0; hh < HP; ++hh) {
-          float a = qf[ps_ * HP + hh][0] * k4[0];
+          const float(&qq)[EPL] = r ? qr[ps_ * HP + hh] : qf[ps_ * HP + hh];
+          float a = qq[0] * k4[0];
 #pragma unroll
-          for (int e = 1; e < EPL; ++e) a = fmaf(qf[ps_ * HP + hh][e], k4[e], a);
+          for (int e = 1; e < EPL; ++e) a = fmaf(qq[e], k4[e], a);
           v[hh * TS + j] = a;
         }
       }
@@ -299,8 +315,16 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
           v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
       }
+      return v[0];
+    };
+
+#pragma unroll
+    for (int ps_ = 0; ps_ < NPASS; ++ps_) {
+      // Reset PE: the tile's first npre rows are prefix slots (uniform per tile)
+      const int npre = RESET && seg_reset ? min(TS, max(0, seg_P - t * TS)) : 0;
+      const float sc = (!RESET || npre == 0) ? tile_scores(0, ps_) : tile_scores(npre, ps_);
       // lane l: score of row l % 16 for head ps_ * HP + l / 16 (log2 domain)
-      const float x = myrow < nvalid ? v[0] : -INFINITY;
+      const float x = myrow < nvalid ? sc : -INFINITY;
       float tmax = x;
 #pragma unroll
       for (int o = 8; o >= 1; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
@@ -459,19 +483,27 @@ struct DecPlan {
   void (*combine)(CombineParams) = nullptr;
 };
 
+// The grid (hence the workspace size) is the same for both position-encoding
+// variants: it uses the smaller of their occupancies.
 template <int D, int G>
-static bool plan_for(int nseq, DecPlan* pl) {
-  auto kp = decode_partial_kernel<D, G, kDecWarps, kDecStages>;
+static bool plan_for(int nseq, bool reset, DecPlan* pl) {
+  auto kc = decode_partial_kernel<D, G, kDecWarps, kDecStages, false>;
+  auto kr = decode_partial_kernel<D, G, kDecWarps, kDecStages, true>;
   pl->smem = dec_smem_bytes<D, G>(nseq);
   if (pl->smem > 227 * 1024) return false;
-  if (cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl->smem) !=
-      cudaSuccess)
-    return false;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kp, kDecWarps * 32, pl->smem) !=
+  int per_sm = 0, per_sm_r = 0;
+  if (cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl->smem) !=
           cudaSuccess ||
-      per_sm < 1)
+      cudaFuncSetAttribute(kr, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl->smem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kc, kDecWarps * 32, pl->smem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_r, kr, kDecWarps * 32, pl->smem) !=
+          cudaSuccess)
     return false;
+  per_sm = per_sm < per_sm_r ? per_sm : per_sm_r;
+  if (per_sm < 1) return false;
+  auto kp = reset ? kr : kc;
   const int sms = device_sm_count();
   if (sms < 1) return false;
   pl->grid = sms * per_sm;
@@ -482,9 +514,9 @@ static bool plan_for(int nseq, DecPlan* pl) {
   return true;
 }
 
-static bool make_plan(int D, int G, int nseq, DecPlan* pl) {
+static bool make_plan(int D, int G, int nseq, bool reset, DecPlan* pl) {
 #define PS_DEC_CASE(DD, GG) \
-  if (D == DD && G == GG) return plan_for<DD, GG>(nseq, pl);
+  if (D == DD && G == GG) return plan_for<DD, GG>(nseq, reset, pl);
   PS_DEC_CASE(128, 1) PS_DEC_CASE(128, 2) PS_DEC_CASE(128, 4) PS_DEC_CASE(128, 8)
   PS_DEC_CASE(64, 1) PS_DEC_CASE(64, 2) PS_DEC_CASE(64, 4) PS_DEC_CASE(64, 8)
 #undef PS_DEC_CASE
@@ -519,7 +551,7 @@ extern "C" ps_status_t ps_decode_workspace_size(int32_t nseq, int32_t n_q_heads,
   ps_status_t st = check_heads(n_q_heads, n_kv_heads, head_dim);
   if (st != PS_OK) return st;
   DecPlan pl;
-  if (!make_plan(head_dim, n_q_heads / n_kv_heads, nseq, &pl)) return PS_ERR_CUDA;
+  if (!make_plan(head_dim, n_q_heads / n_kv_heads, nseq, false, &pl)) return PS_ERR_CUDA;
   *bytes = dec_ws_bytes(pl, nseq, n_kv_heads);
   return PS_OK;
 }
@@ -532,7 +564,9 @@ static ps_status_t prepare_decode(const ps_cache_desc* cache, int32_t n_q_heads,
   st = check_heads(n_q_heads, cache->n_kv_heads, cache->head_dim);
   if (st != PS_OK) return st;
   if (cache->nseq > kMaxDecodeSeqs) return PS_ERR_UNSUPPORTED;
-  if (!make_plan(cache->head_dim, n_q_heads / cache->n_kv_heads, cache->nseq, pl)) return PS_ERR_CUDA;
+  if (!make_plan(cache->head_dim, n_q_heads / cache->n_kv_heads, cache->nseq,
+                 cache->pe_mode == PS_PE_RESET, pl))
+    return PS_ERR_CUDA;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return PS_ERR_WORKSPACE;
   if (ws_bytes < dec_ws_bytes(*pl, cache->nseq, cache->n_kv_heads)) return PS_ERR_WORKSPACE;
   return PS_OK;

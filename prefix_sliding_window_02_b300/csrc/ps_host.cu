@@ -85,6 +85,7 @@ ps_status_t check_cache(const ps_cache_desc* c) {
       c->total_slots < 1 || c->total_slots > 0x7fffffffLL || !(c->rope_theta > 0.0))
     return PS_ERR_INVALID_ARGUMENT;
   if ((int64_t)c->capacity < (int64_t)c->prefix_max + c->window) return PS_ERR_INVALID_ARGUMENT;
+  if (c->pe_mode != PS_PE_CONTINUE && c->pe_mode != PS_PE_RESET) return PS_ERR_INVALID_ARGUMENT;
   if (c->head_dim != 64 && c->head_dim != 128) return PS_ERR_UNSUPPORTED;
   if (!aligned16(c->k_pool) || !aligned16(c->v_pool)) return PS_ERR_ALIGNMENT;
   return PS_OK;

@@ -17,6 +17,7 @@
 //     row straight out of TMEM.
 #include "ps_internal.h"
 #include "ps_tc.cuh"
+#include "ps_rope.cuh"
 #include "ps_tiles.cuh"
 
 namespace ps {
@@ -61,30 +62,16 @@ struct GatherParams {
   RopeTurns turns;
 };
 
-// Rotates 8 rotation pairs: elements 8g..8g+7 of the first half (a) with their
-// partners 8g+64.. of the second half (b); cs holds (cos, sin) of each pair.
-__device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, const float2* cs,
-                                        uint4& ra, uint4& rb) {
-  const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
-  const uint32_t* bw = reinterpret_cast<const uint32_t*>(&b);
-  uint32_t* raw = reinterpret_cast<uint32_t*>(&ra);
-  uint32_t* rbw = reinterpret_cast<uint32_t*>(&rb);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float2 t0 = cs[2 * e], t1 = cs[2 * e + 1];
-    const float x0 = bf16lo(aw[e]), x1 = bf16hi(aw[e]);
-    const float y0 = bf16lo(bw[e]), y1 = bf16hi(bw[e]);
-    raw[e] = pack_bf16(x0 * t0.x - y0 * t0.y, x1 * t1.x - y1 * t1.y);
-    rbw[e] = pack_bf16(y0 * t0.x + x0 * t0.y, y1 * t1.x + x1 * t1.y);
-  }
-}
-
-constexpr int kRopeRows = 4;  // chunk rows per block iteration (256 threads: 4 rows x 64 pairs)
+constexpr int kRopeRows = 8;  // chunk rows per block iteration
+constexpr int kRopeBatch = 4; // items a thread loads before it rotates and stores any
 
 // D = 128.  Phase A: groups of kRopeRows chunk rows; the 64 (cos, sin) pairs of
 // each row's position are computed once into shared memory and shared by all
-// Hq query heads and Hkv key heads of that row.  Phase B: the ring rows
-// (copied, already rotated) and the zero padding of each batch row's key array.
+// Hq query heads and Hkv key heads of that row.  Each thread then loads
+// kRopeBatch items (8 rotation pairs of one row and head each) before it
+// rotates and stores them, to keep enough loads in flight.  Phase B: the ring
+// rows (copied, already rotated) and the zero padding of each batch row's key
+// array.
 __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant__ GatherParams p) {
   constexpr int VEC = 16, HALFV = 8;
   __shared__ float2 cs[kRopeRows][64];
@@ -96,54 +83,70 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
   const int heads = p.hq + p.hkv;
   for (int64_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {
     const int64_t r0 = grp * kRopeRows;
-    {
-      const int rr = threadIdx.x >> 6, i = threadIdx.x & 63;
+    for (int x = threadIdx.x; x < kRopeRows * 64; x += blockDim.x) {
+      const int rr = x >> 6, i = x & 63;
       const int64_t r = r0 + rr;
       if (r < n_rows) {
         const int b = (int)(r / p.S);
         const int32_t pos = p.q_start[b] + (int32_t)(r % p.S);
-        float c, s;
-        rope_cos_sin(pos, p.turns.f[i], c, s);
-        cs[rr][i] = make_float2(c, s);
+        float c, sn;
+        rope_cos_sin(pos, p.turns.f[i], c, sn);
+        cs[rr][i] = make_float2(c, sn);
       }
     }
     __syncthreads();
     const int items = kRopeRows * heads * 8;
-    for (int it = threadIdx.x; it < items; it += blockDim.x) {
-      const int g = it & 7;
-      const int hd = (it >> 3) % heads;
-      const int rr = (it >> 3) / heads;
-      const int64_t r = r0 + rr;
-      if (r >= n_rows) continue;
-      const float2* ang = &cs[rr][8 * g];
-      uint4 ra, rb;
-      if (hd < p.hq) {
-        const int64_t base = (r * p.hq + hd) * VEC;
-        rotate8(p.q[base + g], p.q[base + HALFV + g], ang, ra, rb);
-        p.qh[base + g] = ra;
-        p.qh[base + HALFV + g] = rb;
-      } else {
-        const int h = hd - p.hq;
-        const int b = (int)(r / p.S);
-        const int32_t t = (int32_t)(r % p.S);
-        const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
-        const KeyMap km = make_keymap(p.S, c0, P, p.W, ring);
-        const int32_t n_ring = km.n_keys - p.S;
-        // the ring part must fit the workspace stride: 0 <= P <= the ring's
-        // prefix_max (which ps_prefill sized it by) and q_start >= 0
-        if (c0 < 0 || (ring && (P < 0 || n_ring > p.Skv - p.S))) {
-          set_flag(p.status, c0 < 0 ? PS_DEV_BAD_POS : PS_DEV_BAD_PREFIX);
-          continue;
+    for (int it0 = threadIdx.x; it0 < items; it0 += kRopeBatch * blockDim.x) {
+      uint4 xa[kRopeBatch], xb[kRopeBatch];
+      uint4* dst[kRopeBatch];
+      const float2* ang[kRopeBatch];
+#pragma unroll
+      for (int u = 0; u < kRopeBatch; ++u) {
+        dst[u] = nullptr;
+        const int it = it0 + u * blockDim.x;
+        if (it >= items) continue;
+        const int g = it & 7;
+        const int hd = (it >> 3) % heads;
+        const int rr = (it >> 3) / heads;
+        const int64_t r = r0 + rr;
+        if (r >= n_rows) continue;
+        ang[u] = &cs[rr][8 * g];
+        if (hd < p.hq) {
+          const int64_t base = (r * p.hq + hd) * VEC + g;
+          xa[u] = p.q[base];
+          xb[u] = p.q[base + HALFV];
+          dst[u] = p.qh + base;
+        } else {
+          const int h = hd - p.hq;
+          const int b = (int)(r / p.S);
+          const int32_t t = (int32_t)(r % p.S);
+          const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
+          const KeyMap km = make_keymap(p.S, c0, P, p.W, ring);
+          const int32_t n_ring = km.n_keys - p.S;
+          // the ring part must fit the workspace stride: 0 <= P <= the ring's
+          // prefix_max (which ps_prefill sized it by) and q_start >= 0
+          if (c0 < 0 || (ring && (P < 0 || n_ring > p.Skv - p.S))) {
+            set_flag(p.status, c0 < 0 ? PS_DEV_BAD_POS : PS_DEV_BAD_PREFIX);
+            continue;
+          }
+          const int64_t src = (r * p.hkv + h) * VEC + g;
+          const int64_t d = (((int64_t)b * p.Skv + n_ring + t) * p.hkv + h) * VEC + g;
+          xa[u] = p.k[src];
+          xb[u] = p.k[src + HALFV];
+          dst[u] = p.kh + d;
+          if (p.vg) {
+            p.vg[d] = p.v[src];
+            p.vg[d + HALFV] = p.v[src + HALFV];
+          }
         }
-        const int64_t src = (r * p.hkv + h) * VEC;
-        const int64_t dst = (((int64_t)b * p.Skv + n_ring + t) * p.hkv + h) * VEC;
-        rotate8(p.k[src + g], p.k[src + HALFV + g], ang, ra, rb);
-        p.kh[dst + g] = ra;
-        p.kh[dst + HALFV + g] = rb;
-        if (p.vg) {
-          p.vg[dst + g] = p.v[src + g];
-          p.vg[dst + HALFV + g] = p.v[src + HALFV + g];
-        }
+      }
+#pragma unroll
+      for (int u = 0; u < kRopeBatch; ++u) {
+        if (!dst[u]) continue;
+        uint4 ra, rb;
+        rotate8(xa[u], xb[u], ang[u], ra, rb);
+        dst[u][0] = ra;
+        dst[u][HALFV] = rb;
       }
     }
     __syncthreads();
@@ -498,14 +501,14 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
 namespace ws {
 
 constexpr int kThreads = 320;
-constexpr int kStK = 2, kStV = 2;
+constexpr int kSt = 2;  // steps in flight: each holds a K tile and a V tile
+constexpr int kStK = kSt, kStV = kSt;
 constexpr int kSmem = (2 + kStK + kStV) * kTile + 1024 /*barriers*/ + 1024 /*alignment*/;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 
 struct Bars {
   uint64_t q_full, q_empty;
-  uint64_t k_full[kStK], k_empty[kStK];
-  uint64_t v_full[kStV], v_empty[kStV];
+  uint64_t step_full[kSt], step_empty[kSt];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint32_t tmem_slot;
   int32_t abort;
@@ -690,13 +693,9 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
   if (tid == 32) {
     mbar_init(&bar->q_full, 1);
     mbar_init(&bar->q_empty, 1);
-    for (int s = 0; s < kStK; ++s) {
-      mbar_init(&bar->k_full[s], 1);
-      mbar_init(&bar->k_empty[s], 1);
-    }
-    for (int s = 0; s < kStV; ++s) {
-      mbar_init(&bar->v_full[s], 1);
-      mbar_init(&bar->v_empty[s], 1);
+    for (int s = 0; s < kSt; ++s) {
+      mbar_init(&bar->step_full[s], 1);
+      mbar_init(&bar->step_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
@@ -736,19 +735,26 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           tma_load_4d(sQ + i * kTile + kHalf, &p.tmq, &bar->q_full, 64, it.h0 + i, it.q0r, it.b,
                       pol_q);
         }
-        for (int j = 0; j < it.n_tiles; ++j) {
-          const int gj = g + j, kt = it.tile_at(j);
-          const int sk = gj % kStK, sv = gj % kStV;
-          if (!(ok = wait(&bar->k_empty[sk], ((gj / kStK) & 1) ^ 1, abort))) break;
-          uint8_t* dk = sK + sk * kTile;
-          mbar_arrive_expect_tx(&bar->k_full[sk], kTile);
-          tma_load_4d(dk, &p.tmk, &bar->k_full[sk], 0, it.hk, kt * kBN, it.b, pol_kv);
-          tma_load_4d(dk + kHalf, &p.tmk, &bar->k_full[sk], 64, it.hk, kt * kBN, it.b, pol_kv);
-          if (!(ok = wait(&bar->v_empty[sv], ((gj / kStV) & 1) ^ 1, abort))) break;
-          uint8_t* dv = sV + sv * kTile;
-          mbar_arrive_expect_tx(&bar->v_full[sv], kTile);
-          tma_load_4d(dv, &p.tmv, &bar->v_full[sv], 0, it.hk, kt * kBN, it.b, pol_kv);
-          tma_load_4d(dv + kHalf, &p.tmv, &bar->v_full[sv], 64, it.hk, kt * kBN, it.b, pol_kv);
+        // step j of the item (j = 0..n) brings K(j) (for Q K of tile j) and
+        // V(j-1) (for P V of tile j-1), the operands the issuer uses in the
+        // same step, under one barrier
+        for (int j = 0; j <= it.n_tiles; ++j) {
+          const int gs = g + k + j, st = gs % kSt;
+          if (!(ok = wait(&bar->step_empty[st], ((gs / kSt) & 1) ^ 1, abort))) break;
+          uint64_t* full = &bar->step_full[st];
+          mbar_arrive_expect_tx(full, (j < it.n_tiles ? kTile : 0) + (j > 0 ? kTile : 0));
+          if (j < it.n_tiles) {
+            const int kt = it.tile_at(j);
+            uint8_t* dk = sK + st * kTile;
+            tma_load_4d(dk, &p.tmk, full, 0, it.hk, kt * kBN, it.b, pol_kv);
+            tma_load_4d(dk + kHalf, &p.tmk, full, 64, it.hk, kt * kBN, it.b, pol_kv);
+          }
+          if (j > 0) {
+            const int kt = it.tile_at(j - 1);
+            uint8_t* dv = sV + st * kTile;
+            tma_load_4d(dv, &p.tmv, full, 0, it.hk, kt * kBN, it.b, pol_kv);
+            tma_load_4d(dv + kHalf, &p.tmv, full, 64, it.hk, kt * kBN, it.b, pol_kv);
+          }
         }
         g += it.n_tiles;
         ++k;
@@ -782,16 +788,17 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           tc::mma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, b + ((kk * 2048) >> 4),
                           kIdescPV, acc || kk > 0);
       };
-      // P_i V of tile gt (the item's jt-th); its first one overwrites O_i, which
-      // must wait until the previous item's epilogue has read O_i out
-      auto pv_step = [&](int i, int gt, int jt, int k) -> bool {
-        const int sv = gt % kStV;
+      // P_i V of tile gt (the item's jt-th) from step stage st; the item's first
+      // one overwrites O_i, which must wait until the previous item's epilogue
+      // has read O_i out.  Every mbarrier operation of this thread stalls it for
+      // hundreds of cycles while the tensor-core queue is only a few products
+      // deep, so each step waits on one barrier for both operand tiles and
+      // releases them with one commit.
+      auto pv_step = [&](int i, int gt, int jt, int st, int k) -> bool {
         if (!wait(&bar->p_full[i], gt & 1, abort)) return false;
-        if (i == 0 && !wait(&bar->v_full[sv], (gt / kStV) & 1, abort)) return false;
         if (jt == 0 && !wait(&bar->o_free[i], (k & 1) ^ 1, abort)) return false;
         tc::fence_after();
-        pv(i, sv, jt > 0);
-        if (i == 1) tc::commit(smem_u32(&bar->v_empty[sv]));
+        pv(i, st, jt > 0);
         return true;
       };
       int g = 0, k = 0;
@@ -801,22 +808,20 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         const int n = it.n_tiles;
         if (n <= 0) continue;
         if (!(ok = wait(&bar->q_full, k & 1, abort))) break;
-        for (int j = 0; ok && j < n; ++j) {
-          const int gj = g + j, sk = gj % kStK;
-          if (!(ok = wait(&bar->k_full[sk], (gj / kStK) & 1, abort))) break;
-          tc::fence_after();
+        for (int j = 0; ok && j <= n; ++j) {
+          const int gs = g + k + j, st = gs % kSt;  // step index: n + 1 steps per item
+          if (!(ok = wait(&bar->step_full[st], (gs / kSt) & 1, abort))) break;
           for (int i = 0; i < 2 && ok; ++i) {
-            if (j > 0 && !(ok = pv_step(i, gj - 1, j - 1, k))) break;
-            qk(i, sk);
+            if (j > 0 && !(ok = pv_step(i, g + j - 1, j - 1, st, k))) break;
+            if (j < n) {
+              qk(i, st);
+            } else {
+              tc::commit(smem_u32(&bar->o_done[i]));
+            }
           }
           if (!ok) break;
-          tc::commit(smem_u32(&bar->k_empty[sk]));
-        }
-        if (!ok) break;
-        tc::commit(smem_u32(&bar->q_empty));  // every Q K of this item is issued
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (!(ok = pv_step(i, g + n - 1, n - 1, k))) break;
-          tc::commit(smem_u32(&bar->o_done[i]));
+          tc::commit(smem_u32(&bar->step_empty[st]));
+          if (j == n - 1) tc::commit(smem_u32(&bar->q_empty));  // every Q K of this item is issued
         }
         g += n;
         ++k;

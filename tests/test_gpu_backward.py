@@ -1,0 +1,69 @@
+"""ps_prefill_backward (dq, dk, dv) against the float64 oracle's gradients (GPU).
+
+Tolerance: the kernels feed the probabilities and dS to the tensor cores as
+bf16 (relative rounding 2^-9 per element) and start from the forward's bf16
+O and fp32 LSE, so each gradient tensor is compared per head against the
+oracle as max|g - g_ref| <= 2e-2 * max|g_ref|, with the mean error held to a
+tenth of that.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import attend_backward
+
+from _util import bits_to_bf16_tensor
+
+pytestmark = pytest.mark.gpu
+
+STREAM_DO = 5  # synthetic dO
+
+
+@pytest.fixture(scope="module")
+def ps():
+    import prefix_sliding_window_02_b300 as ps
+    return ps
+
+
+def _close(g, ref, what):
+    """g, ref: [S, H, D] float64; checked per head."""
+    for h in range(ref.shape[1]):
+        scale = float(np.abs(ref[:, h]).max())
+        err = np.abs(g[:, h] - ref[:, h])
+        assert err.max() <= 2e-2 * scale, f"{what} head {h}: max err {err.max():.3e} vs max {scale:.3e}"
+        assert err.mean() <= 2e-3 * scale, f"{what} head {h}: mean err {err.mean():.3e} vs max {scale:.3e}"
+
+
+@pytest.mark.parametrize("B,S,hq,hkv,P,W", [
+    (1, 300, 4, 2, [37], 100),        # ragged tail, prefix and band
+    (2, 257, 2, 2, [5, 0], 1000),     # one query head per KV head; W >= S: causal
+    (1, 384, 8, 2, [0], 128),         # G = 4; plain sliding window
+    (1, 200, 4, 2, [300], 16),        # P >= S: causal through the prefix
+    (2, 1024, 16, 8, [64, 64], 256),  # training-shaped, reduced: 4W tokens, loss on all
+])
+def test_backward_matches_oracle(ps, B, S, hq, hkv, P, W):
+    seed, D, theta = 41, 128, 10000.0
+    pos = np.arange(S)
+    q = np.stack([synth.query_bits(seed, b, pos, hq, D) for b in range(B)])
+    kv = [synth.History(seed, b, hkv, D).rows_bits(pos) for b in range(B)]
+    k = np.stack([x[0] for x in kv])
+    v = np.stack([x[1] for x in kv])
+    do = np.stack([synth.normal_bf16(seed, STREAM_DO, b, pos, hq, D) for b in range(B)])
+    i32 = dict(dtype=torch.int32, device="cuda")
+    tq, tk, tv, tdo = (bits_to_bf16_tensor(x) for x in (q, k, v, do))
+    qs = torch.zeros(B, **i32)
+    pl = torch.tensor(P, **i32)
+    status = torch.zeros(1, **i32)
+    out, lse = ps.prefill(tq, tk, tv, qs, pl, W, rope_theta=theta, status=status)
+    dq, dk, dv = ps.prefill_backward(tq, tk, tv, out, lse, tdo, qs, pl, W, rope_theta=theta,
+                                     status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for b in range(B):
+        rq, rk, rv, _, _ = attend_backward(synth.bits_to_f64(q[b]), synth.bits_to_f64(k[b]),
+                                           synth.bits_to_f64(v[b]), synth.bits_to_f64(do[b]),
+                                           P[b], W, theta)
+        _close(dq[b].double().cpu().numpy(), rq, f"dq b={b}")
+        _close(dk[b].double().cpu().numpy(), rk, f"dk b={b}")
+        _close(dv[b].double().cpu().numpy(), rv, f"dv b={b}")

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import synth
-from oracle import attend
+from oracle import attend, attend_reset_pe
 
 from _util import (append_runs, assert_attention_close, bf16_tensor_to_f64, bits_to_bf16_tensor,
                    live_runs, lse_tol, random_source, synth_source)
@@ -194,3 +194,38 @@ def test_decode_flags_bad_prefix_and_keeps_others(ps):
     assert torch.all(o[1].float() == 0) and torch.all(torch.isinf(lse[1]))
     ref = _oracle_rows(seed, [0], pos, P, W, hq, hkv, D, 1e4)
     assert_attention_close(bf16_tensor_to_f64(o[0]), lse[0].cpu().numpy(), *ref[0], "seq 0")
+
+
+# ---------------------------------------------------------------- Reset PE --
+def test_tiny_decode_reset_pe_240_steps(ps):
+    """Reset PE (cache renumbered in order each step): the tiny workload,
+    every step against the full-history oracle of the renumbered positions."""
+    seed, hq, hkv, D, P, W, theta = 1, 2, 1, 64, 16, 32, 10000.0
+    cache = ps.RingCache(1, hkv, D, W, [P], rope_theta=theta, pe_mode=ps.PS_PE_RESET)
+    append_runs(cache, {0: [(0, P)]}, synth_source(seed, hkv, D))
+    hist = synth.History(seed, 0, hkv, D)
+    for p in range(P, 256):
+        o, lse = _step_decode(ps, cache, seed, p, hq, hkv, D)
+        q = synth.bits_to_f64(synth.query_bits(seed, 0, p, hq, D))[0]
+        o_ref, lse_ref = attend_reset_pe(q, p, P, W, hist.rows, theta)
+        assert_attention_close(bf16_tensor_to_f64(o[0]), lse[0].cpu().numpy(), o_ref, lse_ref, f"p={p}")
+    assert cache.check_status() == 0
+
+
+@pytest.mark.parametrize("nseq,hq,hkv,D,P,W,pos", [
+    (4, 16, 8, 128, [100, 0, 7, 37], 64, [50, 1000, 170, 100]),       # below / above the fill point
+    (3, 16, 8, 128, [100, 512, 64], 4096, [10000, 131072, 4200]),      # prefix / window boundary mid-tile
+    (2, 8, 1, 128, [5, 20], 16, [300, 45]),                            # G = 8
+])
+def test_decode_reset_pe_shapes(ps, nseq, hq, hkv, D, P, W, pos):
+    seed, theta = 14, 10000.0
+    cache = ps.RingCache(nseq, hkv, D, W, P, rope_theta=theta, pe_mode=ps.PS_PE_RESET)
+    append_runs(cache, {s: live_runs(pos[s], P[s], W) for s in range(nseq)}, synth_source(seed, hkv, D))
+    q = _queries(seed, nseq, pos, hq, D)
+    o, lse = cache.decode(q, torch.tensor(pos, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert cache.check_status() == 0
+    for s in range(nseq):
+        qs = synth.bits_to_f64(synth.query_bits(seed, s, pos[s], hq, D))[0]
+        o_ref, l_ref = attend_reset_pe(qs, pos[s], P[s], W, synth.History(seed, s, hkv, D).rows, theta)
+        assert_attention_close(bf16_tensor_to_f64(o[s]), lse[s].cpu().numpy(), o_ref, l_ref, f"seq {s}")

@@ -87,6 +87,7 @@ def test_cache_descriptor_validation(ps, kw, code):
     (dict(block_table=1024, block_size=16, blocks_per_seq=0), 1),   # too few blocks per sequence
     (dict(block_table=1024, block_size=32, blocks_per_seq=1, capacity=40), 1),  # 32 < capacity
     (dict(slot_base=0), 1),                                          # contiguous needs slot_base
+    (dict(pe_mode=2), 1),                                            # unknown position encoding
 ])
 def test_paged_descriptor_validation(ps, kw, code):
     d = _bad_desc(ps, **kw)
