@@ -11,21 +11,32 @@
 // rotation is the rotation by the negative angle; the bf16 rounding of q_hat
 // and k_hat passes gradients straight through).
 //
-// Three kernels, all without atomics:
+// Two launches, no atomics:
 //  1. bwd_prep_kernel rotates Q and K exactly as the forward's pre-pass does
-//     (same angles, same rounding) and forms D_i = dO_i . O_i.
-//  2. bwd_dq_kernel: one CTA per (128-query tile, query head, batch row); it
-//     walks the key tiles the forward visits and accumulates dQ in TMEM.
-//  3. bwd_dkdv_kernel: one CTA per (128-key tile, KV head, batch row); it walks
-//     the query tiles that can admit one of its keys, for every query head of
-//     the group, and accumulates dK and dV in TMEM.
-// Every product is a tcgen05 MMA (bf16 operands, fp32 accumulators in TMEM).
-// Operands that are consumed along K use the 128-byte-swizzled K-major tiles a
-// TMA box {64, 1, 128, 1} writes; the same tiles serve as MN-major B operands
-// (rows along K) for the accumulating products, as V does in the forward.
-// The probabilities and dS are written back into TMEM as bf16 and read as the
-// tensor-memory A operand.
+//     (same angles, same rounding) and stores, per (head, query row), the pair
+//     {LSE * log2(e), D_i = dO_i . O_i}.
+//  2. bwd_kernel runs two kinds of CTA in one grid:
+//       dK/dV CTAs, one per (128-key tile, KV head, batch row): the key tile's
+//         K and V stay in shared memory while 64-query sub-tiles of Q and dO of
+//         every query head of the group stream past;
+//       dQ CTAs, one per (128-query tile, query head, batch row): Q and dO stay
+//         while 64-key sub-tiles of K and V stream past (the forward's tiles).
+//     Both recompute S and dP, so each (query, key) tile pair costs 7 products
+//     instead of the 5 of a single pass that adds dQ with atomics.
+//
+// CTA roles (320 threads): warps 0-7 turn S and dP into P and dS (two warps
+// per TMEM lane quadrant, each on 32 of the sub-tile's 64 columns), warp 8
+// issues the TMA copies, warp 9 issues the tcgen05 MMAs.  TMEM (512 columns):
+// two sub-tile buffers S_b | dP_b (64 + 64 columns each), then the fp32
+// accumulators (dV | dK, or dQ).  P and dS are written back over S and dP as
+// bf16 pairs and read from TMEM as the A operand of the accumulating products.
+// The issuer runs one sub-tile ahead: S, dP of sub-tile i+1 are issued before
+// it waits for dS of sub-tile i, so the tensor cores work while the softmax
+// warps do.  Tensor-core instructions of one thread execute in issue order,
+// which lets S, dP of sub-tile i+2 overwrite the buffer whose P and dS the
+// products of sub-tile i have just read.
 #include "ps_internal.h"
+#include "ps_math.cuh"
 #include "ps_rope.cuh"
 #include "ps_tc.cuh"
 #include "ps_tiles.cuh"
@@ -33,71 +44,86 @@
 namespace ps {
 namespace bwd {
 
-constexpr int kBM = 128, kBN = 128, kHD = 128;
-constexpr int kHalf = kBM * 64 * 2;  // one 64-column swizzled half block: 16 KB
-constexpr int kTile = 2 * kHalf;     // 128 x 128 bf16: 32 KB
-constexpr uint32_t kIdescSS = tc::idesc_bf16(128, 128, false);  // both operands K-major
-constexpr uint32_t kIdescTS = tc::idesc_bf16(128, 128, true);   // B MN-major
-constexpr int kSmem = 6 * kTile + 2048 /*barriers, LSE and D rows*/ + 1024 /*alignment*/;
+constexpr int kBM = 128;                 // rows of the resident tile
+constexpr int kBC = 64;                  // rows of a streamed sub-tile
+constexpr int kHD = 128;                 // head dim
+constexpr int kHalfR = kBM * 128;        // one 64-column swizzled half of a resident tile: 16 KB
+constexpr int kHalfC = kBC * 128;        // the same for a sub-tile: 8 KB
+constexpr int kTileR = 2 * kHalfR;       // 32 KB
+constexpr int kTileC = 2 * kHalfC;       // 16 KB
+constexpr int kSt = 4;                   // sub-tile stages in flight
+constexpr int kStage = 2 * kTileC;       // two sub-tile operands per stage
+constexpr int kLdBytes = kBC * 8;        // {LSE*log2e, D} pairs of one query sub-tile
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kSmem = 2 * kTileR + kSt * kStage + kSt * kLdBytes + 1024 /*barriers*/ +
+                      1024 /*alignment*/;
+constexpr uint32_t kIdescSub = tc::idesc_bf16(128, kBC, false);  // S, dP: N = 64, K-major B
+constexpr uint32_t kIdescAcc = tc::idesc_bf16(128, kHD, true);   // accumulations: B MN-major
+constexpr uint32_t kTAcc = 256;                                  // accumulator columns
 
 struct Params {
-  CUtensorMap tmq;   // rotated Q  {D, Hq, S, B}
-  CUtensorMap tmk;   // rotated K  {D, Hkv, S, B}
-  CUtensorMap tmv;   // V          {D, Hkv, S, B}
-  CUtensorMap tmdo;  // dO         {D, Hq, S, B}
-  const float* lse;   // [B, Hq, S] natural log
-  const float* dsum;  // [B, Hq, S] D_i = dO_i . O_i
+  CUtensorMap tmq_r, tmq_c;    // rotated Q {D, Hq, S, B}: 128-row and 64-row boxes
+  CUtensorMap tmdo_r, tmdo_c;  // dO
+  CUtensorMap tmk_r, tmk_c;    // rotated K {D, Hkv, S, B}
+  CUtensorMap tmv_r, tmv_c;    // V
+  const float2* ld;            // [B, Hq, s_pad] {LSE * log2(e), D}; rows >= S are zero
   const int32_t* q_start;
   const int32_t* prefix_len;
   float* dq;  // [B, S, Hq, D]
   float* dk;  // [B, S, Hkv, D]
   float* dv;  // [B, S, Hkv, D]
   int32_t* status;
-  int32_t S, hq, hkv, W, nq;
+  int32_t S, s_pad, hq, hkv, W, B;
+  int32_t nq;       // 128-row query tiles
+  int32_t n_dkdv;   // CTAs of the dK/dV kind (the first ones of the grid)
   float scale, scale_log2;
   RopeTurns turns;
 };
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
+struct Bars {
+  uint64_t res_full;                       // the resident tiles have landed
+  uint64_t st_full[kSt], st_empty[kSt];    // sub-tile stages
+  uint64_t s_full[2], ds_ready[2];         // TMEM sub-tile buffers
+  uint64_t done;                           // every accumulation has completed
+  uint32_t tmem_slot;
+  int32_t abort;
+};
 
-// Writes one thread's row of a 128-wide fp32 accumulator, scaled and rotated
-// back by -pos when `rot` (dQ, dK), plainly otherwise (dV).  Every thread of
-// the warp calls it (tcgen05.ld is warp-collective); only rows with `valid`
-// store.
-__device__ __forceinline__ void store_row(uint32_t taddr, float* dst, bool valid, float mul,
-                                          bool rot, int32_t pos, const RopeTurns& turns) {
+// TMEM column of the K16 step kk (16 sub-tile columns) of the bf16 pairs a
+// softmax warp pair writes over a 64-column buffer: the warp on columns
+// [32h, 32h+32) packs them into [32h, 32h+16).
+__device__ __forceinline__ uint32_t packed_col(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
+
+// Writes 32 columns (chunk c: [32c, 32c+32) paired with [64+32c, 96+32c)) of
+// one thread's row of a 128-wide fp32 accumulator, scaled and rotated back by
+// -pos when `rot` (dQ, dK), plainly otherwise (dV).  Every thread of the warp
+// calls it (tcgen05.ld is warp-collective); only rows with `valid` store.
+__device__ __forceinline__ void store_chunk(uint32_t taddr, float* dst, int c, bool valid, float mul,
+                                            bool rot, int32_t pos, const RopeTurns& turns) {
+  uint32_t a[32], b[32];
+  tc::ld32(taddr + c * 32, a);
+  tc::ld32(taddr + 64 + c * 32, b);
+  tc::wait_ld();
+  if (!valid) return;
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {  // columns [32c, 32c+32) pair with [64+32c, 96+32c)
-    uint32_t a[32], b[32];
-    tc::ld32(taddr + c * 32, a);
-    tc::ld32(taddr + 64 + c * 32, b);
-    tc::wait_ld();
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float x = __uint_as_float(a[e]) * mul, y = __uint_as_float(b[e]) * mul;
-      float rx = x, ry = y;
-      if (rot) {
-        float cs, sn;
-        rope_cos_sin(pos, turns.f[c * 32 + e], cs, sn);
-        rx = x * cs + y * sn;  // rotation by -angle
-        ry = y * cs - x * sn;
-      }
-      a[e] = __float_as_uint(rx);
-      b[e] = __float_as_uint(ry);
+  for (int e = 0; e < 32; ++e) {
+    const float x = __uint_as_float(a[e]) * mul, y = __uint_as_float(b[e]) * mul;
+    float rx = x, ry = y;
+    if (rot) {
+      float cs, sn;
+      rope_cos_sin(pos, turns.f[c * 32 + e], cs, sn);
+      rx = x * cs + y * sn;  // rotation by -angle
+      ry = y * cs - x * sn;
     }
-    if (valid) {
+    a[e] = __float_as_uint(rx);
+    b[e] = __float_as_uint(ry);
+  }
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        *reinterpret_cast<uint4*>(dst + c * 32 + e) =
-            make_uint4(a[e], a[e + 1], a[e + 2], a[e + 3]);
-        *reinterpret_cast<uint4*>(dst + 64 + c * 32 + e) =
-            make_uint4(b[e], b[e + 1], b[e + 2], b[e + 3]);
-      }
-    }
+  for (int e = 0; e < 32; e += 4) {
+    *reinterpret_cast<uint4*>(dst + c * 32 + e) = make_uint4(a[e], a[e + 1], a[e + 2], a[e + 3]);
+    *reinterpret_cast<uint4*>(dst + 64 + c * 32 + e) =
+        make_uint4(b[e], b[e + 1], b[e + 2], b[e + 3]);
   }
 }
 
@@ -109,11 +135,12 @@ struct PrepParams {
   const uint4* k;   // [B, S, Hkv, D]
   const uint4* o;   // [B, S, Hq, D] forward output
   const uint4* dout;
+  const float* lse; // [B, Hq, S] natural log
   uint4* qh;        // rotated
   uint4* kh;
-  float* dsum;      // [B, Hq, S]
+  float2* ld;       // [B, Hq, s_pad]
   const int32_t* q_start;
-  int32_t B, S, hq, hkv;
+  int32_t B, S, s_pad, hq, hkv;
   RopeTurns turns;
 };
 
@@ -173,407 +200,455 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ P
       acc = warp_sum(acc);
       if (lane == 0) {
         const int b = (int)(r / p.S);
-        p.dsum[((int64_t)b * p.hq + h) * p.S + (r % p.S)] = acc;
+        const int s = (int)(r % p.S);
+        const float l2 = p.lse[((int64_t)b * p.hq + h) * p.S + s] * 1.4426950408889634f;
+        p.ld[((int64_t)b * p.hq + h) * p.s_pad + s] = make_float2(l2, acc);
       }
     }
     __syncthreads();
   }
+  // padding rows [S, s_pad) of every (batch row, head): zero
+  const int pad = p.s_pad - p.S;
+  const int64_t n_pad = (int64_t)p.B * p.hq * pad;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n_pad;
+       t += (int64_t)gridDim.x * blockDim.x)
+    p.ld[(t / pad) * p.s_pad + p.S + (t % pad)] = make_float2(0.f, 0.f);
 }
 
 // ---------------------------------------------------------------------------
-// 2. dQ: one CTA per (query tile, query head, batch row)
+// softmax-side work of one warp on 32 columns of a sub-tile buffer
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128, 1) bwd_dq_kernel(const __grid_constant__ Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~(uintptr_t)1023);
-  uint8_t* sQ = smem;
-  uint8_t* sdO = smem + kTile;
-  uint8_t* sK = smem + 2 * kTile;  // [2]
-  uint8_t* sV = smem + 4 * kTile;  // [2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * kTile);
-  uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_free = bars + 3;   // [2]: the dQ product that read the stage is done
-  uint64_t* s_done = bars + 5;    // S and dP of the current key tile are in TMEM
-  uint64_t* all_done = bars + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int qt = p.nq - 1 - (int)blockIdx.x;  // longest rows first
-  const int h = blockIdx.y, b = blockIdx.z;
+// dQ side: this thread's query row against 32 keys (key indices base..base+31).
+// Keeps key x iff x < A1 or B0 <= x < B1 (indices relative to base); writes
+// dS = P (dP - D) as bf16 pairs over the first 16 of the 32 dP columns.
+template <bool MASK>
+__device__ __forceinline__ void ds_row(uint32_t tS, uint32_t tP, float scale_log2, float lse2,
+                                       float drow, int32_t A1, int32_t B0, int32_t B1) {
+  uint32_t sv[32], pv[32];
+  tc::ld32(tS, sv);
+  tc::ld32(tP, pv);
+  tc::wait_ld();
+  uint32_t packed[16];
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float x0, x1, t0, t1, d0, d1;
+    ffma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), scale_log2, scale_log2,
+          -lse2, -lse2);
+    x0 = ex2(x0);
+    x1 = ex2(x1);
+    fadd2(t0, t1, __uint_as_float(pv[e]), __uint_as_float(pv[e + 1]), -drow, -drow);
+    fmul2(d0, d1, x0, x1, t0, t1);
+    if (MASK) {
+      d0 = ((e < A1) || (e >= B0 && e < B1)) ? d0 : 0.f;
+      d1 = ((e + 1 < A1) || (e + 1 >= B0 && e + 1 < B1)) ? d1 : 0.f;
+    }
+    packed[e / 2] = pack_bf16(d0, d1);
+  }
+  tc::st16(tP, packed);
+}
+
+// dK/dV side: this thread's key row against 32 queries whose {LSE*log2e, D}
+// pairs are ld[0..31].  Keeps query e iff LO <= e <= HI.  Writes P^T over the
+// S^T columns and dS^T over the dP^T columns, as bf16 pairs.
+template <bool MASK>
+__device__ __forceinline__ void ds_col(uint32_t tS, uint32_t tP, float scale_log2,
+                                       const float4* ld, int32_t LO, int32_t HI) {
+  uint32_t sv[32], pv[32];
+  tc::ld32(tS, sv);
+  tc::ld32(tP, pv);
+  tc::wait_ld();
+  uint32_t pk_p[16], pk_s[16];
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const float4 l = ld[e / 2];  // {lse2_e, D_e, lse2_e+1, D_e+1}, same address on every lane
+    float x0, x1, t0, t1, d0, d1;
+    ffma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), scale_log2, scale_log2,
+          -l.x, -l.z);
+    x0 = ex2(x0);
+    x1 = ex2(x1);
+    fadd2(t0, t1, __uint_as_float(pv[e]), __uint_as_float(pv[e + 1]), -l.y, -l.w);
+    if (MASK) {
+      x0 = (e >= LO && e <= HI) ? x0 : 0.f;
+      x1 = (e + 1 >= LO && e + 1 <= HI) ? x1 : 0.f;
+    }
+    fmul2(d0, d1, x0, x1, t0, t1);
+    pk_p[e / 2] = pack_bf16(x0, x1);
+    pk_s[e / 2] = pack_bf16(d0, d1);
+  }
+  tc::st16(tS, pk_p);
+  tc::st16(tP, pk_s);
+}
+
+// ---------------------------------------------------------------------------
+// 2a. dK/dV CTA: key tile kt of KV head hk, batch row b
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* bar, uint32_t tmem,
+                                         int u) {
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + kTileR;
+  uint8_t* sQ = smem + 2 * kTileR;  // stage st: Q at sQ + st * kStage, dO kTileC after it
+  float2* sLd = reinterpret_cast<float2*>(smem + 2 * kTileR + kSt * kStage);  // [kSt][kBC]
+  volatile int32_t* abort = &bar->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int per = p.hkv * p.B;
+  const int kt = u / per;  // prefix tiles (the longest) first
+  const int hk = (u % per) % p.hkv, b = (u % per) / p.hkv;
+  const int G = p.hq / p.hkv;
+  const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
+  const KeyMap km = make_keymap(p.S, c0, P, p.W, false);
+  const int32_t k0r = kt * kBM, k1r = min(p.S, k0r + kBM) - 1;
+  // query sub-tiles that can admit one of these keys: from the one holding the
+  // first key on; prefix keys are seen by every later query, window keys only
+  // by queries at most W - 1 rows later
+  const int n_qs = (p.S + kBC - 1) / kBC;
+  const int qs_begin = k0r / kBC;
+  int qs_end = n_qs;
+  if ((int64_t)c0 + k0r >= P) qs_end = (int)min((int64_t)n_qs, ((int64_t)k1r + p.W - 1) / kBC + 1);
+  const int n = max(0, qs_end - qs_begin) * G;  // (query sub-tile, head of the group) pairs
+
+  if (warp == kProducerWarp) {
+    if (lane == 0 && n > 0) {
+      prefetch_tmap(&p.tmk_r);
+      prefetch_tmap(&p.tmv_r);
+      prefetch_tmap(&p.tmq_c);
+      prefetch_tmap(&p.tmdo_c);
+      const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
+      mbar_arrive_expect_tx(&bar->res_full, 2 * kTileR);
+      tma_load_4d(sK, &p.tmk_r, &bar->res_full, 0, hk, k0r, b, pol_kv);
+      tma_load_4d(sK + kHalfR, &p.tmk_r, &bar->res_full, 64, hk, k0r, b, pol_kv);
+      tma_load_4d(sV, &p.tmv_r, &bar->res_full, 0, hk, k0r, b, pol_kv);
+      tma_load_4d(sV + kHalfR, &p.tmv_r, &bar->res_full, 64, hk, k0r, b, pol_kv);
+      for (int i = 0; i < n; ++i) {
+        const int st = i % kSt;
+        if (!mbar_wait_abort(&bar->st_empty[st], ((i / kSt) & 1) ^ 1, abort)) break;
+        const int qs = qs_begin + i / G, h = hk * G + i % G;
+        uint8_t* dq = sQ + st * kStage;
+        uint64_t* full = &bar->st_full[st];
+        mbar_arrive_expect_tx(full, kStage + kLdBytes);
+        tma_load_4d(dq, &p.tmq_c, full, 0, h, qs * kBC, b, pol_q);
+        tma_load_4d(dq + kHalfC, &p.tmq_c, full, 64, h, qs * kBC, b, pol_q);
+        tma_load_4d(dq + kTileC, &p.tmdo_c, full, 0, h, qs * kBC, b, pol_q);
+        tma_load_4d(dq + kTileC + kHalfC, &p.tmdo_c, full, 64, h, qs * kBC, b, pol_q);
+        bulk_load(sLd + st * kBC, p.ld + ((int64_t)b * p.hq + h) * p.s_pad + qs * kBC, kLdBytes,
+                  full);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && n > 0) {
+      const uint64_t aK = tc::sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t aV = tc::sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t bQ = tc::sdesc_sw128(smem_u32(sQ), 16, 1024);            // K-major B
+      const uint64_t bO = tc::sdesc_sw128(smem_u32(sQ + kTileC), 16, 1024);
+      const uint64_t bQm = tc::sdesc_sw128(smem_u32(sQ), kHalfC, 1024);       // MN-major B
+      const uint64_t bOm = tc::sdesc_sw128(smem_u32(sQ + kTileC), kHalfC, 1024);
+      // S^T = K Q^T and dP^T = V dO^T of sub-tile i into buffer i & 1
+      auto sdp = [&](int i) -> bool {
+        const int st = i % kSt, bf = i & 1;
+        if (!mbar_wait_abort(&bar->st_full[st], (i / kSt) & 1, abort)) return false;
+        tc::fence_after();
+        const uint64_t so = (uint64_t)((st * kStage) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kHD / 16; ++kk) {
+          const uint32_t oa = ((kk >> 2) * kHalfR + (kk & 3) * 32) >> 4;
+          const uint32_t ob = ((kk >> 2) * kHalfC + (kk & 3) * 32) >> 4;
+          tc::mma_bf16(tmem + bf * 128, aK + oa, bQ + so + ob, kIdescSub, kk > 0);
+          tc::mma_bf16(tmem + bf * 128 + 64, aV + oa, bO + so + ob, kIdescSub, kk > 0);
+        }
+        tc::commit(smem_u32(&bar->s_full[bf]));
+        return true;
+      };
+      // dV += P^T dO and dK += dS^T Q of sub-tile i, then release its stage
+      auto acc = [&](int i) -> bool {
+        const int st = i % kSt, bf = i & 1;
+        if (!mbar_wait_abort(&bar->ds_ready[bf], (i >> 1) & 1, abort)) return false;
+        tc::fence_after();
+        const uint64_t so = (uint64_t)((st * kStage) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kBC / 16; ++kk) {
+          const uint32_t ob = (kk * 2048) >> 4;
+          tc::mma_bf16_ts(tmem + kTAcc, tmem + bf * 128 + packed_col(kk), bOm + so + ob,
+                          kIdescAcc, i > 0 || kk > 0);
+          tc::mma_bf16_ts(tmem + kTAcc + 128, tmem + bf * 128 + 64 + packed_col(kk),
+                          bQm + so + ob, kIdescAcc, i > 0 || kk > 0);
+        }
+        tc::commit(smem_u32(&bar->st_empty[st]));
+        return true;
+      };
+      bool ok = mbar_wait_abort(&bar->res_full, 0, abort);
+      for (int i = 0; ok && i < n; ++i) {
+        ok = sdp(i);
+        if (ok && i > 0) ok = acc(i - 1);
+      }
+      if (ok) ok = acc(n - 1);
+      if (ok) tc::commit(smem_u32(&bar->done));
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;  // key row of the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int64_t kpos = (int64_t)c0 + k0r + row;
+    // queries that admit this key: positions [kpos, kend]
+    const int64_t kend = kpos < P ? INT64_MAX / 2 : kpos + p.W - 1;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int st = i % kSt, bf = i & 1;
+      const int qs = qs_begin + i / G;
+      const int32_t qa = qs * kBC, qb = min(p.S, qa + kBC) - 1;
+      const bool masked = qa + kBC > p.S ||
+                          tile_class(km, c0, qa, qb, k0r, k1r, P, p.W) != kFull;
+      // this warp's 32 queries: rows r0 + e, e = 0..31
+      const int32_t r0 = qa + half * 32;
+      const int64_t qp0 = (int64_t)c0 + r0;
+      const int64_t lo64 = kpos - qp0;
+      int64_t hi64 = kend - qp0;
+      if (hi64 > (int64_t)(p.S - 1 - r0)) hi64 = (int64_t)(p.S - 1 - r0);
+      const int32_t lo = (int32_t)(lo64 < 0 ? 0 : (lo64 > 32 ? 32 : lo64));
+      const int32_t hi = (int32_t)(hi64 < -1 ? -1 : (hi64 > 31 ? 31 : hi64));
+      ok = mbar_wait_abort(&bar->s_full[bf], (i >> 1) & 1, abort) &&
+           mbar_wait_abort(&bar->st_full[st], (i / kSt) & 1, abort);  // the LSE / D pairs
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+      const float4* ld = reinterpret_cast<const float4*>(sLd + st * kBC + half * 32);
+      const uint32_t tS = tmem + bf * 128 + half * 32 + lane_off;
+      if (masked)
+        ds_col<true>(tS, tS + 64, p.scale_log2, ld, lo, hi);
+      else
+        ds_col<false>(tS, tS + 64, p.scale_log2, ld, 0, 31);
+      tc::wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar->ds_ready[bf]);
+    }
+    if (ok && n > 0) {
+      ok = mbar_wait_abort(&bar->done, 0, abort);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc::fence_after();
+      const bool valid = k0r + row <= k1r;
+      const int64_t base = (((int64_t)b * p.S + (valid ? k0r + row : 0)) * p.hkv + hk) * kHD;
+      if (n > 0) {
+        store_chunk(tmem + kTAcc + lane_off, p.dv + base, half, valid, 1.f, false, 0, p.turns);
+        store_chunk(tmem + kTAcc + 128 + lane_off, p.dk + base, half, valid, p.scale, true,
+                    (int32_t)kpos, p.turns);
+      } else if (valid) {  // no query admits these keys: zero gradients
+        for (int e = half * 32; e < half * 32 + 32; e += 4) {
+          *reinterpret_cast<float4*>(p.dv + base + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(p.dv + base + 64 + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(p.dk + base + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(p.dk + base + 64 + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2b. dQ CTA: query tile of head h, batch row b
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar, uint32_t tmem,
+                                       int u) {
+  uint8_t* sQ = smem;
+  uint8_t* sdO = smem + kTileR;
+  uint8_t* sK = smem + 2 * kTileR;  // stage st: K at sK + st * kStage, V kTileC after it
+  volatile int32_t* abort = &bar->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int per = p.hq * p.B;
+  const int qt = p.nq - 1 - u / per;  // longest rows first
+  const int h = (u % per) % p.hq, b = (u % per) / p.hq;
   const int hk = h / (p.hq / p.hkv);
   const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
   const KeyMap km = make_keymap(p.S, c0, P, p.W, false);
   const int32_t q0r = qt * kBM, q1r = min(p.S, q0r + kBM) - 1;
   const int64_t q0 = (int64_t)c0 + q0r, q1 = (int64_t)c0 + q1r;
-  // key tiles that can hold an admitted pair: the prefix tiles, then the band
+  // 64-key sub-tiles that can hold an admitted pair: prefix ones, then the band
   const int32_t kc = keys_below(km, q1 + 1);
   const int32_t kP = keys_below(km, P);
-  const int t1_end = (min(kP, kc) + kBN - 1) / kBN;
+  const int t1_end = (min(kP, kc) + kBC - 1) / kBC;
   const int32_t kw = keys_below(km, q0 - p.W + 1);
-  const int t2_begin = max(t1_end, kw / kBN);
-  const int t2_end = (kc + kBN - 1) / kBN;
-  const int n_tiles = t1_end + max(0, t2_end - t2_begin);
-  auto tile_at = [&](int it) { return it < t1_end ? it : t2_begin + (it - t1_end); };
+  const int t2_begin = max(t1_end, kw / kBC);
+  const int t2_end = (kc + kBC - 1) / kBC;
+  const int n = t1_end + max(0, t2_end - t2_begin);
+  auto sub_at = [&](int i) { return i < t1_end ? i : t2_begin + (i - t1_end); };
 
-  if (warp == 0) {
-    tc::alloc(smem_u32(tmem_slot), 512);
-    tc::relinquish();
-  }
-  if (tid == 0) {
-    for (int i = 0; i < 7; ++i) mbar_init(&bars[i], 1);
-    fence_mbar_init();
-  }
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256;  // S | dP -> dS | dQ
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  grid_dependency_wait();
-
-  const uint64_t pol = policy_evict_last();
-  auto load_kv = [&](int stage, int kt) {
-    mbar_arrive_expect_tx(&kv_full[stage], 2 * kTile);
-    tma_load_4d(sK + stage * kTile, &p.tmk, &kv_full[stage], 0, hk, kt * kBN, b, pol);
-    tma_load_4d(sK + stage * kTile + kHalf, &p.tmk, &kv_full[stage], 64, hk, kt * kBN, b, pol);
-    tma_load_4d(sV + stage * kTile, &p.tmv, &kv_full[stage], 0, hk, kt * kBN, b, pol);
-    tma_load_4d(sV + stage * kTile + kHalf, &p.tmv, &kv_full[stage], 64, hk, kt * kBN, b, pol);
-  };
-  const uint64_t dq_ = tc::sdesc_sw128(smem_u32(sQ), 16, 1024);
-  const uint64_t ddo = tc::sdesc_sw128(smem_u32(sdO), 16, 1024);
-  const uint64_t dk_ = tc::sdesc_sw128(smem_u32(sK), 16, 1024);
-  const uint64_t dv_ = tc::sdesc_sw128(smem_u32(sV), 16, 1024);
-  const uint64_t dkm = tc::sdesc_sw128(smem_u32(sK), kHalf, 1024);  // K as an MN-major B
-  if (tid == 0 && n_tiles > 0) {
-    prefetch_tmap(&p.tmq);
-    prefetch_tmap(&p.tmk);
-    prefetch_tmap(&p.tmv);
-    prefetch_tmap(&p.tmdo);
-    mbar_arrive_expect_tx(q_full, 2 * kTile);
-    tma_load_4d(sQ, &p.tmq, q_full, 0, h, q0r, b, pol);
-    tma_load_4d(sQ + kHalf, &p.tmq, q_full, 64, h, q0r, b, pol);
-    tma_load_4d(sdO, &p.tmdo, q_full, 0, h, q0r, b, pol);
-    tma_load_4d(sdO + kHalf, &p.tmdo, q_full, 64, h, q0r, b, pol);
-    for (int i = 0; i < 2 && i < n_tiles; ++i) load_kv(i, tile_at(i));
-  }
-
-  const int row = tid;
-  const int32_t qrow = min(q0r + row, p.S - 1);
-  const int64_t qpos = q0 + row;
-  const float lse2 = p.lse[((int64_t)b * p.hq + h) * p.S + qrow] * 1.4426950408889634f;
-  const float drow = p.dsum[((int64_t)b * p.hq + h) * p.S + qrow];
-  // admitted key indices of this row: [0, a1) and [b0, b1)
-  const int32_t a1 = keys_below(km, min((int64_t)P, qpos + 1));
-  const int32_t b0 = keys_below(km, max((int64_t)0, qpos - p.W + 1));
-  const int32_t b1 = keys_below(km, qpos + 1);
-  bool ok = true;
-  for (int it = 0; it < n_tiles; ++it) {
-    const int st = it & 1;
-    const int kt = tile_at(it);
-    const int32_t ka = kt * kBN;
-    if (tid == 0) {
-      bool w = (it > 0 || mbar_wait(q_full, 0)) && mbar_wait(&kv_full[st], (it >> 1) & 1);
-      if (w) {
+  if (warp == kProducerWarp) {
+    if (lane == 0 && n > 0) {
+      prefetch_tmap(&p.tmq_r);
+      prefetch_tmap(&p.tmdo_r);
+      prefetch_tmap(&p.tmk_c);
+      prefetch_tmap(&p.tmv_c);
+      const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
+      mbar_arrive_expect_tx(&bar->res_full, 2 * kTileR);
+      tma_load_4d(sQ, &p.tmq_r, &bar->res_full, 0, h, q0r, b, pol_q);
+      tma_load_4d(sQ + kHalfR, &p.tmq_r, &bar->res_full, 64, h, q0r, b, pol_q);
+      tma_load_4d(sdO, &p.tmdo_r, &bar->res_full, 0, h, q0r, b, pol_q);
+      tma_load_4d(sdO + kHalfR, &p.tmdo_r, &bar->res_full, 64, h, q0r, b, pol_q);
+      for (int i = 0; i < n; ++i) {
+        const int st = i % kSt;
+        if (!mbar_wait_abort(&bar->st_empty[st], ((i / kSt) & 1) ^ 1, abort)) break;
+        const int ka = sub_at(i) * kBC;
+        uint8_t* dk = sK + st * kStage;
+        uint64_t* full = &bar->st_full[st];
+        mbar_arrive_expect_tx(full, kStage);
+        tma_load_4d(dk, &p.tmk_c, full, 0, hk, ka, b, pol_kv);
+        tma_load_4d(dk + kHalfC, &p.tmk_c, full, 64, hk, ka, b, pol_kv);
+        tma_load_4d(dk + kTileC, &p.tmv_c, full, 0, hk, ka, b, pol_kv);
+        tma_load_4d(dk + kTileC + kHalfC, &p.tmv_c, full, 64, hk, ka, b, pol_kv);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && n > 0) {
+      const uint64_t aQ = tc::sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t aO = tc::sdesc_sw128(smem_u32(sdO), 16, 1024);
+      const uint64_t bK = tc::sdesc_sw128(smem_u32(sK), 16, 1024);               // K-major B
+      const uint64_t bV = tc::sdesc_sw128(smem_u32(sK + kTileC), 16, 1024);
+      const uint64_t bKm = tc::sdesc_sw128(smem_u32(sK), kHalfC, 1024);          // MN-major B
+      // S = Q K^T and dP = dO V^T of sub-tile i into buffer i & 1
+      auto sdp = [&](int i) -> bool {
+        const int st = i % kSt, bf = i & 1;
+        if (!mbar_wait_abort(&bar->st_full[st], (i / kSt) & 1, abort)) return false;
         tc::fence_after();
-        const uint64_t bk = dk_ + (uint64_t)((st * kTile) >> 4), bv = dv_ + (uint64_t)((st * kTile) >> 4);
+        const uint64_t so = (uint64_t)((st * kStage) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-          tc::mma_bf16(tS, dq_ + off, bk + off, kIdescSS, kk > 0);   // S = Q K^T
-          tc::mma_bf16(tP, ddo + off, bv + off, kIdescSS, kk > 0);   // dP = dO V^T
+          const uint32_t oa = ((kk >> 2) * kHalfR + (kk & 3) * 32) >> 4;
+          const uint32_t ob = ((kk >> 2) * kHalfC + (kk & 3) * 32) >> 4;
+          tc::mma_bf16(tmem + bf * 128, aQ + oa, bK + so + ob, kIdescSub, kk > 0);
+          tc::mma_bf16(tmem + bf * 128 + 64, aO + oa, bV + so + ob, kIdescSub, kk > 0);
         }
-      } else {
-        ok = false;
+        tc::commit(smem_u32(&bar->s_full[bf]));
+        return true;
+      };
+      // dQ += dS K of sub-tile i, then release its stage
+      auto acc = [&](int i) -> bool {
+        const int st = i % kSt, bf = i & 1;
+        if (!mbar_wait_abort(&bar->ds_ready[bf], (i >> 1) & 1, abort)) return false;
+        tc::fence_after();
+        const uint64_t so = (uint64_t)((st * kStage) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kBC / 16; ++kk)
+          tc::mma_bf16_ts(tmem + kTAcc, tmem + bf * 128 + 64 + packed_col(kk),
+                          bKm + so + ((kk * 2048) >> 4), kIdescAcc, i > 0 || kk > 0);
+        tc::commit(smem_u32(&bar->st_empty[st]));
+        return true;
+      };
+      bool ok = mbar_wait_abort(&bar->res_full, 0, abort);
+      for (int i = 0; ok && i < n; ++i) {
+        ok = sdp(i);
+        if (ok && i > 0) ok = acc(i - 1);
       }
-      tc::commit(smem_u32(s_done));
-      // the stage two tiles back is free once its dQ product is done: refill it
-      if (w && it >= 1 && it + 1 < n_tiles) {
-        const int sp = (it + 1) & 1;
-        if (mbar_wait(&kv_free[sp], ((it - 1) >> 1) & 1)) {
-          fence_proxy_async_smem();
-          load_kv(sp, tile_at(it + 1));
-        } else {
-          ok = false;
-        }
-      }
+      if (ok) ok = acc(n - 1);
+      if (ok) tc::commit(smem_u32(&bar->done));
     }
-    if (!mbar_wait(s_done, it & 1)) ok = false;
     __syncwarp();
-    tc::fence_after();
-    // dS = P (dP - D) over this row, 32 keys at a time, written as bf16 over dP
-#pragma unroll
-    for (int c = 0; c < kBN / 32; ++c) {
-      uint32_t sv[32], pv[32];
-      tc::ld32(tS + lane_off + c * 32, sv);
-      tc::ld32(tP + lane_off + c * 32, pv);
-      tc::wait_ld();
-      uint32_t packed[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float ds2[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int32_t kx = ka + c * 32 + e + u;
-          const bool keep = (kx < a1) || (kx >= b0 && kx < b1);
-          const float pr = keep ? ex2(__uint_as_float(sv[e + u]) * p.scale_log2 - lse2) : 0.f;
-          ds2[u] = pr * (__uint_as_float(pv[e + u]) - drow);
-        }
-        packed[e / 2] = pack_bf16(ds2[0], ds2[1]);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;  // query row of the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int64_t qpos = q0 + row;
+    const float2 ldr = p.ld[((int64_t)b * p.hq + h) * p.s_pad + q0r + row];  // rows < s_pad
+    // admitted key indices of this row: [0, a1) and [b0, b1)
+    const int32_t a1 = keys_below(km, min((int64_t)P, qpos + 1));
+    const int32_t b0 = keys_below(km, max((int64_t)0, qpos - p.W + 1));
+    const int32_t b1 = keys_below(km, qpos + 1);
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int bf = i & 1;
+      const int32_t ka = sub_at(i) * kBC;
+      const int32_t kb = min(km.n_keys, ka + kBC) - 1;
+      const bool masked = ka + kBC > km.n_keys ||
+                          tile_class(km, c0, q0r, q1r, ka, kb, P, p.W) != kFull;
+      const int32_t base = ka + half * 32;
+      ok = mbar_wait_abort(&bar->s_full[bf], (i >> 1) & 1, abort);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
       }
-      // chunk c's 16 packed columns land on dP columns already read (16c < 32c + 32)
-      uint32_t* pk = packed;
-      asm volatile(
-          "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
-          "%10, %11, %12, %13, %14, %15, %16};" ::"r"(tP + lane_off + c * 16),
-          "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]),
-          "r"(pk[7]), "r"(pk[8]), "r"(pk[9]), "r"(pk[10]), "r"(pk[11]), "r"(pk[12]), "r"(pk[13]),
-          "r"(pk[14]), "r"(pk[15])
-          : "memory");
-    }
-    tc::wait_st();
-    tc::fence_before();
-    ok = __syncthreads_and(ok) != 0;
-    if (!ok) break;
-    if (tid == 0) {  // dQ += dS K
       tc::fence_after();
-      const uint64_t bk = dkm + (uint64_t)((st * kTile) >> 4);
-#pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk)
-        tc::mma_bf16_ts(tQ, tP + kk * 8, bk + ((kk * 2048) >> 4), kIdescTS, it > 0 || kk > 0);
-      tc::commit(smem_u32(&kv_free[st]));
+      const uint32_t tS = tmem + bf * 128 + half * 32 + lane_off;
+      if (masked)
+        ds_row<true>(tS, tS + 64, p.scale_log2, ldr.x, ldr.y, a1 - base, b0 - base, b1 - base);
+      else
+        ds_row<false>(tS, tS + 64, p.scale_log2, ldr.x, ldr.y, 0, 0, 0);
+      tc::wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar->ds_ready[bf]);
+    }
+    if (ok && n > 0) {
+      ok = mbar_wait_abort(&bar->done, 0, abort);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc::fence_after();
+      const bool valid = q0r + row <= q1r;
+      float* dst = p.dq + (((int64_t)b * p.S + (valid ? q0r + row : 0)) * p.hq + h) * kHD;
+      if (n > 0) {
+        store_chunk(tmem + kTAcc + lane_off, dst, half, valid, p.scale, true, (int32_t)qpos,
+                    p.turns);
+      } else if (valid) {
+        for (int e = half * 32; e < half * 32 + 32; e += 4) {
+          *reinterpret_cast<float4*>(dst + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(dst + 64 + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
     }
   }
-  if (tid == 0) tc::commit(smem_u32(all_done));
-  if (ok && n_tiles > 0 && !mbar_wait(all_done, 0)) ok = false;
-  ok = __syncthreads_and(ok) != 0;
-  if (ok && n_tiles > 0) {
-    tc::fence_after();
-    const bool valid = q0r + row <= q1r;
-    store_row(tQ + lane_off, p.dq + (((int64_t)b * p.S + (valid ? q0r + row : 0)) * p.hq + h) * kHD,
-              valid, p.scale, true, (int32_t)qpos, p.turns);
-  } else if (!ok && tid == 0) {
-    set_flag(p.status, PS_DEV_TIMEOUT);
-  }
-  tc::fence_before();
-  __syncthreads();
-  if (!ok) {  // let copies and products already issued land before releasing memory
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 100000ull) {
-    }
-    __syncthreads();
-  }
-  tc::fence_after();
-  if (warp == 0) tc::dealloc(tmem, 512);
 }
 
-// ---------------------------------------------------------------------------
-// 3. dK, dV: one CTA per (key tile, KV head, batch row)
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128, 1) bwd_dkdv_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
-  uint8_t* sK = smem;
-  uint8_t* sV = smem + kTile;
-  uint8_t* sQ = smem + 2 * kTile;   // [2]
-  uint8_t* sdO = smem + 4 * kTile;  // [2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * kTile);
-  uint64_t* kv_full = bars + 0;
-  uint64_t* q_full = bars + 1;  // [2]
-  uint64_t* q_free = bars + 3;  // [2]
-  uint64_t* s_done = bars + 5;
-  uint64_t* all_done = bars + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
-  float* sl = reinterpret_cast<float*>(bars + 16);  // [2][128] LSE (log2) then D of a query tile
-
+  Bars* bar = reinterpret_cast<Bars*>(smem + 2 * kTileR + kSt * kStage + kSt * kLdBytes);
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int kt = (int)blockIdx.x;
-  const int hk = blockIdx.y, b = blockIdx.z;
-  const int G = p.hq / p.hkv;
-  const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
-  const int32_t k0r = kt * kBN, k1r = min(p.S, k0r + kBN) - 1;
-  const int64_t kpos0 = (int64_t)c0 + k0r, kpos1 = (int64_t)c0 + k1r;
-  // query tiles that can admit one of these keys: from the tile holding the
-  // first key onwards; prefix keys are seen by every later query, window keys
-  // only by queries up to W - 1 positions later
-  const int qt_begin = k0r / kBM;
-  int qt_end = p.nq;
-  if (kpos0 >= P) {
-    const int64_t last = kpos1 + p.W - 1 - c0;  // last query row that sees key k1r
-    qt_end = (int)min((int64_t)p.nq, last / kBM + 1);
-  }
-  const int n_q = max(0, qt_end - qt_begin);
-  const int n_iter = n_q * G;  // (query tile, head of the group) pairs
-
   if (warp == 0) {
-    tc::alloc(smem_u32(tmem_slot), 512);
+    tc::alloc(smem_u32(&bar->tmem_slot), 512);
     tc::relinquish();
   }
-  if (tid == 0) {
-    for (int i = 0; i < 7; ++i) mbar_init(&bars[i], 1);
+  if (tid == 32) {
+    mbar_init(&bar->res_full, 1);
+    for (int s = 0; s < kSt; ++s) {
+      mbar_init(&bar->st_full[s], 1);
+      mbar_init(&bar->st_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar->s_full[i], 1);
+      mbar_init(&bar->ds_ready[i], 8);  // one arrival per softmax warp
+    }
+    mbar_init(&bar->done, 1);
+    bar->abort = 0;
     fence_mbar_init();
   }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  const uint32_t tmem = *tmem_slot;
-  // S^T -> P^T | dP^T -> dS^T | dV | dK
-  const uint32_t tS = tmem, tP = tmem + 128, tV = tmem + 256, tK = tmem + 384;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  grid_dependency_wait();
+  const uint32_t tmem = bar->tmem_slot;
+  grid_dependency_wait();  // rotated Q / K and the LSE / D pairs come from the pre-pass
 
-  const uint64_t pol = policy_evict_last();
-  auto load_q = [&](int stage, int j) {  // pair j: query tile qt_begin + j / G, head hk*G + j % G
-    const int qt = qt_begin + j / G, h = hk * G + j % G;
-    mbar_arrive_expect_tx(&q_full[stage], 2 * kTile);
-    tma_load_4d(sQ + stage * kTile, &p.tmq, &q_full[stage], 0, h, qt * kBM, b, pol);
-    tma_load_4d(sQ + stage * kTile + kHalf, &p.tmq, &q_full[stage], 64, h, qt * kBM, b, pol);
-    tma_load_4d(sdO + stage * kTile, &p.tmdo, &q_full[stage], 0, h, qt * kBM, b, pol);
-    tma_load_4d(sdO + stage * kTile + kHalf, &p.tmdo, &q_full[stage], 64, h, qt * kBM, b, pol);
-  };
-  const uint64_t dk_ = tc::sdesc_sw128(smem_u32(sK), 16, 1024);
-  const uint64_t dv_ = tc::sdesc_sw128(smem_u32(sV), 16, 1024);
-  const uint64_t dq_ = tc::sdesc_sw128(smem_u32(sQ), 16, 1024);
-  const uint64_t ddo = tc::sdesc_sw128(smem_u32(sdO), 16, 1024);
-  const uint64_t dqm = tc::sdesc_sw128(smem_u32(sQ), kHalf, 1024);   // Q as an MN-major B
-  const uint64_t ddom = tc::sdesc_sw128(smem_u32(sdO), kHalf, 1024); // dO as an MN-major B
-  if (tid == 0 && n_iter > 0) {
-    prefetch_tmap(&p.tmq);
-    prefetch_tmap(&p.tmk);
-    prefetch_tmap(&p.tmv);
-    prefetch_tmap(&p.tmdo);
-    mbar_arrive_expect_tx(kv_full, 2 * kTile);
-    tma_load_4d(sK, &p.tmk, kv_full, 0, hk, k0r, b, pol);
-    tma_load_4d(sK + kHalf, &p.tmk, kv_full, 64, hk, k0r, b, pol);
-    tma_load_4d(sV, &p.tmv, kv_full, 0, hk, k0r, b, pol);
-    tma_load_4d(sV + kHalf, &p.tmv, kv_full, 64, hk, k0r, b, pol);
-    for (int i = 0; i < 2 && i < n_iter; ++i) load_q(i, i);
-  }
+  const int u = (int)blockIdx.x;
+  if (u < p.n_dkdv)
+    dkdv_cta(p, smem, bar, tmem, u);
+  else
+    dq_cta(p, smem, bar, tmem, u - p.n_dkdv);
 
-  const int row = tid;  // key row of the tile
-  const int64_t kpos = kpos0 + row;
-  // queries that admit this key: positions [kpos, kend] (prefix keys: all later ones)
-  const int64_t kend = kpos < P ? INT64_MAX : kpos + p.W - 1;
-  bool ok = true;
-  for (int it = 0; it < n_iter; ++it) {
-    const int st = it & 1;
-    const int qt = qt_begin + it / G, h = hk * G + it % G;
-    const int32_t q0r = qt * kBM;
-    const int64_t qp0 = (int64_t)c0 + q0r;
-    // LSE (log2) and D of the tile's 128 queries, for every key row
-    __syncthreads();  // the previous iteration's readers of sl are done
-    {
-      const int32_t qr = min(q0r + tid, p.S - 1);
-      sl[tid] = p.lse[((int64_t)b * p.hq + h) * p.S + qr] * 1.4426950408889634f;
-      sl[128 + tid] = p.dsum[((int64_t)b * p.hq + h) * p.S + qr];
-    }
-    if (tid == 0) {
-      bool w = (it > 0 || mbar_wait(kv_full, 0)) && mbar_wait(&q_full[st], (it >> 1) & 1);
-      if (w) {
-        tc::fence_after();
-        const uint64_t bq = dq_ + (uint64_t)((st * kTile) >> 4), bo = ddo + (uint64_t)((st * kTile) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kHD / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-          tc::mma_bf16(tS, dk_ + off, bq + off, kIdescSS, kk > 0);   // S^T = K Q^T
-          tc::mma_bf16(tP, dv_ + off, bo + off, kIdescSS, kk > 0);   // dP^T = V dO^T
-        }
-      } else {
-        ok = false;
-      }
-      tc::commit(smem_u32(s_done));
-      if (w && it >= 1 && it + 1 < n_iter) {
-        const int sp = (it + 1) & 1;
-        if (mbar_wait(&q_free[sp], ((it - 1) >> 1) & 1)) {
-          fence_proxy_async_smem();
-          load_q(sp, it + 1);
-        } else {
-          ok = false;
-        }
-      }
-    }
-    __syncthreads();  // sl is written
-    if (!mbar_wait(s_done, it & 1)) ok = false;
-    __syncwarp();
-    tc::fence_after();
-#pragma unroll
-    for (int c = 0; c < kBM / 32; ++c) {
-      uint32_t sv[32], pv[32];
-      tc::ld32(tS + lane_off + c * 32, sv);
-      tc::ld32(tP + lane_off + c * 32, pv);
-      tc::wait_ld();
-      uint32_t pk_p[16], pk_s[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float pr2[2], ds2[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int i = c * 32 + e + u;  // query of the tile
-          const int64_t qpos = qp0 + i;
-          const bool keep = q0r + i < p.S && qpos >= kpos && qpos <= kend;
-          const float pr = keep ? ex2(__uint_as_float(sv[e + u]) * p.scale_log2 - sl[i]) : 0.f;
-          pr2[u] = pr;
-          ds2[u] = pr * (__uint_as_float(pv[e + u]) - sl[128 + i]);
-        }
-        pk_p[e / 2] = pack_bf16(pr2[0], pr2[1]);
-        pk_s[e / 2] = pack_bf16(ds2[0], ds2[1]);
-      }
-      uint32_t* a = pk_p;
-      asm volatile(
-          "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
-          "%10, %11, %12, %13, %14, %15, %16};" ::"r"(tS + lane_off + c * 16),
-          "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
-          "r"(a[8]), "r"(a[9]), "r"(a[10]), "r"(a[11]), "r"(a[12]), "r"(a[13]), "r"(a[14]),
-          "r"(a[15])
-          : "memory");
-      uint32_t* d = pk_s;
-      asm volatile(
-          "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
-          "%10, %11, %12, %13, %14, %15, %16};" ::"r"(tP + lane_off + c * 16),
-          "r"(d[0]), "r"(d[1]), "r"(d[2]), "r"(d[3]), "r"(d[4]), "r"(d[5]), "r"(d[6]), "r"(d[7]),
-          "r"(d[8]), "r"(d[9]), "r"(d[10]), "r"(d[11]), "r"(d[12]), "r"(d[13]), "r"(d[14]),
-          "r"(d[15])
-          : "memory");
-    }
-    tc::wait_st();
-    tc::fence_before();
-    ok = __syncthreads_and(ok) != 0;
-    if (!ok) break;
-    if (tid == 0) {  // dV += P^T dO, dK += dS^T Q
-      tc::fence_after();
-      const uint64_t bo = ddom + (uint64_t)((st * kTile) >> 4), bq = dqm + (uint64_t)((st * kTile) >> 4);
-#pragma unroll
-      for (int kk = 0; kk < kBM / 16; ++kk) {
-        tc::mma_bf16_ts(tV, tS + kk * 8, bo + ((kk * 2048) >> 4), kIdescTS, it > 0 || kk > 0);
-        tc::mma_bf16_ts(tK, tP + kk * 8, bq + ((kk * 2048) >> 4), kIdescTS, it > 0 || kk > 0);
-      }
-      tc::commit(smem_u32(&q_free[st]));
-    }
-  }
-  if (tid == 0) tc::commit(smem_u32(all_done));
-  if (ok && n_iter > 0 && !mbar_wait(all_done, 0)) ok = false;
-  ok = __syncthreads_and(ok) != 0;
-  if (ok) {
-    tc::fence_after();
-    const bool valid = k0r + row <= k1r;
-    const int64_t base = (((int64_t)b * p.S + (valid ? k0r + row : 0)) * p.hkv + hk) * kHD;
-    if (n_iter > 0) {
-      store_row(tV + lane_off, p.dv + base, valid, 1.f, false, 0, p.turns);
-      store_row(tK + lane_off, p.dk + base, valid, p.scale, true, (int32_t)kpos, p.turns);
-    } else if (valid) {  // no query admits these keys: zero gradients
-      for (int e = 0; e < kHD; e += 4) {
-        *reinterpret_cast<float4*>(p.dv + base + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(p.dk + base + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-  } else if (tid == 0) {
-    set_flag(p.status, PS_DEV_TIMEOUT);
-  }
   tc::fence_before();
   __syncthreads();
-  if (!ok) {
+  if (bar->abort) {
+    if (tid == 0) set_flag(p.status, PS_DEV_TIMEOUT);
+    // copies and products already issued finish on their own within microseconds;
+    // give them time before the CTA's shared and tensor memory are released
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < 100000ull) {
     }
@@ -586,15 +661,17 @@ __global__ void __launch_bounds__(128, 1) bwd_dkdv_kernel(const __grid_constant_
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t q_off, k_off, d_off, total;
+  size_t q_off, k_off, ld_off, total;
+  int32_t s_pad;
 };
 
 static Layout layout(int B, int S, int hq, int hkv, int D) {
   Layout L;
+  L.s_pad = (S + kBM - 1) / kBM * kBM;
   L.q_off = 0;
   L.k_off = align256((size_t)B * S * hq * D * 2);
-  L.d_off = L.k_off + align256((size_t)B * S * hkv * D * 2);
-  L.total = L.d_off + align256((size_t)B * hq * S * 4);
+  L.ld_off = L.k_off + align256((size_t)B * S * hkv * D * 2);
+  L.total = L.ld_off + align256((size_t)B * hq * L.s_pad * 8);
   return L;
 }
 
@@ -628,13 +705,16 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
       n_q_heads % n_kv_heads || !(scale > 0.f) || !(rope_theta > 0.0))
     return PS_ERR_INVALID_ARGUMENT;
   if (head_dim != bwd::kHD) return PS_ERR_UNSUPPORTED;
-  if (batch > 65535 || n_q_heads > 65535) return PS_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(d_out) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return PS_ERR_ALIGNMENT;
   const bwd::Layout L = bwd::layout(batch, seqlen, n_q_heads, n_kv_heads, head_dim);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PS_ERR_WORKSPACE;
   if (workspace_bytes < L.total) return PS_ERR_WORKSPACE;
+  const int32_t nq = (seqlen + bwd::kBM - 1) / bwd::kBM;
+  const int64_t n_dkdv = (int64_t)nq * n_kv_heads * batch;
+  const int64_t n_dq = (int64_t)nq * n_q_heads * batch;
+  if (n_dkdv + n_dq > 0x7fffffffLL) return PS_ERR_UNSUPPORTED;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = (cudaStream_t)stream;
 
@@ -643,12 +723,14 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
   g.k = static_cast<const uint4*>(k);
   g.o = static_cast<const uint4*>(out);
   g.dout = static_cast<const uint4*>(d_out);
+  g.lse = lse;
   g.qh = reinterpret_cast<uint4*>(ws + L.q_off);
   g.kh = reinterpret_cast<uint4*>(ws + L.k_off);
-  g.dsum = reinterpret_cast<float*>(ws + L.d_off);
+  g.ld = reinterpret_cast<float2*>(ws + L.ld_off);
   g.q_start = q_start;
   g.B = batch;
   g.S = seqlen;
+  g.s_pad = L.s_pad;
   g.hq = n_q_heads;
   g.hkv = n_kv_heads;
   make_rope_turns(rope_theta, head_dim, &g.turns);
@@ -669,19 +751,20 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
   const uint64_t kd[4] = {(uint64_t)head_dim, (uint64_t)n_kv_heads, (uint64_t)seqlen, (uint64_t)batch};
   const uint64_t ks[3] = {(uint64_t)head_dim * 2, (uint64_t)n_kv_heads * head_dim * 2,
                           (uint64_t)seqlen * n_kv_heads * head_dim * 2};
-  const uint32_t box[4] = {64u, 1u, (uint32_t)bwd::kBM, 1u};
-  const bool okm =
-      encode_tmap(&p.tmq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ws + L.q_off, qd, qs, box,
-                  CU_TENSOR_MAP_SWIZZLE_128B) &&
-      encode_tmap(&p.tmk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ws + L.k_off, kd, ks, box,
-                  CU_TENSOR_MAP_SWIZZLE_128B) &&
-      encode_tmap(&p.tmv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, kd, ks, box,
-                  CU_TENSOR_MAP_SWIZZLE_128B) &&
-      encode_tmap(&p.tmdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, d_out, qd, qs, box,
-                  CU_TENSOR_MAP_SWIZZLE_128B);
+  const uint32_t box_r[4] = {64u, 1u, (uint32_t)bwd::kBM, 1u};
+  const uint32_t box_c[4] = {64u, 1u, (uint32_t)bwd::kBC, 1u};
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const bool okm = encode_tmap(&p.tmq_r, bf, 4, ws + L.q_off, qd, qs, box_r, sw) &&
+                   encode_tmap(&p.tmq_c, bf, 4, ws + L.q_off, qd, qs, box_c, sw) &&
+                   encode_tmap(&p.tmdo_r, bf, 4, d_out, qd, qs, box_r, sw) &&
+                   encode_tmap(&p.tmdo_c, bf, 4, d_out, qd, qs, box_c, sw) &&
+                   encode_tmap(&p.tmk_r, bf, 4, ws + L.k_off, kd, ks, box_r, sw) &&
+                   encode_tmap(&p.tmk_c, bf, 4, ws + L.k_off, kd, ks, box_c, sw) &&
+                   encode_tmap(&p.tmv_r, bf, 4, v, kd, ks, box_r, sw) &&
+                   encode_tmap(&p.tmv_c, bf, 4, v, kd, ks, box_c, sw);
   if (!okm) return PS_ERR_CUDA;
-  p.lse = lse;
-  p.dsum = reinterpret_cast<const float*>(ws + L.d_off);
+  p.ld = reinterpret_cast<const float2*>(ws + L.ld_off);
   p.q_start = q_start;
   p.prefix_len = prefix_len;
   p.dq = dq;
@@ -689,23 +772,20 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
   p.dv = dv;
   p.status = status;
   p.S = seqlen;
+  p.s_pad = L.s_pad;
   p.hq = n_q_heads;
   p.hkv = n_kv_heads;
   p.W = window;
-  p.nq = (seqlen + bwd::kBM - 1) / bwd::kBM;
+  p.B = batch;
+  p.nq = nq;
+  p.n_dkdv = (int32_t)n_dkdv;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   make_rope_turns(rope_theta, head_dim, &p.turns);
-  if (cudaFuncSetAttribute(bwd::bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           bwd::kSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(bwd::bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(bwd::bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            bwd::kSmem) != cudaSuccess)
     return PS_ERR_CUDA;
-  if (launch_dependent(bwd::bwd_dq_kernel, dim3((unsigned)p.nq, (unsigned)n_q_heads, (unsigned)batch),
-                       dim3(128), (size_t)bwd::kSmem, s, p) != cudaSuccess)
-    return PS_ERR_CUDA;
-  if (launch_dependent(bwd::bwd_dkdv_kernel,
-                       dim3((unsigned)p.nq, (unsigned)n_kv_heads, (unsigned)batch), dim3(128),
+  if (launch_dependent(bwd::bwd_kernel, dim3((unsigned)(n_dkdv + n_dq)), dim3(bwd::kThreads),
                        (size_t)bwd::kSmem, s, p) != cudaSuccess)
     return PS_ERR_CUDA;
   return launch_status();

@@ -16,6 +16,7 @@
 //     cores with fp32 accumulators in TMEM; softmax runs one thread per query
 //     row straight out of TMEM.
 #include "ps_internal.h"
+#include "ps_math.cuh"
 #include "ps_tc.cuh"
 #include "ps_rope.cuh"
 #include "ps_tiles.cuh"
@@ -218,12 +219,6 @@ struct PrefillParams {
   int32_t S, hq, hkv, W, with_ring, nq, B;
   float scale_log2;
 };
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -569,29 +564,6 @@ __device__ __forceinline__ Item make_item(const PrefillParams& p, int u) {
 }
 
 }  // namespace ws
-
-// Packed fp32x2 arithmetic and the three-input max of sm_100+: two elements
-// (or two new candidates) per instruction on the softmax critical path.
-__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
-                                      float c0, float c1) {
-  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-
-__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
 
 // One query row's share of a 128-key tile: S from TMEM, optional element mask
 // (keep column c iff c < A1 or B0 <= c < B1), online-softmax bookkeeping with a
