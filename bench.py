@@ -455,27 +455,27 @@ def backward_report(ps, torch, B, S, P, W, steps, seed, bf16_peak):
 
 def backward_executed_flops(S, P, W, hq, hkv, D, c0=0):
     """FLOPs of the tensor-core products the backward issues for one batch row:
-    each dQ CTA (128 queries) runs S, dP and dQ over its 64-key sub-tiles, each
-    dK/dV CTA (128 keys) runs S, dP, dV and dK over its 64-query sub-tiles for
-    every query head of its group."""
+    each dQ CTA (128 queries) runs S, dP and dQ over the forward's 128-key
+    tiles, each dK/dV CTA (128 keys) runs S, dP, dV and dK over the 128-query
+    tiles that can see its keys, for every query head of its group."""
     def cdiv(a, b):
         return -(-a // b)
 
     def clamp(x):
         return max(0, min(S, x))
 
-    sub = 2.0 * 128 * 64 * D
+    tile = 2.0 * 128 * 128 * D
     n_dq = n_kv = 0
-    n_qs = cdiv(S, 64)
-    for t in range(cdiv(S, 128)):
+    nq = cdiv(S, 128)
+    for t in range(nq):
         r0, r1 = t * 128, min(S, t * 128 + 128) - 1
-        kc, kp = clamp(c0 + r1 + 1 - c0), clamp(P - c0)
-        t1 = cdiv(min(kp, kc), 64)
-        t2b = max(t1, clamp(c0 + r0 - W + 1 - c0) // 64)
-        n_dq += t1 + max(0, cdiv(kc, 64) - t2b)
-        qe = n_qs if c0 + r0 < P else min(n_qs, (r1 + W - 1) // 64 + 1)
-        n_kv += max(0, qe - r0 // 64)
-    return sub * (3 * hq * n_dq + 4 * hq * n_kv)
+        kc, kp = clamp(r1 + 1), clamp(P - c0)
+        t1 = cdiv(min(kp, kc), 128)
+        t2b = max(t1, clamp(r0 - W + 1) // 128)
+        n_dq += t1 + max(0, cdiv(kc, 128) - t2b)
+        qe = nq if c0 + r0 < P else min(nq, (r1 + W - 1) // 128 + 1)
+        n_kv += max(0, qe - t)
+    return tile * (3 * hq * n_dq + 4 * hq * n_kv)
 
 
 # ---- CPU oracle -----------------------------------------------------------
@@ -544,6 +544,9 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill leg")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the ragged-decode and flatness legs")
+    ap.add_argument("--only", choices=["prefill", "train", "backward"],
+                    help="run one prefill leg alone (--prefill-steps timed calls, few launches "
+                         "before them) and print its report instead of the contract line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -566,6 +569,8 @@ def main():
     import prefix_sliding_window_02_b300 as ps
 
     hbm_peak, bf16_peak, bf16_sustained, peak_src = peaks()
+    if args.only:
+        return only_leg(ps, torch, args, bf16_peak)
     d = DEC
     seed = d["seed"] + 101 * rank
     P = decode_prefix_lens(seed, d["nseq"])
@@ -667,6 +672,20 @@ def main():
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def only_leg(ps, torch, args, bf16_peak):
+    """One prefill leg by itself, e.g. as the program a profiler captures."""
+    n = args.prefill_steps
+    if args.only == "prefill":
+        r = prefill_report(ps, torch, "prefill 1 x 32768 tokens, P=100, W=4096, Hq 16 / Hkv 8, "
+                           "D 128, one layer", 1, PRE["S"], PRE["P"], PRE["W"], n, 17, bf16_peak, 0)
+    elif args.only == "train":
+        r = prefill_report(ps, torch, "training forward 8 x 8192 tokens, P=256, W=2048, Hq 16 / "
+                           "Hkv 8, D 128, one layer", 8, 8192, 256, 2048, n, 18, bf16_peak, 0)
+    else:
+        r = backward_report(ps, torch, 8, 8192, 256, 2048, n, 20, bf16_peak)
+    print(json.dumps({"leg": args.only, **r}), flush=True)
 
 
 def reference_arm(args, world, rank):

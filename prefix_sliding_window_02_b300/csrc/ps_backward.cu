@@ -17,24 +17,30 @@
 //     {LSE * log2(e), D_i = dO_i . O_i}.
 //  2. bwd_kernel runs two kinds of CTA in one grid:
 //       dK/dV CTAs, one per (128-key tile, KV head, batch row): the key tile's
-//         K and V stay in shared memory while 64-query sub-tiles of Q and dO of
+//         K and V stay in shared memory while 128-query tiles of Q and dO of
 //         every query head of the group stream past;
 //       dQ CTAs, one per (128-query tile, query head, batch row): Q and dO stay
-//         while 64-key sub-tiles of K and V stream past (the forward's tiles).
+//         while the forward's 128-key tiles of K and V stream past.
 //     Both recompute S and dP, so each (query, key) tile pair costs 7 products
 //     instead of the 5 of a single pass that adds dQ with atomics.
 //
-// CTA roles (320 threads): warps 0-7 turn S and dP into P and dS (two warps
-// per TMEM lane quadrant, each on 32 of the sub-tile's 64 columns), warp 8
-// issues the TMA copies, warp 9 issues the tcgen05 MMAs.  TMEM (512 columns):
-// two sub-tile buffers S_b | dP_b (64 + 64 columns each), then the fp32
-// accumulators (dV | dK, or dQ).  P and dS are written back over S and dP as
-// bf16 pairs and read from TMEM as the A operand of the accumulating products.
-// The issuer runs one sub-tile ahead: S, dP of sub-tile i+1 are issued before
-// it waits for dS of sub-tile i, so the tensor cores work while the softmax
-// warps do.  Tensor-core instructions of one thread execute in issue order,
-// which lets S, dP of sub-tile i+2 overwrite the buffer whose P and dS the
-// products of sub-tile i have just read.
+// Every product is a tcgen05 MMA with M = N = 128: on this tensor core one
+// instruction costs about the same pipe time for N = 64 as for N = 128, so
+// narrower products would halve the rate.  TMEM (512 columns) holds two step
+// buffers of 128 columns and the fp32 accumulators (dV | dK, or dQ).  A step
+// (one streamed tile) runs in its buffer: S is computed there, the softmax
+// warps turn it into P (kept in registers; in a dK/dV CTA also written back
+// as bf16 for dV += P^T dO), dP then overwrites the buffer, and the softmax
+// warps turn it into dS, written back as bf16 over its first columns, the
+// tensor-memory A operand of dQ += dS K or dK += dS^T Q.  The issuer orders
+// the products as dP(t), S(t+1), dQ / dK(t), so S(t+1) runs while the softmax
+// warps compute dS(t), and dS(t)'s product runs while they compute P(t+1).
+// Tensor-core instructions of one thread execute in issue order, which lets
+// a product overwrite a buffer that an earlier product has just read.
+//
+// CTA roles (320 threads): warps 0-7 are the softmax warps (two per TMEM lane
+// quadrant, each on 64 of a step's 128 columns), warp 8 issues the TMA copies,
+// warp 9 issues the MMAs.
 #include "ps_internal.h"
 #include "ps_math.cuh"
 #include "ps_rope.cuh"
@@ -44,30 +50,38 @@
 namespace ps {
 namespace bwd {
 
-constexpr int kBM = 128;                 // rows of the resident tile
-constexpr int kBC = 64;                  // rows of a streamed sub-tile
+constexpr int kT = 128;                  // rows of every tile (resident and streamed)
 constexpr int kHD = 128;                 // head dim
-constexpr int kHalfR = kBM * 128;        // one 64-column swizzled half of a resident tile: 16 KB
-constexpr int kHalfC = kBC * 128;        // the same for a sub-tile: 8 KB
-constexpr int kTileR = 2 * kHalfR;       // 32 KB
-constexpr int kTileC = 2 * kHalfC;       // 16 KB
-constexpr int kSt = 4;                   // sub-tile stages in flight
-constexpr int kStage = 2 * kTileC;       // two sub-tile operands per stage
-constexpr int kLdBytes = kBC * 8;        // {LSE*log2e, D} pairs of one query sub-tile
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
-constexpr int kSmem = 2 * kTileR + kSt * kStage + kSt * kLdBytes + 1024 /*barriers*/ +
-                      1024 /*alignment*/;
-constexpr uint32_t kIdescSub = tc::idesc_bf16(128, kBC, false);  // S, dP: N = 64, K-major B
-constexpr uint32_t kIdescAcc = tc::idesc_bf16(128, kHD, true);   // accumulations: B MN-major
+constexpr int kHalf = kT * 128;          // one 64-column swizzled half of a tile: 16 KB
+constexpr int kTile = 2 * kHalf;         // 32 KB
+constexpr int kLdBytes = kT * 8;         // {LSE*log2e, D} pairs of one query tile
+constexpr int kSoftWarps = 8;
+constexpr int kParts = kSoftWarps / 4;   // softmax warps per TMEM lane quadrant
+constexpr int kNC = kT / kParts;         // step columns per softmax warp
+constexpr int kPairs = 64 / kParts;      // accumulator rotation pairs per warp in the epilogue
+constexpr int kProducerWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
+constexpr int kThreads = 32 * (kSoftWarps + 2);
+// Streamed tiles: ring A holds the operand used by S(t) and by the last
+// product of step t (K in a dQ CTA, Q in a dK/dV CTA), ring B the one used by
+// dP(t) (V, or dO).  A slot of ring A frees late, so a dQ CTA gives it three
+// slots; a dK/dV CTA also stages the query tile's LSE / D pairs and has room
+// for two.
+constexpr int kSaQ = 3, kSaKV = 2, kSb = 2;
+constexpr int kOffA = 2 * kTile;                 // ring A, after the two resident tiles
+constexpr int kOffB = kOffA + kSaQ * kTile;      // ring B (same place in both roles)
+constexpr int kOffLd = kOffA + kSaKV * kTile;    // dK/dV: LSE / D slots, where a dQ CTA
+                                                 // has its third ring-A slot
+constexpr int kOffBars = kOffB + kSb * kTile;
+constexpr int kSmem = kOffBars + 256 /*barriers*/ + 1024 /*alignment*/;
+static_assert(kOffLd + kSaKV * kLdBytes <= kOffB, "LSE / D slots fit in the spare slot");
+constexpr uint32_t kIdescS = tc::idesc_bf16(128, 128, false);   // S, dP: both operands K-major
+constexpr uint32_t kIdescAcc = tc::idesc_bf16(128, 128, true);  // accumulations: B MN-major
 constexpr uint32_t kTAcc = 256;                                  // accumulator columns
 
 struct Params {
-  CUtensorMap tmq_r, tmq_c;    // rotated Q {D, Hq, S, B}: 128-row and 64-row boxes
-  CUtensorMap tmdo_r, tmdo_c;  // dO
-  CUtensorMap tmk_r, tmk_c;    // rotated K {D, Hkv, S, B}
-  CUtensorMap tmv_r, tmv_c;    // V
-  const float2* ld;            // [B, Hq, s_pad] {LSE * log2(e), D}; rows >= S are zero
+  CUtensorMap tmq, tmdo;  // rotated Q, dO  {D, Hq, S, B}, 128-row boxes
+  CUtensorMap tmk, tmv;   // rotated K, V   {D, Hkv, S, B}
+  const float2* ld;       // [B, Hq, s_pad] {LSE * log2(e), D}; rows >= S are zero
   const int32_t* q_start;
   const int32_t* prefix_len;
   float* dq;  // [B, S, Hq, D]
@@ -75,44 +89,53 @@ struct Params {
   float* dv;  // [B, S, Hkv, D]
   int32_t* status;
   int32_t S, s_pad, hq, hkv, W, B;
-  int32_t nq;       // 128-row query tiles
+  int32_t nq;       // 128-row tiles
   int32_t n_dkdv;   // CTAs of the dK/dV kind (the first ones of the grid)
   float scale, scale_log2;
   RopeTurns turns;
 };
 
 struct Bars {
-  uint64_t res_full;                       // the resident tiles have landed
-  uint64_t st_full[kSt], st_empty[kSt];    // sub-tile stages
-  uint64_t s_full[2], ds_ready[2];         // TMEM sub-tile buffers
-  uint64_t done;                           // every accumulation has completed
+  uint64_t res_full;                         // the resident tiles have landed
+  uint64_t a_full[kSaQ], a_empty[kSaQ];      // ring A
+  uint64_t b_full[kSb], b_empty[kSb];        // ring B
+  uint64_t s_full[2], p_ready[2];            // step buffers: S computed / P taken
+  uint64_t dp_full[2], ds_ready[2];          //               dP computed / dS written
+  uint64_t done;                             // every product has completed
   uint32_t tmem_slot;
   int32_t abort;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
-// TMEM column of the K16 step kk (16 sub-tile columns) of the bf16 pairs a
-// softmax warp pair writes over a 64-column buffer: the warp on columns
-// [32h, 32h+32) packs them into [32h, 32h+16).
-__device__ __forceinline__ uint32_t packed_col(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
+__device__ __forceinline__ void tld(uint32_t taddr, uint32_t (&r)[32]) { tc::ld32(taddr, r); }
+__device__ __forceinline__ void tld(uint32_t taddr, uint32_t (&r)[16]) { tc::ld16(taddr, r); }
 
-// Writes 32 columns (chunk c: [32c, 32c+32) paired with [64+32c, 96+32c)) of
-// one thread's row of a 128-wide fp32 accumulator, scaled and rotated back by
-// -pos when `rot` (dQ, dK), plainly otherwise (dV).  Every thread of the warp
-// calls it (tcgen05.ld is warp-collective); only rows with `valid` store.
+// TMEM column of the K16 step kk (16 step columns) of the bf16 pairs the
+// softmax warps write over a buffer: the warp on columns [c0, c0 + kNC) packs
+// them into [c0, c0 + kNC / 2).
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+  return (16 * kk) / kNC * kNC + (16 * kk) % kNC / 2;
+}
+
+// Writes kPairs rotation pairs (chunk c: columns [c kPairs, (c+1) kPairs) with
+// their partners 64 further on) of one thread's row of a 128-wide fp32
+// accumulator, scaled and rotated back by -pos when `rot` (dQ, dK), plainly
+// otherwise (dV).  Every thread of the warp calls it (tcgen05.ld is
+// warp-collective); only rows with `valid` store.
 __device__ __forceinline__ void store_chunk(uint32_t taddr, float* dst, int c, bool valid, float mul,
                                             bool rot, int32_t pos, const RopeTurns& turns) {
-  uint32_t a[32], b[32];
-  tc::ld32(taddr + c * 32, a);
-  tc::ld32(taddr + 64 + c * 32, b);
+  uint32_t a[kPairs], b[kPairs];
+  tld(taddr + c * kPairs, a);
+  tld(taddr + 64 + c * kPairs, b);
   tc::wait_ld();
   if (!valid) return;
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
+  for (int e = 0; e < kPairs; ++e) {
     const float x = __uint_as_float(a[e]) * mul, y = __uint_as_float(b[e]) * mul;
     float rx = x, ry = y;
     if (rot) {
       float cs, sn;
-      rope_cos_sin(pos, turns.f[c * 32 + e], cs, sn);
+      rope_cos_sin(pos, turns.f[c * kPairs + e], cs, sn);
       rx = x * cs + y * sn;  // rotation by -angle
       ry = y * cs - x * sn;
     }
@@ -120,9 +143,9 @@ __device__ __forceinline__ void store_chunk(uint32_t taddr, float* dst, int c, b
     b[e] = __float_as_uint(ry);
   }
 #pragma unroll
-  for (int e = 0; e < 32; e += 4) {
-    *reinterpret_cast<uint4*>(dst + c * 32 + e) = make_uint4(a[e], a[e + 1], a[e + 2], a[e + 3]);
-    *reinterpret_cast<uint4*>(dst + 64 + c * 32 + e) =
+  for (int e = 0; e < kPairs; e += 4) {
+    *reinterpret_cast<uint4*>(dst + c * kPairs + e) = make_uint4(a[e], a[e + 1], a[e + 2], a[e + 3]);
+    *reinterpret_cast<uint4*>(dst + 64 + c * kPairs + e) =
         make_uint4(b[e], b[e + 1], b[e + 2], b[e + 3]);
   }
 }
@@ -144,8 +167,11 @@ struct PrepParams {
   RopeTurns turns;
 };
 
-constexpr int kPrepRows = 4;
+constexpr int kPrepRows = 16;
 
+// One block takes kPrepRows rows (batch row, position) at a time: the angles
+// of those rows, then every 16-byte group of their Q and K rows, then D for
+// every (row, query head) with a half-warp per pair (8 elements per lane).
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ PrepParams p) {
   constexpr int VEC = 16, HALFV = 8;
   __shared__ float2 cs[kPrepRows][64];
@@ -155,8 +181,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ P
   const int heads = p.hq + p.hkv;
   for (int64_t r0 = (int64_t)blockIdx.x * kPrepRows; r0 < n_rows;
        r0 += (int64_t)gridDim.x * kPrepRows) {
-    {
-      const int rr = threadIdx.x >> 6, i = threadIdx.x & 63;
+    for (int t = threadIdx.x; t < kPrepRows * 64; t += blockDim.x) {
+      const int rr = t >> 6, i = t & 63;
       const int64_t r = r0 + rr;
       if (r < n_rows) {
         const int b = (int)(r / p.S);
@@ -186,19 +212,21 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ P
         p.kh[base + HALFV] = rb;
       }
     }
-    // D_i = dO_i . O_i: one warp per (row, query head), 4 elements per lane
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int w = warp; w < kPrepRows * p.hq; w += blockDim.x / 32) {
+    // D_i = dO_i . O_i and the stored pair, one half-warp per (row, query head)
+    const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
+    for (int w = hw; w < kPrepRows * p.hq; w += blockDim.x / 16) {
       const int64_t r = r0 + w / p.hq;
       const int h = w % p.hq;
-      if (r >= n_rows) continue;
-      const uint2* o2 = reinterpret_cast<const uint2*>(p.o) + (r * p.hq + h) * 32 + lane;
-      const uint2* d2 = reinterpret_cast<const uint2*>(p.dout) + (r * p.hq + h) * 32 + lane;
-      const uint2 a = *o2, d = *d2;
-      float acc = bf16lo(a.x) * bf16lo(d.x) + bf16hi(a.x) * bf16hi(d.x) +
-                  bf16lo(a.y) * bf16lo(d.y) + bf16hi(a.y) * bf16hi(d.y);
-      acc = warp_sum(acc);
-      if (lane == 0) {
+      float acc = 0.f;
+      if (r < n_rows) {
+        const uint4 a = p.o[(r * p.hq + h) * VEC + l16], d = p.dout[(r * p.hq + h) * VEC + l16];
+        acc = bf16lo(a.x) * bf16lo(d.x) + bf16hi(a.x) * bf16hi(d.x) + bf16lo(a.y) * bf16lo(d.y) +
+              bf16hi(a.y) * bf16hi(d.y) + bf16lo(a.z) * bf16lo(d.z) + bf16hi(a.z) * bf16hi(d.z) +
+              bf16lo(a.w) * bf16lo(d.w) + bf16hi(a.w) * bf16hi(d.w);
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (l16 == 0 && r < n_rows) {
         const int b = (int)(r / p.S);
         const int s = (int)(r % p.S);
         const float l2 = p.lse[((int64_t)b * p.hq + h) * p.S + s] * 1.4426950408889634f;
@@ -216,68 +244,137 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ P
 }
 
 // ---------------------------------------------------------------------------
-// softmax-side work of one warp on 32 columns of a sub-tile buffer
+// softmax-side work of one warp on its kNC columns of a step buffer
 // ---------------------------------------------------------------------------
 
-// dQ side: this thread's query row against 32 keys (key indices base..base+31).
-// Keeps key x iff x < A1 or B0 <= x < B1 (indices relative to base); writes
-// dS = P (dP - D) as bf16 pairs over the first 16 of the 32 dP columns.
+// dQ side, first half: this thread's query row against kNC keys (key indices
+// base..).  P = exp2(S * scale_log2 - lse2), zero unless key x (relative to
+// base) has x < A1 or B0 <= x < B1; kept in registers.
 template <bool MASK>
-__device__ __forceinline__ void ds_row(uint32_t tS, uint32_t tP, float scale_log2, float lse2,
-                                       float drow, int32_t A1, int32_t B0, int32_t B1) {
-  uint32_t sv[32], pv[32];
-  tc::ld32(tS, sv);
-  tc::ld32(tP, pv);
-  tc::wait_ld();
-  uint32_t packed[16];
+__device__ __forceinline__ void p_row(uint32_t tS, float scale_log2, float lse2, int32_t A1,
+                                      int32_t B0, int32_t B1, float (&pr)[kNC]) {
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    float x0, x1, t0, t1, d0, d1;
-    ffma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), scale_log2, scale_log2,
-          -lse2, -lse2);
-    x0 = ex2(x0);
-    x1 = ex2(x1);
-    fadd2(t0, t1, __uint_as_float(pv[e]), __uint_as_float(pv[e + 1]), -drow, -drow);
-    fmul2(d0, d1, x0, x1, t0, t1);
-    if (MASK) {
-      d0 = ((e < A1) || (e >= B0 && e < B1)) ? d0 : 0.f;
-      d1 = ((e + 1 < A1) || (e + 1 >= B0 && e + 1 < B1)) ? d1 : 0.f;
+  for (int c = 0; c < kNC / 32; ++c) {
+    uint32_t sv[32];
+    tc::ld32(tS + 32 * c, sv);
+    tc::wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int x = 32 * c + e;
+      float x0, x1;
+      ffma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), scale_log2, scale_log2,
+            -lse2, -lse2);
+      x0 = ex2(x0);
+      x1 = ex2(x1);
+      if (MASK) {
+        x0 = ((x < A1) || (x >= B0 && x < B1)) ? x0 : 0.f;
+        x1 = ((x + 1 < A1) || (x + 1 >= B0 && x + 1 < B1)) ? x1 : 0.f;
+      }
+      pr[x] = x0;
+      pr[x + 1] = x1;
     }
-    packed[e / 2] = pack_bf16(d0, d1);
   }
-  tc::st16(tP, packed);
 }
 
-// dK/dV side: this thread's key row against 32 queries whose {LSE*log2e, D}
-// pairs are ld[0..31].  Keeps query e iff LO <= e <= HI.  Writes P^T over the
-// S^T columns and dS^T over the dP^T columns, as bf16 pairs.
-template <bool MASK>
-__device__ __forceinline__ void ds_col(uint32_t tS, uint32_t tP, float scale_log2,
-                                       const float4* ld, int32_t LO, int32_t HI) {
-  uint32_t sv[32], pv[32];
-  tc::ld32(tS, sv);
-  tc::ld32(tP, pv);
-  tc::wait_ld();
-  uint32_t pk_p[16], pk_s[16];
+// dQ side, second half: dS = P (dP - D) over the same columns, written as
+// bf16 pairs over the first kNC / 2 of them (32 columns at a time, each chunk
+// packed into 16 columns the warp has already read).
+__device__ __forceinline__ void ds_row(uint32_t tP, float drow, const float (&pr)[kNC]) {
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    const float4 l = ld[e / 2];  // {lse2_e, D_e, lse2_e+1, D_e+1}, same address on every lane
-    float x0, x1, t0, t1, d0, d1;
-    ffma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), scale_log2, scale_log2,
-          -l.x, -l.z);
-    x0 = ex2(x0);
-    x1 = ex2(x1);
-    fadd2(t0, t1, __uint_as_float(pv[e]), __uint_as_float(pv[e + 1]), -l.y, -l.w);
-    if (MASK) {
-      x0 = (e >= LO && e <= HI) ? x0 : 0.f;
-      x1 = (e + 1 >= LO && e + 1 <= HI) ? x1 : 0.f;
+  for (int c = 0; c < kNC / 32; ++c) {
+    uint32_t pv[32];  // the bf16 pairs are packed into its first half as it is consumed
+    tc::ld32(tP + 32 * c, pv);
+    tc::wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      float t0, t1, d0, d1;
+      fadd2(t0, t1, __uint_as_float(pv[e]), __uint_as_float(pv[e + 1]), -drow, -drow);
+      fmul2(d0, d1, pr[32 * c + e], pr[32 * c + e + 1], t0, t1);
+      pv[e / 2] = pack_bf16(d0, d1);
     }
-    fmul2(d0, d1, x0, x1, t0, t1);
-    pk_p[e / 2] = pack_bf16(x0, x1);
-    pk_s[e / 2] = pack_bf16(d0, d1);
+    tc::st16(tP + 16 * c, reinterpret_cast<const uint32_t(&)[16]>(pv));
   }
-  tc::st16(tS, pk_p);
-  tc::st16(tP, pk_s);
+}
+
+// dK/dV side, first half: this thread's key row against kNC queries whose
+// {LSE*log2e, D} pairs are ld[0..kNC) (as float4: two queries each).  P^T is
+// zero unless query e has LO <= e <= HI; kept in registers and written as bf16
+// pairs over the first kNC / 2 columns for dV += P^T dO.
+template <bool MASK>
+__device__ __forceinline__ void p_col(uint32_t tS, float scale_log2, const float4* ld, int32_t LO,
+                                      int32_t HI, float (&pr)[kNC]) {
+#pragma unroll
+  for (int c = 0; c < kNC / 32; ++c) {
+    uint32_t sv[32];  // the bf16 pairs are packed into its first half as it is consumed
+    tc::ld32(tS + 32 * c, sv);
+    tc::wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int x = 32 * c + e;
+      const float4 l = ld[x / 2];  // same address on every lane
+      float x0, x1;
+      ffma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), scale_log2, scale_log2,
+            -l.x, -l.z);
+      x0 = ex2(x0);
+      x1 = ex2(x1);
+      if (MASK) {
+        x0 = (x >= LO && x <= HI) ? x0 : 0.f;
+        x1 = (x + 1 >= LO && x + 1 <= HI) ? x1 : 0.f;
+      }
+      pr[x] = x0;
+      pr[x + 1] = x1;
+      sv[e / 2] = pack_bf16(x0, x1);
+    }
+    tc::st16(tS + 16 * c, reinterpret_cast<const uint32_t(&)[16]>(sv));
+  }
+}
+
+// dK/dV side, second half: dS^T = P^T (dP^T - D) as bf16 pairs.
+__device__ __forceinline__ void ds_col(uint32_t tP, const float4* ld, const float (&pr)[kNC]) {
+#pragma unroll
+  for (int c = 0; c < kNC / 32; ++c) {
+    uint32_t pv[32];
+    tc::ld32(tP + 32 * c, pv);
+    tc::wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int x = 32 * c + e;
+      const float4 l = ld[x / 2];
+      float t0, t1, d0, d1;
+      fadd2(t0, t1, __uint_as_float(pv[e]), __uint_as_float(pv[e + 1]), -l.y, -l.w);
+      fmul2(d0, d1, pr[x], pr[x + 1], t0, t1);
+      pv[e / 2] = pack_bf16(d0, d1);
+    }
+    tc::st16(tP + 16 * c, reinterpret_cast<const uint32_t(&)[16]>(pv));
+  }
+}
+
+// Hands a step buffer from the softmax warps back to the issuer.
+__device__ __forceinline__ void release(uint64_t* bar, int lane, bool stored) {
+  if (stored) tc::wait_st();
+  tc::fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+// One 128-wide product: 8 MMAs (K16 steps) into the accumulator d_tmem.
+__device__ __forceinline__ void mma_ss8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < kHD / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+    tc::mma_bf16(d_tmem, adesc + off, bdesc + off, kIdescS, acc || kk > 0);
+  }
+}
+
+// d_tmem (+)= A (bf16 pairs in TMEM at a_tmem, packed as the softmax warps
+// write them) x B (128 rows of a tile, MN-major).
+__device__ __forceinline__ void mma_ts8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc_mn,
+                                        bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < kT / 16; ++kk)
+    tc::mma_bf16_ts(d_tmem, a_tmem + packed_col(kk), bdesc_mn + ((kk * 2048) >> 4), kIdescAcc,
+                    acc || kk > 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -285,10 +382,12 @@ __device__ __forceinline__ void ds_col(uint32_t tS, uint32_t tP, float scale_log
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* bar, uint32_t tmem,
                                          int u) {
+  constexpr int kSa = kSaKV;
   uint8_t* sK = smem;
-  uint8_t* sV = smem + kTileR;
-  uint8_t* sQ = smem + 2 * kTileR;  // stage st: Q at sQ + st * kStage, dO kTileC after it
-  float2* sLd = reinterpret_cast<float2*>(smem + 2 * kTileR + kSt * kStage);  // [kSt][kBC]
+  uint8_t* sV = smem + kTile;
+  uint8_t* sA = smem + kOffA;  // Q tiles
+  uint8_t* sB = smem + kOffB;  // dO tiles
+  float2* sLd = reinterpret_cast<float2*>(smem + kOffLd);  // [kSa][kT]
   volatile int32_t* abort = &bar->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -298,41 +397,40 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
   const int G = p.hq / p.hkv;
   const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
   const KeyMap km = make_keymap(p.S, c0, P, p.W, false);
-  const int32_t k0r = kt * kBM, k1r = min(p.S, k0r + kBM) - 1;
-  // query sub-tiles that can admit one of these keys: from the one holding the
+  const int32_t k0r = kt * kT, k1r = min(p.S, k0r + kT) - 1;
+  // query tiles that can admit one of these keys: from the tile holding the
   // first key on; prefix keys are seen by every later query, window keys only
   // by queries at most W - 1 rows later
-  const int n_qs = (p.S + kBC - 1) / kBC;
-  const int qs_begin = k0r / kBC;
-  int qs_end = n_qs;
-  if ((int64_t)c0 + k0r >= P) qs_end = (int)min((int64_t)n_qs, ((int64_t)k1r + p.W - 1) / kBC + 1);
-  const int n = max(0, qs_end - qs_begin) * G;  // (query sub-tile, head of the group) pairs
+  int qt_end = p.nq;
+  if ((int64_t)c0 + k0r >= P) qt_end = (int)min((int64_t)p.nq, ((int64_t)k1r + p.W - 1) / kT + 1);
+  const int n = max(0, qt_end - kt) * G;  // steps: (query tile, head of the group)
 
   if (warp == kProducerWarp) {
     if (lane == 0 && n > 0) {
-      prefetch_tmap(&p.tmk_r);
-      prefetch_tmap(&p.tmv_r);
-      prefetch_tmap(&p.tmq_c);
-      prefetch_tmap(&p.tmdo_c);
+      prefetch_tmap(&p.tmk);
+      prefetch_tmap(&p.tmv);
+      prefetch_tmap(&p.tmq);
+      prefetch_tmap(&p.tmdo);
       const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
-      mbar_arrive_expect_tx(&bar->res_full, 2 * kTileR);
-      tma_load_4d(sK, &p.tmk_r, &bar->res_full, 0, hk, k0r, b, pol_kv);
-      tma_load_4d(sK + kHalfR, &p.tmk_r, &bar->res_full, 64, hk, k0r, b, pol_kv);
-      tma_load_4d(sV, &p.tmv_r, &bar->res_full, 0, hk, k0r, b, pol_kv);
-      tma_load_4d(sV + kHalfR, &p.tmv_r, &bar->res_full, 64, hk, k0r, b, pol_kv);
-      for (int i = 0; i < n; ++i) {
-        const int st = i % kSt;
-        if (!mbar_wait_abort(&bar->st_empty[st], ((i / kSt) & 1) ^ 1, abort)) break;
-        const int qs = qs_begin + i / G, h = hk * G + i % G;
-        uint8_t* dq = sQ + st * kStage;
-        uint64_t* full = &bar->st_full[st];
-        mbar_arrive_expect_tx(full, kStage + kLdBytes);
-        tma_load_4d(dq, &p.tmq_c, full, 0, h, qs * kBC, b, pol_q);
-        tma_load_4d(dq + kHalfC, &p.tmq_c, full, 64, h, qs * kBC, b, pol_q);
-        tma_load_4d(dq + kTileC, &p.tmdo_c, full, 0, h, qs * kBC, b, pol_q);
-        tma_load_4d(dq + kTileC + kHalfC, &p.tmdo_c, full, 64, h, qs * kBC, b, pol_q);
-        bulk_load(sLd + st * kBC, p.ld + ((int64_t)b * p.hq + h) * p.s_pad + qs * kBC, kLdBytes,
-                  full);
+      mbar_arrive_expect_tx(&bar->res_full, 2 * kTile);
+      tma_load_4d(sK, &p.tmk, &bar->res_full, 0, hk, k0r, b, pol_kv);
+      tma_load_4d(sK + kHalf, &p.tmk, &bar->res_full, 64, hk, k0r, b, pol_kv);
+      tma_load_4d(sV, &p.tmv, &bar->res_full, 0, hk, k0r, b, pol_kv);
+      tma_load_4d(sV + kHalf, &p.tmv, &bar->res_full, 64, hk, k0r, b, pol_kv);
+      for (int t = 0; t < n; ++t) {
+        const int qt = kt + t / G, h = hk * G + t % G;
+        const int sa = t % kSa, sb = t % kSb;
+        if (!mbar_wait_abort(&bar->a_empty[sa], ((t / kSa) & 1) ^ 1, abort)) break;
+        uint64_t* fa = &bar->a_full[sa];
+        mbar_arrive_expect_tx(fa, kTile + kLdBytes);
+        tma_load_4d(sA + sa * kTile, &p.tmq, fa, 0, h, qt * kT, b, pol_q);
+        tma_load_4d(sA + sa * kTile + kHalf, &p.tmq, fa, 64, h, qt * kT, b, pol_q);
+        bulk_load(sLd + sa * kT, p.ld + ((int64_t)b * p.hq + h) * p.s_pad + qt * kT, kLdBytes, fa);
+        if (!mbar_wait_abort(&bar->b_empty[sb], ((t / kSb) & 1) ^ 1, abort)) break;
+        uint64_t* fb = &bar->b_full[sb];
+        mbar_arrive_expect_tx(fb, kTile);
+        tma_load_4d(sB + sb * kTile, &p.tmdo, fb, 0, h, qt * kT, b, pol_q);
+        tma_load_4d(sB + sb * kTile + kHalf, &p.tmdo, fb, 64, h, qt * kT, b, pol_q);
       }
     }
     __syncwarp();
@@ -340,92 +438,93 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
     if (lane == 0 && n > 0) {
       const uint64_t aK = tc::sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t aV = tc::sdesc_sw128(smem_u32(sV), 16, 1024);
-      const uint64_t bQ = tc::sdesc_sw128(smem_u32(sQ), 16, 1024);            // K-major B
-      const uint64_t bO = tc::sdesc_sw128(smem_u32(sQ + kTileC), 16, 1024);
-      const uint64_t bQm = tc::sdesc_sw128(smem_u32(sQ), kHalfC, 1024);       // MN-major B
-      const uint64_t bOm = tc::sdesc_sw128(smem_u32(sQ + kTileC), kHalfC, 1024);
-      // S^T = K Q^T and dP^T = V dO^T of sub-tile i into buffer i & 1
-      auto sdp = [&](int i) -> bool {
-        const int st = i % kSt, bf = i & 1;
-        if (!mbar_wait_abort(&bar->st_full[st], (i / kSt) & 1, abort)) return false;
+      const uint64_t bQ = tc::sdesc_sw128(smem_u32(sA), 16, 1024);       // K-major
+      const uint64_t bQm = tc::sdesc_sw128(smem_u32(sA), kHalf, 1024);   // MN-major
+      const uint64_t bO = tc::sdesc_sw128(smem_u32(sB), 16, 1024);
+      const uint64_t bOm = tc::sdesc_sw128(smem_u32(sB), kHalf, 1024);
+      auto soa = [](int t) { return (uint64_t)(((t % kSa) * kTile) >> 4); };
+      auto sob = [](int t) { return (uint64_t)(((t % kSb) * kTile) >> 4); };
+      // per step t (buffer t & 1): dV += P^T dO, dP^T = V dO^T, then S^T of
+      // step t+1, then dK += dS^T Q
+      bool ok = mbar_wait_abort(&bar->res_full, 0, abort) &&
+                mbar_wait_abort(&bar->a_full[0], 0, abort);
+      if (ok) {
         tc::fence_after();
-        const uint64_t so = (uint64_t)((st * kStage) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kHD / 16; ++kk) {
-          const uint32_t oa = ((kk >> 2) * kHalfR + (kk & 3) * 32) >> 4;
-          const uint32_t ob = ((kk >> 2) * kHalfC + (kk & 3) * 32) >> 4;
-          tc::mma_bf16(tmem + bf * 128, aK + oa, bQ + so + ob, kIdescSub, kk > 0);
-          tc::mma_bf16(tmem + bf * 128 + 64, aV + oa, bO + so + ob, kIdescSub, kk > 0);
-        }
-        tc::commit(smem_u32(&bar->s_full[bf]));
-        return true;
-      };
-      // dV += P^T dO and dK += dS^T Q of sub-tile i, then release its stage
-      auto acc = [&](int i) -> bool {
-        const int st = i % kSt, bf = i & 1;
-        if (!mbar_wait_abort(&bar->ds_ready[bf], (i >> 1) & 1, abort)) return false;
-        tc::fence_after();
-        const uint64_t so = (uint64_t)((st * kStage) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kBC / 16; ++kk) {
-          const uint32_t ob = (kk * 2048) >> 4;
-          tc::mma_bf16_ts(tmem + kTAcc, tmem + bf * 128 + packed_col(kk), bOm + so + ob,
-                          kIdescAcc, i > 0 || kk > 0);
-          tc::mma_bf16_ts(tmem + kTAcc + 128, tmem + bf * 128 + 64 + packed_col(kk),
-                          bQm + so + ob, kIdescAcc, i > 0 || kk > 0);
-        }
-        tc::commit(smem_u32(&bar->st_empty[st]));
-        return true;
-      };
-      bool ok = mbar_wait_abort(&bar->res_full, 0, abort);
-      for (int i = 0; ok && i < n; ++i) {
-        ok = sdp(i);
-        if (ok && i > 0) ok = acc(i - 1);
+        mma_ss8(tmem, aK, bQ + soa(0), false);  // S^T(0) = K Q(0)^T
+        tc::commit(smem_u32(&bar->s_full[0]));
       }
-      if (ok) ok = acc(n - 1);
+      for (int t = 0; ok && t < n; ++t) {
+        const int bf = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        const uint32_t tb = tmem + bf * 128;
+        if (!(ok = mbar_wait_abort(&bar->p_ready[bf], ph, abort) &&
+                   mbar_wait_abort(&bar->b_full[t % kSb], (t / kSb) & 1, abort)))
+          break;
+        tc::fence_after();
+        mma_ts8(tmem + kTAcc, tb, bOm + sob(t), t > 0);  // dV += P^T dO
+        mma_ss8(tb, aV, bO + sob(t), false);              // dP^T = V dO^T
+        tc::commit(smem_u32(&bar->dp_full[bf]));
+        tc::commit(smem_u32(&bar->b_empty[t % kSb]));
+        if (t + 1 < n) {
+          if (!(ok = mbar_wait_abort(&bar->a_full[(t + 1) % kSa], ((t + 1) / kSa) & 1, abort)))
+            break;
+          tc::fence_after();
+          mma_ss8(tmem + (bf ^ 1) * 128, aK, bQ + soa(t + 1), false);
+          tc::commit(smem_u32(&bar->s_full[bf ^ 1]));
+        }
+        if (!(ok = mbar_wait_abort(&bar->ds_ready[bf], ph, abort))) break;
+        tc::fence_after();
+        mma_ts8(tmem + kTAcc + 128, tb, bQm + soa(t), t > 0);  // dK += dS^T Q
+        tc::commit(smem_u32(&bar->a_empty[t % kSa]));
+      }
       if (ok) tc::commit(smem_u32(&bar->done));
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int quad = warp & 3, half = warp >> 2;
+    const int quad = warp & 3, part = warp >> 2;
     const int row = quad * 32 + lane;  // key row of the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const int64_t kpos = (int64_t)c0 + k0r + row;
     // queries that admit this key: positions [kpos, kend]
     const int64_t kend = kpos < P ? INT64_MAX / 2 : kpos + p.W - 1;
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
-      const int st = i % kSt, bf = i & 1;
-      const int qs = qs_begin + i / G;
-      const int32_t qa = qs * kBC, qb = min(p.S, qa + kBC) - 1;
-      const bool masked = qa + kBC > p.S ||
-                          tile_class(km, c0, qa, qb, k0r, k1r, P, p.W) != kFull;
-      // this warp's 32 queries: rows r0 + e, e = 0..31
-      const int32_t r0 = qa + half * 32;
+    float pr[kNC];
+    for (int t = 0; t < n; ++t) {
+      const int bf = t & 1, sa = t % kSa;
+      const uint32_t ph = (t >> 1) & 1;
+      const int32_t qa = (kt + t / G) * kT, qb = min(p.S, qa + kT) - 1;
+      const bool masked = qa + kT > p.S || tile_class(km, c0, qa, qb, k0r, k1r, P, p.W) != kFull;
+      // this warp's kNC queries: rows r0 + e
+      const int32_t r0 = qa + part * kNC;
       const int64_t qp0 = (int64_t)c0 + r0;
       const int64_t lo64 = kpos - qp0;
       int64_t hi64 = kend - qp0;
       if (hi64 > (int64_t)(p.S - 1 - r0)) hi64 = (int64_t)(p.S - 1 - r0);
-      const int32_t lo = (int32_t)(lo64 < 0 ? 0 : (lo64 > 32 ? 32 : lo64));
-      const int32_t hi = (int32_t)(hi64 < -1 ? -1 : (hi64 > 31 ? 31 : hi64));
-      ok = mbar_wait_abort(&bar->s_full[bf], (i >> 1) & 1, abort) &&
-           mbar_wait_abort(&bar->st_full[st], (i / kSt) & 1, abort);  // the LSE / D pairs
+      const int32_t lo = (int32_t)(lo64 < 0 ? 0 : (lo64 > kNC ? kNC : lo64));
+      const int32_t hi = (int32_t)(hi64 < -1 ? -1 : (hi64 > kNC - 1 ? kNC - 1 : hi64));
+      const uint32_t tS = tmem + bf * 128 + part * kNC + lane_off;
+      const float4* ld = reinterpret_cast<const float4*>(sLd + sa * kT + part * kNC);
+      ok = mbar_wait_abort(&bar->s_full[bf], ph, abort) &&
+           mbar_wait_abort(&bar->a_full[sa], (t / kSa) & 1, abort);  // the LSE / D pairs
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc::fence_after();
-      const float4* ld = reinterpret_cast<const float4*>(sLd + st * kBC + half * 32);
-      const uint32_t tS = tmem + bf * 128 + half * 32 + lane_off;
       if (masked)
-        ds_col<true>(tS, tS + 64, p.scale_log2, ld, lo, hi);
+        p_col<true>(tS, p.scale_log2, ld, lo, hi, pr);
       else
-        ds_col<false>(tS, tS + 64, p.scale_log2, ld, 0, 31);
-      tc::wait_st();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar->ds_ready[bf]);
+        p_col<false>(tS, p.scale_log2, ld, 0, kNC - 1, pr);
+      release(&bar->p_ready[bf], lane, true);
+      ok = mbar_wait_abort(&bar->dp_full[bf], ph, abort);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+      ds_col(tS, ld, pr);
+      release(&bar->ds_ready[bf], lane, true);
     }
     if (ok && n > 0) {
       ok = mbar_wait_abort(&bar->done, 0, abort);
@@ -436,11 +535,11 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
       const bool valid = k0r + row <= k1r;
       const int64_t base = (((int64_t)b * p.S + (valid ? k0r + row : 0)) * p.hkv + hk) * kHD;
       if (n > 0) {
-        store_chunk(tmem + kTAcc + lane_off, p.dv + base, half, valid, 1.f, false, 0, p.turns);
-        store_chunk(tmem + kTAcc + 128 + lane_off, p.dk + base, half, valid, p.scale, true,
+        store_chunk(tmem + kTAcc + lane_off, p.dv + base, part, valid, 1.f, false, 0, p.turns);
+        store_chunk(tmem + kTAcc + 128 + lane_off, p.dk + base, part, valid, p.scale, true,
                     (int32_t)kpos, p.turns);
       } else if (valid) {  // no query admits these keys: zero gradients
-        for (int e = half * 32; e < half * 32 + 32; e += 4) {
+        for (int e = part * kPairs; e < part * kPairs + kPairs; e += 4) {
           *reinterpret_cast<float4*>(p.dv + base + e) = make_float4(0.f, 0.f, 0.f, 0.f);
           *reinterpret_cast<float4*>(p.dv + base + 64 + e) = make_float4(0.f, 0.f, 0.f, 0.f);
           *reinterpret_cast<float4*>(p.dk + base + e) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -456,9 +555,11 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar, uint32_t tmem,
                                        int u) {
+  constexpr int kSa = kSaQ;
   uint8_t* sQ = smem;
-  uint8_t* sdO = smem + kTileR;
-  uint8_t* sK = smem + 2 * kTileR;  // stage st: K at sK + st * kStage, V kTileC after it
+  uint8_t* sdO = smem + kTile;
+  uint8_t* sA = smem + kOffA;  // K tiles
+  uint8_t* sB = smem + kOffB;  // V tiles
   volatile int32_t* abort = &bar->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -468,41 +569,43 @@ __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar
   const int hk = h / (p.hq / p.hkv);
   const int32_t c0 = p.q_start[b], P = p.prefix_len[b];
   const KeyMap km = make_keymap(p.S, c0, P, p.W, false);
-  const int32_t q0r = qt * kBM, q1r = min(p.S, q0r + kBM) - 1;
+  const int32_t q0r = qt * kT, q1r = min(p.S, q0r + kT) - 1;
   const int64_t q0 = (int64_t)c0 + q0r, q1 = (int64_t)c0 + q1r;
-  // 64-key sub-tiles that can hold an admitted pair: prefix ones, then the band
+  // key tiles that can hold an admitted pair (the forward's): prefix tiles, then the band
   const int32_t kc = keys_below(km, q1 + 1);
   const int32_t kP = keys_below(km, P);
-  const int t1_end = (min(kP, kc) + kBC - 1) / kBC;
+  const int t1_end = (min(kP, kc) + kT - 1) / kT;
   const int32_t kw = keys_below(km, q0 - p.W + 1);
-  const int t2_begin = max(t1_end, kw / kBC);
-  const int t2_end = (kc + kBC - 1) / kBC;
+  const int t2_begin = max(t1_end, kw / kT);
+  const int t2_end = (kc + kT - 1) / kT;
   const int n = t1_end + max(0, t2_end - t2_begin);
-  auto sub_at = [&](int i) { return i < t1_end ? i : t2_begin + (i - t1_end); };
+  auto tile_at = [&](int i) { return i < t1_end ? i : t2_begin + (i - t1_end); };
 
   if (warp == kProducerWarp) {
     if (lane == 0 && n > 0) {
-      prefetch_tmap(&p.tmq_r);
-      prefetch_tmap(&p.tmdo_r);
-      prefetch_tmap(&p.tmk_c);
-      prefetch_tmap(&p.tmv_c);
+      prefetch_tmap(&p.tmq);
+      prefetch_tmap(&p.tmdo);
+      prefetch_tmap(&p.tmk);
+      prefetch_tmap(&p.tmv);
       const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
-      mbar_arrive_expect_tx(&bar->res_full, 2 * kTileR);
-      tma_load_4d(sQ, &p.tmq_r, &bar->res_full, 0, h, q0r, b, pol_q);
-      tma_load_4d(sQ + kHalfR, &p.tmq_r, &bar->res_full, 64, h, q0r, b, pol_q);
-      tma_load_4d(sdO, &p.tmdo_r, &bar->res_full, 0, h, q0r, b, pol_q);
-      tma_load_4d(sdO + kHalfR, &p.tmdo_r, &bar->res_full, 64, h, q0r, b, pol_q);
-      for (int i = 0; i < n; ++i) {
-        const int st = i % kSt;
-        if (!mbar_wait_abort(&bar->st_empty[st], ((i / kSt) & 1) ^ 1, abort)) break;
-        const int ka = sub_at(i) * kBC;
-        uint8_t* dk = sK + st * kStage;
-        uint64_t* full = &bar->st_full[st];
-        mbar_arrive_expect_tx(full, kStage);
-        tma_load_4d(dk, &p.tmk_c, full, 0, hk, ka, b, pol_kv);
-        tma_load_4d(dk + kHalfC, &p.tmk_c, full, 64, hk, ka, b, pol_kv);
-        tma_load_4d(dk + kTileC, &p.tmv_c, full, 0, hk, ka, b, pol_kv);
-        tma_load_4d(dk + kTileC + kHalfC, &p.tmv_c, full, 64, hk, ka, b, pol_kv);
+      mbar_arrive_expect_tx(&bar->res_full, 2 * kTile);
+      tma_load_4d(sQ, &p.tmq, &bar->res_full, 0, h, q0r, b, pol_q);
+      tma_load_4d(sQ + kHalf, &p.tmq, &bar->res_full, 64, h, q0r, b, pol_q);
+      tma_load_4d(sdO, &p.tmdo, &bar->res_full, 0, h, q0r, b, pol_q);
+      tma_load_4d(sdO + kHalf, &p.tmdo, &bar->res_full, 64, h, q0r, b, pol_q);
+      for (int t = 0; t < n; ++t) {
+        const int ka = tile_at(t) * kT;
+        const int sa = t % kSa, sb = t % kSb;
+        if (!mbar_wait_abort(&bar->a_empty[sa], ((t / kSa) & 1) ^ 1, abort)) break;
+        uint64_t* fa = &bar->a_full[sa];
+        mbar_arrive_expect_tx(fa, kTile);
+        tma_load_4d(sA + sa * kTile, &p.tmk, fa, 0, hk, ka, b, pol_kv);
+        tma_load_4d(sA + sa * kTile + kHalf, &p.tmk, fa, 64, hk, ka, b, pol_kv);
+        if (!mbar_wait_abort(&bar->b_empty[sb], ((t / kSb) & 1) ^ 1, abort)) break;
+        uint64_t* fb = &bar->b_full[sb];
+        mbar_arrive_expect_tx(fb, kTile);
+        tma_load_4d(sB + sb * kTile, &p.tmv, fb, 0, hk, ka, b, pol_kv);
+        tma_load_4d(sB + sb * kTile + kHalf, &p.tmv, fb, 64, hk, ka, b, pol_kv);
       }
     }
     __syncwarp();
@@ -510,50 +613,48 @@ __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar
     if (lane == 0 && n > 0) {
       const uint64_t aQ = tc::sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t aO = tc::sdesc_sw128(smem_u32(sdO), 16, 1024);
-      const uint64_t bK = tc::sdesc_sw128(smem_u32(sK), 16, 1024);               // K-major B
-      const uint64_t bV = tc::sdesc_sw128(smem_u32(sK + kTileC), 16, 1024);
-      const uint64_t bKm = tc::sdesc_sw128(smem_u32(sK), kHalfC, 1024);          // MN-major B
-      // S = Q K^T and dP = dO V^T of sub-tile i into buffer i & 1
-      auto sdp = [&](int i) -> bool {
-        const int st = i % kSt, bf = i & 1;
-        if (!mbar_wait_abort(&bar->st_full[st], (i / kSt) & 1, abort)) return false;
+      const uint64_t bK = tc::sdesc_sw128(smem_u32(sA), 16, 1024);       // K-major
+      const uint64_t bKm = tc::sdesc_sw128(smem_u32(sA), kHalf, 1024);   // MN-major
+      const uint64_t bV = tc::sdesc_sw128(smem_u32(sB), 16, 1024);
+      auto soa = [](int t) { return (uint64_t)(((t % kSa) * kTile) >> 4); };
+      auto sob = [](int t) { return (uint64_t)(((t % kSb) * kTile) >> 4); };
+      // per step t (buffer t & 1): dP = dO V^T, then S of step t+1, then dQ += dS K
+      bool ok = mbar_wait_abort(&bar->res_full, 0, abort) &&
+                mbar_wait_abort(&bar->a_full[0], 0, abort);
+      if (ok) {
         tc::fence_after();
-        const uint64_t so = (uint64_t)((st * kStage) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kHD / 16; ++kk) {
-          const uint32_t oa = ((kk >> 2) * kHalfR + (kk & 3) * 32) >> 4;
-          const uint32_t ob = ((kk >> 2) * kHalfC + (kk & 3) * 32) >> 4;
-          tc::mma_bf16(tmem + bf * 128, aQ + oa, bK + so + ob, kIdescSub, kk > 0);
-          tc::mma_bf16(tmem + bf * 128 + 64, aO + oa, bV + so + ob, kIdescSub, kk > 0);
-        }
-        tc::commit(smem_u32(&bar->s_full[bf]));
-        return true;
-      };
-      // dQ += dS K of sub-tile i, then release its stage
-      auto acc = [&](int i) -> bool {
-        const int st = i % kSt, bf = i & 1;
-        if (!mbar_wait_abort(&bar->ds_ready[bf], (i >> 1) & 1, abort)) return false;
-        tc::fence_after();
-        const uint64_t so = (uint64_t)((st * kStage) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kBC / 16; ++kk)
-          tc::mma_bf16_ts(tmem + kTAcc, tmem + bf * 128 + 64 + packed_col(kk),
-                          bKm + so + ((kk * 2048) >> 4), kIdescAcc, i > 0 || kk > 0);
-        tc::commit(smem_u32(&bar->st_empty[st]));
-        return true;
-      };
-      bool ok = mbar_wait_abort(&bar->res_full, 0, abort);
-      for (int i = 0; ok && i < n; ++i) {
-        ok = sdp(i);
-        if (ok && i > 0) ok = acc(i - 1);
+        mma_ss8(tmem, aQ, bK + soa(0), false);  // S(0) = Q K(0)^T
+        tc::commit(smem_u32(&bar->s_full[0]));
       }
-      if (ok) ok = acc(n - 1);
+      for (int t = 0; ok && t < n; ++t) {
+        const int bf = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        const uint32_t tb = tmem + bf * 128;
+        if (!(ok = mbar_wait_abort(&bar->p_ready[bf], ph, abort) &&
+                   mbar_wait_abort(&bar->b_full[t % kSb], (t / kSb) & 1, abort)))
+          break;
+        tc::fence_after();
+        mma_ss8(tb, aO, bV + sob(t), false);  // dP = dO V^T
+        tc::commit(smem_u32(&bar->dp_full[bf]));
+        tc::commit(smem_u32(&bar->b_empty[t % kSb]));
+        if (t + 1 < n) {
+          if (!(ok = mbar_wait_abort(&bar->a_full[(t + 1) % kSa], ((t + 1) / kSa) & 1, abort)))
+            break;
+          tc::fence_after();
+          mma_ss8(tmem + (bf ^ 1) * 128, aQ, bK + soa(t + 1), false);
+          tc::commit(smem_u32(&bar->s_full[bf ^ 1]));
+        }
+        if (!(ok = mbar_wait_abort(&bar->ds_ready[bf], ph, abort))) break;
+        tc::fence_after();
+        mma_ts8(tmem + kTAcc, tb, bKm + soa(t), t > 0);  // dQ += dS K
+        tc::commit(smem_u32(&bar->a_empty[t % kSa]));
+      }
       if (ok) tc::commit(smem_u32(&bar->done));
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int quad = warp & 3, half = warp >> 2;
+    const int quad = warp & 3, part = warp >> 2;
     const int row = quad * 32 + lane;  // query row of the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const int64_t qpos = q0 + row;
@@ -563,28 +664,35 @@ __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar
     const int32_t b0 = keys_below(km, max((int64_t)0, qpos - p.W + 1));
     const int32_t b1 = keys_below(km, qpos + 1);
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
-      const int bf = i & 1;
-      const int32_t ka = sub_at(i) * kBC;
-      const int32_t kb = min(km.n_keys, ka + kBC) - 1;
-      const bool masked = ka + kBC > km.n_keys ||
+    float pr[kNC];
+    for (int t = 0; t < n; ++t) {
+      const int bf = t & 1;
+      const uint32_t ph = (t >> 1) & 1;
+      const int32_t ka = tile_at(t) * kT;
+      const int32_t kb = min(km.n_keys, ka + kT) - 1;
+      const bool masked = ka + kT > km.n_keys ||
                           tile_class(km, c0, q0r, q1r, ka, kb, P, p.W) != kFull;
-      const int32_t base = ka + half * 32;
-      ok = mbar_wait_abort(&bar->s_full[bf], (i >> 1) & 1, abort);
+      const int32_t base = ka + part * kNC;
+      const uint32_t tS = tmem + bf * 128 + part * kNC + lane_off;
+      ok = mbar_wait_abort(&bar->s_full[bf], ph, abort);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc::fence_after();
-      const uint32_t tS = tmem + bf * 128 + half * 32 + lane_off;
       if (masked)
-        ds_row<true>(tS, tS + 64, p.scale_log2, ldr.x, ldr.y, a1 - base, b0 - base, b1 - base);
+        p_row<true>(tS, p.scale_log2, ldr.x, a1 - base, b0 - base, b1 - base, pr);
       else
-        ds_row<false>(tS, tS + 64, p.scale_log2, ldr.x, ldr.y, 0, 0, 0);
-      tc::wait_st();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar->ds_ready[bf]);
+        p_row<false>(tS, p.scale_log2, ldr.x, 0, 0, 0, pr);
+      release(&bar->p_ready[bf], lane, false);
+      ok = mbar_wait_abort(&bar->dp_full[bf], ph, abort);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+      ds_row(tS, ldr.y, pr);
+      release(&bar->ds_ready[bf], lane, true);
     }
     if (ok && n > 0) {
       ok = mbar_wait_abort(&bar->done, 0, abort);
@@ -595,10 +703,10 @@ __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar
       const bool valid = q0r + row <= q1r;
       float* dst = p.dq + (((int64_t)b * p.S + (valid ? q0r + row : 0)) * p.hq + h) * kHD;
       if (n > 0) {
-        store_chunk(tmem + kTAcc + lane_off, dst, half, valid, p.scale, true, (int32_t)qpos,
+        store_chunk(tmem + kTAcc + lane_off, dst, part, valid, p.scale, true, (int32_t)qpos,
                     p.turns);
       } else if (valid) {
-        for (int e = half * 32; e < half * 32 + 32; e += 4) {
+        for (int e = part * kPairs; e < part * kPairs + kPairs; e += 4) {
           *reinterpret_cast<float4*>(dst + e) = make_float4(0.f, 0.f, 0.f, 0.f);
           *reinterpret_cast<float4*>(dst + 64 + e) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -611,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
-  Bars* bar = reinterpret_cast<Bars*>(smem + 2 * kTileR + kSt * kStage + kSt * kLdBytes);
+  Bars* bar = reinterpret_cast<Bars*>(smem + kOffBars);
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
     tc::alloc(smem_u32(&bar->tmem_slot), 512);
@@ -619,13 +727,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   }
   if (tid == 32) {
     mbar_init(&bar->res_full, 1);
-    for (int s = 0; s < kSt; ++s) {
-      mbar_init(&bar->st_full[s], 1);
-      mbar_init(&bar->st_empty[s], 1);
+    for (int s = 0; s < kSaQ; ++s) {
+      mbar_init(&bar->a_full[s], 1);
+      mbar_init(&bar->a_empty[s], 1);
+    }
+    for (int s = 0; s < kSb; ++s) {
+      mbar_init(&bar->b_full[s], 1);
+      mbar_init(&bar->b_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
-      mbar_init(&bar->ds_ready[i], 8);  // one arrival per softmax warp
+      mbar_init(&bar->p_ready[i], kSoftWarps);  // one arrival per softmax warp
+      mbar_init(&bar->dp_full[i], 1);
+      mbar_init(&bar->ds_ready[i], kSoftWarps);
     }
     mbar_init(&bar->done, 1);
     bar->abort = 0;
@@ -667,7 +781,7 @@ struct Layout {
 
 static Layout layout(int B, int S, int hq, int hkv, int D) {
   Layout L;
-  L.s_pad = (S + kBM - 1) / kBM * kBM;
+  L.s_pad = (S + kT - 1) / kT * kT;
   L.q_off = 0;
   L.k_off = align256((size_t)B * S * hq * D * 2);
   L.ld_off = L.k_off + align256((size_t)B * S * hkv * D * 2);
@@ -711,7 +825,7 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
   const bwd::Layout L = bwd::layout(batch, seqlen, n_q_heads, n_kv_heads, head_dim);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PS_ERR_WORKSPACE;
   if (workspace_bytes < L.total) return PS_ERR_WORKSPACE;
-  const int32_t nq = (seqlen + bwd::kBM - 1) / bwd::kBM;
+  const int32_t nq = (seqlen + bwd::kT - 1) / bwd::kT;
   const int64_t n_dkdv = (int64_t)nq * n_kv_heads * batch;
   const int64_t n_dq = (int64_t)nq * n_q_heads * batch;
   if (n_dkdv + n_dq > 0x7fffffffLL) return PS_ERR_UNSUPPORTED;
@@ -751,18 +865,13 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
   const uint64_t kd[4] = {(uint64_t)head_dim, (uint64_t)n_kv_heads, (uint64_t)seqlen, (uint64_t)batch};
   const uint64_t ks[3] = {(uint64_t)head_dim * 2, (uint64_t)n_kv_heads * head_dim * 2,
                           (uint64_t)seqlen * n_kv_heads * head_dim * 2};
-  const uint32_t box_r[4] = {64u, 1u, (uint32_t)bwd::kBM, 1u};
-  const uint32_t box_c[4] = {64u, 1u, (uint32_t)bwd::kBC, 1u};
+  const uint32_t box[4] = {64u, 1u, (uint32_t)bwd::kT, 1u};
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const bool okm = encode_tmap(&p.tmq_r, bf, 4, ws + L.q_off, qd, qs, box_r, sw) &&
-                   encode_tmap(&p.tmq_c, bf, 4, ws + L.q_off, qd, qs, box_c, sw) &&
-                   encode_tmap(&p.tmdo_r, bf, 4, d_out, qd, qs, box_r, sw) &&
-                   encode_tmap(&p.tmdo_c, bf, 4, d_out, qd, qs, box_c, sw) &&
-                   encode_tmap(&p.tmk_r, bf, 4, ws + L.k_off, kd, ks, box_r, sw) &&
-                   encode_tmap(&p.tmk_c, bf, 4, ws + L.k_off, kd, ks, box_c, sw) &&
-                   encode_tmap(&p.tmv_r, bf, 4, v, kd, ks, box_r, sw) &&
-                   encode_tmap(&p.tmv_c, bf, 4, v, kd, ks, box_c, sw);
+  const bool okm = encode_tmap(&p.tmq, bf, 4, ws + L.q_off, qd, qs, box, sw) &&
+                   encode_tmap(&p.tmdo, bf, 4, d_out, qd, qs, box, sw) &&
+                   encode_tmap(&p.tmk, bf, 4, ws + L.k_off, kd, ks, box, sw) &&
+                   encode_tmap(&p.tmv, bf, 4, v, kd, ks, box, sw);
   if (!okm) return PS_ERR_CUDA;
   p.ld = reinterpret_cast<const float2*>(ws + L.ld_off);
   p.q_start = q_start;

@@ -110,6 +110,23 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
 }
 
 // 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : PS_R8(0), PS_R8(8)
+      : "r"(taddr));
+}
+
+// 8 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                   taddr),
+               PS_W8(0)
+               : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
