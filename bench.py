@@ -602,6 +602,14 @@ def main():
     del cache, q, k, v
     torch.cuda.empty_cache()
 
+    # the other decode legs run before the prefill legs, whose power draw can
+    # leave the next few hundred milliseconds of decode slower
+    ragged = flat = comparators = None
+    if not args.no_extra and (rank == 0 or world == 1):
+        ragged = ragged_leg(ps, torch, 100, 4, hbm_peak)
+        flat = flatness_leg(ps, torch, 20, seed, hbm_peak)
+        comparators = comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak)
+
     # prefill (one layer) and the truncated-backprop training forward
     try:
         if args.no_prefill:
@@ -618,12 +626,6 @@ def main():
     except Exception as e:  # noqa: BLE001
         pre = {"unavailable": f"{type(e).__name__}: {e}"}
         train = None
-
-    ragged = flat = comparators = None
-    if not args.no_extra and (rank == 0 or world == 1):
-        ragged = ragged_leg(ps, torch, 100, 4, hbm_peak)
-        flat = flatness_leg(ps, torch, 20, seed, hbm_peak)
-        comparators = comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak)
 
     if not args.no_baselines and (rank == 0 or world == 1):
         fsteps = min(args.steps, 30)
