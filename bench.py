@@ -182,6 +182,28 @@ def decode_setup(ps, torch, seed, W, P, pos0, n_steps, full_causal=False):
     return cache, q, k, v, pos, L
 
 
+def max_over_ranks(dist, value: float, device: str) -> float:
+    """The slowest rank's value (every rank gets it); the value itself without
+    a process group.  Replicas run independent batches, so the job's time is the
+    slowest replica's."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(base: int, rank: int) -> int:
+    """Seed of a replica's synthetic batch: every rank decodes its own sequences."""
+    return base + 101 * rank
+
+
+def job_tokens_per_s(world: int, nseq: int, steps: int, total_ms: float) -> float:
+    """Whole-job decode rate: every replica's tokens over the slowest replica's time."""
+    return world * nseq * steps / (total_ms / 1e3)
+
+
 def run_decode(ps, torch, cache, q, k, v, pos, steps, warmup, dist=None, per_kernel=True):
     """Times `steps` decode steps (append + partial + combine) after `warmup`.
 
@@ -216,11 +238,7 @@ def run_decode(ps, torch, cache, q, k, v, pos, steps, warmup, dist=None, per_ker
         step(warmup + i)
     e1.record(stream)
     torch.cuda.synchronize()
-    total_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(dist, e0.elapsed_time(e1), "cuda")
     kern_ms = None
     if per_kernel:
         # the same steps again (the ring's later slots are simply overwritten again):
@@ -572,7 +590,7 @@ def main():
     if args.only:
         return only_leg(ps, torch, args, bf16_peak)
     d = DEC
-    seed = d["seed"] + 101 * rank
+    seed = replica_seed(d["seed"], rank)
     P = decode_prefix_lens(seed, d["nseq"])
     n_steps = args.warmup + args.steps
     cache, q, k, v, pos, L = decode_setup(ps, torch, seed, d["W"], P, d["pos0"], n_steps)
@@ -581,7 +599,7 @@ def main():
     assert cache.check_status() == 0
     assert torch.isfinite(out.float()).all()
     ms_step = total_ms / args.steps
-    value = world * d["nseq"] * args.steps / (total_ms / 1e3)
+    value = job_tokens_per_s(world, d["nseq"], args.steps, total_ms)
 
     kv_bytes = float(np.sum(2 * d["hkv"] * L * d["D"] * 2))  # K and V of the live slots
     q_bytes = d["nseq"] * d["hq"] * d["D"] * 2

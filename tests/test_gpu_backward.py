@@ -67,3 +67,36 @@ def test_backward_matches_oracle(ps, B, S, hq, hkv, P, W):
         _close(dq[b].double().cpu().numpy(), rq, f"dq b={b}")
         _close(dk[b].double().cpu().numpy(), rk, f"dk b={b}")
         _close(dv[b].double().cpu().numpy(), rv, f"dv b={b}")
+
+
+@pytest.mark.parametrize("B,S,hq,hkv,P,W,c0", [
+    (2, 300, 4, 2, [100, 100], 64, [50, 1000]),  # chunk starts inside / after the prefix
+    (1, 256, 2, 1, [40], 128, [7]),              # unaligned start: RoPE at odd positions
+])
+def test_backward_chunk_offset(ps, B, S, hq, hkv, P, W, c0):
+    """A chunk at positions q_start .. q_start + S - 1 (no cached history): the mask
+    and the rotations use absolute positions."""
+    seed, D, theta = 43, 128, 10000.0
+    pos = [c + np.arange(S) for c in c0]
+    q = np.stack([synth.query_bits(seed, b, pos[b], hq, D) for b in range(B)])
+    kv = [synth.History(seed, b, hkv, D).rows_bits(pos[b]) for b in range(B)]
+    k = np.stack([x[0] for x in kv])
+    v = np.stack([x[1] for x in kv])
+    do = np.stack([synth.normal_bf16(seed, STREAM_DO, b, pos[b], hq, D) for b in range(B)])
+    i32 = dict(dtype=torch.int32, device="cuda")
+    tq, tk, tv, tdo = (bits_to_bf16_tensor(x) for x in (q, k, v, do))
+    qs = torch.tensor(c0, **i32)
+    pl = torch.tensor(P, **i32)
+    status = torch.zeros(1, **i32)
+    out, lse = ps.prefill(tq, tk, tv, qs, pl, W, rope_theta=theta, status=status)
+    dq, dk, dv = ps.prefill_backward(tq, tk, tv, out, lse, tdo, qs, pl, W, rope_theta=theta,
+                                     status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for b in range(B):
+        rq, rk, rv, _, _ = attend_backward(synth.bits_to_f64(q[b]), synth.bits_to_f64(k[b]),
+                                           synth.bits_to_f64(v[b]), synth.bits_to_f64(do[b]),
+                                           P[b], W, theta, positions=pos[b])
+        _close(dq[b].double().cpu().numpy(), rq, f"dq b={b}")
+        _close(dk[b].double().cpu().numpy(), rk, f"dk b={b}")
+        _close(dv[b].double().cpu().numpy(), rv, f"dv b={b}")
