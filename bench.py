@@ -156,7 +156,7 @@ def fill_random(cache, runs_per_seq, gen, torch, chunk_tokens=1 << 21):
 
 
 # ---- decode ---------------------------------------------------------------
-def decode_setup(ps, torch, seed, W, P, pos0, n_steps, full_causal=False):
+def decode_setup(ps, torch, seed, W, P, pos0, n_steps, full_causal=False, pe_mode=0):
     """Ring cache holding, per sequence, the live K/V of positions < pos0[s]
     (random values), plus every step's q, k, v and positions resident in HBM.
     pos0 is one position for all sequences or one per sequence."""
@@ -167,7 +167,8 @@ def decode_setup(ps, torch, seed, W, P, pos0, n_steps, full_causal=False):
         W = int(pos0.max()) + n_steps + 1
         P = np.zeros(nseq, dtype=np.int64)
     cache = ps.RingCache(nseq, d["hkv"], d["D"], W, P, rope_theta=d["theta"],
-                         prefix_max=int(max(P.max(), d["Pmax"] if not full_causal else 0)), zero=False)
+                         prefix_max=int(max(P.max(), d["Pmax"] if not full_causal else 0)), zero=False,
+                         pe_mode=pe_mode)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(seed)
     runs = {s: live_runs(int(pos0[s]) - 1, int(P[s]), W) for s in range(nseq)}
@@ -252,10 +253,11 @@ def run_decode(ps, torch, cache, q, k, v, pos, steps, warmup, dist=None, per_ker
     return total_ms, kern_ms, out, lse
 
 
-def decode_leg(ps, torch, name, P, W, pos0, steps, warmup, seed, hbm_peak):
+def decode_leg(ps, torch, name, P, W, pos0, steps, warmup, seed, hbm_peak, pe_mode=0):
     """One decode workload: append + partial + combine per step, one layer."""
     d = DEC
-    cache, q, k, v, pos, L = decode_setup(ps, torch, seed, W, P, pos0, steps + warmup)
+    cache, q, k, v, pos, L = decode_setup(ps, torch, seed, W, P, pos0, steps + warmup,
+                                          pe_mode=pe_mode)
     total_ms, kern_ms, out, lse = run_decode(ps, torch, cache, q, k, v, pos, steps, warmup)
     assert cache.check_status() == 0 and torch.isfinite(out.float()).all()
     nseq = len(P)
@@ -304,7 +306,8 @@ def flatness_leg(ps, torch, steps, seed, hbm_peak):
 def comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak):
     """The same library on the same shapes with a plain sliding window (P = 0)
     and a StreamingLLM-style 4-token sink (P = 4): decode at the steady-decode
-    shapes, prefill at the 32K prefill shape."""
+    shapes, prefill at the 32K prefill shape; and Reset PE decode at the
+    steady-decode shapes."""
     d = DEC
     out = {}
     for name, pval in (("sliding_window_P0", 0), ("streaming_sink_P4", 4)):
@@ -319,6 +322,13 @@ def comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak):
             rep.update({"prefill_ms": pr["ms"], "prefill_tflops_algorithmic": pr["tflops_algorithmic"],
                         "prefill_frac_of_measured_bf16": pr["frac_of_measured_bf16_burst"]})
         out[name] = rep
+    # Reset PE: the same steady-decode shapes with the cache renumbered per query
+    P = decode_prefix_lens(seed, d["nseq"])
+    r = decode_leg(ps, torch, "decode, 64 x 131072, W 4096, Reset PE", P, d["W"], d["pos0"], 100, 5,
+                   seed + 13, hbm_peak, pe_mode=ps.PS_PE_RESET)
+    out["reset_pe"] = {"decode_tok_s_per_layer": r["tok_s_per_layer"], "decode_step_ms": r["step_ms"],
+                       "decode_partial_ms": r["partial_kernel_ms"], "decode_partial_gbs": r["partial_gbs"],
+                       "decode_partial_frac_of_measured_hbm": r["partial_frac_of_measured_hbm"]}
     return out
 
 
