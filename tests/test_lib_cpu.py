@@ -108,3 +108,34 @@ def test_tile_grid_matches_oracle_shapes(ps):
             kpos = list(range(q0, q0 + S))
         c = tile_classes(np.arange(q0, q0 + S), np.array(kpos), P, W, bm, bn)
         assert (nq, nk) == c.shape
+
+
+def test_backward_host_validation(ps):
+    """ps_prefill_backward rejects bad arguments before any CUDA call."""
+    lib = ps.lib
+    b = ctypes.c_size_t()
+    assert lib.ps_prefill_backward_workspace_size(1, 300, 4, 2, 128, ctypes.byref(b)) == 0
+    need = b.value
+    # rotated Q (1 x 300 x 4 x 128 bf16), rotated K, {LSE, D} pairs over 384 padded rows
+    assert need >= 300 * 4 * 128 * 2 + 300 * 2 * 128 * 2 + 4 * 384 * 8
+    assert lib.ps_prefill_backward_workspace_size(1, 300, 4, 3, 128, ctypes.byref(b)) == 1  # Hq % Hkv
+    assert lib.ps_prefill_backward_workspace_size(1, 300, 4, 2, 64, ctypes.byref(b)) == 2   # head_dim
+    assert lib.ps_prefill_backward_workspace_size(0, 300, 4, 2, 128, ctypes.byref(b)) == 1
+    fake = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: validation fails first
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    i32 = ctypes.c_void_p(1 << 21)
+    f = ctypes.c_void_p(1 << 22)
+
+    def call(q=fake, W=64, hd=128, ws=fake, ws_bytes=need, dq=f, scale=0.088):
+        return lib.ps_prefill_backward(q, fake, fake, fake, f, fake, 1, 300, i32, i32, W, 4, 2, hd,
+                                       ctypes.c_float(scale), ctypes.c_double(1e4), dq, f, f, ws,
+                                       ws_bytes, None, None)
+
+    assert call(q=None) == 1          # null pointer
+    assert call(W=0) == 1             # window < 1
+    assert call(scale=0.0) == 1       # scale must be positive
+    assert call(hd=64) == 2           # head_dim 128 only
+    assert call(q=odd) == 3           # 16-byte alignment
+    assert call(ws=None) == 4         # no workspace
+    assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == 4  # workspace not 256-byte aligned
+    assert call(ws_bytes=need - 1) == 4  # workspace too small
