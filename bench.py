@@ -333,37 +333,32 @@ def comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak):
 
 
 def run_decode_e2e(ps, torch, cache, steps, warmup, seed):
-    """Same decode step through host buffers: pinned host -> device copies of the
-    step's q, k, v, pos; append + decode; device -> host copy of O and LSE."""
+    """Same decode step through host buffers, with the package's DecodeGraph: per
+    step one pinned host -> device copy of the step's packed q, k, v, pos, one
+    graph replay (append + decode), one device -> host copy of the packed O and
+    LSE, and a stream synchronisation."""
     d = DEC
-    nseq = d["nseq"]
-    gen = torch.Generator().manual_seed(seed)
+    nseq, hq, hkv, D = d["nseq"], d["hq"], d["hkv"], d["D"]
+    g = ps.DecodeGraph(cache, hq)
     n = steps + warmup
-    hq_ = torch.randn(n, nseq, d["hq"], d["D"], generator=gen).to(torch.bfloat16).pin_memory()
-    hk = torch.randn(n, nseq, d["hkv"], d["D"], generator=gen).to(torch.bfloat16).pin_memory()
-    hv = torch.randn(n, nseq, d["hkv"], d["D"], generator=gen).to(torch.bfloat16).pin_memory()
+    gen = torch.Generator().manual_seed(seed)
+    hin = torch.zeros(n, g.inp.numel(), dtype=torch.uint8).pin_memory()
+    for name, heads in (("q", hq), ("k", hkv), ("v", hkv)):
+        o, nb = g.in_layout[name]
+        hin[:, o:o + nb].view(torch.bfloat16).view(n, nseq, heads, D).copy_(
+            torch.randn(n, nseq, heads, D, generator=gen).to(torch.bfloat16))
     start = d["pos0"] + 100000  # positions after the device-resident run
-    hpos = (start + torch.arange(n, dtype=torch.int32))[:, None].repeat(1, nseq).contiguous().pin_memory()
-    dq = torch.empty(nseq, d["hq"], d["D"], dtype=torch.bfloat16, device="cuda")
-    dk = torch.empty(nseq, d["hkv"], d["D"], dtype=torch.bfloat16, device="cuda")
-    dv = torch.empty_like(dk)
-    dpos = torch.empty(nseq, dtype=torch.int32, device="cuda")
-    out = torch.empty_like(dq)
-    lse = torch.empty(nseq, d["hq"], dtype=torch.float32, device="cuda")
-    ho = torch.empty(nseq, d["hq"], d["D"], dtype=torch.bfloat16).pin_memory()
-    hl = torch.empty(nseq, d["hq"], dtype=torch.float32).pin_memory()
-    ws = cache.workspace(d["hq"])
+    o, nb = g.in_layout["pos"]
+    hin[:, o:o + nb].view(torch.int32).copy_(
+        (start + torch.arange(n, dtype=torch.int32))[:, None].repeat(1, nseq))
+    hres = torch.empty(g.res.numel(), dtype=torch.uint8).pin_memory()
+    stream = torch.cuda.current_stream()
 
     def step(i):
-        dq.copy_(hq_[i], non_blocking=True)
-        dk.copy_(hk[i], non_blocking=True)
-        dv.copy_(hv[i], non_blocking=True)
-        dpos.copy_(hpos[i], non_blocking=True)
-        cache.append_tokens(dpos, dk, dv)
-        cache.decode(dq, dpos, out=out, lse=lse, workspace=ws)
-        ho.copy_(out, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        g.inp.copy_(hin[i], non_blocking=True)
+        g.replay()
+        hres.copy_(g.res, non_blocking=True)
+        stream.synchronize()
 
     for i in range(warmup):
         step(i)
@@ -371,9 +366,7 @@ def run_decode_e2e(ps, torch, cache, steps, warmup, seed):
     for i in range(steps):
         step(warmup + i)
     dt = time.perf_counter() - t0
-    h2d = (dq.numel() + dk.numel() + dv.numel()) * 2 + dpos.numel() * 4
-    d2h = out.numel() * 2 + lse.numel() * 4
-    return dt, h2d, d2h
+    return dt, g.inp.numel(), g.res.numel()
 
 
 # ---- prefill --------------------------------------------------------------
@@ -625,8 +618,9 @@ def main():
         dt, h2d, d2h = run_decode_e2e(ps, torch, cache, min(args.steps, 200), 5, seed + 7)
         e2e = {"value": d["nseq"] * min(args.steps, 200) / dt, "unit": "tok/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "how": "pinned host -> device copies of q, k, v, pos; ps_kv_append + ps_decode; "
-                      "device -> host O and LSE; stream sync each step; host wall clock"}
+               "how": "per step: one pinned host -> device copy of the packed q, k, v, pos; "
+                      "DecodeGraph replay (ps_kv_append + ps_decode captured in a CUDA graph); "
+                      "one device -> host copy of the packed O and LSE; stream sync; host wall clock"}
     del cache, q, k, v
     torch.cuda.empty_cache()
 

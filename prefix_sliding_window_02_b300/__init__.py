@@ -15,7 +15,7 @@ from ._lib import (CacheDesc, PsError, check, lib, PS_DEV_BAD_POS, PS_DEV_BAD_PR
                    PS_DEV_BAD_RUN, PS_DEV_BAD_SEQ, PS_DEV_BAD_SLOT, PS_DEV_TIMEOUT, PS_PE_CONTINUE,
                    PS_PE_RESET)
 
-__all__ = ["RingCache", "ring_slots", "decode_workspace_size", "prefill_workspace_size",
+__all__ = ["RingCache", "DecodeGraph", "ring_slots", "decode_workspace_size", "prefill_workspace_size",
            "prefill", "prefill_backward", "prefill_tile_grid", "prefill_tile_classes", "PsError",
            "lib"]
 
@@ -262,6 +262,65 @@ def prefill_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: tor
                                   _vp(dk), _vp(dv), _vp(ws), ws.numel(), _vp(status),
                                   _stream(stream)), "ps_prefill_backward")
     return dq, dk, dv
+
+
+class DecodeGraph:
+    """One decode step of a RingCache (ps_kv_append of one token per sequence, then
+    ps_decode) captured once in a CUDA graph over fixed device buffers.
+
+    The step's inputs live in one packed device buffer ``inp`` (views ``q`` [nseq, Hq,
+    D], ``k``, ``v`` [nseq, Hkv, D] bf16 raw, ``pos`` [nseq] int32) and its results in
+    one packed buffer ``res`` (views ``out`` [nseq, Hq, D] bf16, ``lse`` [nseq, Hq]
+    fp32), so a caller moves a step's data with one copy each way; ``replay()``
+    launches the three kernels of the step from the graph.  ``in_layout`` /
+    ``res_layout`` give (offset, nbytes) of each view, for packing host buffers the
+    same way.  The graph keeps the cache, its workspace and these buffers alive.
+    """
+
+    def __init__(self, cache: "RingCache", n_q_heads: int, scale: Optional[float] = None):
+        nseq, hkv, D = cache.nseq, cache.n_kv_heads, cache.head_dim
+        dev = cache.k_pool.device
+
+        def layout(parts):
+            out, off = {}, 0
+            for name, nbytes in parts:
+                out[name] = (off, nbytes)
+                off += (nbytes + 255) // 256 * 256
+            return out, off
+
+        self.in_layout, n_in = layout([("q", nseq * n_q_heads * D * 2), ("k", nseq * hkv * D * 2),
+                                       ("v", nseq * hkv * D * 2), ("pos", nseq * 4)])
+        self.res_layout, n_res = layout([("out", nseq * n_q_heads * D * 2),
+                                         ("lse", nseq * n_q_heads * 4)])
+        self.inp = torch.zeros(n_in, dtype=torch.uint8, device=dev)
+        self.res = torch.zeros(n_res, dtype=torch.uint8, device=dev)
+
+        def view(buf, lay, name, dtype, shape):
+            o, n = lay[name]
+            return buf[o:o + n].view(dtype).view(*shape)
+
+        self.q = view(self.inp, self.in_layout, "q", BF16, (nseq, n_q_heads, D))
+        self.k = view(self.inp, self.in_layout, "k", BF16, (nseq, hkv, D))
+        self.v = view(self.inp, self.in_layout, "v", BF16, (nseq, hkv, D))
+        self.pos = view(self.inp, self.in_layout, "pos", torch.int32, (nseq,))
+        self.out = view(self.res, self.res_layout, "out", BF16, (nseq, n_q_heads, D))
+        self.lse = view(self.res, self.res_layout, "lse", torch.float32, (nseq, n_q_heads))
+        self._seq = torch.arange(nseq, dtype=torch.int32, device=dev)
+        self._cu = torch.arange(nseq + 1, dtype=torch.int32, device=dev)
+        self._ws = torch.empty(decode_workspace_size(nseq, n_q_heads, hkv, D), dtype=torch.uint8,
+                               device=dev)
+        self.cache = cache
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        # relaxed: the decode call queries occupancy and sets kernel attributes on the host
+        with torch.cuda.graph(self.graph, capture_error_mode="relaxed"):
+            cache.append(self._seq, self.pos, self._cu, self.k, self.v)
+            cache.decode(self.q, self.pos, scale=scale, out=self.out, lse=self.lse,
+                         workspace=self._ws)
+
+    def replay(self) -> None:
+        """Append the step's tokens and decode them (asynchronous, current stream)."""
+        self.graph.replay()
 
 
 def prefill_tile_grid(seqlen: int, q_start: int, prefix_len: int, window: int,

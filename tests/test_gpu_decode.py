@@ -229,3 +229,41 @@ def test_decode_reset_pe_shapes(ps, nseq, hq, hkv, D, P, W, pos):
         qs = synth.bits_to_f64(synth.query_bits(seed, s, pos[s], hq, D))[0]
         o_ref, l_ref = attend_reset_pe(qs, pos[s], P[s], W, synth.History(seed, s, hkv, D).rows, theta)
         assert_attention_close(bf16_tensor_to_f64(o[s]), lse[s].cpu().numpy(), o_ref, l_ref, f"seq {s}")
+
+
+def test_decode_graph_replays_the_eager_step(ps):
+    """DecodeGraph (append + decode captured once, replayed per step) gives the same
+    bits as the eager calls on an identical cache, and stays within the oracle's
+    tolerance, across steps that evict."""
+    seed, nseq, hq, hkv, D, W, theta = 17, 3, 4, 2, 128, 64, 10000.0
+    P = np.array([5, 40, 0])
+    pos0 = np.array([100, 70, 300])
+    caches = []
+    for _ in range(2):
+        c = ps.RingCache(nseq, hkv, D, W, P, rope_theta=theta)
+        runs = {s: live_runs(int(pos0[s]) - 1, int(P[s]), W) for s in range(nseq)}
+        append_runs(c, runs, synth_source(seed, hkv, D))
+        caches.append(c)
+    torch.cuda.synchronize()
+    eager, graphed = caches
+    g = ps.DecodeGraph(graphed, hq)
+    for step in range(20):
+        pos = pos0 + step
+        kv = [synth.History(seed, s, hkv, D).rows_bits([int(pos[s])]) for s in range(nseq)]
+        k = bits_to_bf16_tensor(np.concatenate([x[0] for x in kv]))
+        v = bits_to_bf16_tensor(np.concatenate([x[1] for x in kv]))
+        q = _queries(seed, nseq, pos, hq, D)
+        tpos = torch.tensor(pos, dtype=torch.int32, device="cuda")
+        eager.append_tokens(tpos, k, v)
+        o_e, l_e = eager.decode(q, tpos)
+        g.q.copy_(q)
+        g.k.copy_(k)
+        g.v.copy_(v)
+        g.pos.copy_(tpos)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(g.out, o_e) and torch.equal(g.lse, l_e), step
+    ref = _oracle_rows(seed, range(nseq), pos, P, W, hq, hkv, D, theta)
+    for s in range(nseq):
+        assert_attention_close(g.out[s].float().cpu().numpy(), g.lse[s].cpu().numpy(), *ref[s])
+    assert eager.check_status() == 0 and graphed.check_status() == 0
