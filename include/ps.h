@@ -247,8 +247,11 @@ ps_status_t ps_prefill(const void* q, const void* k, const void* v, int32_t batc
                        int32_t* status, void* stream);
 
 /*
- * ps_prefill_backward_workspace_size: device workspace for ps_prefill_backward
- * (rotated Q and K, and D = rowsum(dO * O)).
+ * ps_prefill_backward_workspace_size: device workspace for ps_prefill_backward:
+ * rotated Q and K (bf16), and per (batch row, query head, row rounded up to 128)
+ * the pair {LSE * log2(e), D = rowsum(dO * O)} (fp32).  Errors: null `bytes`,
+ * batch / seqlen / heads < 1 or Hq % Hkv != 0 -> PS_ERR_INVALID_ARGUMENT;
+ * head_dim != 128 -> PS_ERR_UNSUPPORTED.
  */
 ps_status_t ps_prefill_backward_workspace_size(int32_t batch, int32_t seqlen, int32_t n_q_heads,
                                                int32_t n_kv_heads, int32_t head_dim,
@@ -267,7 +270,16 @@ ps_status_t ps_prefill_backward_workspace_size(int32_t batch, int32_t seqlen, in
  *     query heads of each group).  The rotation is differentiated exactly; the
  *     bf16 rounding of the rotated q and k passes gradients straight through.
  *   Probabilities and dS enter the tensor-core products as bf16.
- *   head_dim 128 only.
+ *   workspace : device, 256-byte aligned, at least the size above; the caller
+ *     owns it and may reuse it once the call's stream work has completed.
+ *   status : device int32 word or NULL; PS_DEV_TIMEOUT if a bounded wait gave up.
+ * Errors (host, before any launch): a null pointer, batch / seqlen / window /
+ * heads < 1, Hq % Hkv != 0, scale <= 0 or rope_theta <= 0 -> PS_ERR_INVALID_ARGUMENT;
+ * head_dim != 128 -> PS_ERR_UNSUPPORTED; a tensor not 16-byte aligned ->
+ * PS_ERR_ALIGNMENT; workspace missing, misaligned or too small -> PS_ERR_WORKSPACE;
+ * a failed launch -> PS_ERR_CUDA.  Two launches on `stream` (a pre-pass, then one
+ * grid of dK/dV and dQ CTAs using 230,656 bytes of shared memory and all 512 TMEM
+ * columns per CTA); asynchronous, no synchronisation.
  */
 ps_status_t ps_prefill_backward(const void* q, const void* k, const void* v, const void* out,
                                 const float* lse, const void* d_out, int32_t batch,
