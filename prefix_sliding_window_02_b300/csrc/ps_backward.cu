@@ -851,7 +851,7 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
   {
     const int64_t groups = ((int64_t)batch * seqlen + bwd::kPrepRows - 1) / bwd::kPrepRows;
     const int sms = device_sm_count();
-    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;
     const int64_t blocks = groups < cap ? groups : cap;
     if (launch_dependent(bwd::bwd_prep_kernel, dim3((unsigned)blocks), dim3(256), 0, s, g) !=
         cudaSuccess)

@@ -1031,7 +1031,7 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
     const int64_t extra = (int64_t)batch * (L.skv - seqlen) * n_kv_heads * 16;
     int64_t blocks = groups > (extra + 255) / 256 ? groups : (extra + 255) / 256;
     const int sms = device_sm_count();
-    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;  // 16 x 8 KB of smem per SM
     if (blocks > cap) blocks = cap;
     if (launch_dependent(rope_gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s, g) !=
         cudaSuccess)
