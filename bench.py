@@ -20,7 +20,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -258,7 +257,7 @@ def decode_leg(ps, torch, name, P, W, pos0, steps, warmup, seed, hbm_peak, pe_mo
     d = DEC
     cache, q, k, v, pos, L = decode_setup(ps, torch, seed, W, P, pos0, steps + warmup,
                                           pe_mode=pe_mode)
-    total_ms, kern_ms, out, lse = run_decode(ps, torch, cache, q, k, v, pos, steps, warmup)
+    total_ms, kern_ms, out, _ = run_decode(ps, torch, cache, q, k, v, pos, steps, warmup)
     assert cache.check_status() == 0 and torch.isfinite(out.float()).all()
     nseq = len(P)
     kv = float(np.sum(2 * d["hkv"] * L * d["D"] * 2))
@@ -534,7 +533,6 @@ def oracle_baseline(budget_s=20.0):
              d["theta"], d["seed"]) for s in range(d["nseq"])]
     ctx = mp.get_context("spawn")
     with ctx.Pool(cores) as pool:
-        t0 = time.perf_counter()
         times = pool.map(_oracle_worker, jobs[:cores])   # calibrate
         per_seq = statistics.median(times)
         n = int(max(cores, min(len(jobs) * 8, budget_s * cores / max(per_seq, 1e-3))))
@@ -589,7 +587,7 @@ def main():
         torch.cuda.set_device(0)
     import prefix_sliding_window_02_b300 as ps
 
-    hbm_peak, bf16_peak, bf16_sustained, peak_src = peaks()
+    hbm_peak, bf16_peak, _, peak_src = peaks()
     if args.only:
         return only_leg(ps, torch, args, bf16_peak)
     d = DEC
@@ -598,7 +596,7 @@ def main():
     n_steps = args.warmup + args.steps
     cache, q, k, v, pos, L = decode_setup(ps, torch, seed, d["W"], P, d["pos0"], n_steps)
     clocks = ClockSampler(local)
-    total_ms, kern_ms, out, lse = run_decode(ps, torch, cache, q, k, v, pos, args.steps, args.warmup, dist)
+    total_ms, kern_ms, out, _ = run_decode(ps, torch, cache, q, k, v, pos, args.steps, args.warmup, dist)
     assert cache.check_status() == 0
     assert torch.isfinite(out.float()).all()
     ms_step = total_ms / args.steps
