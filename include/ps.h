@@ -226,7 +226,9 @@ ps_status_t ps_prefill_workspace_size(int32_t batch, int32_t seqlen, int32_t n_q
  * "PrefixSliding如何丢掉中间Token？").
  *   q : device bf16 [batch, seqlen, n_q_heads, head_dim]; k, v : device bf16
  *       [batch, seqlen, n_kv_heads, head_dim]; raw, rotated here.
- *   q_start : device int32 [batch]: absolute position of the chunk's first token.
+ *   q_start : device int32 [batch]: absolute position of the chunk's first token;
+ *       0 <= q_start and q_start + seqlen <= 2^31 - 1 (a negative value sets
+ *       PS_DEV_BAD_POS; that row's outputs are then undefined).
  *   prefix_len : device int32 [batch]: P of each row.
  *   ring == NULL: the keys are the chunk's own tokens.
  *   ring != NULL: the keys are the ring's live entries of sequence ring_seq[b]
@@ -263,7 +265,8 @@ ps_status_t ps_prefill_backward_workspace_size(int32_t batch, int32_t seqlen, in
  * scaling", agihunt.info, paragraph on RL, back-propagates through the last
  * 4W tokens under the same mask).
  *   q, k, v, q_start, prefix_len, window, heads, scale, rope_theta: as given
- *     to ps_prefill; out (bf16 [batch, seqlen, n_q_heads, head_dim]) and lse
+ *     to ps_prefill (without a ring; q_start within [0, 2^31 - 1 - seqlen], not
+ *     checked here); out (bf16 [batch, seqlen, n_q_heads, head_dim]) and lse
  *     (fp32 [batch, n_q_heads, seqlen]) are its results; d_out: bf16 like out.
  *   dq : device fp32 [batch, seqlen, n_q_heads, head_dim], gradient of raw q;
  *   dk, dv : device fp32 [batch, seqlen, n_kv_heads, head_dim] (summed over the
