@@ -37,6 +37,18 @@ def _need(t: torch.Tensor, dtype, name: str):
                          f"{t.dtype} on {t.device} (contiguous={t.is_contiguous()})")
 
 
+def _shape(t: torch.Tensor, shape, name: str):
+    """The library trusts the sizes it is given: check every tensor against the
+    shape the call implies before any pointer reaches it."""
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _dims(t: torch.Tensor, n: int, name: str, what: str):
+    if t.dim() != n:
+        raise ValueError(f"{name}: expected {what}, got shape {tuple(t.shape)}")
+
+
 class RingCache:
     """Bounded per-sequence K/V cache of ``prefix_max + window`` slots.
 
@@ -107,6 +119,13 @@ class RingCache:
                k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
         """ps_kv_append: runs r = tokens [cu[r], cu[r+1]) of sequence seq_idx[r]
         at positions pos0[r], pos0[r] + 1, ...  k, v: [n_tokens, Hkv, D] bf16, raw."""
+        _dims(k, 3, "k", "[n_tokens, Hkv, D]")
+        _dims(seq_idx, 1, "seq_idx", "[n_runs]")
+        n_tok, n_runs = k.shape[0], seq_idx.shape[0]
+        _shape(k, (n_tok, self.n_kv_heads, self.head_dim), "k")
+        _shape(v, (n_tok, self.n_kv_heads, self.head_dim), "v")
+        _shape(pos0, (n_runs,), "pos0")
+        _shape(cu_tokens, (n_runs + 1,), "cu_tokens")
         for t, n in ((seq_idx, "seq_idx"), (pos0, "pos0"), (cu_tokens, "cu_tokens")):
             _need(t, torch.int32, n)
         _need(k, BF16, "k")
@@ -118,6 +137,8 @@ class RingCache:
     def append_tokens(self, pos: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None,
                       _cu: dict = {}) -> None:
         """One token per sequence (the decode step): k, v [nseq, Hkv, D], pos [nseq]."""
+        _shape(pos, (self.nseq,), "pos")
+        _shape(k, (self.nseq, self.n_kv_heads, self.head_dim), "k")
         key = (self.nseq, k.device)
         if key not in _cu:
             _cu[key] = (torch.arange(self.nseq, dtype=torch.int32, device=k.device),
@@ -126,6 +147,12 @@ class RingCache:
         self.append(seq, pos, cu, k, v, stream)
 
     # ------------------------------------------------------------ decode ----
+    def _check_q(self, q: torch.Tensor, pos: torch.Tensor) -> int:
+        _dims(q, 3, "q", "[nseq, Hq, D]")
+        _shape(q, (self.nseq, q.shape[1], self.head_dim), "q")
+        _shape(pos, (self.nseq,), "pos")
+        return q.shape[1]
+
     def workspace(self, n_q_heads: int) -> torch.Tensor:
         need = decode_workspace_size(self.nseq, n_q_heads, self.n_kv_heads, self.head_dim)
         if self._ws is None or self._ws.numel() < need:
@@ -136,9 +163,13 @@ class RingCache:
                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                workspace: Optional[torch.Tensor] = None, stream=None):
         """ps_decode: q [nseq, Hq, D] bf16 raw; pos [nseq] int32.  Returns (out, lse)."""
+        hq = self._check_q(q, pos)
+        if out is not None:
+            _shape(out, q.shape, "out")
+        if lse is not None:
+            _shape(lse, (self.nseq, hq), "lse")
         _need(q, BF16, "q")
         _need(pos, torch.int32, "pos")
-        hq = q.shape[1]
         if scale is None:
             scale = 1.0 / math.sqrt(self.head_dim)
         if out is None:
@@ -153,9 +184,9 @@ class RingCache:
     def decode_partial(self, q: torch.Tensor, pos: torch.Tensor, scale: Optional[float] = None,
                        workspace: Optional[torch.Tensor] = None, stream=None) -> None:
         """ps_decode_partial: the K/V-streaming launch of ps_decode."""
+        hq = self._check_q(q, pos)
         _need(q, BF16, "q")
         _need(pos, torch.int32, "pos")
-        hq = q.shape[1]
         if scale is None:
             scale = 1.0 / math.sqrt(self.head_dim)
         ws = self.workspace(hq) if workspace is None else workspace
@@ -166,6 +197,9 @@ class RingCache:
     def decode_combine(self, out: torch.Tensor, lse: torch.Tensor,
                        workspace: Optional[torch.Tensor] = None, stream=None) -> None:
         """ps_decode_combine: merges the partial records into out [nseq,Hq,D] and lse [nseq,Hq]."""
+        _dims(out, 3, "out", "[nseq, Hq, D]")
+        _shape(out, (self.nseq, out.shape[1], self.head_dim), "out")
+        _shape(lse, (self.nseq, out.shape[1]), "lse")
         _need(out, BF16, "out")
         _need(lse, torch.float32, "lse")
         hq = out.shape[1]
@@ -203,6 +237,18 @@ def prefill_workspace_size(batch: int, seqlen: int, n_q_heads: int, n_kv_heads: 
     return b.value
 
 
+def _check_prefill_shapes(q, k, v, q_start, prefix_len):
+    _dims(q, 4, "q", "[B, S, Hq, D]")
+    _dims(k, 4, "k", "[B, S, Hkv, D]")
+    B, S, hq, D = q.shape
+    hkv = k.shape[2]
+    _shape(k, (B, S, hkv, D), "k")
+    _shape(v, (B, S, hkv, D), "v")
+    _shape(q_start, (B,), "q_start")
+    _shape(prefix_len, (B,), "prefix_len")
+    return B, S, hq, D, hkv
+
+
 def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_start: torch.Tensor,
             prefix_len: torch.Tensor, window: int, scale: Optional[float] = None,
             rope_theta: float = 10000.0, ring: Optional[RingCache] = None,
@@ -210,12 +256,17 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_start: torch.Te
             lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
             status: Optional[torch.Tensor] = None, stream=None):
     """ps_prefill: q [B,S,Hq,D], k, v [B,S,Hkv,D] bf16 raw.  Returns (out, lse [B,Hq,S])."""
+    B, S, hq, D, hkv = _check_prefill_shapes(q, k, v, q_start, prefix_len)
+    if out is not None:
+        _shape(out, q.shape, "out")
+    if lse is not None:
+        _shape(lse, (B, hq, S), "lse")
+    if ring_seq is not None:
+        _shape(ring_seq, (B,), "ring_seq")
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, BF16, n)
     _need(q_start, torch.int32, "q_start")
     _need(prefix_len, torch.int32, "prefix_len")
-    B, S, hq, D = q.shape
-    hkv = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -240,13 +291,15 @@ def prefill_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: tor
                      rope_theta: float = 10000.0, status: Optional[torch.Tensor] = None,
                      stream=None):
     """ps_prefill_backward: returns fp32 (dq [B,S,Hq,D], dk, dv [B,S,Hkv,D])."""
+    B, S, hq, D, hkv = _check_prefill_shapes(q, k, v, q_start, prefix_len)
+    _shape(out, q.shape, "out")
+    _shape(d_out, q.shape, "d_out")
+    _shape(lse, (B, hq, S), "lse")
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (d_out, "d_out")):
         _need(t, BF16, n)
     _need(lse, torch.float32, "lse")
     _need(q_start, torch.int32, "q_start")
     _need(prefix_len, torch.int32, "prefix_len")
-    B, S, hq, D = q.shape
-    hkv = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
