@@ -54,16 +54,48 @@ def live_runs(p, P, W):
 
 
 # ---- clocks ---------------------------------------------------------------
+CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+                "clocks.mem")
+THROTTLE_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def summarize_clocks(lines):
+    """Summary of nvidia-smi samples (CLOCK_FIELDS, csv, no header, no units):
+    median SM and memory clocks over the samples drawing at least half the
+    peak power (the loaded ones), the highest SM clock limit, and every throttle
+    reason seen active under load."""
+    rows = []
+    for line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:8],
+                         float(parts[8])))
+        except ValueError:
+            continue
+    if not rows:
+        return None
+    pmax = max(r[2] for r in rows)
+    load = [r for r in rows if r[2] >= 0.5 * pmax] or rows
+    reasons = sorted({THROTTLE_NAMES[i] for r in load for i, v in enumerate(r[3][1:5])
+                      if "Active" in v and "Not" not in v})
+    return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in rows),
+            "mem_mhz": statistics.median(r[4] for r in load), "reasons": reasons,
+            "samples": len(rows), "samples_under_load": len(load), "power_w_max": pmax}
+
+
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples the GPU's clocks, power and throttle reasons every 100 ms while
+    the benchmark runs (nvidia-smi in the background)."""
 
     def __init__(self, index: int):
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.p = subprocess.Popen(
-                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={CLOCK_FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
@@ -79,26 +111,9 @@ class ClockSampler:
         except Exception:
             self.p.kill()
         self.f.flush()
-        rows = []
-        for line in open(self.f.name):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
-            except ValueError:
-                continue
+        lines = open(self.f.name).read().splitlines()
         os.unlink(self.f.name)
-        if not rows:
-            return None
-        pmax = max(r[2] for r in rows)
-        load = [r for r in rows if r[2] >= 0.5 * pmax] or rows
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in load for i, v in enumerate(r[3][1:5]) if "Active" in v
-                          and "Not" not in v})
-        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows), "samples_under_load": len(load),
-                "power_w_max": pmax}
+        return summarize_clocks(lines)
 
 
 # ---- helpers --------------------------------------------------------------

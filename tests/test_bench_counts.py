@@ -36,3 +36,14 @@ def test_backward_products_cover_every_reached_tile(S, P, W):
     # and it visits nothing beyond the forward's tile ranges: at most the causal triangle
     nq = -(-S // 128)
     assert issued <= 7 * tile * nq * (nq + 1) // 2
+
+
+def test_clock_summary_reads_loaded_samples_and_reasons():
+    idle = "345, 2032, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active, 3996"
+    busy = "2032, 2032, 900.0, 0x4, Not Active, Not Active, Not Active, Active, 3996"
+    slow = "1500, 2032, 880.0, 0x8, Active, Not Active, Not Active, Not Active, 3996"
+    r = bench.summarize_clocks([idle, busy, busy, slow, "garbage", ""])
+    assert r["samples"] == 4 and r["samples_under_load"] == 3
+    assert r["sm_mhz"] == 2032 and r["sm_max_mhz"] == 2032 and r["mem_mhz"] == 3996
+    assert r["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert bench.summarize_clocks(["x"]) is None
