@@ -310,8 +310,7 @@ def test_tile_classes_causal_closed_form():
 
 def test_tile_classes_golden_counts():
     """Regression values for the two prefill workloads, written by
-    tests/golden/make_golden.py (oracle only) and also derived independently
-    when the hot-path scope was surveyed."""
+    tests/golden/make_golden.py from the oracle only."""
     g = json.load(open(os.path.join(GOLDEN, "tile_counts.json")))
     for case in g["cases"]:
         pos = np.arange(case["S"])
