@@ -26,8 +26,9 @@ something other than itself):
                     renumbered position; equals attend while nothing has been
                     evicted; window-only keys (P = 0) are a uniform shift
   attend_backward   torch autograd of scaled_dot_product_attention in float64
-                    (explicit mask, GQA by repeat); central finite differences
-                    of the forward through RoPE; its forward equals attend
+                    (explicit mask, GQA by repeat), also for chunks at offset
+                    positions; central finite differences of the forward through
+                    RoPE; its forward equals attend
 """
 from .prefix_sliding import (  # noqa: F401
     FULL, PARTIAL, SKIP, RingSim, allowed, attend, attend_backward, attend_reset_pe, masked_attention,

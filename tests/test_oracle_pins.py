@@ -450,6 +450,40 @@ def test_backward_matches_torch_autograd_of_sdpa(monkeypatch, S, P, W):
     assert np.allclose(dv, tv.grad.numpy(), atol=1e-10)
 
 
+@pytest.mark.parametrize("S,c0,P,W", [(20, 5, 12, 6), (18, 37, 10, 5), (16, 3, 0, 4)])
+def test_backward_at_offset_positions_matches_torch_autograd(monkeypatch, S, c0, P, W):
+    """A chunk at positions c0 .. c0 + S - 1 with no earlier keys: rotations and
+    the mask use absolute positions (prefix keys only where c0 + j < P)."""
+    monkeypatch.setattr(_ops, "round_bf16", lambda x: np.asarray(x, dtype=np.float64))
+    hq, hkv, d, theta = 2, 1, 8, 100.0
+    q, k, v, do = _bwd_inputs(S + 3 * c0, S, hq, hkv, d)
+    positions = c0 + np.arange(S)
+    dq, dk, dv, o, _ = _ops.attend_backward(q, k, v, do, P, W, theta, positions=positions)
+    pos = torch.tensor(positions, dtype=torch.float64)
+    inv = theta ** (-2.0 * torch.arange(d // 2, dtype=torch.float64) / d)
+    ang = pos[:, None] * inv[None, :]
+    c, s_ = torch.cos(ang)[:, None, :], torch.sin(ang)[:, None, :]
+
+    def rot(x):
+        x1, x2 = x[..., : d // 2], x[..., d // 2:]
+        return torch.cat([x1 * c - x2 * s_, x2 * c + x1 * s_], dim=-1)
+
+    tq = torch.tensor(q, requires_grad=True)
+    tk = torch.tensor(k, requires_grad=True)
+    tv = torch.tensor(v, requires_grad=True)
+    qh = rot(tq).permute(1, 0, 2)
+    kh = rot(tk).permute(1, 0, 2).repeat_interleave(hq // hkv, 0)
+    vh = tv.permute(1, 0, 2).repeat_interleave(hq // hkv, 0)
+    jj, pp = torch.meshgrid(pos, pos, indexing="xy")
+    mask = (jj <= pp) & ((jj < P) | (jj > pp - W))
+    out = torch.nn.functional.scaled_dot_product_attention(qh, kh, vh, attn_mask=mask)
+    out.backward(torch.tensor(do).permute(1, 0, 2))
+    assert np.allclose(o, out.detach().permute(1, 0, 2).numpy(), atol=1e-12)
+    assert np.allclose(dq, tq.grad.numpy(), atol=1e-10)
+    assert np.allclose(dk, tk.grad.numpy(), atol=1e-10)
+    assert np.allclose(dv, tv.grad.numpy(), atol=1e-10)
+
+
 def test_backward_matches_finite_differences(monkeypatch):
     """Rounding off: d(sum(dO * O))/dq, dk, dv by central differences."""
     monkeypatch.setattr(_ops, "round_bf16", lambda x: np.asarray(x, dtype=np.float64))
