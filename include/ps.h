@@ -18,8 +18,10 @@
  *     (e.g. torch tensors).  The library never allocates, frees or keeps them.
  *   - "bf16" is IEEE bfloat16 (__nv_bfloat16), stored row-major as documented.
  *   - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL is
- *     the legacy default stream) and never synchronises.  The library is
- *     stateless and thread-safe.
+ *     the legacy default stream) and never synchronises.  The library keeps no
+ *     state between calls and is thread-safe, with one exception:
+ *     ps_decode_noalloc uses a scratch array inside the library that all its
+ *     calls share (see its comment).
  *   - Host-side checks run before any launch and return a ps_status_t.
  *     Checks that need device data (per-sequence prefix lengths, positions,
  *     pool bases) run inside the kernels: a failing sequence is skipped and
@@ -163,7 +165,7 @@ ps_status_t ps_decode_workspace_size(int32_t nseq, int32_t n_q_heads, int32_t n_
  *         [0, min(pos[s]+1, P_s+W)).
  *   out : device bf16 [nseq, n_q_heads, head_dim]; lse : device fp32 [nseq, n_q_heads].
  *   workspace : device, >= ps_decode_workspace_size bytes, 256-byte aligned.
- * Work is split evenly over all SMs in 32-slot tiles regardless of per-sequence
+ * Work is split evenly over all SMs in 16-slot tiles regardless of per-sequence
  * length (no host synchronisation), then a second kernel merges the partial
  * softmax results by their log-sum-exp.  n_q_heads / n_kv_heads in {1,2,4,8}.
  */
@@ -198,10 +200,13 @@ ps_status_t ps_decode_combine(const ps_cache_desc* cache, int32_t n_q_heads, voi
  *   these shapes exceeds 4 MiB; 4 MiB holds, on a 148-SM B300, 256 sequences
  *   at Hkv = 8, head_dim 128 and two query heads per KV head.
  *   The first call on each device looks up the array's device address with
- *   that device current; make that first call before any stream capture.
- *   All calls share the one array and nothing in it needs to start at zero;
- *   calls whose kernels overlap on the GPU (several streams, or threads on
- *   one device) race on it, so serialise them.
+ *   that device current (and again if the device's context has been
+ *   destroyed and re-created since); make that first call before any stream
+ *   capture.  All calls share the one array and nothing in it needs to start
+ *   at zero: every call rewrites the per-sequence tile counts, segment
+ *   bounds and partial records it later reads.  Calls whose kernels overlap
+ *   on the GPU (several streams, or threads on one device) race on the
+ *   array, so serialise them.
  */
 ps_status_t ps_decode_noalloc(const ps_cache_desc* cache, const void* q, const int32_t* pos,
                               int32_t n_q_heads, float scale, void* out, float* lse,
@@ -310,6 +315,14 @@ ps_status_t ps_prefill_tile_grid(int32_t seqlen, int32_t q_start, int32_t prefix
 ps_status_t ps_prefill_tile_classes(int32_t seqlen, int32_t q_start, int32_t prefix_len,
                                     int32_t window, int32_t with_ring, int32_t bm, int32_t bn,
                                     uint8_t* out, void* stream);
+
+/*
+ * ps_device_code_version: the compute capability the library's kernels were
+ * compiled for, as the CUDA runtime reports it for a loaded kernel on the
+ * current device (major * 10 + minor: 103 for sm_103a).  Needs a device;
+ * PS_ERR_CUDA if none can be used, PS_ERR_INVALID_ARGUMENT for a null pointer.
+ */
+ps_status_t ps_device_code_version(int32_t* version);
 
 /*
  * ps_check_device_status: synchronously copy the device status word to

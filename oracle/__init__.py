@@ -29,8 +29,12 @@ something other than itself):
                     (explicit mask, GQA by repeat), also for chunks at offset
                     positions; central finite differences of the forward through
                     RoPE; its forward equals attend
+  attend_backward_at
+                    torch autograd of scaled_dot_product_attention (selected
+                    rows of dq, dk, dv), at position 0 and at an offset
 """
 from .prefix_sliding import (  # noqa: F401
-    FULL, PARTIAL, SKIP, RingSim, allowed, attend, attend_backward, attend_reset_pe, masked_attention,
+    FULL, PARTIAL, SKIP, RingSim, allowed, attend, attend_backward, attend_backward_at,
+    attend_reset_pe, masked_attention,
     reset_positions, ring_slot, rope, round_bf16, tile_classes, visible_positions,
 )

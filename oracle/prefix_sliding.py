@@ -249,6 +249,66 @@ def attend_backward(q_raw, k_raw, v, d_out, P: int, W: int, theta: float,
     return dq_raw, dk_raw, dv, out, lse
 
 
+def attend_backward_at(q_raw, k_raw, v, d_out, P: int, W: int, theta: float, q_rows, k_rows,
+                       scale: float | None = None, positions=None, rows_per_pass: int = 64):
+    """Selected rows of the gradients ``attend_backward`` returns, for sequences
+    too long to form all of them: dq at the query rows ``q_rows`` and dk, dv at
+    the key rows ``k_rows``.
+
+    Same forward, rounding contract and backward formulas as
+    ``attend_backward``.  A query row's dq needs only that row's softmax; a
+    key's dk and dv need every query row that admits the key.  So the function
+    visits the rows of ``q_rows`` and every row that admits one of ``k_rows``.
+    For each visited row i and query head h it forms the scores against every
+    key of the sequence, sets the ones the mask refuses to -inf (weight 0), and
+    takes P, dP, D_i and dS as ``attend_backward`` does.  Rows are independent;
+    ``rows_per_pass`` of them go through each matrix product together.
+    Returns dq [len(q_rows), Hq, D], dk and dv [len(k_rows), Hkv, D].
+    """
+    q_raw = np.asarray(q_raw, dtype=np.float64)
+    k_raw = np.asarray(k_raw, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    d_out = np.asarray(d_out, dtype=np.float64)
+    S, hq, d = q_raw.shape
+    hkv = k_raw.shape[1]
+    group = hq // hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pos = np.arange(S) if positions is None else np.asarray(positions)
+    q_rows = np.asarray(q_rows, dtype=np.int64)
+    k_rows = np.asarray(k_rows, dtype=np.int64)
+    q_hat = round_bf16(rope(q_raw, pos, theta))
+    k_hat = round_bf16(rope(k_raw, pos, theta))
+    dq_hat = np.zeros((len(q_rows), hq, d))
+    dk_hat = np.zeros((len(k_rows), hkv, d))
+    dv = np.zeros((len(k_rows), hkv, d))
+    need = set(q_rows.tolist())
+    for j in k_rows:
+        need.update(np.nonzero(allowed(pos, pos[j], P, W))[0].tolist())
+    need = np.array(sorted(need), dtype=np.int64)
+    for a in range(0, len(need), rows_per_pass):
+        rows = need[a:a + rows_per_pass]
+        keep = allowed(pos[rows][:, None], pos[None, :], P, W)         # [R, S]
+        for kv in range(hkv):
+            for h in range(kv * group, (kv + 1) * group):
+                s = (q_hat[rows, h, :] @ k_hat[:, kv, :].T) * scale     # [R, S]
+                s = np.where(keep, s, -np.inf)
+                m = s.max(axis=1, keepdims=True)
+                lse = m + np.log(np.exp(s - m).sum(axis=1, keepdims=True))
+                pr = np.exp(s - lse)
+                dp = d_out[rows, h, :] @ v[:, kv, :].T
+                ds = pr * (dp - (pr * dp).sum(axis=1, keepdims=True))
+                for r, i in enumerate(rows):
+                    for n in np.nonzero(q_rows == i)[0]:
+                        dq_hat[n, h] = scale * (ds[r] @ k_hat[:, kv, :])
+                for n, j in enumerate(k_rows):
+                    dk_hat[n, kv] += scale * (ds[:, j] @ q_hat[rows, h, :])
+                    dv[n, kv] += pr[:, j] @ d_out[rows, h, :]
+    dq = rope(dq_hat, -pos[q_rows], theta)
+    dk = rope(dk_hat, -pos[k_rows], theta)
+    return dq, dk, dv
+
+
 # --------------------------------------------------------------------------
 # the bounded cache ([EXP] "伪代码" invariant: size prefix_len + W)
 # --------------------------------------------------------------------------

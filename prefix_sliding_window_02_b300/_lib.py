@@ -26,7 +26,7 @@ EXPORTS = (
     "ps_decode", "ps_decode_partial", "ps_decode_combine", "ps_decode_noalloc",
     "ps_prefill_workspace_size", "ps_prefill", "ps_prefill_tile_grid", "ps_prefill_tile_classes",
     "ps_prefill_backward_workspace_size", "ps_prefill_backward",
-    "ps_check_device_status",
+    "ps_check_device_status", "ps_device_code_version",
 )
 
 
@@ -76,6 +76,7 @@ def _load():
                                                 ctypes.POINTER(i32), ctypes.POINTER(i32)]),
         "ps_prefill_tile_classes": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, i32, vp, vp]),
         "ps_check_device_status": (ctypes.c_int, [vp, ctypes.POINTER(i32)]),
+        "ps_device_code_version": (ctypes.c_int, [ctypes.POINTER(i32)]),
         "ps_prefill_backward_workspace_size": (ctypes.c_int, [i32, i32, i32, i32, i32,
                                                               ctypes.POINTER(sz)]),
         "ps_prefill_backward": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32,

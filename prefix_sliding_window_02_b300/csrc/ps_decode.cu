@@ -416,8 +416,9 @@ struct CombineParams {
 };
 
 // One warp per (sequence, query head): merge the partial softmax records of the
-// warps that covered its segment, first to last as the partial kernel
-// recorded them, in one pass with a running maximum (all loads independent).
+// warps that covered its segment, first to last, in one pass with a running
+// maximum.  The cost is one record per warp that touched the segment, never a
+// scan over the warps that did not.
 template <int D, int G>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ CombineParams p) {
   using S = DecShape<D, G>;
@@ -438,15 +439,10 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
     return;
   }
   const int64_t sg = (int64_t)s * p.hkv + h;
-  const int w0 = p.seg_warps[2 * sg], w1 = p.seg_warps[2 * sg + 1];
   const int64_t N = (int64_t)p.seg_tiles[p.nseq] * p.hkv;
   const int64_t NW = p.nwarps_total;
-  // with fewer tiles than warps, warps between w0 and w1 may own no tile and
-  // wrote no record; otherwise every warp owns at least one
-  const bool dense = N >= NW;
   float M = -INFINITY, l = 0.f, a[EPL] = {};
-  for (int w = w0; w <= w1; ++w) {
-    if (!dense && N * w / NW == N * (w + 1) / NW) continue;
+  auto merge = [&](int w) {
     const float* r = p.rec + (size_t)(w + sg) * S::REC;
     const float mw = r[G * D + gg], lw = r[G * D + G + gg];
     float aw[EPL];
@@ -458,6 +454,24 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
 #pragma unroll
     for (int e = 0; e < EPL; ++e) a[e] = a[e] * f_old + aw[e] * f_new;
     M = mn;
+  };
+  if (N >= NW) {
+    // every warp owns at least one tile: the segment's records are those of
+    // its first through last warp
+    const int w0 = p.seg_warps[2 * sg], w1 = p.seg_warps[2 * sg + 1];
+    for (int w = w0; w <= w1; ++w) merge(w);
+  } else {
+    // fewer tiles than warps: each warp owns at most one tile, so the records
+    // are one per tile.  Warp w owns tiles [floor(N w / NW), floor(N (w+1) / NW)),
+    // so tile g belongs to w(g) = floor(((g + 1) NW - 1) / N); the lanes find the
+    // owners of 32 tiles at a time.
+    const int64_t g0 = (int64_t)p.seg_tiles[s] * p.hkv + (int64_t)h * nt;
+    for (int t0 = 0; t0 < nt; t0 += 32) {
+      int wl = 0;
+      if (t0 + lane < nt) wl = (int)(((g0 + t0 + lane + 1) * NW - 1) / N);
+      const int cnt = min(32, nt - t0);
+      for (int i = 0; i < cnt; ++i) merge(__shfl_sync(0xffffffffu, wl, i));
+    }
   }
   const float inv = 1.f / l;
 #pragma unroll

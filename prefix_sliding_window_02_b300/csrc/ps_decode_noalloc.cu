@@ -11,6 +11,8 @@
 // until the process exits.
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "ps_internal.h"
 
 namespace {
@@ -22,19 +24,42 @@ __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+std::once_flag g_ctx_once;
 
 // Device address of g_decode_scratch on the current device.  In host code the
 // array's name stands for a host-side shadow, not for device memory, so the
-// address must come from the runtime, once per device, with that device current.
+// address must come from the runtime with the device current.  It is looked
+// up once per device and cached together with the device's current context:
+// if that context is destroyed and re-created (cudaDeviceReset, or the
+// primary context released and retained again), the module is loaded anew,
+// the array may sit elsewhere, and the address is looked up again.
 ps_status_t scratch_for_current_device(void** out) {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  });
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PS_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return PS_ERR_UNSUPPORTED;
+  if (!g_ctx_current) return PS_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return PS_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!ctx || !g_scratch_ptr[dev] || g_scratch_ctx[dev] != ctx) {
+    // first use on this device, or its context changed: the lookup also makes
+    // the runtime's context current when none was
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return PS_ERR_CUDA;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return PS_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
   return PS_OK;

@@ -198,3 +198,14 @@ extern "C" ps_status_t ps_kv_append(const ps_cache_desc* cache, const int32_t* s
     return PS_ERR_CUDA;
   return launch_status();
 }
+
+extern "C" ps_status_t ps_device_code_version(int32_t* version) {
+  if (!version) return PS_ERR_INVALID_ARGUMENT;
+  cudaFuncAttributes a;
+  if (cudaFuncGetAttributes(&a, ring_slots_kernel) != cudaSuccess) {
+    cudaGetLastError();
+    return PS_ERR_CUDA;
+  }
+  *version = a.binaryVersion;
+  return PS_OK;
+}

@@ -6,26 +6,47 @@ import torch
 
 import synth
 
-# Tolerances for bf16 inputs with fp32 accumulation, read as an absolute plus a
-# relative term per element (the numpy/torch allclose convention):
-#     |O_gpu - O_ref| <= O_ABS + O_REL * |O_ref|   and   |LSE_gpu - LSE_ref| <= LSE_ABS.
-# O is returned in bf16, whose rounding alone is half an ulp of the value
-# (0.0156 for |O| in [4, 8)), so a purely absolute 1e-2 bound cannot hold for
-# large outputs of any bf16-output kernel; the relative term covers that.
+# Tolerances (bf16 inputs, fp32 accumulation), as the target states them:
+#     max |O_gpu - O_ref| <= 1e-2 absolute,
+#     max |O_gpu - O_ref| / max |O_ref| <= 2e-2 relative,
+#     |LSE_gpu - LSE_ref| <= 1e-3.
+# Both O bounds are applied to the maximum error, per query head.  The relative
+# one is checked per query row (max over the row's D elements), which is
+# stronger than checking it once over a whole output tensor.
+# One allowance, derived from the output format: O is returned in bf16, so even
+# an exact kernel is off by up to half a bf16 spacing of the value, 2^(e-9) for
+# |O| in [2^(e-1), 2^e): 0.0156 for |O| in [4, 8).  An element may therefore
+# miss by half a spacing of |O_ref| + 1e-2 (the value may round in the binade
+# above) plus 1e-3 of arithmetic error.  Below |O_ref| ~ 3.99 that sum is under
+# 1e-2, so the allowance only ever applies to elements with |O_ref| >= 3.99.
 O_ABS = 1e-2
 O_REL = 2e-2
 LSE_ABS = 1e-3
+BF16_ARITH_SLACK = 1e-3
 
 
-def lse_tol(qscale_log2: int = 0) -> float:
-    """LSE bound for queries scaled by 2**qscale_log2 (stress cases only).
+def half_ulp_bf16(x) -> np.ndarray:
+    """Half the spacing of bf16 values at magnitude |x| (bf16 keeps 8 significant bits)."""
+    _, e = np.frexp(np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126))
+    return np.ldexp(1.0, e - 9)
 
-    Both sides round the rotated query to bf16; the kernel rotates in fp32 and
-    the oracle in fp64, so an element lying almost exactly between two bf16
+
+def o_abs_bound(o_ref) -> np.ndarray:
+    """Per-element absolute bound on |O_gpu - O_ref|: 1e-2, or the bf16 allowance above."""
+    return np.maximum(O_ABS, half_ulp_bf16(np.abs(o_ref) + O_ABS) + BF16_ARITH_SLACK)
+
+
+def lse_tol_stress(qscale_log2: int) -> float:
+    """LSE bound for the stress cases whose queries are scaled by 2**qscale_log2.
+
+    This is a separate reading, used only where q is scaled up on purpose (to
+    sharpen the softmax); unscaled inputs keep 1e-3.  Both sides round the
+    rotated query to bf16, the kernel after an fp32 rotation and the oracle
+    after an fp64 one, so an element lying almost exactly between two bf16
     values can round to different neighbours (about one element in 10^4).  One
-    such flip moves a score by one bf16 ulp of q_i times |k_i| / sqrt(D), and
-    the LSE of a row dominated by that key by the same amount; scaling q by 2^s
-    scales the ulp, hence the bound, by 2^s.  Unscaled inputs keep 1e-3.
+    such flip moves a score by one bf16 spacing of q_i times |k_i| / sqrt(D),
+    and the LSE of a row dominated by that key by as much; scaling q by 2^s
+    scales the spacing, hence the bound, by 2^s.
     """
     return LSE_ABS * 2.0 ** qscale_log2
 
@@ -96,12 +117,15 @@ def random_source(seed, hkv, d, device="cuda"):
 
 
 def assert_attention_close(o_gpu, lse_gpu, o_ref, lse_ref, what="", lse_abs=LSE_ABS):
-    """o_*: [H, D]; lse_*: [H].  Checks each head against the stated tolerances."""
+    """o_*: [H, D]; lse_*: [H].  Checks each query head of one row against the bounds above."""
     for h in range(o_ref.shape[0]):
         err = np.abs(o_gpu[h] - o_ref[h])
-        bound = O_ABS + O_REL * np.abs(o_ref[h])
+        bound = o_abs_bound(o_ref[h])
         i = int(np.argmax(err - bound))
-        dl = float(abs(lse_gpu[h] - lse_ref[h]))
         assert err[i] <= bound[i], (f"{what} head {h}: |dO| = {err[i]:.3e} at element {i} "
                                     f"(|O_ref| = {abs(o_ref[h][i]):.3e}, bound {bound[i]:.3e})")
+        omax = float(np.abs(o_ref[h]).max())
+        assert err.max() <= O_REL * omax, (f"{what} head {h}: max|dO| = {err.max():.3e} is more "
+                                           f"than {O_REL} of max|O_ref| = {omax:.3e}")
+        dl = float(abs(lse_gpu[h] - lse_ref[h]))
         assert dl <= lse_abs, f"{what} head {h}: |dLSE| = {dl:.3e}"

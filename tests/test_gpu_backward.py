@@ -100,3 +100,43 @@ def test_backward_chunk_offset(ps, B, S, hq, hkv, P, W, c0):
         _close(dq[b].double().cpu().numpy(), rq, f"dq b={b}")
         _close(dk[b].double().cpu().numpy(), rk, f"dk b={b}")
         _close(dv[b].double().cpu().numpy(), rv, f"dv b={b}")
+
+
+def test_training_backward_full_size_sampled():
+    """The 8 x 8,192 training backward (P = 256, W = 2,048, 16/8 heads) in the launch
+    configuration the benchmark times.  Batch row 0: dq at the mask's edges and
+    dk, dv of prefix keys, band keys and the last key (these need every query row
+    that sees them).  Batch row 7: dq rows only.  The oracle's selected-row
+    gradients use the same formulas as its whole-sequence ones."""
+    import prefix_sliding_window_02_b300 as ps
+    from oracle import attend_backward_at
+    seed, B, S, hq, hkv, D, P, W, theta = 42, 8, 8192, 16, 8, 128, 256, 2048, 10000.0
+    pos = np.arange(S)
+    q = np.stack([synth.query_bits(seed, b, pos, hq, D) for b in range(B)])
+    kv = [synth.History(seed, b, hkv, D).rows_bits(pos) for b in range(B)]
+    k = np.stack([x[0] for x in kv])
+    v = np.stack([x[1] for x in kv])
+    do = np.stack([synth.normal_bf16(seed, STREAM_DO, b, pos, hq, D) for b in range(B)])
+    i32 = dict(dtype=torch.int32, device="cuda")
+    tq, tk, tv, tdo = (bits_to_bf16_tensor(x) for x in (q, k, v, do))
+    qs = torch.zeros(B, **i32)
+    pl = torch.full((B,), P, **i32)
+    status = torch.zeros(1, **i32)
+    out, lse = ps.prefill(tq, tk, tv, qs, pl, W, rope_theta=theta, status=status)
+    dq, dk, dv = ps.prefill_backward(tq, tk, tv, out, lse, tdo, qs, pl, W, rope_theta=theta,
+                                     status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert all(torch.isfinite(g).all() for g in (dq, dk, dv))
+    rng = np.random.default_rng(7)
+    q_rows = sorted(set([0, 1, 127, 128, 255, 256, 2047, 2048, 2303, 2304, 4095, 8191]
+                        + rng.integers(0, S, 6).tolist()))
+    samples = {0: (q_rows, [0, 131, 255, 256, 2047, 2048, 5000, 8190, 8191]), 7: (q_rows, [])}
+    for b, (qr, kr) in samples.items():
+        rq, rk, rv = attend_backward_at(synth.bits_to_f64(q[b]), synth.bits_to_f64(k[b]),
+                                        synth.bits_to_f64(v[b]), synth.bits_to_f64(do[b]), P, W,
+                                        theta, qr, kr)
+        _close(dq[b, qr].double().cpu().numpy(), rq, f"dq b={b}")
+        if kr:
+            _close(dk[b, kr].double().cpu().numpy(), rk, f"dk b={b}")
+            _close(dv[b, kr].double().cpu().numpy(), rv, f"dv b={b}")

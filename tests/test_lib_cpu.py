@@ -31,10 +31,30 @@ def test_library_exports_every_declared_symbol(ps):
     assert set(syms) <= set(ps._lib.EXPORTS) | set()
 
 
-def test_library_is_built_for_sm_103a(ps):
-    # the fatbin section names the target architecture (text scan of the ELF)
-    blob = open(ps._lib.LIB_PATH, "rb").read()
-    assert b"sm_103a" in blob
+def test_build_targets_sm_103a_only():
+    """The build compiles every kernel for sm_103a and nothing else (the GPU test
+    asks the runtime which code it loaded)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_ps_build", os.path.join(ROOT, "prefix_sliding_window_02_b300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    assert mod.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_code_version_query_needs_a_device(ps):
+    v = ctypes.c_int32(0)
+    assert ps.lib.ps_device_code_version(None) == 1
+    import torch
+    if not torch.cuda.is_available():
+        assert ps.lib.ps_device_code_version(ctypes.byref(v)) == 5  # PS_ERR_CUDA
+
+
+@pytest.mark.gpu
+def test_loaded_kernels_are_sm_103(ps):
+    v = ctypes.c_int32(0)
+    assert ps.lib.ps_device_code_version(ctypes.byref(v)) == 0
+    assert v.value == 103
 
 
 def test_status_strings(ps):

@@ -517,3 +517,66 @@ def test_backward_forward_equals_attend():
     for p in range(S):
         o_ref, l_ref = attend(q[p], p, P, W, hist.rows, theta)
         assert np.allclose(o[p], o_ref, atol=1e-13) and np.allclose(lse[p], l_ref, atol=1e-13)
+
+
+def _autograd_grads(q, k, v, do, P, W, theta, positions):
+    """torch autograd of SDPA (float64) with the explicit mask, through the rotation."""
+    S, hq, d = q.shape
+    hkv = k.shape[1]
+    pos = torch.tensor(positions, dtype=torch.float64)
+    inv = theta ** (-2.0 * torch.arange(d // 2, dtype=torch.float64) / d)
+    ang = pos[:, None] * inv[None, :]
+    c, s_ = torch.cos(ang)[:, None, :], torch.sin(ang)[:, None, :]
+
+    def rot(x):
+        x1, x2 = x[..., : d // 2], x[..., d // 2:]
+        return torch.cat([x1 * c - x2 * s_, x2 * c + x1 * s_], dim=-1)
+
+    tq = torch.tensor(q, requires_grad=True)
+    tk = torch.tensor(k, requires_grad=True)
+    tv = torch.tensor(v, requires_grad=True)
+    qh = rot(tq).permute(1, 0, 2)
+    kh = rot(tk).permute(1, 0, 2).repeat_interleave(hq // hkv, 0)
+    vh = tv.permute(1, 0, 2).repeat_interleave(hq // hkv, 0)
+    jj, pp = torch.meshgrid(pos, pos, indexing="xy")
+    mask = (jj <= pp) & ((jj < P) | (jj > pp - W))
+    out = torch.nn.functional.scaled_dot_product_attention(qh, kh, vh, attn_mask=mask)
+    out.backward(torch.tensor(do).permute(1, 0, 2))
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+@pytest.mark.parametrize("S,c0,P,W,hq,hkv", [(40, 0, 6, 9, 4, 2), (33, 0, 0, 5, 2, 2),
+                                             (30, 17, 20, 6, 4, 1), (28, 0, 28, 4, 2, 1)])
+def test_backward_at_selected_rows_matches_torch_autograd(monkeypatch, S, c0, P, W, hq, hkv):
+    """Rounding off: dq at chosen query rows and dk, dv at chosen key rows (prefix
+    keys, keys at the prefix / window edge, the last key) equal the same rows of
+    torch autograd through SDPA with the explicit mask."""
+    monkeypatch.setattr(_ops, "round_bf16", lambda x: np.asarray(x, dtype=np.float64))
+    d, theta = 8, 100.0
+    q, k, v, do = _bwd_inputs(S * 5 + P + c0, S, hq, hkv, d)
+    positions = c0 + np.arange(S)
+    q_rows = [0, 1, P // 2, max(P - 1, 0), min(P, S - 1), S // 2, S - 1]
+    k_rows = [0, max(P - 1, 0), min(P, S - 1), S - W, S - 2, S - 1]
+    dq, dk, dv = _ops.attend_backward_at(q, k, v, do, P, W, theta, q_rows, k_rows,
+                                         positions=positions)
+    gq, gk, gv = _autograd_grads(q, k, v, do, P, W, theta, positions)
+    assert np.allclose(dq, gq[q_rows], atol=1e-10)
+    assert np.allclose(dk, gk[k_rows], atol=1e-10)
+    assert np.allclose(dv, gv[k_rows], atol=1e-10)
+
+
+def test_backward_at_rounds_like_backward():
+    """With the bf16 rounding contract on, the selected rows equal the same rows of
+    the whole-sequence gradients."""
+    seed, S, hq, hkv, d, P, W, theta = 27, 36, 4, 2, 16, 5, 11, 1e4
+    hist = synth.History(seed, 0, hkv, d)
+    pos = np.arange(S)
+    q = synth.bits_to_f64(synth.query_bits(seed, 0, pos, hq, d))
+    k, v = hist.rows(pos)
+    do = synth.bits_to_f64(synth.normal_bf16(seed, 5, 0, pos, hq, d))
+    full = attend_backward(q, k, v, do, P, W, theta)
+    rows = [0, 4, 5, 20, 35]
+    dq, dk, dv = _ops.attend_backward_at(q, k, v, do, P, W, theta, rows, rows)
+    assert np.allclose(dq, full[0][rows], atol=1e-12)
+    assert np.allclose(dk, full[1][rows], atol=1e-12)
+    assert np.allclose(dv, full[2][rows], atol=1e-12)

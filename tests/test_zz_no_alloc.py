@@ -66,6 +66,54 @@ def test_noalloc_decode_matches_workspace_decode_twice(ps):
                                    f"call {step + 1}, seq {s}")
 
 
+def test_noalloc_scratch_left_by_a_different_layout(ps):
+    """The scratch keeps whatever the previous call wrote.  A large call (many
+    sequences, one of them refused by the device checks so that it owns no
+    tiles) leaves its tile counts, segment bounds and records behind; the next,
+    small call (fewer tiles than warps, so each warp owns at most one tile) must
+    not read any of them.  Both calls are compared with ps_decode on a fresh
+    workspace and with the oracle."""
+    from oracle import attend
+    seed, hq, hkv, D, W, theta = 43, 16, 8, 128, 256, 10000.0
+    scale = 1.0 / np.sqrt(D)
+
+    def run(nseq, P, pos, bad=None):
+        cache = ps.RingCache(nseq, hkv, D, W, P, rope_theta=theta, prefix_max=max(P))
+        append_runs(cache, {s: live_runs(pos[s], P[s], W) for s in range(nseq)},
+                    synth_source(seed, hkv, D))
+        if bad is not None:
+            cache.prefix_len[bad] = 10 ** 6  # above prefix_max: sequence refused, no tiles
+        q = bits_to_bf16_tensor(np.concatenate(
+            [synth.query_bits(seed, s, pos[s], hq, D) for s in range(nseq)]))
+        tpos = torch.tensor(pos, dtype=torch.int32, device="cuda")
+        ws = torch.empty(ps.decode_workspace_size(nseq, hq, hkv, D), dtype=torch.uint8,
+                         device="cuda")
+        o_ws, l_ws = cache.decode(q, tpos, scale=scale, workspace=ws)
+        o_na, l_na = _noalloc(ps, cache, q, tpos, scale)
+        torch.cuda.synchronize()
+        flags = cache.check_status()
+        assert flags == (ps.PS_DEV_BAD_PREFIX if bad is not None else 0)
+        for s in range(nseq):
+            if s == bad:
+                assert torch.all(o_na[s].float() == 0) and torch.all(torch.isinf(l_na[s]))
+                continue
+            assert_attention_close(bf16_tensor_to_f64(o_na[s]), l_na[s].cpu().numpy(),
+                                   bf16_tensor_to_f64(o_ws[s]), l_ws[s].cpu().numpy().astype(np.float64),
+                                   f"nseq {nseq}, seq {s} vs ps_decode")
+            if s < 6:
+                qs = synth.bits_to_f64(synth.query_bits(seed, s, pos[s], hq, D))[0]
+                o_ref, l_ref = attend(qs, pos[s], P[s], W, synth.History(seed, s, hkv, D).rows, theta)
+                assert_attention_close(bf16_tensor_to_f64(o_na[s]), l_na[s].cpu().numpy(), o_ref,
+                                       l_ref, f"nseq {nseq}, seq {s} vs oracle")
+
+    rng = np.random.default_rng(4)
+    n_big = 96
+    P_big = rng.integers(0, 64, n_big).tolist()
+    pos_big = rng.integers(300, 5000, n_big).tolist()
+    run(n_big, P_big, pos_big, bad=5)                    # many tiles, one sequence without any
+    run(2, [3, 0], [20, 40])                             # 2 x 8 heads x 3 tiles: far fewer than warps
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch(ps):
     # 2,048 sequences x 8 KV heads need far more than the 4 MiB of fixed scratch;
     # the call must refuse before touching any pointer it was given.
