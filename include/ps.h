@@ -116,9 +116,10 @@ typedef struct ps_cache_desc {
  *     entry (L - 1, with L the keys it sees).  The pages do not give the rule;
  *     this is the plainest one.  Keys stay stored rotated at their absolute
  *     positions; window keys keep their distance to the query, so only the
- *     prefix keys see a different query rotation (at L - 1).  ps_decode
- *     honours it.  ps_kv_append stores keys the same way in both modes;
- *     ps_prefill computes Continue PE only.
+ *     prefix keys see a different query rotation: at L - 1 = min(p, P + W - 1).
+ *     ps_decode (from the cache's pe_mode) and ps_prefill (its pe_mode
+ *     argument) honour it; ps_kv_append stores keys the same way in both
+ *     modes; ps_prefill_backward differentiates Continue PE only.
  */
 #define PS_PE_CONTINUE 0
 #define PS_PE_RESET 1
@@ -213,13 +214,15 @@ ps_status_t ps_decode_noalloc(const ps_cache_desc* cache, const void* q, const i
                               void* stream);
 
 /*
- * ps_prefill_workspace_size: device workspace for ps_prefill (rotated Q and K
- * and, with a ring, the gathered cached keys and values).
+ * ps_prefill_workspace_size: device workspace for ps_prefill (rotated Q and K,
+ * with a ring the gathered cached keys and values, and under Reset PE the
+ * query rotated at its renumbered position).
  *   ring_rows_max : 0 without a ring, else the ring's prefix_max + window.
+ *   pe_mode : PS_PE_CONTINUE or PS_PE_RESET, as passed to ps_prefill.
  */
 ps_status_t ps_prefill_workspace_size(int32_t batch, int32_t seqlen, int32_t n_q_heads,
                                       int32_t n_kv_heads, int32_t head_dim,
-                                      int32_t ring_rows_max, size_t* bytes);
+                                      int32_t ring_rows_max, int32_t pe_mode, size_t* bytes);
 
 /*
  * ps_prefill: tiled forward of Prefix-Sliding attention for a chunk of
@@ -235,6 +238,9 @@ ps_status_t ps_prefill_workspace_size(int32_t batch, int32_t seqlen, int32_t n_q
  *       0 <= q_start and q_start + seqlen <= 2^31 - 1 (a negative value sets
  *       PS_DEV_BAD_POS; that row's outputs are then undefined).
  *   prefix_len : device int32 [batch]: P of each row.
+ *   pe_mode : PS_PE_CONTINUE, or PS_PE_RESET: prefix keys are scored with the
+ *       query rotated at min(p, P + W - 1) instead of p (see PS_PE_RESET); must
+ *       equal ring->pe_mode when a ring is given.
  *   ring == NULL: the keys are the chunk's own tokens.
  *   ring != NULL: the keys are the ring's live entries of sequence ring_seq[b]
  *       (positions < q_start[b], as left by ps_kv_append) followed by the
@@ -248,7 +254,7 @@ ps_status_t ps_prefill_workspace_size(int32_t batch, int32_t seqlen, int32_t n_q
 ps_status_t ps_prefill(const void* q, const void* k, const void* v, int32_t batch,
                        int32_t seqlen, const int32_t* q_start, const int32_t* prefix_len,
                        int32_t window, int32_t n_q_heads, int32_t n_kv_heads,
-                       int32_t head_dim, float scale, double rope_theta,
+                       int32_t head_dim, float scale, double rope_theta, int32_t pe_mode,
                        const ps_cache_desc* ring, const int32_t* ring_seq, void* out,
                        float* lse, void* workspace, size_t workspace_bytes,
                        int32_t* status, void* stream);
@@ -323,6 +329,20 @@ ps_status_t ps_prefill_tile_classes(int32_t seqlen, int32_t q_start, int32_t pre
  * PS_ERR_CUDA if none can be used, PS_ERR_INVALID_ARGUMENT for a null pointer.
  */
 ps_status_t ps_device_code_version(int32_t* version);
+
+/*
+ * ps_test_force_wait_timeout: test hook for the kernels' bounded waits.  Every
+ * wait of a kernel on a copy, a tensor-core product or another role gives up
+ * after a time limit (2 s), sets PS_DEV_TIMEOUT in the status word, lets the
+ * copies and products it has already issued finish (each wait for them again
+ * bounded) and returns, so the context stays usable.  With enable = 1, the
+ * decode partial kernel and the prefill tile kernels launched afterwards use
+ * wait_limit_ns (1e3 .. 2e9) as that limit, and CTA 0 of each skips its first
+ * K/V copy, so one wait is sure to run out: the call sets PS_DEV_TIMEOUT and
+ * its results are undefined.  enable = 0 restores the defaults.  Process-wide
+ * and not synchronised with calls in flight: for tests only.
+ */
+ps_status_t ps_test_force_wait_timeout(int32_t enable, int64_t wait_limit_ns);
 
 /*
  * ps_check_device_status: synchronously copy the device status word to

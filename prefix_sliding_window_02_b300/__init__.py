@@ -230,10 +230,11 @@ def decode_workspace_size(nseq: int, n_q_heads: int, n_kv_heads: int, head_dim: 
 
 
 def prefill_workspace_size(batch: int, seqlen: int, n_q_heads: int, n_kv_heads: int,
-                           head_dim: int, ring_rows_max: int = 0) -> int:
+                           head_dim: int, ring_rows_max: int = 0, pe_mode: int = 0) -> int:
     b = ctypes.c_size_t(0)
     check(lib.ps_prefill_workspace_size(batch, seqlen, n_q_heads, n_kv_heads, head_dim,
-                                        ring_rows_max, ctypes.byref(b)), "ps_prefill_workspace_size")
+                                        ring_rows_max, pe_mode, ctypes.byref(b)),
+          "ps_prefill_workspace_size")
     return b.value
 
 
@@ -254,8 +255,9 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_start: torch.Te
             rope_theta: float = 10000.0, ring: Optional[RingCache] = None,
             ring_seq: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-            status: Optional[torch.Tensor] = None, stream=None):
-    """ps_prefill: q [B,S,Hq,D], k, v [B,S,Hkv,D] bf16 raw.  Returns (out, lse [B,Hq,S])."""
+            status: Optional[torch.Tensor] = None, stream=None, pe_mode: Optional[int] = None):
+    """ps_prefill: q [B,S,Hq,D], k, v [B,S,Hkv,D] bf16 raw.  Returns (out, lse [B,Hq,S]).
+    ``pe_mode`` defaults to the ring's (PS_PE_CONTINUE without a ring)."""
     B, S, hq, D, hkv = _check_prefill_shapes(q, k, v, q_start, prefix_len)
     if out is not None:
         _shape(out, q.shape, "out")
@@ -274,12 +276,14 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_start: torch.Te
     if lse is None:
         lse = torch.empty(B, hq, S, dtype=torch.float32, device=q.device)
     ring_rows = 0 if ring is None else ring.prefix_max + ring.window
+    if pe_mode is None:
+        pe_mode = PS_PE_CONTINUE if ring is None else ring.pe_mode
     if workspace is None:
-        workspace = torch.empty(prefill_workspace_size(B, S, hq, hkv, D, ring_rows),
+        workspace = torch.empty(prefill_workspace_size(B, S, hq, hkv, D, ring_rows, pe_mode),
                                 dtype=torch.uint8, device=q.device)
     desc = None if ring is None else ctypes.byref(ring.desc)
     check(lib.ps_prefill(_vp(q), _vp(k), _vp(v), B, S, _vp(q_start), _vp(prefix_len), window, hq,
-                         hkv, D, ctypes.c_float(scale), ctypes.c_double(rope_theta), desc,
+                         hkv, D, ctypes.c_float(scale), ctypes.c_double(rope_theta), pe_mode, desc,
                          _vp(ring_seq), _vp(out), _vp(lse), _vp(workspace), workspace.numel(),
                          _vp(status), _stream(stream)), "ps_prefill")
     return out, lse

@@ -26,7 +26,7 @@ EXPORTS = (
     "ps_decode", "ps_decode_partial", "ps_decode_combine", "ps_decode_noalloc",
     "ps_prefill_workspace_size", "ps_prefill", "ps_prefill_tile_grid", "ps_prefill_tile_classes",
     "ps_prefill_backward_workspace_size", "ps_prefill_backward",
-    "ps_check_device_status", "ps_device_code_version",
+    "ps_check_device_status", "ps_device_code_version", "ps_test_force_wait_timeout",
 )
 
 
@@ -69,14 +69,16 @@ def _load():
         "ps_decode_partial": (ctypes.c_int, [pdesc, vp, vp, i32, f32, vp, sz, vp]),
         "ps_decode_combine": (ctypes.c_int, [pdesc, i32, vp, vp, vp, sz, vp]),
         "ps_decode_noalloc": (ctypes.c_int, [pdesc, vp, vp, i32, f32, vp, vp, vp]),
-        "ps_prefill_workspace_size": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]),
+        "ps_prefill_workspace_size": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, i32,
+                                                     ctypes.POINTER(sz)]),
         "ps_prefill": (ctypes.c_int, [vp, vp, vp, i32, i32, vp, vp, i32, i32, i32, i32, f32, f64,
-                                      pdesc, vp, vp, vp, vp, sz, vp, vp]),
+                                      i32, pdesc, vp, vp, vp, vp, sz, vp, vp]),
         "ps_prefill_tile_grid": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, i32,
                                                 ctypes.POINTER(i32), ctypes.POINTER(i32)]),
         "ps_prefill_tile_classes": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, i32, vp, vp]),
         "ps_check_device_status": (ctypes.c_int, [vp, ctypes.POINTER(i32)]),
         "ps_device_code_version": (ctypes.c_int, [ctypes.POINTER(i32)]),
+        "ps_test_force_wait_timeout": (ctypes.c_int, [i32, i64]),
         "ps_prefill_backward_workspace_size": (ctypes.c_int, [i32, i32, i32, i32, i32,
                                                               ctypes.POINTER(sz)]),
         "ps_prefill_backward": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32,

@@ -44,6 +44,8 @@ struct DecodeParams {
   int32_t nseq, hq, hkv, window, prefix_max;
   int32_t nwarps_total;
   float scale_log2;  // softmax scale * log2(e)
+  uint64_t wait_ns;  // bounded-wait limit
+  int32_t drop_first_load;  // test hook: warp 0 of CTA 0 skips its first tile copy
   RopeTurns turns;
 };
 
@@ -197,7 +199,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
   if (lane == 0) {
     nxt.init(pfx, p.nseq, p.hkv, lo);
     for (int k = 0; k < STAGES && nxt.g < hi; ++k) {
-      issue(k);
+      // test hook: no copy and no arrival, so the first wait is sure to run out
+      if (!(k == 0 && p.drop_first_load && blockIdx.x == 0 && warp == 0)) issue(k);
       nxt.next(pfx, p.nseq, p.hkv);
     }
   }
@@ -259,11 +262,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
       }
     }
 
-    if (!mbar_wait(&my_bars[st], (parity >> st) & 1u)) {
+    // the lanes decide together: shuffles and the drain below need the whole warp
+    if (!__all_sync(0xffffffffu, mbar_wait(&my_bars[st], (parity >> st) & 1u, p.wait_ns))) {
       ok = false;
       break;
     }
-    __syncwarp();
     parity ^= 1u << st;
     consumed = cur.g + 1;
 
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     const int64_t issued_end = min(hi, consumed + STAGES);
     for (int64_t g = consumed + 1; g < issued_end; ++g) {
       const int sg = (int)((g - lo) % STAGES);
-      if (!mbar_wait(&my_bars[sg], (parity >> sg) & 1u)) break;
+      if (!mbar_wait(&my_bars[sg], (parity >> sg) & 1u, p.wait_ns)) break;
       parity ^= 1u << sg;
     }
   }
@@ -628,6 +631,9 @@ extern "C" ps_status_t ps_decode_partial(const ps_cache_desc* cache, const void*
   p.prefix_max = cache->prefix_max;
   p.nwarps_total = pl.nwarps;
   p.scale_log2 = scale * 1.4426950408889634f;
+  const WaitHooks hooks = wait_hooks();
+  p.wait_ns = hooks.wait_ns;
+  p.drop_first_load = hooks.drop_first_load;
   make_rope_turns(cache->rope_theta, D, &p.turns);
   if (launch_dependent(pl.partial, dim3(pl.grid), dim3(kDecWarps * 32), pl.smem,
                        (cudaStream_t)stream, p) != cudaSuccess)

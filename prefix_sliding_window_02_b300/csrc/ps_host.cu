@@ -1,6 +1,7 @@
 // ps_host.cu -- status strings, RoPE turn table, tensor-map encoding, cache checks.
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -22,6 +23,21 @@ void make_rope_turns(double theta, int head_dim, RopeTurns* out) {
     turns = turns - floorl(turns);
     out->f[i] = (unsigned long long)ldexpl(turns, 64);
   }
+}
+
+static std::atomic<uint64_t> g_wait_ns{kWaitLimitNs};
+static std::atomic<int32_t> g_drop_first_load{0};
+
+WaitHooks wait_hooks() {
+  WaitHooks h;
+  h.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  h.drop_first_load = g_drop_first_load.load(std::memory_order_relaxed);
+  return h;
+}
+
+void set_wait_hooks(uint64_t wait_ns, int32_t drop_first_load) {
+  g_wait_ns.store(wait_ns, std::memory_order_relaxed);
+  g_drop_first_load.store(drop_first_load, std::memory_order_relaxed);
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -112,4 +128,12 @@ extern "C" ps_status_t ps_check_device_status(const int32_t* status, int32_t* ho
   if (cudaMemcpy(&v, status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return PS_ERR_CUDA;
   *host_flags = v;
   return v ? PS_ERR_DEVICE : PS_OK;
+}
+
+extern "C" ps_status_t ps_test_force_wait_timeout(int32_t enable, int64_t wait_limit_ns) {
+  if (enable != 0 && enable != 1) return PS_ERR_INVALID_ARGUMENT;
+  if (enable && (wait_limit_ns < 1000 || wait_limit_ns > (int64_t)ps::kWaitLimitNs))
+    return PS_ERR_INVALID_ARGUMENT;
+  ps::set_wait_hooks(enable ? (uint64_t)wait_limit_ns : ps::kWaitLimitNs, enable);
+  return PS_OK;
 }

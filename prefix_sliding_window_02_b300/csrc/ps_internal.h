@@ -20,6 +20,15 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
 
 int device_sm_count();  // SM count of the current device (0 on failure)
 
+// Settings of the wait-timeout test hook (ps_test_force_wait_timeout): the
+// bounded-wait limit the kernels get, and whether CTA 0 skips its first K/V copy.
+struct WaitHooks {
+  uint64_t wait_ns;
+  int32_t drop_first_load;
+};
+WaitHooks wait_hooks();
+void set_wait_hooks(uint64_t wait_ns, int32_t drop_first_load);
+
 // Launches `kernel` with programmatic stream serialisation: it may be scheduled
 // before the previous kernel in `stream` completes (see grid_dependency_wait).
 template <typename... Args>

@@ -47,6 +47,7 @@ struct GatherParams {
   const uint4* k;  // [B, S, Hkv, D]
   const uint4* v;
   uint4* qh;       // [B, S, Hq, D]       rotated
+  uint4* qr;       // [B, S, Hq, D]       rotated at the Reset PE position, or null
   uint4* kh;       // [B, Skv, Hkv, D]    rotated (ring part gathered)
   uint4* vg;       // [B, Skv, Hkv, D]    gathered values (ring only) or null
   const int32_t* q_start;
@@ -68,7 +69,9 @@ constexpr int kRopeBatch = 4; // items a thread loads before it rotates and stor
 
 // D = 128.  Phase A: groups of kRopeRows chunk rows; the 64 (cos, sin) pairs of
 // each row's position are computed once into shared memory and shared by all
-// Hq query heads and Hkv key heads of that row.  Each thread then loads
+// Hq query heads and Hkv key heads of that row.  Under Reset PE the query is
+// also rotated at min(p, P + W - 1), its position once the cache is renumbered
+// (prefix keys keep theirs), into qr.  Each thread then loads
 // kRopeBatch items (8 rotation pairs of one row and head each) before it
 // rotates and stores them, to keep enough loads in flight.  Phase B: the ring
 // rows (copied, already rotated) and the zero padding of each batch row's key
@@ -76,6 +79,7 @@ constexpr int kRopeBatch = 4; // items a thread loads before it rotates and stor
 __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant__ GatherParams p) {
   constexpr int VEC = 16, HALFV = 8;
   __shared__ float2 cs[kRopeRows][64];
+  __shared__ float2 csr[kRopeRows][64];  // Reset PE query angles
   grid_dependency_wait();  // inputs and workspace may be in use by earlier stream work
   allow_dependents();      // the tile kernel may set up meanwhile; it waits for this one
   const bool ring = p.k_pool != nullptr;
@@ -93,6 +97,11 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
         float c, sn;
         rope_cos_sin(pos, p.turns.f[i], c, sn);
         cs[rr][i] = make_float2(c, sn);
+        if (p.qr) {
+          const int64_t last = (int64_t)p.prefix_len[b] + p.W - 1;  // renumbered position cap
+          if ((int64_t)pos > last && last >= 0) rope_cos_sin((int32_t)last, p.turns.f[i], c, sn);
+          csr[rr][i] = make_float2(c, sn);
+        }
       }
     }
     __syncthreads();
@@ -100,10 +109,12 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
     for (int it0 = threadIdx.x; it0 < items; it0 += kRopeBatch * blockDim.x) {
       uint4 xa[kRopeBatch], xb[kRopeBatch];
       uint4* dst[kRopeBatch];
+      uint4* dstr[kRopeBatch];
       const float2* ang[kRopeBatch];
 #pragma unroll
       for (int u = 0; u < kRopeBatch; ++u) {
         dst[u] = nullptr;
+        dstr[u] = nullptr;
         const int it = it0 + u * blockDim.x;
         if (it >= items) continue;
         const int g = it & 7;
@@ -117,6 +128,7 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
           xa[u] = p.q[base];
           xb[u] = p.q[base + HALFV];
           dst[u] = p.qh + base;
+          if (p.qr) dstr[u] = p.qr + base;
         } else {
           const int h = hd - p.hq;
           const int b = (int)(r / p.S);
@@ -148,6 +160,12 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
         rotate8(xa[u], xb[u], ang[u], ra, rb);
         dst[u][0] = ra;
         dst[u][HALFV] = rb;
+        if (dstr[u]) {
+          const float2* angr = &csr[0][0] + (ang[u] - &cs[0][0]);
+          rotate8(xa[u], xb[u], angr, ra, rb);
+          dstr[u][0] = ra;
+          dstr[u][HALFV] = rb;
+        }
       }
     }
     __syncthreads();
@@ -209,6 +227,7 @@ constexpr int kSmemPrefill = kTile * 6 + 1024 /*barriers*/ + 1024 /*alignment*/;
 
 struct PrefillParams {
   CUtensorMap tmq;  // rotated Q  {D, Hq, S, B}
+  CUtensorMap tmqr; // Q rotated at the Reset PE position (same layout); unused otherwise
   CUtensorMap tmk;  // rotated K  {D, Hkv, Skv, B}
   CUtensorMap tmv;  // values     {D, Hkv, S or Skv, B}
   __nv_bfloat16* out;
@@ -217,8 +236,70 @@ struct PrefillParams {
   const int32_t* prefix_len;
   int32_t* status;
   int32_t S, hq, hkv, W, with_ring, nq, B;
+  int32_t reset;  // Reset PE: prefix keys are scored with the tmqr query
   float scale_log2;
+  uint64_t wait_ns;          // bounded-wait limit
+  int32_t drop_first_load;   // test hook: CTA 0 skips its first K/V copy
 };
+
+// The key tiles one 128-row query tile visits, in order: the tiles that hold
+// prefix keys, [0, t1_end), then the band of tiles that can hold window keys of
+// some row, [t2_begin, t2_end); tiles in neither hold no admitted pair.
+//
+// Reset PE (agihunt.info paragraph on position encodings; the renumbering is
+// the one ps_decode uses): the cache is renumbered for each query, prefix keys
+// keep their positions, the window keys follow them in order and the query at
+// absolute position p becomes the newest entry, min(p, P + W - 1).  Window keys
+// keep their distance to the query; prefix keys see the query rotated at
+// min(p, P + W - 1) instead of p, which differs only for rows p > P + W - 1.
+// For a tile with such rows the prefix tiles are visited with that second
+// query ("renumbered visits", [0, n0)); if one tile holds both the last prefix
+// key and later keys that some row admits, it is visited twice: first for its
+// prefix keys (renumbered query), then for its later keys (absolute query).
+enum : int { kVisitAll = 0, kVisitPrefixPart = 1, kVisitLaterPart = 2 };
+
+struct Visits {
+  int t1_end, t2_begin, n;  // n = visits
+  int n0;                   // visits [0, n0) use the renumbered query
+  int ts;                   // visit of the split tile's prefix part, or -1
+  int32_t kP;               // keys with position < P
+
+  __device__ __forceinline__ int tile(int j) const {
+    if (ts < 0) return j < t1_end ? j : t2_begin + (j - t1_end);
+    if (j <= ts) return j;
+    return j == ts + 1 ? ts : t2_begin + (j - t1_end - 1);
+  }
+  __device__ __forceinline__ int mode(int j) const {
+    if (ts < 0) return kVisitAll;
+    return j == ts ? kVisitPrefixPart : (j == ts + 1 ? kVisitLaterPart : kVisitAll);
+  }
+};
+
+__device__ __forceinline__ Visits make_visits(const KeyMap& km, int64_t q0, int64_t q1, int32_t P,
+                                              int32_t W, bool reset) {
+  Visits v;
+  const int32_t kc = keys_below(km, q1 + 1);  // keys at or before the last query
+  v.kP = keys_below(km, P);                   // prefix keys
+  v.t1_end = (min(v.kP, kc) + kBN - 1) / kBN;
+  const int32_t kw = keys_below(km, q0 - W + 1);
+  v.t2_begin = max(v.t1_end, kw / kBN);
+  const int t2_end = (kc + kBN - 1) / kBN;
+  v.n = v.t1_end + max(0, t2_end - v.t2_begin);
+  v.n0 = 0;
+  v.ts = -1;
+  if (reset && v.kP > 0 && q1 > (int64_t)P + W - 1) {
+    // here kc >= kP, so tiles [0, t1_end) hold exactly the prefix keys
+    v.n0 = v.t1_end;
+    if (v.kP % kBN) {
+      const int32_t ka = v.kP, kb = min(km.n_keys, v.t1_end * kBN) - 1;
+      if (kb >= ka && interval_any(q0, q1, key_pos(km, ka), key_pos(km, kb), P, W)) {
+        v.ts = v.t1_end - 1;
+        v.n += 1;
+      }
+    }
+  }
+  return v;
+}
 
 __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -245,14 +326,9 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
   const int64_t q0 = (int64_t)c0 + q0r, q1 = (int64_t)c0 + q1r;
 
   // key tiles that can hold an admitted pair: the prefix tiles, then the band
-  const int32_t kc = keys_below(km, q1 + 1);  // keys at or before the last query
-  const int32_t kP = keys_below(km, P);       // prefix keys
-  const int t1_end = (min(kP, kc) + kBN - 1) / kBN;
-  const int32_t kw = keys_below(km, q0 - p.W + 1);
-  const int t2_begin = max(t1_end, kw / kBN);
-  const int t2_end = (kc + kBN - 1) / kBN;
-  const int n_tiles = t1_end + max(0, t2_end - t2_begin);
-  auto tile_at = [&](int it) { return it < t1_end ? it : t2_begin + (it - t1_end); };
+  const Visits vs = make_visits(km, q0, q1, P, p.W, p.reset != 0);
+  const int n_tiles = vs.n;
+  auto tile_at = [&](int it) { return vs.tile(it); };
 
   if (warp == 0) {
     tc::alloc(smem_u32(tmem_slot), 256);
@@ -275,7 +351,12 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
 
   const uint64_t pol_q = policy_evict_first();
   const uint64_t pol_kv = policy_evict_last();
+  // test hook: CTA (0, 0, 0) skips its first K / V copy and arrival
+  const int dropped = p.drop_first_load && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0
+                          ? 0 : -1;
+  int load_no = 0;
   auto load_kv = [&](int stage, int kt) {
+    if (load_no++ == dropped) return;
     uint8_t* dk = sK0 + stage * kTile;
     uint8_t* dv = sV0 + stage * kTile;
     mbar_arrive_expect_tx(&kv_full[stage], 2 * kTile);
@@ -285,10 +366,15 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
     tma_load_4d(dv + kHalf, &p.tmv, &kv_full[stage], 64, hk, kt * kBN, b, pol_kv);
   };
   int issued = 0;  // key tiles whose loads were issued (thread 0)
-  if (tid == 0 && n_tiles > 0) {
+  int q_pending = -1;  // parity of a Q load issued but not yet waited for (thread 0)
+  auto load_q = [&](const CUtensorMap* m, int parity) {
     mbar_arrive_expect_tx(q_full, kTile);
-    tma_load_4d(sQ, &p.tmq, q_full, 0, h, q0r, b, pol_q);
-    tma_load_4d(sQ + kHalf, &p.tmq, q_full, 64, h, q0r, b, pol_q);
+    tma_load_4d(sQ, m, q_full, 0, h, q0r, b, pol_q);
+    tma_load_4d(sQ + kHalf, m, q_full, 64, h, q0r, b, pol_q);
+    q_pending = parity;
+  };
+  if (tid == 0 && n_tiles > 0) {
+    load_q(vs.n0 > 0 ? &p.tmqr : &p.tmq, 0);  // Reset PE: renumbered query first
     for (; issued < 2 && issued < n_tiles; ++issued) load_kv(issued, tile_at(issued));
   }
 
@@ -304,12 +390,19 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
     const int32_t ka = kt * kBN;
     const int32_t kb = min(km.n_keys, ka + kBN) - 1;
     const uint8_t cls = tile_class(km, c0, q0r, q1r, ka, kb, P, p.W);
-    const bool masked = cls != kFull || ka + kBN > km.n_keys;
+    const int mode = vs.mode(it);
+    const bool masked = cls != kFull || ka + kBN > km.n_keys || mode != kVisitAll;
 
     if (tid == 0) {
       bool w = true;
-      if (it == 0) w = mbar_wait(q_full, 0);
-      w = w && mbar_wait(&kv_full[st], (it >> 1) & 1);
+      // Reset PE: after the renumbered visits the query at its own position
+      // replaces the renumbered one (every Q K reading sQ has completed)
+      if (it > 0 && it == vs.n0) load_q(&p.tmq, 1);
+      if (it == 0 || it == vs.n0) {
+        w = mbar_wait(q_full, q_pending, p.wait_ns);
+        if (w) q_pending = -1;
+      }
+      w = w && mbar_wait(&kv_full[st], (it >> 1) & 1, p.wait_ns);
       if (w) {
         tc::fence_after();
         const uint32_t aq = smem_u32(sQ), ak = smem_u32(sK0 + st * kTile);
@@ -324,7 +417,7 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
       }
       tc::commit(smem_u32(s_done));  // arrives at once if nothing was issued
     }
-    if (!mbar_wait(s_done, it & 1)) ok = false;
+    if (!mbar_wait(s_done, it & 1, p.wait_ns)) ok = false;
     // tcgen05.ld / st are warp-collective (.sync.aligned): reconverge after the
     // per-thread spin above before touching tensor memory
     __syncwarp();
@@ -344,7 +437,9 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
 #pragma unroll
       for (int j = 0; j < kBN; ++j) {
         const int32_t kidx = ka + j;
-        const bool keep = kidx < km.n_keys && admitted(qpos, key_pos(km, kidx), P, p.W);
+        const bool keep = kidx < km.n_keys && admitted(qpos, key_pos(km, kidx), P, p.W) &&
+                          (mode != kVisitPrefixPart || kidx < vs.kP) &&
+                          (mode != kVisitLaterPart || kidx >= vs.kP);
         s[j] = keep ? s[j] : -INFINITY;
       }
     }
@@ -365,7 +460,7 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
 
     // ---- the previous P V must be done before P and O are touched
     if (it > 0) {
-      if (!mbar_wait(o_done, (it - 1) & 1)) ok = false;
+      if (!mbar_wait(o_done, (it - 1) & 1, p.wait_ns)) ok = false;
       tc::fence_after();
       if (tid == 0 && ok && issued < n_tiles) {  // its K/V stage is free: prefetch
         fence_proxy_async_smem();
@@ -429,7 +524,7 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
   }
 
   if (ok && n_tiles > 0) {
-    if (!mbar_wait(o_done, (n_tiles - 1) & 1)) ok = false;
+    if (!mbar_wait(o_done, (n_tiles - 1) & 1, p.wait_ns)) ok = false;
     tc::fence_after();
   }
   ok = __all_sync(0xffffffffu, ok);
@@ -460,8 +555,10 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
   if (!ok && tid == 0) {
     set_flag(p.status, PS_DEV_TIMEOUT);
     // let what was issued land before the CTA's shared memory goes away (bounded)
-    for (int t = it; t < issued; ++t) mbar_wait(&kv_full[t & 1], (t >> 1) & 1);
-    if (committed_pv > 0) mbar_wait(o_done, (committed_pv - 1) & 1);
+    for (int t = it; t < issued; ++t)
+      if (t != dropped) mbar_wait(&kv_full[t & 1], (t >> 1) & 1, p.wait_ns);
+    if (q_pending >= 0) mbar_wait(q_full, q_pending, p.wait_ns);
+    if (committed_pv > 0) mbar_wait(o_done, (committed_pv - 1) & 1, p.wait_ns);
   }
   tc::fence_before();
   __syncthreads();
@@ -505,23 +602,15 @@ struct Bars {
   uint64_t q_full, q_empty;
   uint64_t step_full[kSt], step_empty[kSt];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+  uint64_t drain;  // after an abort: the issuer's products have completed
   uint32_t tmem_slot;
   int32_t abort;
 };
 
 // Bounded wait that also gives up as soon as another role has given up.
-__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      return false;
-    }
-  }
+__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort,
+                                     uint64_t limit_ns) {
+  return mbar_wait_abort(bar, parity, abort, limit_ns);
 }
 
 // One work item and the key tiles it visits: the prefix tiles, then the band
@@ -531,10 +620,9 @@ struct Item {
   int32_t c0, P, q0r, q1r;
   int64_t q0, q1;
   KeyMap km;
-  int t1_end, t2_begin, n_tiles;
-  __device__ __forceinline__ int tile_at(int j) const {
-    return j < t1_end ? j : t2_begin + (j - t1_end);
-  }
+  Visits v;  // n_tiles = v.n visits
+  int n_tiles;
+  __device__ __forceinline__ int tile_at(int j) const { return v.tile(j); }
 };
 
 __device__ __forceinline__ Item make_item(const PrefillParams& p, int u) {
@@ -553,13 +641,8 @@ __device__ __forceinline__ Item make_item(const PrefillParams& p, int u) {
   it.q1r = min(p.S, it.q0r + kBM) - 1;
   it.q0 = (int64_t)it.c0 + it.q0r;
   it.q1 = (int64_t)it.c0 + it.q1r;
-  const int32_t kc = keys_below(it.km, it.q1 + 1);
-  const int32_t kP = keys_below(it.km, it.P);
-  it.t1_end = (min(kP, kc) + kBN - 1) / kBN;
-  const int32_t kw = keys_below(it.km, it.q0 - p.W + 1);
-  it.t2_begin = max(it.t1_end, kw / kBN);
-  const int t2_end = (kc + kBN - 1) / kBN;
-  it.n_tiles = it.t1_end + max(0, t2_end - it.t2_begin);
+  it.v = make_visits(it.km, it.q0, it.q1, it.P, p.W, p.reset != 0);
+  it.n_tiles = it.v.n;
   return it;
 }
 
@@ -675,6 +758,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       mbar_init(&bar->o_done[i], 1);
       mbar_init(&bar->o_free[i], 4);
     }
+    mbar_init(&bar->drain, 1);
     bar->abort = 0;
     fence_mbar_init();
   }
@@ -683,6 +767,12 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
   tc::fence_after();
   const uint32_t tmem = bar->tmem_slot;
   grid_dependency_wait();  // rotated Q / K come from the pre-pass
+  // What the producer has in flight, for the drain after an abort: the parity of
+  // its last Q load and the last step loaded into each stage (-1: none).
+  int last_q = -1;
+  int last_step[kSt];
+#pragma unroll
+  for (int s = 0; s < kSt; ++s) last_step[s] = -1;
 
   // Every role walks the same item sequence; items without tiles (only
   // possible for invalid inputs) are skipped by all of them alike.
@@ -695,26 +785,37 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       prefetch_tmap(&p.tmv);
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      int g = 0, k = 0;
+      int g = 0, k = 0, kq = 0;  // kq: Q loads so far (q_full / q_empty phases)
       bool ok = true;
+      auto load_q = [&](const Item& it, const CUtensorMap* m) -> bool {
+        // every Q K of the previous Q load has completed
+        if (!wait(&bar->q_empty, (kq & 1) ^ 1, abort, p.wait_ns)) return false;
+        mbar_arrive_expect_tx(&bar->q_full, 2 * kTile);
+        for (int i = 0; i < 2; ++i) {
+          tma_load_4d(sQ + i * kTile, m, &bar->q_full, 0, it.h0 + i, it.q0r, it.b, pol_q);
+          tma_load_4d(sQ + i * kTile + kHalf, m, &bar->q_full, 64, it.h0 + i, it.q0r, it.b, pol_q);
+        }
+        last_q = kq & 1;
+        ++kq;
+        return true;
+      };
       for (int u = blockIdx.x; ok && u < n_items; u += gridDim.x) {
         const Item it = make_item(p, u);
         if (it.n_tiles <= 0) continue;
-        if (!(ok = wait(&bar->q_empty, (k & 1) ^ 1, abort))) break;  // previous item's Q K done
-        mbar_arrive_expect_tx(&bar->q_full, 2 * kTile);
-        for (int i = 0; i < 2; ++i) {
-          tma_load_4d(sQ + i * kTile, &p.tmq, &bar->q_full, 0, it.h0 + i, it.q0r, it.b, pol_q);
-          tma_load_4d(sQ + i * kTile + kHalf, &p.tmq, &bar->q_full, 64, it.h0 + i, it.q0r, it.b,
-                      pol_q);
-        }
+        // Reset PE: the renumbered query serves the first n0 visits
+        if (!(ok = load_q(it, it.v.n0 > 0 ? &p.tmqr : &p.tmq))) break;
         // step j of the item (j = 0..n) brings K(j) (for Q K of tile j) and
         // V(j-1) (for P V of tile j-1), the operands the issuer uses in the
         // same step, under one barrier
         for (int j = 0; j <= it.n_tiles; ++j) {
           const int gs = g + k + j, st = gs % kSt;
-          if (!(ok = wait(&bar->step_empty[st], ((gs / kSt) & 1) ^ 1, abort))) break;
+          if (!(ok = wait(&bar->step_empty[st], ((gs / kSt) & 1) ^ 1, abort, p.wait_ns))) break;
+          // test hook: CTA 0 leaves its first step without copies or arrival, so
+          // the issuer's wait for it is sure to run out
+          if (p.drop_first_load && blockIdx.x == 0 && gs == 0) continue;
           uint64_t* full = &bar->step_full[st];
           mbar_arrive_expect_tx(full, (j < it.n_tiles ? kTile : 0) + (j > 0 ? kTile : 0));
+          last_step[st] = gs;
           if (j < it.n_tiles) {
             const int kt = it.tile_at(j);
             uint8_t* dk = sK + st * kTile;
@@ -727,6 +828,8 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             tma_load_4d(dv, &p.tmv, full, 0, it.hk, kt * kBN, it.b, pol_kv);
             tma_load_4d(dv + kHalf, &p.tmv, full, 64, it.hk, kt * kBN, it.b, pol_kv);
           }
+          // the query at its own position for the visits after the renumbered ones
+          if (j == it.v.n0 && j > 0 && j < it.n_tiles && !(ok = load_q(it, &p.tmq))) break;
         }
         g += it.n_tiles;
         ++k;
@@ -767,25 +870,31 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       // deep, so each step waits on one barrier for both operand tiles and
       // releases them with one commit.
       auto pv_step = [&](int i, int gt, int jt, int st, int k) -> bool {
-        if (!wait(&bar->p_full[i], gt & 1, abort)) return false;
-        if (jt == 0 && !wait(&bar->o_free[i], (k & 1) ^ 1, abort)) return false;
+        if (!wait(&bar->p_full[i], gt & 1, abort, p.wait_ns)) return false;
+        if (jt == 0 && !wait(&bar->o_free[i], (k & 1) ^ 1, abort, p.wait_ns)) return false;
         tc::fence_after();
         pv(i, st, jt > 0);
         return true;
       };
-      int g = 0, k = 0;
+      int g = 0, k = 0, kq = 0;  // kq: Q loads consumed
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_items; u += gridDim.x) {
         const Item it = make_item(p, u);
-        const int n = it.n_tiles;
+        const int n = it.n_tiles, n0 = it.v.n0;
         if (n <= 0) continue;
-        if (!(ok = wait(&bar->q_full, k & 1, abort))) break;
+        if (!(ok = wait(&bar->q_full, kq & 1, abort, p.wait_ns))) break;
+        ++kq;
         for (int j = 0; ok && j <= n; ++j) {
           const int gs = g + k + j, st = gs % kSt;  // step index: n + 1 steps per item
-          if (!(ok = wait(&bar->step_full[st], (gs / kSt) & 1, abort))) break;
+          if (!(ok = wait(&bar->step_full[st], (gs / kSt) & 1, abort, p.wait_ns))) break;
           for (int i = 0; i < 2 && ok; ++i) {
             if (j > 0 && !(ok = pv_step(i, g + j - 1, j - 1, st, k))) break;
             if (j < n) {
+              if (i == 0 && j == n0 && j > 0) {  // Reset PE: the second query has landed
+                if (!(ok = wait(&bar->q_full, kq & 1, abort, p.wait_ns))) break;
+                ++kq;
+                tc::fence_after();
+              }
               qk(i, st);
             } else {
               tc::commit(smem_u32(&bar->o_done[i]));
@@ -793,7 +902,8 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           }
           if (!ok) break;
           tc::commit(smem_u32(&bar->step_empty[st]));
-          if (j == n - 1) tc::commit(smem_u32(&bar->q_empty));  // every Q K of this item is issued
+          // every Q K reading the current Q is issued: it may be replaced
+          if (j == n - 1 || (j == n0 - 1 && n0 > 0)) tc::commit(smem_u32(&bar->q_empty));
         }
         g += n;
         ++k;
@@ -823,9 +933,15 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         const int kt = it.tile_at(j);
         const int32_t ka = kt * kBN;
         const int32_t kb = min(it.km.n_keys, ka + kBN) - 1;
+        const int mode = it.v.mode(j);
         const bool masked = tile_class(it.km, it.c0, it.q0r, it.q1r, ka, kb, it.P, p.W) != kFull ||
-                            ka + kBN > it.km.n_keys;
-        ok = wait(&bar->s_full[i], (g + j) & 1, abort);
+                            ka + kBN > it.km.n_keys || mode != kVisitAll;
+        // kept columns: c < A1 (prefix keys) or B0 <= c < B1 (window keys); a
+        // split tile's two visits keep only the keys before / after the prefix
+        const int32_t A1 = mode == kVisitLaterPart ? 0 : a1 - ka;
+        const int32_t B0 = mode == kVisitPrefixPart ? 0 : (mode == kVisitLaterPart ? max(b0, it.v.kP) : b0) - ka;
+        const int32_t B1 = mode == kVisitPrefixPart ? 0 : b1 - ka;
+        ok = wait(&bar->s_full[i], (g + j) & 1, abort, p.wait_ns);
         // tcgen05.ld / st are warp-collective (.sync.aligned): the warp decides
         // together and reconverges here after the per-thread spin
         if (!__all_sync(0xffffffffu, ok)) {
@@ -835,7 +951,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         tc::fence_after();
         float alpha;
         if (masked)
-          alpha = softmax_tile<true>(tS, j, p.scale_log2, a1 - ka, b0 - ka, b1 - ka, m_used, l);
+          alpha = softmax_tile<true>(tS, j, p.scale_log2, A1, B0, B1, m_used, l);
         else
           alpha = softmax_tile<false>(tS, j, p.scale_log2, 0, 0, 0, m_used, l);
         if (__any_sync(0xffffffffu, alpha != 1.f)) {  // alpha is 1 on the other rows
@@ -858,7 +974,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
-      ok = wait(&bar->o_done[i], k & 1, abort);
+      ok = wait(&bar->o_done[i], k & 1, abort, p.wait_ns);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -900,11 +1016,21 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
   tc::fence_before();
   __syncthreads();
   if (*abort) {
+    // A wait gave up.  Before shared and tensor memory are released, everything
+    // issued must have landed: the producer waits (bounded) for each copy it
+    // issued -- a completed phase answers at once, and no later phase of these
+    // barriers can complete now -- and the issuer commits once more and waits
+    // until all its products have completed.
     if (tid == 0) set_flag(p.status, PS_DEV_TIMEOUT);
-    // copies and products already issued finish on their own within microseconds;
-    // give them time before the CTA's shared and tensor memory are released
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 100000ull) {
+    if (warp == kProducerWarp && lane == 0) {
+      if (last_q >= 0) mbar_wait(&bar->q_full, (uint32_t)last_q, p.wait_ns);
+#pragma unroll
+      for (int s = 0; s < kSt; ++s)
+        if (last_step[s] >= 0)
+          mbar_wait(&bar->step_full[s], (uint32_t)((last_step[s] / kSt) & 1), p.wait_ns);
+    } else if (warp == kMmaWarp && lane == 0) {
+      tc::commit(smem_u32(&bar->drain));
+      mbar_wait(&bar->drain, 0, p.wait_ns);
     }
     __syncthreads();
   }
@@ -915,17 +1041,20 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct PrefillLayout {
-  size_t q_off, k_off, v_off, total;
+  size_t q_off, k_off, v_off, qr_off, total;
   int32_t skv;
 };
 
-static PrefillLayout prefill_layout(int B, int S, int hq, int hkv, int D, int ring_rows) {
+// [rotated Q][rotated K (ring rows, chunk)][gathered V, with a ring][Reset PE Q]
+static PrefillLayout prefill_layout(int B, int S, int hq, int hkv, int D, int ring_rows,
+                                    bool reset) {
   PrefillLayout L;
   L.skv = S + ring_rows;
   L.q_off = 0;
   L.k_off = align256((size_t)B * S * hq * D * 2);
   L.v_off = L.k_off + align256((size_t)B * L.skv * hkv * D * 2);
-  L.total = L.v_off + (ring_rows > 0 ? align256((size_t)B * L.skv * hkv * D * 2) : 0);
+  L.qr_off = L.v_off + (ring_rows > 0 ? align256((size_t)B * L.skv * hkv * D * 2) : 0);
+  L.total = L.qr_off + (reset ? align256((size_t)B * S * hq * D * 2) : 0);
   return L;
 }
 
@@ -966,12 +1095,15 @@ extern "C" ps_status_t ps_prefill_tile_classes(int32_t seqlen, int32_t q_start,
 
 extern "C" ps_status_t ps_prefill_workspace_size(int32_t batch, int32_t seqlen, int32_t n_q_heads,
                                                  int32_t n_kv_heads, int32_t head_dim,
-                                                 int32_t ring_rows_max, size_t* bytes) {
+                                                 int32_t ring_rows_max, int32_t pe_mode,
+                                                 size_t* bytes) {
   if (!bytes || batch < 1 || seqlen < 1 || n_q_heads < 1 || n_kv_heads < 1 || ring_rows_max < 0 ||
-      n_q_heads % n_kv_heads)
+      n_q_heads % n_kv_heads || (pe_mode != PS_PE_CONTINUE && pe_mode != PS_PE_RESET))
     return PS_ERR_INVALID_ARGUMENT;
   if (head_dim != 128) return PS_ERR_UNSUPPORTED;
-  *bytes = prefill_layout(batch, seqlen, n_q_heads, n_kv_heads, head_dim, ring_rows_max).total;
+  *bytes = prefill_layout(batch, seqlen, n_q_heads, n_kv_heads, head_dim, ring_rows_max,
+                          pe_mode == PS_PE_RESET)
+               .total;
   return PS_OK;
 }
 
@@ -979,13 +1111,16 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
                                   int32_t seqlen, const int32_t* q_start,
                                   const int32_t* prefix_len, int32_t window, int32_t n_q_heads,
                                   int32_t n_kv_heads, int32_t head_dim, float scale,
-                                  double rope_theta, const ps_cache_desc* ring,
+                                  double rope_theta, int32_t pe_mode, const ps_cache_desc* ring,
                                   const int32_t* ring_seq, void* out, float* lse, void* workspace,
                                   size_t workspace_bytes, int32_t* status, void* stream) {
   if (!q || !k || !v || !q_start || !prefix_len || !out || !lse) return PS_ERR_INVALID_ARGUMENT;
   if (batch < 1 || seqlen < 1 || window < 1 || n_q_heads < 1 || n_kv_heads < 1 ||
       n_q_heads % n_kv_heads || !(scale > 0.f) || !(rope_theta > 0.0))
     return PS_ERR_INVALID_ARGUMENT;
+  if (pe_mode != PS_PE_CONTINUE && pe_mode != PS_PE_RESET) return PS_ERR_INVALID_ARGUMENT;
+  if (ring && ring->pe_mode != pe_mode) return PS_ERR_INVALID_ARGUMENT;
+  const bool reset = pe_mode == PS_PE_RESET;
   if (head_dim != kHD) return PS_ERR_UNSUPPORTED;
   if (batch > 65535 || n_q_heads > 65535) return PS_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return PS_ERR_ALIGNMENT;
@@ -997,7 +1132,8 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
       return PS_ERR_INVALID_ARGUMENT;
     ring_rows = ring->prefix_max + ring->window;
   }
-  const PrefillLayout L = prefill_layout(batch, seqlen, n_q_heads, n_kv_heads, head_dim, ring_rows);
+  const PrefillLayout L =
+      prefill_layout(batch, seqlen, n_q_heads, n_kv_heads, head_dim, ring_rows, reset);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PS_ERR_WORKSPACE;
   if (workspace_bytes < L.total) return PS_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1008,6 +1144,7 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
   g.k = static_cast<const uint4*>(k);
   g.v = static_cast<const uint4*>(v);
   g.qh = reinterpret_cast<uint4*>(ws + L.q_off);
+  g.qr = reset ? reinterpret_cast<uint4*>(ws + L.qr_off) : nullptr;
   g.kh = reinterpret_cast<uint4*>(ws + L.k_off);
   g.vg = ring ? reinterpret_cast<uint4*>(ws + L.v_off) : nullptr;
   g.q_start = q_start;
@@ -1052,6 +1189,9 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
   const uint32_t box[4] = {64u, 1u, (uint32_t)kBM, 1u};
   bool okm = encode_tmap(&p.tmq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ws + L.q_off, qd, qs, box,
                          CU_TENSOR_MAP_SWIZZLE_128B) &&
+             encode_tmap(&p.tmqr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                         ws + (reset ? L.qr_off : L.q_off), qd, qs, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B) &&
              encode_tmap(&p.tmk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ws + L.k_off, kd, ks, box,
                          CU_TENSOR_MAP_SWIZZLE_128B);
   if (ring)
@@ -1071,6 +1211,10 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
   p.hkv = n_kv_heads;
   p.W = window;
   p.with_ring = ring ? 1 : 0;
+  p.reset = reset ? 1 : 0;
+  const WaitHooks hooks = wait_hooks();
+  p.wait_ns = hooks.wait_ns;
+  p.drop_first_load = hooks.drop_first_load;
   p.nq = (seqlen + kBM - 1) / kBM;
   p.B = batch;
   p.scale_log2 = scale * 1.4426950408889634f;

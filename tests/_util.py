@@ -36,6 +36,22 @@ def o_abs_bound(o_ref) -> np.ndarray:
     return np.maximum(O_ABS, half_ulp_bf16(np.abs(o_ref) + O_ABS) + BF16_ARITH_SLACK)
 
 
+def o_abs_bound_stress(o_ref, abs_weighted) -> np.ndarray:
+    """Per-element O bound for the stress cases whose queries are scaled up.
+
+    A separate reading, used only where q is scaled up on purpose: the
+    tensor-core kernels feed the probabilities to the P V product in bf16 (a
+    choice of the GPU path that the oracle does not model), which moves each
+    term p_j v_j by up to 2^-9 of itself.  On unscaled inputs these errors have
+    random signs over thousands of keys and vanish; when a sharp softmax puts
+    the weight on a few keys they add up to at most 2^-9 sum_j p_j |v_j| / l,
+    which ``abs_weighted`` gives (the oracle's attention over |v|).  The bound is
+    the strict one, or that amount plus the bf16 output allowance.
+    """
+    return np.maximum(o_abs_bound(o_ref), half_ulp_bf16(np.abs(o_ref) + O_ABS)
+                      + 2.0 ** -9 * np.abs(abs_weighted) + BF16_ARITH_SLACK)
+
+
 def lse_tol_stress(qscale_log2: int) -> float:
     """LSE bound for the stress cases whose queries are scaled by 2**qscale_log2.
 
@@ -116,11 +132,14 @@ def random_source(seed, hkv, d, device="cuda"):
     return src
 
 
-def assert_attention_close(o_gpu, lse_gpu, o_ref, lse_ref, what="", lse_abs=LSE_ABS):
-    """o_*: [H, D]; lse_*: [H].  Checks each query head of one row against the bounds above."""
+def assert_attention_close(o_gpu, lse_gpu, o_ref, lse_ref, what="", lse_abs=LSE_ABS,
+                           abs_weighted=None):
+    """o_*: [H, D]; lse_*: [H].  Checks each query head of one row against the bounds
+    above (``abs_weighted``: stress cases only, see ``o_abs_bound_stress``)."""
     for h in range(o_ref.shape[0]):
         err = np.abs(o_gpu[h] - o_ref[h])
-        bound = o_abs_bound(o_ref[h])
+        bound = o_abs_bound(o_ref[h]) if abs_weighted is None else \
+            o_abs_bound_stress(o_ref[h], abs_weighted[h])
         i = int(np.argmax(err - bound))
         assert err[i] <= bound[i], (f"{what} head {h}: |dO| = {err[i]:.3e} at element {i} "
                                     f"(|O_ref| = {abs(o_ref[h][i]):.3e}, bound {bound[i]:.3e})")

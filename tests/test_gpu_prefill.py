@@ -9,8 +9,8 @@ import pytest
 import torch
 
 import synth
-from oracle import (FULL, PARTIAL, SKIP, attend, masked_attention, rope, round_bf16, tile_classes,
-                    visible_positions)
+from oracle import (FULL, PARTIAL, SKIP, attend, attend_reset_pe, masked_attention, rope, round_bf16,
+                    tile_classes, visible_positions)
 
 from _util import (append_runs, assert_attention_close, bf16_tensor_to_f64, bits_to_bf16_tensor,
                    lse_tol_stress, synth_source)
@@ -67,28 +67,36 @@ def _inputs(seed, B, S, q_start, hq, hkv, D, qscale=0):
     return q, k, v
 
 
-def _run(ps, q, k, v, q_start, P, W, theta, ring=None):
+def _run(ps, q, k, v, q_start, P, W, theta, ring=None, pe_mode=None):
     i32 = dict(dtype=torch.int32, device="cuda")
     status = torch.zeros(1, **i32)
     out, lse = ps.prefill(bits_to_bf16_tensor(q), bits_to_bf16_tensor(k), bits_to_bf16_tensor(v),
                           torch.tensor(q_start, **i32), torch.tensor(P, **i32), W,
-                          rope_theta=theta, ring=ring, status=status)
+                          rope_theta=theta, ring=ring, status=status, pe_mode=pe_mode)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return out, lse
 
 
-def _check_rows(seed, out, lse, q, q_start, P, W, theta, rows_per_b, hkv, what="", qs=0):
+def _check_rows(seed, out, lse, q, q_start, P, W, theta, rows_per_b, hkv, what="", qs=0,
+                reference=attend):
     B = out.shape[0]
     D = out.shape[3]
     for b in range(B):
         hist = synth.History(seed, b, hkv, D)
         ob = out[b]
+        def abs_rows(js, hist=hist):
+            k_, v_ = hist.rows(js)
+            return k_, np.abs(v_)
         for r in rows_per_b[b]:
             p = q_start[b] + r
-            o_ref, l_ref = attend(synth.bits_to_f64(q[b, r]), p, P[b], W, hist.rows, theta)
+            qr = synth.bits_to_f64(q[b, r])
+            o_ref, l_ref = reference(qr, p, P[b], W, hist.rows, theta)
+            # stress cases (q scaled up): the bf16 P V allowance needs sum p|v| / l
+            aw = reference(qr, p, P[b], W, abs_rows, theta)[0] if qs else None
             assert_attention_close(bf16_tensor_to_f64(ob[r]), lse[b, :, r].cpu().numpy(), o_ref,
-                                   l_ref, f"{what} b={b} row={r}", lse_abs=lse_tol_stress(qs))
+                                   l_ref, f"{what} b={b} row={r}", lse_abs=lse_tol_stress(qs),
+                                   abs_weighted=aw)
 
 
 @pytest.mark.parametrize("B,S,hq,hkv,P,W,qs", [
@@ -212,3 +220,47 @@ def test_training_forward_sampled_rows(ps):
             for _ in range(B)]
     _check_rows(seed, out, lse, q, [0] * B, [P] * B, W, theta, rows, hkv, "train")
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+# ---------------------------------------------------------------- Reset PE --
+@pytest.mark.parametrize("B,S,hq,hkv,P,W", [
+    (2, 400, 4, 2, [37, 128], 64),     # split prefix tile (P % 128 != 0) and a tile-aligned prefix
+    (1, 300, 2, 2, [100], 100),        # one query head per KV head (the single-head kernel)
+    (1, 520, 4, 2, [200], 30),         # prefix spans two tiles, narrow window
+    (2, 260, 4, 2, [0, 300], 50),      # no prefix keys / everything inside the prefix
+])
+def test_prefill_reset_pe_all_rows(ps, B, S, hq, hkv, P, W):
+    """Reset PE: prefix keys see the query rotated at min(p, P + W - 1), window
+    keys at p; every row against the oracle's renumbered attention."""
+    seed, D, theta = 36, 128, 10000.0
+    q, k, v = _inputs(seed, B, S, [0] * B, hq, hkv, D)
+    out, lse = _run(ps, q, k, v, [0] * B, P, W, theta, pe_mode=ps.PS_PE_RESET)
+    _check_rows(seed, out, lse, q, [0] * B, P, W, theta, [range(S)] * B, hkv, "reset",
+                reference=attend_reset_pe)
+
+
+def test_prefill_reset_pe_several_items_per_cta(ps):
+    """Reset PE through the persistent kernel with several items per CTA (the
+    second query load per item): rows at the mask's edges and a random sample."""
+    seed, B, S, hq, hkv, D, P, W, theta = 37, 2, 4096, 16, 8, 128, [100, 256], 512, 10000.0
+    q, k, v = _inputs(seed, B, S, [0] * B, hq, hkv, D)
+    out, lse = _run(ps, q, k, v, [0] * B, P, W, theta, pe_mode=ps.PS_PE_RESET)
+    rng = np.random.default_rng(2)
+    rows = [sorted(set([0, 99, 100, 127, 128, 255, 256, 611, 612, 613, 767, 768, 4095]
+                       + rng.integers(0, S, 40).tolist())) for _ in range(B)]
+    _check_rows(seed, out, lse, q, [0] * B, P, W, theta, rows, hkv, "reset multi-item",
+                reference=attend_reset_pe)
+
+
+@pytest.mark.parametrize("c0,S,hq", [(300, 150, 4), (50, 150, 4), (84, 64, 2), (5000, 130, 4)])
+def test_prefill_extend_from_ring_reset_pe(ps, c0, S, hq):
+    """Chunked extend against a Reset PE ring: cached keys stay rotated at their
+    absolute positions; the chunk's queries are renumbered for the prefix keys."""
+    seed, B, hkv, D, P, W, theta = 38, 2, 2, 128, 20, 64, 10000.0
+    cache = ps.RingCache(B, hkv, D, W, [P] * B, rope_theta=theta, pe_mode=ps.PS_PE_RESET)
+    append_runs(cache, {b: [(0, c0)] for b in range(B)}, synth_source(seed, hkv, D))
+    q, k, v = _inputs(seed, B, S, [c0] * B, hq, hkv, D)
+    out, lse = _run(ps, q, k, v, [c0] * B, [P] * B, W, theta, ring=cache)
+    _check_rows(seed, out, lse, q, [c0] * B, [P] * B, W, theta, [range(S)] * B, hkv,
+                "reset extend", reference=attend_reset_pe)
+    assert cache.check_status() == 0

@@ -159,3 +159,30 @@ def test_backward_host_validation(ps):
     assert call(ws=None) == 4         # no workspace
     assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == 4  # workspace not 256-byte aligned
     assert call(ws_bytes=need - 1) == 4  # workspace too small
+
+
+def test_prefill_position_encoding_validation(ps):
+    """ps_prefill takes PS_PE_CONTINUE or PS_PE_RESET, and with a ring only the
+    ring's own mode; ps_prefill_workspace_size grows by one query array under
+    Reset PE.  All refused on the host, before any CUDA call."""
+    lib = ps.lib
+    b0, b1 = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.ps_prefill_workspace_size(2, 300, 4, 2, 128, 0, 0, ctypes.byref(b0)) == 0
+    assert lib.ps_prefill_workspace_size(2, 300, 4, 2, 128, 0, 1, ctypes.byref(b1)) == 0
+    assert b1.value - b0.value >= 2 * 300 * 4 * 128 * 2
+    assert lib.ps_prefill_workspace_size(2, 300, 4, 2, 128, 0, 2, ctypes.byref(b0)) == 1
+    fake = ctypes.c_void_p(1 << 20)
+    i32 = ctypes.c_void_p(1 << 21)
+
+    def call(pe_mode, ring=None):
+        return lib.ps_prefill(fake, fake, fake, 1, 300, i32, i32, 64, 4, 2, 128,
+                              ctypes.c_float(0.088), ctypes.c_double(1e4), pe_mode,
+                              ctypes.byref(ring) if ring is not None else None, None, fake,
+                              ctypes.c_void_p(1 << 22), None, 0, None, None)
+    assert call(2) == 1                                  # unknown position encoding
+    assert call(-1) == 1
+    ring = _bad_desc(ps, n_kv_heads=2, window=64, capacity=80, prefix_max=16)
+    assert call(1, ring) == 1                            # ring is Continue PE
+    ring.pe_mode = 1
+    assert call(0, ring) == 1                            # ring is Reset PE
+    assert call(1, ring) == 4                            # consistent: fails later, on the workspace
