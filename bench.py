@@ -302,18 +302,76 @@ def ragged_leg(ps, torch, steps, seed, hbm_peak):
     return rep
 
 
-def flatness_leg(ps, torch, steps, seed, hbm_peak):
+def step_times(ps, torch, cache, q, k, v, pos, steps, warmup):
+    """Per-step device times (ms) of `steps` decode steps (append + partial +
+    combine), each bracketed by events on the launching stream, after `warmup`."""
+    nseq, hq, D = q.shape[1], q.shape[2], q.shape[3]
+    out = torch.empty(nseq, hq, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(nseq, hq, dtype=torch.float32, device="cuda")
+    ws = cache.workspace(hq)
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        cache.append_tokens(pos[i], k[i], v[i])
+        cache.decode(q[i], pos[i], out=out, lse=lse, workspace=ws)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(steps):
+        cache.append_tokens(pos[warmup + i], k[warmup + i], v[warmup + i])
+        cache.decode(q[warmup + i], pos[warmup + i], out=out, lse=lse, workspace=ws)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    assert cache.check_status() == 0 and torch.isfinite(out.float()).all()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+
+
+def flatness_leg(ps, torch, seed, steps=200, rounds=2):
     """Steady-decode shapes at growing positions: cost must stop growing once
-    every sequence's window is full (p >= P + W - 1)."""
+    every sequence's window is full (p >= P + W - 1).  Each position is measured
+    `rounds` times in a shuffled order (a fresh cache each time), `steps` steps
+    each; per position the median and minimum step time over all its steps."""
     d = DEC
     P = decode_prefix_lens(seed, d["nseq"])
     W = d["W"]
+    labels = (("P+W/2", P + W // 2), ("P+W", P + W), ("2(P+W)", 2 * (P + W)),
+              ("32768", np.full(d["nseq"], 32768)), ("131072", np.full(d["nseq"], 131072)),
+              ("262143", np.full(d["nseq"], 262143 - steps - 8)))
+    order = [i for _ in range(rounds) for i in range(len(labels))]
+    np.random.default_rng(seed).shuffle(order)
+    times = {i: [] for i in range(len(labels))}
+    live = {}
+    for i in order:
+        label, pos0 = labels[i]
+        cache, q, k, v, pos, L = decode_setup(ps, torch, seed + 31 * i, W, P, pos0, steps + 5)
+        times[i].append(step_times(ps, torch, cache, q, k, v, pos, steps, 5))
+        live[i] = float(np.mean(L))
+        del cache, q, k, v, pos
+        torch.cuda.empty_cache()
     out = []
-    for label, pos0 in (("P+W/2", P + W // 2), ("P+W", P + W), ("2(P+W)", 2 * (P + W)),
-                        ("32768", 32768), ("131072", 131072), ("262143", 262143 - steps - 8)):
-        r = decode_leg(ps, torch, f"p = {label}", P, W, pos0, steps, 3, seed, hbm_peak)
-        out.append({"p": label, "live_slots_mean": r["live_slots_mean"], "step_ms": r["step_ms"],
-                    "partial_kernel_ms": r["partial_kernel_ms"], "tok_s_per_layer": r["tok_s_per_layer"]})
+    for i, (label, _) in enumerate(labels):
+        allt = [t for run in times[i] for t in run]
+        out.append({"p": label, "live_slots_mean": live[i], "step_ms_median": statistics.median(allt),
+                    "step_ms_min": min(allt),
+                    "step_ms_median_per_round": [statistics.median(r) for r in times[i]],
+                    "tok_s_per_layer": d["nseq"] / (statistics.median(allt) / 1e3)})
+    full = [o["step_ms_median"] for o in out if o["p"] != "P+W/2"]
+    return {"positions": out, "steps_per_round": steps, "rounds": rounds, "order": order,
+            "max_over_min_median_full_window": max(full) / min(full)}
+
+
+def small_batch_leg(ps, torch, seed, steps=200):
+    """Decode latency of one sequence (16 / 8 heads, D 128, P 100, W 4,096): the
+    step (append + partial + combine) at p = 1,000 (still causal) and p = P + W
+    (window full)."""
+    out = {}
+    P = np.array([100])
+    for label, p0 in (("p=1000", 1000), ("p=P+W", 100 + 4096)):
+        cache, q, k, v, pos, L = decode_setup(ps, torch, seed, 4096, P, p0, steps + 5)
+        t = step_times(ps, torch, cache, q, k, v, pos, steps, 5)
+        out[label] = {"step_us_median": 1e3 * statistics.median(t), "step_us_min": 1e3 * min(t),
+                      "live_slots": int(L[0])}
+        del cache, q, k, v, pos
+        torch.cuda.empty_cache()
     return out
 
 
@@ -380,7 +438,31 @@ def run_decode_e2e(ps, torch, cache, steps, warmup, seed):
     for i in range(steps):
         step(warmup + i)
     dt = time.perf_counter() - t0
-    return dt, g.inp.numel(), g.res.numel()
+
+    # where an end-to-end step goes: the same steps again, with events between
+    # the copy in, the replay and the copy out, and the host clock around each
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    host = []
+    for i in range(steps):
+        h0 = time.perf_counter()
+        e = ev[i]
+        e[0].record(stream)
+        g.inp.copy_(hin[warmup + i], non_blocking=True)
+        e[1].record(stream)
+        g.replay()
+        e[2].record(stream)
+        hres.copy_(g.res, non_blocking=True)
+        e[3].record(stream)
+        stream.synchronize()
+        host.append(1e3 * (time.perf_counter() - h0))
+    med = statistics.median
+    parts = {"h2d_ms": med(e[0].elapsed_time(e[1]) for e in ev),
+             "replay_ms": med(e[1].elapsed_time(e[2]) for e in ev),
+             "d2h_ms": med(e[2].elapsed_time(e[3]) for e in ev),
+             "device_ms": med(e[0].elapsed_time(e[3]) for e in ev),
+             "host_step_ms": med(host)}
+    parts["host_only_ms"] = parts["host_step_ms"] - parts["device_ms"]
+    return dt, g.inp.numel(), g.res.numel(), parts
 
 
 # ---- prefill --------------------------------------------------------------
@@ -654,9 +736,10 @@ def main():
     full = None
     pre = None
     if rank == 0 or world == 1:
-        dt, h2d, d2h = run_decode_e2e(ps, torch, cache, min(args.steps, 200), 5, seed + 7)
+        dt, h2d, d2h, parts = run_decode_e2e(ps, torch, cache, min(args.steps, 200), 5, seed + 7)
         e2e = {"value": d["nseq"] * min(args.steps, 200) / dt, "unit": "tok/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "breakdown_median": parts,
                "how": "per step: one pinned host -> device copy of the packed q, k, v, pos; "
                       "DecodeGraph replay (ps_kv_append + ps_decode captured in a CUDA graph); "
                       "one device -> host copy of the packed O and LSE; stream sync; host wall clock"}
@@ -665,10 +748,11 @@ def main():
 
     # the other decode legs run before the prefill legs, whose power draw can
     # leave the next few hundred milliseconds of decode slower
-    ragged = flat = comparators = None
+    ragged = flat = comparators = small = None
     if not args.no_extra and (rank == 0 or world == 1):
         ragged = ragged_leg(ps, torch, 100, 4, hbm_peak)
-        flat = flatness_leg(ps, torch, 20, seed, hbm_peak)
+        flat = flatness_leg(ps, torch, seed)
+        small = small_batch_leg(ps, torch, seed + 21)
         comparators = comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak)
 
     # prefill (one layer) and the truncated-backprop training forward
@@ -731,6 +815,7 @@ def main():
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "frac_of_8tbs": achieved / 8000.0},
         "prefill": pre, "train_forward": train, "ragged_decode": ragged, "flatness": flat,
+        "small_batch_decode": small,
         "comparators": comparators,
         "full_causal": full, "e2e": e2e,
         "gpu_launches": 3 * args.steps, "clocks": clk, "cpu_baseline": cpu,
