@@ -249,7 +249,7 @@ ps_status_t ps_prefill_workspace_size(int32_t batch, int32_t seqlen, int32_t n_q
  *   out : device bf16 [batch, seqlen, n_q_heads, head_dim];
  *   lse : device fp32 [batch, n_q_heads, seqlen] (natural log).
  *   status : device int32 word or NULL.
- * Uses tcgen05 tensor cores with TMEM accumulators.  head_dim 128 only.
+ * Uses tcgen05 tensor cores with TMEM accumulators.  head_dim 64 or 128.
  */
 ps_status_t ps_prefill(const void* q, const void* k, const void* v, int32_t batch,
                        int32_t seqlen, const int32_t* q_start, const int32_t* prefix_len,
@@ -264,7 +264,7 @@ ps_status_t ps_prefill(const void* q, const void* k, const void* v, int32_t batc
  * rotated Q and K (bf16), and per (batch row, query head, row rounded up to 128)
  * the pair {LSE * log2(e), D = rowsum(dO * O)} (fp32).  Errors: null `bytes`,
  * batch / seqlen / heads < 1 or Hq % Hkv != 0 -> PS_ERR_INVALID_ARGUMENT;
- * head_dim != 128 -> PS_ERR_UNSUPPORTED.
+ * head_dim not 64 or 128 -> PS_ERR_UNSUPPORTED.
  */
 ps_status_t ps_prefill_backward_workspace_size(int32_t batch, int32_t seqlen, int32_t n_q_heads,
                                                int32_t n_kv_heads, int32_t head_dim,
@@ -289,7 +289,7 @@ ps_status_t ps_prefill_backward_workspace_size(int32_t batch, int32_t seqlen, in
  *   status : device int32 word or NULL; PS_DEV_TIMEOUT if a bounded wait gave up.
  * Errors (host, before any launch): a null pointer, batch / seqlen / window /
  * heads < 1, Hq % Hkv != 0, scale <= 0 or rope_theta <= 0 -> PS_ERR_INVALID_ARGUMENT;
- * head_dim != 128 -> PS_ERR_UNSUPPORTED; a tensor not 16-byte aligned ->
+ * head_dim not 64 or 128 -> PS_ERR_UNSUPPORTED; a tensor not 16-byte aligned ->
  * PS_ERR_ALIGNMENT; workspace missing, misaligned or too small -> PS_ERR_WORKSPACE;
  * a failed launch -> PS_ERR_CUDA.  Two launches on `stream` (a pre-pass, then one
  * grid of dK/dV and dQ CTAs using 230,656 bytes of shared memory and all 512 TMEM
@@ -336,10 +336,10 @@ ps_status_t ps_device_code_version(int32_t* version);
  * after a time limit (2 s), sets PS_DEV_TIMEOUT in the status word, lets the
  * copies and products it has already issued finish (each wait for them again
  * bounded) and returns, so the context stays usable.  With enable = 1, the
- * decode partial kernel and the prefill tile kernels launched afterwards use
- * wait_limit_ns (1e3 .. 2e9) as that limit, and CTA 0 of each skips its first
- * K/V copy, so one wait is sure to run out: the call sets PS_DEV_TIMEOUT and
- * its results are undefined.  enable = 0 restores the defaults.  Process-wide
+ * decode partial kernel, the prefill tile kernels and the backward kernel
+ * launched afterwards use wait_limit_ns (1e3 .. 2e9) as that limit, and CTA 0
+ * of each skips its first streamed copy, so one wait is sure to run out: the
+ * call sets PS_DEV_TIMEOUT and its results are undefined.  enable = 0 restores the defaults.  Process-wide
  * and not synchronised with calls in flight: for tests only.
  */
 ps_status_t ps_test_force_wait_timeout(int32_t enable, int64_t wait_limit_ns);

@@ -51,14 +51,13 @@ namespace ps {
 namespace bwd {
 
 constexpr int kT = 128;                  // rows of every tile (resident and streamed)
-constexpr int kHD = 128;                 // head dim
+constexpr int kHD = 128;                 // largest head dim: shared-memory slots are sized for it
 constexpr int kHalf = kT * 128;          // one 64-column swizzled half of a tile: 16 KB
-constexpr int kTile = 2 * kHalf;         // 32 KB
+constexpr int kTile = 2 * kHalf;         // one slot: 32 KB
 constexpr int kLdBytes = kT * 8;         // {LSE*log2e, D} pairs of one query tile
 constexpr int kSoftWarps = 8;
 constexpr int kParts = kSoftWarps / 4;   // softmax warps per TMEM lane quadrant
 constexpr int kNC = kT / kParts;         // step columns per softmax warp
-constexpr int kPairs = 64 / kParts;      // accumulator rotation pairs per warp in the epilogue
 constexpr int kProducerWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
 constexpr int kThreads = 32 * (kSoftWarps + 2);
 // Streamed tiles: ring A holds the operand used by S(t) and by the last
@@ -75,8 +74,18 @@ constexpr int kOffBars = kOffB + kSb * kTile;
 constexpr int kSmem = kOffBars + 256 /*barriers*/ + 1024 /*alignment*/;
 static_assert(kOffLd + kSaKV * kLdBytes <= kOffB, "LSE / D slots fit in the spare slot");
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, 128, false);   // S, dP: both operands K-major
-constexpr uint32_t kIdescAcc = tc::idesc_bf16(128, 128, true);  // accumulations: B MN-major
 constexpr uint32_t kTAcc = 256;                                  // accumulator columns
+
+// Per head dim D (64 or 128): the bytes a 128-row tile fills of its slot, its
+// 64-column halves, the accumulations' instruction descriptor (N = D, B
+// MN-major) and the rotation pairs each softmax warp writes in the epilogue.
+template <int D>
+struct Geo {
+  static constexpr int kBytes = kT * D * 2;
+  static constexpr int kHalves = D / 64;
+  static constexpr uint32_t kIdescAcc = tc::idesc_bf16(128, D, true);
+  static constexpr int kPairs = D / 2 / kParts;
+};
 
 struct Params {
   CUtensorMap tmq, tmdo;  // rotated Q, dO  {D, Hq, S, B}, 128-row boxes
@@ -92,6 +101,8 @@ struct Params {
   int32_t nq;       // 128-row tiles
   int32_t n_dkdv;   // CTAs of the dK/dV kind (the first ones of the grid)
   float scale, scale_log2;
+  uint64_t wait_ns;          // bounded-wait limit
+  int32_t drop_first_load;   // test hook: CTA 0 skips its first streamed copy
   RopeTurns turns;
 };
 
@@ -102,10 +113,20 @@ struct Bars {
   uint64_t s_full[2], p_ready[2];            // step buffers: S computed / P taken
   uint64_t dp_full[2], ds_ready[2];          //               dP computed / dS written
   uint64_t done;                             // every product has completed
+  uint64_t drain;                            // after an abort: the issuer's products completed
   uint32_t tmem_slot;
   int32_t abort;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
+
+// The copies the producer has issued, for the drain after an abort: whether the
+// resident tiles were requested, and the phase parity of the last load into
+// each slot of rings A and B (-1: none).
+struct Inflight {
+  int res;
+  int a[kSaQ];
+  int b[kSb];
+};
 
 __device__ __forceinline__ void tld(uint32_t taddr, uint32_t (&r)[32]) { tc::ld32(taddr, r); }
 __device__ __forceinline__ void tld(uint32_t taddr, uint32_t (&r)[16]) { tc::ld16(taddr, r); }
@@ -117,16 +138,18 @@ __device__ __forceinline__ uint32_t packed_col(int kk) {
   return (16 * kk) / kNC * kNC + (16 * kk) % kNC / 2;
 }
 
-// Writes kPairs rotation pairs (chunk c: columns [c kPairs, (c+1) kPairs) with
-// their partners 64 further on) of one thread's row of a 128-wide fp32
-// accumulator, scaled and rotated back by -pos when `rot` (dQ, dK), plainly
-// otherwise (dV).  Every thread of the warp calls it (tcgen05.ld is
-// warp-collective); only rows with `valid` store.
+// Writes NP rotation pairs (chunk c: columns [c NP, (c+1) NP) with their
+// partners D/2 further on) of one thread's row of a D-wide fp32 accumulator,
+// scaled and rotated back by -pos when `rot` (dQ, dK), plainly otherwise (dV).
+// Every thread of the warp calls it (tcgen05.ld is warp-collective); only rows
+// with `valid` store.
+template <int D>
 __device__ __forceinline__ void store_chunk(uint32_t taddr, float* dst, int c, bool valid, float mul,
                                             bool rot, int32_t pos, const RopeTurns& turns) {
+  constexpr int kPairs = Geo<D>::kPairs, kH = D / 2;
   uint32_t a[kPairs], b[kPairs];
   tld(taddr + c * kPairs, a);
-  tld(taddr + 64 + c * kPairs, b);
+  tld(taddr + kH + c * kPairs, b);
   tc::wait_ld();
   if (!valid) return;
 #pragma unroll
@@ -145,7 +168,7 @@ __device__ __forceinline__ void store_chunk(uint32_t taddr, float* dst, int c, b
 #pragma unroll
   for (int e = 0; e < kPairs; e += 4) {
     *reinterpret_cast<uint4*>(dst + c * kPairs + e) = make_uint4(a[e], a[e + 1], a[e + 2], a[e + 3]);
-    *reinterpret_cast<uint4*>(dst + 64 + c * kPairs + e) =
+    *reinterpret_cast<uint4*>(dst + kH + c * kPairs + e) =
         make_uint4(b[e], b[e + 1], b[e + 2], b[e + 3]);
   }
 }
@@ -172,17 +195,18 @@ constexpr int kPrepRows = 16;
 // One block takes kPrepRows rows (batch row, position) at a time: the angles
 // of those rows, then every 16-byte group of their Q and K rows, then D for
 // every (row, query head) with a half-warp per pair (8 elements per lane).
+template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ PrepParams p) {
-  constexpr int VEC = 16, HALFV = 8;
-  __shared__ float2 cs[kPrepRows][64];
+  constexpr int VEC = D / 8, HALFV = D / 16, NPAIR = D / 2, NG = D / 16;
+  __shared__ float2 cs[kPrepRows][NPAIR];
   grid_dependency_wait();
   allow_dependents();
   const int64_t n_rows = (int64_t)p.B * p.S;
   const int heads = p.hq + p.hkv;
   for (int64_t r0 = (int64_t)blockIdx.x * kPrepRows; r0 < n_rows;
        r0 += (int64_t)gridDim.x * kPrepRows) {
-    for (int t = threadIdx.x; t < kPrepRows * 64; t += blockDim.x) {
-      const int rr = t >> 6, i = t & 63;
+    for (int t = threadIdx.x; t < kPrepRows * NPAIR; t += blockDim.x) {
+      const int rr = t / NPAIR, i = t % NPAIR;
       const int64_t r = r0 + rr;
       if (r < n_rows) {
         const int b = (int)(r / p.S);
@@ -193,10 +217,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ P
       }
     }
     __syncthreads();
-    for (int it = threadIdx.x; it < kPrepRows * heads * 8; it += blockDim.x) {
-      const int g = it & 7;
-      const int hd = (it >> 3) % heads;
-      const int rr = (it >> 3) / heads;
+    for (int it = threadIdx.x; it < kPrepRows * heads * NG; it += blockDim.x) {
+      const int g = it % NG;
+      const int hd = (it / NG) % heads;
+      const int rr = (it / NG) / heads;
       const int64_t r = r0 + rr;
       if (r >= n_rows) continue;
       uint4 ra, rb;
@@ -218,7 +242,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ P
       const int64_t r = r0 + w / p.hq;
       const int h = w % p.hq;
       float acc = 0.f;
-      if (r < n_rows) {
+      if (r < n_rows && l16 < VEC) {  // 8 elements per lane
         const uint4 a = p.o[(r * p.hq + h) * VEC + l16], d = p.dout[(r * p.hq + h) * VEC + l16];
         acc = bf16lo(a.x) * bf16lo(d.x) + bf16hi(a.x) * bf16hi(d.x) + bf16lo(a.y) * bf16lo(d.y) +
               bf16hi(a.y) * bf16hi(d.y) + bf16lo(a.z) * bf16lo(d.z) + bf16hi(a.z) * bf16hi(d.z) +
@@ -357,32 +381,37 @@ __device__ __forceinline__ void release(uint64_t* bar, int lane, bool stored) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-// One 128-wide product: 8 MMAs (K16 steps) into the accumulator d_tmem.
+// One 128 x 128 product over the head dim: D / 16 MMAs (K16 steps) into the
+// accumulator d_tmem.
+template <int D>
 __device__ __forceinline__ void mma_ss8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                         bool acc) {
 #pragma unroll
-  for (int kk = 0; kk < kHD / 16; ++kk) {
+  for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
     tc::mma_bf16(d_tmem, adesc + off, bdesc + off, kIdescS, acc || kk > 0);
   }
 }
 
 // d_tmem (+)= A (bf16 pairs in TMEM at a_tmem, packed as the softmax warps
-// write them) x B (128 rows of a tile, MN-major).
+// write them) x B (128 rows of a tile, MN-major, N = D).
+template <int D>
 __device__ __forceinline__ void mma_ts8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc_mn,
                                         bool acc) {
 #pragma unroll
   for (int kk = 0; kk < kT / 16; ++kk)
-    tc::mma_bf16_ts(d_tmem, a_tmem + packed_col(kk), bdesc_mn + ((kk * 2048) >> 4), kIdescAcc,
-                    acc || kk > 0);
+    tc::mma_bf16_ts(d_tmem, a_tmem + packed_col(kk), bdesc_mn + ((kk * 2048) >> 4),
+                    Geo<D>::kIdescAcc, acc || kk > 0);
 }
 
 // ---------------------------------------------------------------------------
 // 2a. dK/dV CTA: key tile kt of KV head hk, batch row b
 // ---------------------------------------------------------------------------
+template <int D>
 __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* bar, uint32_t tmem,
-                                         int u) {
+                                         int u, Inflight& fl) {
   constexpr int kSa = kSaKV;
+  constexpr int kB = Geo<D>::kBytes, kNH = Geo<D>::kHalves;
   uint8_t* sK = smem;
   uint8_t* sV = smem + kTile;
   uint8_t* sA = smem + kOffA;  // Q tiles
@@ -412,25 +441,31 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
       prefetch_tmap(&p.tmq);
       prefetch_tmap(&p.tmdo);
       const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
-      mbar_arrive_expect_tx(&bar->res_full, 2 * kTile);
-      tma_load_4d(sK, &p.tmk, &bar->res_full, 0, hk, k0r, b, pol_kv);
-      tma_load_4d(sK + kHalf, &p.tmk, &bar->res_full, 64, hk, k0r, b, pol_kv);
-      tma_load_4d(sV, &p.tmv, &bar->res_full, 0, hk, k0r, b, pol_kv);
-      tma_load_4d(sV + kHalf, &p.tmv, &bar->res_full, 64, hk, k0r, b, pol_kv);
+      mbar_arrive_expect_tx(&bar->res_full, 2 * kB);
+      for (int x = 0; x < kNH; ++x) {
+        tma_load_4d(sK + x * kHalf, &p.tmk, &bar->res_full, 64 * x, hk, k0r, b, pol_kv);
+        tma_load_4d(sV + x * kHalf, &p.tmv, &bar->res_full, 64 * x, hk, k0r, b, pol_kv);
+      }
+      fl.res = 1;
       for (int t = 0; t < n; ++t) {
         const int qt = kt + t / G, h = hk * G + t % G;
         const int sa = t % kSa, sb = t % kSb;
-        if (!mbar_wait_abort(&bar->a_empty[sa], ((t / kSa) & 1) ^ 1, abort)) break;
+        if (!mbar_wait_abort(&bar->a_empty[sa], ((t / kSa) & 1) ^ 1, abort, p.wait_ns)) break;
         uint64_t* fa = &bar->a_full[sa];
-        mbar_arrive_expect_tx(fa, kTile + kLdBytes);
-        tma_load_4d(sA + sa * kTile, &p.tmq, fa, 0, h, qt * kT, b, pol_q);
-        tma_load_4d(sA + sa * kTile + kHalf, &p.tmq, fa, 64, h, qt * kT, b, pol_q);
-        bulk_load(sLd + sa * kT, p.ld + ((int64_t)b * p.hq + h) * p.s_pad + qt * kT, kLdBytes, fa);
-        if (!mbar_wait_abort(&bar->b_empty[sb], ((t / kSb) & 1) ^ 1, abort)) break;
+        // test hook: CTA 0 leaves its first ring-A slot without copy or arrival
+        if (!(t == 0 && p.drop_first_load && blockIdx.x == 0)) {
+          mbar_arrive_expect_tx(fa, kB + kLdBytes);
+          for (int x = 0; x < kNH; ++x)
+            tma_load_4d(sA + sa * kTile + x * kHalf, &p.tmq, fa, 64 * x, h, qt * kT, b, pol_q);
+          bulk_load(sLd + sa * kT, p.ld + ((int64_t)b * p.hq + h) * p.s_pad + qt * kT, kLdBytes, fa);
+          fl.a[sa] = (t / kSa) & 1;
+        }
+        if (!mbar_wait_abort(&bar->b_empty[sb], ((t / kSb) & 1) ^ 1, abort, p.wait_ns)) break;
         uint64_t* fb = &bar->b_full[sb];
-        mbar_arrive_expect_tx(fb, kTile);
-        tma_load_4d(sB + sb * kTile, &p.tmdo, fb, 0, h, qt * kT, b, pol_q);
-        tma_load_4d(sB + sb * kTile + kHalf, &p.tmdo, fb, 64, h, qt * kT, b, pol_q);
+        mbar_arrive_expect_tx(fb, kB);
+        for (int x = 0; x < kNH; ++x)
+          tma_load_4d(sB + sb * kTile + x * kHalf, &p.tmdo, fb, 64 * x, h, qt * kT, b, pol_q);
+        fl.b[sb] = (t / kSb) & 1;
       }
     }
     __syncwarp();
@@ -446,35 +481,35 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
       auto sob = [](int t) { return (uint64_t)(((t % kSb) * kTile) >> 4); };
       // per step t (buffer t & 1): dV += P^T dO, dP^T = V dO^T, then S^T of
       // step t+1, then dK += dS^T Q
-      bool ok = mbar_wait_abort(&bar->res_full, 0, abort) &&
-                mbar_wait_abort(&bar->a_full[0], 0, abort);
+      bool ok = mbar_wait_abort(&bar->res_full, 0, abort, p.wait_ns) &&
+                mbar_wait_abort(&bar->a_full[0], 0, abort, p.wait_ns);
       if (ok) {
         tc::fence_after();
-        mma_ss8(tmem, aK, bQ + soa(0), false);  // S^T(0) = K Q(0)^T
+        mma_ss8<D>(tmem, aK, bQ + soa(0), false);  // S^T(0) = K Q(0)^T
         tc::commit(smem_u32(&bar->s_full[0]));
       }
       for (int t = 0; ok && t < n; ++t) {
         const int bf = t & 1;
         const uint32_t ph = (t >> 1) & 1;
         const uint32_t tb = tmem + bf * 128;
-        if (!(ok = mbar_wait_abort(&bar->p_ready[bf], ph, abort) &&
-                   mbar_wait_abort(&bar->b_full[t % kSb], (t / kSb) & 1, abort)))
+        if (!(ok = mbar_wait_abort(&bar->p_ready[bf], ph, abort, p.wait_ns) &&
+                   mbar_wait_abort(&bar->b_full[t % kSb], (t / kSb) & 1, abort, p.wait_ns)))
           break;
         tc::fence_after();
-        mma_ts8(tmem + kTAcc, tb, bOm + sob(t), t > 0);  // dV += P^T dO
-        mma_ss8(tb, aV, bO + sob(t), false);              // dP^T = V dO^T
+        mma_ts8<D>(tmem + kTAcc, tb, bOm + sob(t), t > 0);  // dV += P^T dO
+        mma_ss8<D>(tb, aV, bO + sob(t), false);              // dP^T = V dO^T
         tc::commit(smem_u32(&bar->dp_full[bf]));
         tc::commit(smem_u32(&bar->b_empty[t % kSb]));
         if (t + 1 < n) {
-          if (!(ok = mbar_wait_abort(&bar->a_full[(t + 1) % kSa], ((t + 1) / kSa) & 1, abort)))
+          if (!(ok = mbar_wait_abort(&bar->a_full[(t + 1) % kSa], ((t + 1) / kSa) & 1, abort, p.wait_ns)))
             break;
           tc::fence_after();
-          mma_ss8(tmem + (bf ^ 1) * 128, aK, bQ + soa(t + 1), false);
+          mma_ss8<D>(tmem + (bf ^ 1) * 128, aK, bQ + soa(t + 1), false);
           tc::commit(smem_u32(&bar->s_full[bf ^ 1]));
         }
-        if (!(ok = mbar_wait_abort(&bar->ds_ready[bf], ph, abort))) break;
+        if (!(ok = mbar_wait_abort(&bar->ds_ready[bf], ph, abort, p.wait_ns))) break;
         tc::fence_after();
-        mma_ts8(tmem + kTAcc + 128, tb, bQm + soa(t), t > 0);  // dK += dS^T Q
+        mma_ts8<D>(tmem + kTAcc + 128, tb, bQm + soa(t), t > 0);  // dK += dS^T Q
         tc::commit(smem_u32(&bar->a_empty[t % kSa]));
       }
       if (ok) tc::commit(smem_u32(&bar->done));
@@ -505,8 +540,8 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
       const int32_t hi = (int32_t)(hi64 < -1 ? -1 : (hi64 > kNC - 1 ? kNC - 1 : hi64));
       const uint32_t tS = tmem + bf * 128 + part * kNC + lane_off;
       const float4* ld = reinterpret_cast<const float4*>(sLd + sa * kT + part * kNC);
-      ok = mbar_wait_abort(&bar->s_full[bf], ph, abort) &&
-           mbar_wait_abort(&bar->a_full[sa], (t / kSa) & 1, abort);  // the LSE / D pairs
+      ok = mbar_wait_abort(&bar->s_full[bf], ph, abort, p.wait_ns) &&
+           mbar_wait_abort(&bar->a_full[sa], (t / kSa) & 1, abort, p.wait_ns);  // the LSE / D pairs
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -517,7 +552,7 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
       else
         p_col<false>(tS, p.scale_log2, ld, 0, kNC - 1, pr);
       release(&bar->p_ready[bf], lane, true);
-      ok = mbar_wait_abort(&bar->dp_full[bf], ph, abort);
+      ok = mbar_wait_abort(&bar->dp_full[bf], ph, abort, p.wait_ns);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -527,23 +562,24 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
       release(&bar->ds_ready[bf], lane, true);
     }
     if (ok && n > 0) {
-      ok = mbar_wait_abort(&bar->done, 0, abort);
+      ok = mbar_wait_abort(&bar->done, 0, abort, p.wait_ns);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
       tc::fence_after();
       const bool valid = k0r + row <= k1r;
-      const int64_t base = (((int64_t)b * p.S + (valid ? k0r + row : 0)) * p.hkv + hk) * kHD;
+      const int64_t base = (((int64_t)b * p.S + (valid ? k0r + row : 0)) * p.hkv + hk) * D;
       if (n > 0) {
-        store_chunk(tmem + kTAcc + lane_off, p.dv + base, part, valid, 1.f, false, 0, p.turns);
-        store_chunk(tmem + kTAcc + 128 + lane_off, p.dk + base, part, valid, p.scale, true,
-                    (int32_t)kpos, p.turns);
+        store_chunk<D>(tmem + kTAcc + lane_off, p.dv + base, part, valid, 1.f, false, 0, p.turns);
+        store_chunk<D>(tmem + kTAcc + 128 + lane_off, p.dk + base, part, valid, p.scale, true,
+                       (int32_t)kpos, p.turns);
       } else if (valid) {  // no query admits these keys: zero gradients
+        constexpr int kPairs = Geo<D>::kPairs;
         for (int e = part * kPairs; e < part * kPairs + kPairs; e += 4) {
           *reinterpret_cast<float4*>(p.dv + base + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(p.dv + base + 64 + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(p.dv + base + D / 2 + e) = make_float4(0.f, 0.f, 0.f, 0.f);
           *reinterpret_cast<float4*>(p.dk + base + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(p.dk + base + 64 + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(p.dk + base + D / 2 + e) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
     }
@@ -553,9 +589,11 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
 // ---------------------------------------------------------------------------
 // 2b. dQ CTA: query tile of head h, batch row b
 // ---------------------------------------------------------------------------
+template <int D>
 __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar, uint32_t tmem,
-                                       int u) {
+                                       int u, Inflight& fl) {
   constexpr int kSa = kSaQ;
+  constexpr int kB = Geo<D>::kBytes, kNH = Geo<D>::kHalves;
   uint8_t* sQ = smem;
   uint8_t* sdO = smem + kTile;
   uint8_t* sA = smem + kOffA;  // K tiles
@@ -588,24 +626,27 @@ __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar
       prefetch_tmap(&p.tmk);
       prefetch_tmap(&p.tmv);
       const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
-      mbar_arrive_expect_tx(&bar->res_full, 2 * kTile);
-      tma_load_4d(sQ, &p.tmq, &bar->res_full, 0, h, q0r, b, pol_q);
-      tma_load_4d(sQ + kHalf, &p.tmq, &bar->res_full, 64, h, q0r, b, pol_q);
-      tma_load_4d(sdO, &p.tmdo, &bar->res_full, 0, h, q0r, b, pol_q);
-      tma_load_4d(sdO + kHalf, &p.tmdo, &bar->res_full, 64, h, q0r, b, pol_q);
+      mbar_arrive_expect_tx(&bar->res_full, 2 * kB);
+      for (int x = 0; x < kNH; ++x) {
+        tma_load_4d(sQ + x * kHalf, &p.tmq, &bar->res_full, 64 * x, h, q0r, b, pol_q);
+        tma_load_4d(sdO + x * kHalf, &p.tmdo, &bar->res_full, 64 * x, h, q0r, b, pol_q);
+      }
+      fl.res = 1;
       for (int t = 0; t < n; ++t) {
         const int ka = tile_at(t) * kT;
         const int sa = t % kSa, sb = t % kSb;
-        if (!mbar_wait_abort(&bar->a_empty[sa], ((t / kSa) & 1) ^ 1, abort)) break;
+        if (!mbar_wait_abort(&bar->a_empty[sa], ((t / kSa) & 1) ^ 1, abort, p.wait_ns)) break;
         uint64_t* fa = &bar->a_full[sa];
-        mbar_arrive_expect_tx(fa, kTile);
-        tma_load_4d(sA + sa * kTile, &p.tmk, fa, 0, hk, ka, b, pol_kv);
-        tma_load_4d(sA + sa * kTile + kHalf, &p.tmk, fa, 64, hk, ka, b, pol_kv);
-        if (!mbar_wait_abort(&bar->b_empty[sb], ((t / kSb) & 1) ^ 1, abort)) break;
+        mbar_arrive_expect_tx(fa, kB);
+        for (int x = 0; x < kNH; ++x)
+          tma_load_4d(sA + sa * kTile + x * kHalf, &p.tmk, fa, 64 * x, hk, ka, b, pol_kv);
+        fl.a[sa] = (t / kSa) & 1;
+        if (!mbar_wait_abort(&bar->b_empty[sb], ((t / kSb) & 1) ^ 1, abort, p.wait_ns)) break;
         uint64_t* fb = &bar->b_full[sb];
-        mbar_arrive_expect_tx(fb, kTile);
-        tma_load_4d(sB + sb * kTile, &p.tmv, fb, 0, hk, ka, b, pol_kv);
-        tma_load_4d(sB + sb * kTile + kHalf, &p.tmv, fb, 64, hk, ka, b, pol_kv);
+        mbar_arrive_expect_tx(fb, kB);
+        for (int x = 0; x < kNH; ++x)
+          tma_load_4d(sB + sb * kTile + x * kHalf, &p.tmv, fb, 64 * x, hk, ka, b, pol_kv);
+        fl.b[sb] = (t / kSb) & 1;
       }
     }
     __syncwarp();
@@ -619,34 +660,34 @@ __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar
       auto soa = [](int t) { return (uint64_t)(((t % kSa) * kTile) >> 4); };
       auto sob = [](int t) { return (uint64_t)(((t % kSb) * kTile) >> 4); };
       // per step t (buffer t & 1): dP = dO V^T, then S of step t+1, then dQ += dS K
-      bool ok = mbar_wait_abort(&bar->res_full, 0, abort) &&
-                mbar_wait_abort(&bar->a_full[0], 0, abort);
+      bool ok = mbar_wait_abort(&bar->res_full, 0, abort, p.wait_ns) &&
+                mbar_wait_abort(&bar->a_full[0], 0, abort, p.wait_ns);
       if (ok) {
         tc::fence_after();
-        mma_ss8(tmem, aQ, bK + soa(0), false);  // S(0) = Q K(0)^T
+        mma_ss8<D>(tmem, aQ, bK + soa(0), false);  // S(0) = Q K(0)^T
         tc::commit(smem_u32(&bar->s_full[0]));
       }
       for (int t = 0; ok && t < n; ++t) {
         const int bf = t & 1;
         const uint32_t ph = (t >> 1) & 1;
         const uint32_t tb = tmem + bf * 128;
-        if (!(ok = mbar_wait_abort(&bar->p_ready[bf], ph, abort) &&
-                   mbar_wait_abort(&bar->b_full[t % kSb], (t / kSb) & 1, abort)))
+        if (!(ok = mbar_wait_abort(&bar->p_ready[bf], ph, abort, p.wait_ns) &&
+                   mbar_wait_abort(&bar->b_full[t % kSb], (t / kSb) & 1, abort, p.wait_ns)))
           break;
         tc::fence_after();
-        mma_ss8(tb, aO, bV + sob(t), false);  // dP = dO V^T
+        mma_ss8<D>(tb, aO, bV + sob(t), false);  // dP = dO V^T
         tc::commit(smem_u32(&bar->dp_full[bf]));
         tc::commit(smem_u32(&bar->b_empty[t % kSb]));
         if (t + 1 < n) {
-          if (!(ok = mbar_wait_abort(&bar->a_full[(t + 1) % kSa], ((t + 1) / kSa) & 1, abort)))
+          if (!(ok = mbar_wait_abort(&bar->a_full[(t + 1) % kSa], ((t + 1) / kSa) & 1, abort, p.wait_ns)))
             break;
           tc::fence_after();
-          mma_ss8(tmem + (bf ^ 1) * 128, aQ, bK + soa(t + 1), false);
+          mma_ss8<D>(tmem + (bf ^ 1) * 128, aQ, bK + soa(t + 1), false);
           tc::commit(smem_u32(&bar->s_full[bf ^ 1]));
         }
-        if (!(ok = mbar_wait_abort(&bar->ds_ready[bf], ph, abort))) break;
+        if (!(ok = mbar_wait_abort(&bar->ds_ready[bf], ph, abort, p.wait_ns))) break;
         tc::fence_after();
-        mma_ts8(tmem + kTAcc, tb, bKm + soa(t), t > 0);  // dQ += dS K
+        mma_ts8<D>(tmem + kTAcc, tb, bKm + soa(t), t > 0);  // dQ += dS K
         tc::commit(smem_u32(&bar->a_empty[t % kSa]));
       }
       if (ok) tc::commit(smem_u32(&bar->done));
@@ -674,7 +715,7 @@ __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar
                           tile_class(km, c0, q0r, q1r, ka, kb, P, p.W) != kFull;
       const int32_t base = ka + part * kNC;
       const uint32_t tS = tmem + bf * 128 + part * kNC + lane_off;
-      ok = mbar_wait_abort(&bar->s_full[bf], ph, abort);
+      ok = mbar_wait_abort(&bar->s_full[bf], ph, abort, p.wait_ns);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -685,7 +726,7 @@ __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar
       else
         p_row<false>(tS, p.scale_log2, ldr.x, 0, 0, 0, pr);
       release(&bar->p_ready[bf], lane, false);
-      ok = mbar_wait_abort(&bar->dp_full[bf], ph, abort);
+      ok = mbar_wait_abort(&bar->dp_full[bf], ph, abort, p.wait_ns);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -695,26 +736,28 @@ __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar
       release(&bar->ds_ready[bf], lane, true);
     }
     if (ok && n > 0) {
-      ok = mbar_wait_abort(&bar->done, 0, abort);
+      ok = mbar_wait_abort(&bar->done, 0, abort, p.wait_ns);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
       tc::fence_after();
       const bool valid = q0r + row <= q1r;
-      float* dst = p.dq + (((int64_t)b * p.S + (valid ? q0r + row : 0)) * p.hq + h) * kHD;
+      float* dst = p.dq + (((int64_t)b * p.S + (valid ? q0r + row : 0)) * p.hq + h) * D;
       if (n > 0) {
-        store_chunk(tmem + kTAcc + lane_off, dst, part, valid, p.scale, true, (int32_t)qpos,
-                    p.turns);
+        store_chunk<D>(tmem + kTAcc + lane_off, dst, part, valid, p.scale, true, (int32_t)qpos,
+                       p.turns);
       } else if (valid) {
+        constexpr int kPairs = Geo<D>::kPairs;
         for (int e = part * kPairs; e < part * kPairs + kPairs; e += 4) {
           *reinterpret_cast<float4*>(dst + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(dst + 64 + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(dst + D / 2 + e) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
     }
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -742,6 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       mbar_init(&bar->ds_ready[i], kSoftWarps);
     }
     mbar_init(&bar->done, 1);
+    mbar_init(&bar->drain, 1);
     bar->abort = 0;
     fence_mbar_init();
   }
@@ -752,19 +796,34 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   grid_dependency_wait();  // rotated Q / K and the LSE / D pairs come from the pre-pass
 
   const int u = (int)blockIdx.x;
+  Inflight fl;
+  fl.res = 0;
+  for (int s = 0; s < kSaQ; ++s) fl.a[s] = -1;
+  for (int s = 0; s < kSb; ++s) fl.b[s] = -1;
   if (u < p.n_dkdv)
-    dkdv_cta(p, smem, bar, tmem, u);
+    dkdv_cta<D>(p, smem, bar, tmem, u, fl);
   else
-    dq_cta(p, smem, bar, tmem, u - p.n_dkdv);
+    dq_cta<D>(p, smem, bar, tmem, u - p.n_dkdv, fl);
 
   tc::fence_before();
   __syncthreads();
   if (bar->abort) {
+    // A wait gave up.  Before shared and tensor memory are released, everything
+    // issued must have landed: the producer waits (bounded) for the last load
+    // into each slot -- a completed phase answers at once, and no later phase
+    // can complete now -- and the issuer commits once more and waits until all
+    // its products have completed.
     if (tid == 0) set_flag(p.status, PS_DEV_TIMEOUT);
-    // copies and products already issued finish on their own within microseconds;
-    // give them time before the CTA's shared and tensor memory are released
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 100000ull) {
+    const int lane = tid & 31;
+    if (warp == kProducerWarp && lane == 0) {
+      if (fl.res) mbar_wait(&bar->res_full, 0, p.wait_ns);
+      for (int s = 0; s < kSaQ; ++s)
+        if (fl.a[s] >= 0) mbar_wait(&bar->a_full[s], (uint32_t)fl.a[s], p.wait_ns);
+      for (int s = 0; s < kSb; ++s)
+        if (fl.b[s] >= 0) mbar_wait(&bar->b_full[s], (uint32_t)fl.b[s], p.wait_ns);
+    } else if (warp == kMmaWarp && lane == 0) {
+      tc::commit(smem_u32(&bar->drain));
+      mbar_wait(&bar->drain, 0, p.wait_ns);
     }
     __syncthreads();
   }
@@ -800,7 +859,7 @@ extern "C" ps_status_t ps_prefill_backward_workspace_size(int32_t batch, int32_t
   if (!bytes || batch < 1 || seqlen < 1 || n_q_heads < 1 || n_kv_heads < 1 ||
       n_q_heads % n_kv_heads)
     return PS_ERR_INVALID_ARGUMENT;
-  if (head_dim != bwd::kHD) return PS_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PS_ERR_UNSUPPORTED;
   *bytes = bwd::layout(batch, seqlen, n_q_heads, n_kv_heads, head_dim).total;
   return PS_OK;
 }
@@ -818,7 +877,7 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
   if (batch < 1 || seqlen < 1 || window < 1 || n_q_heads < 1 || n_kv_heads < 1 ||
       n_q_heads % n_kv_heads || !(scale > 0.f) || !(rope_theta > 0.0))
     return PS_ERR_INVALID_ARGUMENT;
-  if (head_dim != bwd::kHD) return PS_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PS_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(d_out) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return PS_ERR_ALIGNMENT;
@@ -853,8 +912,8 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
     const int sms = device_sm_count();
     const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;
     const int64_t blocks = groups < cap ? groups : cap;
-    if (launch_dependent(bwd::bwd_prep_kernel, dim3((unsigned)blocks), dim3(256), 0, s, g) !=
-        cudaSuccess)
+    if (launch_dependent(head_dim == 128 ? bwd::bwd_prep_kernel<128> : bwd::bwd_prep_kernel<64>,
+                         dim3((unsigned)blocks), dim3(256), 0, s, g) != cudaSuccess)
       return PS_ERR_CUDA;
   }
 
@@ -890,11 +949,15 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
   p.n_dkdv = (int32_t)n_dkdv;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
+  const WaitHooks hooks = wait_hooks();
+  p.wait_ns = hooks.wait_ns;
+  p.drop_first_load = hooks.drop_first_load;
   make_rope_turns(rope_theta, head_dim, &p.turns);
-  if (cudaFuncSetAttribute(bwd::bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           bwd::kSmem) != cudaSuccess)
+  auto kern = head_dim == 128 ? bwd::bwd_kernel<128> : bwd::bwd_kernel<64>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bwd::kSmem) !=
+      cudaSuccess)
     return PS_ERR_CUDA;
-  if (launch_dependent(bwd::bwd_kernel, dim3((unsigned)(n_dkdv + n_dq)), dim3(bwd::kThreads),
+  if (launch_dependent(kern, dim3((unsigned)(n_dkdv + n_dq)), dim3(bwd::kThreads),
                        (size_t)bwd::kSmem, s, p) != cudaSuccess)
     return PS_ERR_CUDA;
   return launch_status();

@@ -67,19 +67,21 @@ struct GatherParams {
 constexpr int kRopeRows = 8;  // chunk rows per block iteration
 constexpr int kRopeBatch = 4; // items a thread loads before it rotates and stores any
 
-// D = 128.  Phase A: groups of kRopeRows chunk rows; the 64 (cos, sin) pairs of
-// each row's position are computed once into shared memory and shared by all
-// Hq query heads and Hkv key heads of that row.  Under Reset PE the query is
+// D = 64 or 128.  Phase A: groups of kRopeRows chunk rows; the D/2 (cos, sin)
+// pairs of each row's position are computed once into shared memory and shared
+// by all Hq query heads and Hkv key heads of that row.  Under Reset PE the query is
 // also rotated at min(p, P + W - 1), its position once the cache is renumbered
 // (prefix keys keep theirs), into qr.  Each thread then loads
 // kRopeBatch items (8 rotation pairs of one row and head each) before it
 // rotates and stores them, to keep enough loads in flight.  Phase B: the ring
 // rows (copied, already rotated) and the zero padding of each batch row's key
 // array.
+// RESET: also write qr (a separate instance keeps the other's registers down).
+template <bool RESET, int D>
 __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant__ GatherParams p) {
-  constexpr int VEC = 16, HALFV = 8;
-  __shared__ float2 cs[kRopeRows][64];
-  __shared__ float2 csr[kRopeRows][64];  // Reset PE query angles
+  constexpr int VEC = D / 8, HALFV = D / 16, NPAIR = D / 2, NG = D / 16;  // NG groups of 8 pairs
+  __shared__ float2 cs[kRopeRows][NPAIR];
+  __shared__ float2 csr[RESET ? kRopeRows : 1][NPAIR];  // Reset PE query angles
   grid_dependency_wait();  // inputs and workspace may be in use by earlier stream work
   allow_dependents();      // the tile kernel may set up meanwhile; it waits for this one
   const bool ring = p.k_pool != nullptr;
@@ -88,8 +90,8 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
   const int heads = p.hq + p.hkv;
   for (int64_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {
     const int64_t r0 = grp * kRopeRows;
-    for (int x = threadIdx.x; x < kRopeRows * 64; x += blockDim.x) {
-      const int rr = x >> 6, i = x & 63;
+    for (int x = threadIdx.x; x < kRopeRows * NPAIR; x += blockDim.x) {
+      const int rr = x / NPAIR, i = x % NPAIR;
       const int64_t r = r0 + rr;
       if (r < n_rows) {
         const int b = (int)(r / p.S);
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
         float c, sn;
         rope_cos_sin(pos, p.turns.f[i], c, sn);
         cs[rr][i] = make_float2(c, sn);
-        if (p.qr) {
+        if (RESET) {
           const int64_t last = (int64_t)p.prefix_len[b] + p.W - 1;  // renumbered position cap
           if ((int64_t)pos > last && last >= 0) rope_cos_sin((int32_t)last, p.turns.f[i], c, sn);
           csr[rr][i] = make_float2(c, sn);
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
       }
     }
     __syncthreads();
-    const int items = kRopeRows * heads * 8;
+    const int items = kRopeRows * heads * NG;
     for (int it0 = threadIdx.x; it0 < items; it0 += kRopeBatch * blockDim.x) {
       uint4 xa[kRopeBatch], xb[kRopeBatch];
       uint4* dst[kRopeBatch];
@@ -117,9 +119,9 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
         dstr[u] = nullptr;
         const int it = it0 + u * blockDim.x;
         if (it >= items) continue;
-        const int g = it & 7;
-        const int hd = (it >> 3) % heads;
-        const int rr = (it >> 3) / heads;
+        const int g = it % NG;
+        const int hd = (it / NG) % heads;
+        const int rr = (it / NG) / heads;
         const int64_t r = r0 + rr;
         if (r >= n_rows) continue;
         ang[u] = &cs[rr][8 * g];
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
           xa[u] = p.q[base];
           xb[u] = p.q[base + HALFV];
           dst[u] = p.qh + base;
-          if (p.qr) dstr[u] = p.qr + base;
+          if (RESET) dstr[u] = p.qr + base;
         } else {
           const int h = hd - p.hq;
           const int b = (int)(r / p.S);
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
         rotate8(xa[u], xb[u], ang[u], ra, rb);
         dst[u][0] = ra;
         dst[u][HALFV] = rb;
-        if (dstr[u]) {
+        if (RESET && dstr[u]) {
           const float2* angr = &csr[0][0] + (ang[u] - &cs[0][0]);
           rotate8(xa[u], xb[u], angr, ra, rb);
           dstr[u][0] = ra;
@@ -218,12 +220,19 @@ __global__ void __launch_bounds__(256) rope_gather_kernel(const __grid_constant_
 // ---------------------------------------------------------------------------
 // 2. tile kernel
 // ---------------------------------------------------------------------------
-constexpr int kBM = 128, kBN = 128, kHD = 128;
+constexpr int kBM = 128, kBN = 128;
 constexpr int kHalf = kBM * 64 * 2;  // one 64-column swizzled half block: 16 KB
-constexpr int kTile = 2 * kHalf;     // 128 x 128 bf16: 32 KB
+constexpr int kPTile = 2 * kHalf;    // 128 x 128 bf16 probabilities: 32 KB
 constexpr uint32_t kIdescQK = tc::idesc_bf16(kBM, kBN, false);
-constexpr uint32_t kIdescPV = tc::idesc_bf16(kBM, kHD, true);
-constexpr int kSmemPrefill = kTile * 6 + 1024 /*barriers*/ + 1024 /*alignment*/;
+
+// Q, K and V tiles of 128 rows for head dim D (64 or 128): D / 64 half blocks.
+template <int D>
+struct Geom {
+  static constexpr int kTile = kBM * D * 2;
+  static constexpr int kHalves = D / 64;
+  static constexpr uint32_t kIdescPV = tc::idesc_bf16(kBM, D, true);
+  static constexpr int kSmemSingle = 5 * kTile + kPTile + 1024 /*barriers*/ + 1024 /*alignment*/;
+};
 
 struct PrefillParams {
   CUtensorMap tmq;  // rotated Q  {D, Hq, S, B}
@@ -301,7 +310,10 @@ __device__ __forceinline__ Visits make_visits(const KeyMap& km, int64_t q0, int6
   return v;
 }
 
+template <int D>
 __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  constexpr int kTile = Geom<D>::kTile, kHalves = Geom<D>::kHalves;
+  constexpr uint32_t kIdescPV = Geom<D>::kIdescPV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -309,7 +321,7 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
   uint8_t* sK0 = smem + kTile;
   uint8_t* sV0 = smem + 3 * kTile;
   uint8_t* sP = smem + 5 * kTile;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * kTile);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kPTile);
   uint64_t* q_full = bars + 0;
   uint64_t* kv_full = bars + 1;  // [2]
   uint64_t* s_done = bars + 3;
@@ -360,17 +372,17 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
     uint8_t* dk = sK0 + stage * kTile;
     uint8_t* dv = sV0 + stage * kTile;
     mbar_arrive_expect_tx(&kv_full[stage], 2 * kTile);
-    tma_load_4d(dk, &p.tmk, &kv_full[stage], 0, hk, kt * kBN, b, pol_kv);
-    tma_load_4d(dk + kHalf, &p.tmk, &kv_full[stage], 64, hk, kt * kBN, b, pol_kv);
-    tma_load_4d(dv, &p.tmv, &kv_full[stage], 0, hk, kt * kBN, b, pol_kv);
-    tma_load_4d(dv + kHalf, &p.tmv, &kv_full[stage], 64, hk, kt * kBN, b, pol_kv);
+    for (int hh = 0; hh < kHalves; ++hh) {
+      tma_load_4d(dk + hh * kHalf, &p.tmk, &kv_full[stage], 64 * hh, hk, kt * kBN, b, pol_kv);
+      tma_load_4d(dv + hh * kHalf, &p.tmv, &kv_full[stage], 64 * hh, hk, kt * kBN, b, pol_kv);
+    }
   };
   int issued = 0;  // key tiles whose loads were issued (thread 0)
   int q_pending = -1;  // parity of a Q load issued but not yet waited for (thread 0)
   auto load_q = [&](const CUtensorMap* m, int parity) {
     mbar_arrive_expect_tx(q_full, kTile);
-    tma_load_4d(sQ, m, q_full, 0, h, q0r, b, pol_q);
-    tma_load_4d(sQ + kHalf, m, q_full, 64, h, q0r, b, pol_q);
+    for (int hh = 0; hh < kHalves; ++hh)
+      tma_load_4d(sQ + hh * kHalf, m, q_full, 64 * hh, h, q0r, b, pol_q);
     q_pending = parity;
   };
   if (tid == 0 && n_tiles > 0) {
@@ -407,7 +419,7 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
         tc::fence_after();
         const uint32_t aq = smem_u32(sQ), ak = smem_u32(sK0 + st * kTile);
 #pragma unroll
-        for (int kk = 0; kk < kHD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
           tc::mma_bf16(tS, tc::sdesc_sw128(aq + off, 16, 1024), tc::sdesc_sw128(ak + off, 16, 1024),
                        kIdescQK, kk > 0);
@@ -471,7 +483,7 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
     __syncwarp();
     if (__any_sync(0xffffffffu, rescale)) {  // warp-uniform: alpha is 1 on the other rows
 #pragma unroll
-      for (int c = 0; c < kHD / 32; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tc::ld32(tO + lane_off + c * 32, r);
         tc::wait_ld();
@@ -531,9 +543,9 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
   if (ok && n_tiles > 0) {
     const float inv = 1.f / l;
     const int32_t qrow = q0r + row;
-    __nv_bfloat16* orow = p.out + (((int64_t)b * p.S + qrow) * p.hq + h) * kHD;
+    __nv_bfloat16* orow = p.out + (((int64_t)b * p.S + qrow) * p.hq + h) * D;
 #pragma unroll
-    for (int c = 0; c < kHD / 32; ++c) {
+    for (int c = 0; c < D / 32; ++c) {
       uint32_t r[32];
       tc::ld32(tO + lane_off + c * 32, r);
       tc::wait_ld();
@@ -595,7 +607,10 @@ namespace ws {
 constexpr int kThreads = 320;
 constexpr int kSt = 2;  // steps in flight: each holds a K tile and a V tile
 constexpr int kStK = kSt, kStV = kSt;
-constexpr int kSmem = (2 + kStK + kStV) * kTile + 1024 /*barriers*/ + 1024 /*alignment*/;
+template <int D>
+constexpr int smem_bytes() {
+  return (2 + kStK + kStV) * Geom<D>::kTile + 1024 /*barriers*/ + 1024 /*alignment*/;
+}
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 
 struct Bars {
@@ -726,9 +741,12 @@ __device__ __forceinline__ float softmax_tile(uint32_t tS, int j, float scale_lo
   return alpha;
 }
 
+template <int D>
 __global__ void __launch_bounds__(ws::kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ PrefillParams p) {
   using namespace ws;
+  constexpr int kTile = Geom<D>::kTile, kHalves = Geom<D>::kHalves;
+  constexpr uint32_t kIdescPV = Geom<D>::kIdescPV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -791,10 +809,10 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         // every Q K of the previous Q load has completed
         if (!wait(&bar->q_empty, (kq & 1) ^ 1, abort, p.wait_ns)) return false;
         mbar_arrive_expect_tx(&bar->q_full, 2 * kTile);
-        for (int i = 0; i < 2; ++i) {
-          tma_load_4d(sQ + i * kTile, m, &bar->q_full, 0, it.h0 + i, it.q0r, it.b, pol_q);
-          tma_load_4d(sQ + i * kTile + kHalf, m, &bar->q_full, 64, it.h0 + i, it.q0r, it.b, pol_q);
-        }
+        for (int i = 0; i < 2; ++i)
+          for (int hh = 0; hh < kHalves; ++hh)
+            tma_load_4d(sQ + i * kTile + hh * kHalf, m, &bar->q_full, 64 * hh, it.h0 + i, it.q0r,
+                        it.b, pol_q);
         last_q = kq & 1;
         ++kq;
         return true;
@@ -819,14 +837,14 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           if (j < it.n_tiles) {
             const int kt = it.tile_at(j);
             uint8_t* dk = sK + st * kTile;
-            tma_load_4d(dk, &p.tmk, full, 0, it.hk, kt * kBN, it.b, pol_kv);
-            tma_load_4d(dk + kHalf, &p.tmk, full, 64, it.hk, kt * kBN, it.b, pol_kv);
+            for (int hh = 0; hh < kHalves; ++hh)
+              tma_load_4d(dk + hh * kHalf, &p.tmk, full, 64 * hh, it.hk, kt * kBN, it.b, pol_kv);
           }
           if (j > 0) {
             const int kt = it.tile_at(j - 1);
             uint8_t* dv = sV + st * kTile;
-            tma_load_4d(dv, &p.tmv, full, 0, it.hk, kt * kBN, it.b, pol_kv);
-            tma_load_4d(dv + kHalf, &p.tmv, full, 64, it.hk, kt * kBN, it.b, pol_kv);
+            for (int hh = 0; hh < kHalves; ++hh)
+              tma_load_4d(dv + hh * kHalf, &p.tmv, full, 64 * hh, it.hk, kt * kBN, it.b, pol_kv);
           }
           // the query at its own position for the visits after the renumbered ones
           if (j == it.v.n0 && j > 0 && j < it.n_tiles && !(ok = load_q(it, &p.tmq))) break;
@@ -850,7 +868,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       auto qk = [&](int i, int sk) {
         const uint64_t a = dq + (uint64_t)((i * kTile) >> 4), b = dk + (uint64_t)((sk * kTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kHD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
           tc::mma_bf16(tmem + i * 128, a + off, b + off, kIdescQK, kk > 0);
         }
@@ -958,7 +976,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           // O_i already holds every P V issued before S_i(j), which has completed,
           // and P_i(j) V is not issued before this thread arrives below
 #pragma unroll 1
-          for (int c = 0; c < kHD / 32; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tc::ld32(tO + c * 32, o);
             tc::wait_ld();
@@ -982,13 +1000,13 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       tc::fence_after();
       const int32_t qrow = it.q0r + row;
       const float inv = 1.f / l;
-      __nv_bfloat16* orow = p.out + (((int64_t)it.b * p.S + qrow) * p.hq + it.h0 + i) * kHD;
+      __nv_bfloat16* orow = p.out + (((int64_t)it.b * p.S + qrow) * p.hq + it.h0 + i) * D;
 #pragma unroll
-      for (int c = 0; c < kHD / 32; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tc::ld32(tO + c * 32, o);
         tc::wait_ld();
-        if (c == kHD / 32 - 1) {  // O_i is read out: the next item may overwrite it
+        if (c == D / 32 - 1) {  // O_i is read out: the next item may overwrite it
           tc::fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bar->o_free[i]);
@@ -1062,6 +1080,37 @@ static PrefillLayout prefill_layout(int B, int S, int hq, int hkv, int D, int ri
 
 using namespace ps;
 
+// The tile kernel for head dim D: pairs of query heads when the group size is
+// even, else one head per CTA.  cudaFuncSetAttribute is cheap and per device;
+// it runs every time rather than behind a flag that would be wrong on a second
+// device.
+template <int D>
+static ps_status_t launch_tiles(const PrefillParams& p, int group, int n_q_heads, int batch,
+                                cudaStream_t s) {
+  if (group % 2 == 0) {
+    constexpr int smem = ws::smem_bytes<D>();
+    if (cudaFuncSetAttribute(prefill_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return PS_ERR_CUDA;
+    const int64_t n_items = (int64_t)p.nq * (n_q_heads / 2) * batch;
+    if (n_items > 0x7fffffffLL) return PS_ERR_UNSUPPORTED;
+    const int sms = device_sm_count();
+    const int64_t grid = n_items < (sms > 0 ? sms : 148) ? n_items : (sms > 0 ? sms : 148);
+    if (launch_dependent(prefill_pair_kernel<D>, dim3((unsigned)grid), dim3(ws::kThreads),
+                         (size_t)smem, s, p) != cudaSuccess)
+      return PS_ERR_CUDA;
+  } else {
+    constexpr int smem = Geom<D>::kSmemSingle;
+    if (cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return PS_ERR_CUDA;
+    dim3 grid((unsigned)p.nq, (unsigned)n_q_heads, (unsigned)batch);
+    if (launch_dependent(prefill_kernel<D>, grid, dim3(128), (size_t)smem, s, p) != cudaSuccess)
+      return PS_ERR_CUDA;
+  }
+  return PS_OK;
+}
+
 extern "C" ps_status_t ps_prefill_tile_grid(int32_t seqlen, int32_t q_start, int32_t prefix_len,
                                             int32_t window, int32_t with_ring, int32_t bm,
                                             int32_t bn, int32_t* nq, int32_t* nk) {
@@ -1100,7 +1149,7 @@ extern "C" ps_status_t ps_prefill_workspace_size(int32_t batch, int32_t seqlen, 
   if (!bytes || batch < 1 || seqlen < 1 || n_q_heads < 1 || n_kv_heads < 1 || ring_rows_max < 0 ||
       n_q_heads % n_kv_heads || (pe_mode != PS_PE_CONTINUE && pe_mode != PS_PE_RESET))
     return PS_ERR_INVALID_ARGUMENT;
-  if (head_dim != 128) return PS_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PS_ERR_UNSUPPORTED;
   *bytes = prefill_layout(batch, seqlen, n_q_heads, n_kv_heads, head_dim, ring_rows_max,
                           pe_mode == PS_PE_RESET)
                .total;
@@ -1121,7 +1170,7 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
   if (pe_mode != PS_PE_CONTINUE && pe_mode != PS_PE_RESET) return PS_ERR_INVALID_ARGUMENT;
   if (ring && ring->pe_mode != pe_mode) return PS_ERR_INVALID_ARGUMENT;
   const bool reset = pe_mode == PS_PE_RESET;
-  if (head_dim != kHD) return PS_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PS_ERR_UNSUPPORTED;
   if (batch > 65535 || n_q_heads > 65535) return PS_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return PS_ERR_ALIGNMENT;
   int ring_rows = 0;
@@ -1165,13 +1214,15 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
   make_rope_turns(rope_theta, head_dim, &g.turns);
   {
     const int64_t groups = ((int64_t)batch * seqlen + kRopeRows - 1) / kRopeRows;
-    const int64_t extra = (int64_t)batch * (L.skv - seqlen) * n_kv_heads * 16;
+    const int64_t extra = (int64_t)batch * (L.skv - seqlen) * n_kv_heads * (head_dim / 8);
     int64_t blocks = groups > (extra + 255) / 256 ? groups : (extra + 255) / 256;
     const int sms = device_sm_count();
     const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;  // 16 x 8 KB of smem per SM
     if (blocks > cap) blocks = cap;
-    if (launch_dependent(rope_gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s, g) !=
-        cudaSuccess)
+    void (*pre)(GatherParams) =
+        head_dim == 128 ? (reset ? rope_gather_kernel<true, 128> : rope_gather_kernel<false, 128>)
+                        : (reset ? rope_gather_kernel<true, 64> : rope_gather_kernel<false, 64>);
+    if (launch_dependent(pre, dim3((unsigned)blocks), dim3(256), 0, s, g) != cudaSuccess)
       return PS_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return PS_ERR_CUDA;
   }
@@ -1218,28 +1269,9 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
   p.nq = (seqlen + kBM - 1) / kBM;
   p.B = batch;
   p.scale_log2 = scale * 1.4426950408889634f;
-  // cudaFuncSetAttribute is cheap and per device; call it every time rather
-  // than caching a flag that would be wrong on a second device
   const int group = n_q_heads / n_kv_heads;
-  if (group % 2 == 0) {
-    if (cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             ws::kSmem) != cudaSuccess)
-      return PS_ERR_CUDA;
-    const int64_t n_items = (int64_t)p.nq * (n_q_heads / 2) * batch;
-    if (n_items > 0x7fffffffLL) return PS_ERR_UNSUPPORTED;
-    const int sms = device_sm_count();
-    const int64_t grid = n_items < (sms > 0 ? sms : 148) ? n_items : (sms > 0 ? sms : 148);
-    if (launch_dependent(prefill_pair_kernel, dim3((unsigned)grid), dim3(ws::kThreads),
-                         (size_t)ws::kSmem, s, p) != cudaSuccess)
-      return PS_ERR_CUDA;
-  } else {
-    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemPrefill) != cudaSuccess)
-      return PS_ERR_CUDA;
-    dim3 grid((unsigned)p.nq, (unsigned)n_q_heads, (unsigned)batch);
-    if (launch_dependent(prefill_kernel, grid, dim3(128), (size_t)kSmemPrefill, s, p) !=
-        cudaSuccess)
-      return PS_ERR_CUDA;
-  }
+  const ps_status_t st = head_dim == 128 ? launch_tiles<128>(p, group, n_q_heads, batch, s)
+                                         : launch_tiles<64>(p, group, n_q_heads, batch, s);
+  if (st != PS_OK) return st;
   return launch_status();
 }

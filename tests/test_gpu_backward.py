@@ -35,15 +35,16 @@ def _close(g, ref, what):
         assert err.mean() <= 2e-3 * scale, f"{what} head {h}: mean err {err.mean():.3e} vs max {scale:.3e}"
 
 
-@pytest.mark.parametrize("B,S,hq,hkv,P,W", [
-    (1, 300, 4, 2, [37], 100),        # ragged tail, prefix and band
-    (2, 257, 2, 2, [5, 0], 1000),     # one query head per KV head; W >= S: causal
-    (1, 384, 8, 2, [0], 128),         # G = 4; plain sliding window
-    (1, 200, 4, 2, [300], 16),        # P >= S: causal through the prefix
-    (2, 1024, 16, 8, [64, 64], 256),  # training-shaped, reduced: 4W tokens, loss on all
+@pytest.mark.parametrize("B,S,hq,hkv,P,W,D", [
+    (1, 300, 4, 2, [37], 100, 128),        # ragged tail, prefix and band
+    (1, 300, 4, 2, [37], 100, 64),    # the same at head_dim 64
+    (2, 257, 2, 2, [5, 0], 1000, 128),     # one query head per KV head; W >= S: causal
+    (1, 384, 8, 2, [0], 128, 128),         # G = 4; plain sliding window
+    (1, 200, 4, 2, [300], 16, 128),        # P >= S: causal through the prefix
+    (2, 1024, 16, 8, [64, 64], 256, 128),  # training-shaped, reduced: 4W tokens, loss on all
 ])
-def test_backward_matches_oracle(ps, B, S, hq, hkv, P, W):
-    seed, D, theta = 41, 128, 10000.0
+def test_backward_matches_oracle(ps, B, S, hq, hkv, P, W, D):
+    seed, theta = 41, 10000.0
     pos = np.arange(S)
     q = np.stack([synth.query_bits(seed, b, pos, hq, D) for b in range(B)])
     kv = [synth.History(seed, b, hkv, D).rows_bits(pos) for b in range(B)]

@@ -264,3 +264,27 @@ def test_prefill_extend_from_ring_reset_pe(ps, c0, S, hq):
     _check_rows(seed, out, lse, q, [c0] * B, [P] * B, W, theta, [range(S)] * B, hkv,
                 "reset extend", reference=attend_reset_pe)
     assert cache.check_status() == 0
+
+
+# ------------------------------------------------------------- head_dim 64 --
+@pytest.mark.parametrize("B,S,hq,hkv,P,W,pe", [
+    (2, 300, 4, 2, [37, 0], 100, 0),     # pairs of query heads, ragged tail
+    (1, 257, 2, 2, [5], 1000, 0),        # one query head per KV head; W >= S
+    (1, 400, 4, 2, [37], 64, 1),         # Reset PE with a split prefix tile
+])
+def test_prefill_head_dim_64_all_rows(ps, B, S, hq, hkv, P, W, pe):
+    seed, D, theta = 39, 64, 10000.0
+    q, k, v = _inputs(seed, B, S, [0] * B, hq, hkv, D)
+    out, lse = _run(ps, q, k, v, [0] * B, P, W, theta, pe_mode=pe)
+    _check_rows(seed, out, lse, q, [0] * B, P, W, theta, [range(S)] * B, hkv, "D=64",
+                reference=attend_reset_pe if pe else attend)
+
+
+def test_prefill_head_dim_64_extend_from_ring(ps):
+    seed, B, hq, hkv, D, P, W, theta, c0, S = 40, 2, 4, 2, 64, 20, 64, 10000.0, 300, 150
+    cache = ps.RingCache(B, hkv, D, W, [P] * B, rope_theta=theta)
+    append_runs(cache, {b: [(0, c0)] for b in range(B)}, synth_source(seed, hkv, D))
+    q, k, v = _inputs(seed, B, S, [c0] * B, hq, hkv, D)
+    out, lse = _run(ps, q, k, v, [c0] * B, [P] * B, W, theta, ring=cache)
+    _check_rows(seed, out, lse, q, [c0] * B, [P] * B, W, theta, [range(S)] * B, hkv, "D=64 extend")
+    assert cache.check_status() == 0

@@ -96,3 +96,35 @@ def test_prefill_wait_times_out_then_recovers(ps, hq, hkv):
             o_ref, l_ref = attend(synth.bits_to_f64(q[b, r]), r, P[b], W, hist.rows, theta)
             assert_attention_close(bf16_tensor_to_f64(out[b, r]), lse[b, :, r].cpu().numpy(),
                                    o_ref, l_ref, f"after timeout, b={b} row={r}")
+
+
+def test_backward_wait_times_out_then_recovers(ps):
+    from oracle import attend_backward
+    seed, B, S, hq, hkv, D, P, W, theta = 53, 1, 300, 4, 2, 128, [37], 100, 10000.0
+    pos = np.arange(S)
+    q = synth.query_bits(seed, 0, pos, hq, D)[None]
+    k, v = synth.History(seed, 0, hkv, D).rows_bits(pos)
+    do = synth.normal_bf16(seed, 5, 0, pos, hq, D)[None]
+    tq, tk, tv, tdo = (bits_to_bf16_tensor(x) for x in (q, k[None], v[None], do))
+    i32 = dict(dtype=torch.int32, device="cuda")
+    qs, pl = torch.zeros(B, **i32), torch.tensor(P, **i32)
+    status = torch.zeros(1, **i32)
+    out, lse = ps.prefill(tq, tk, tv, qs, pl, W, rope_theta=theta, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    with forced_timeout(ps):
+        ps.prefill_backward(tq, tk, tv, out, lse, tdo, qs, pl, W, rope_theta=theta, status=status)
+        torch.cuda.synchronize()
+    assert int(status.item()) == ps.PS_DEV_TIMEOUT
+    status.zero_()
+    dq, dk, dv = ps.prefill_backward(tq, tk, tv, out, lse, tdo, qs, pl, W, rope_theta=theta,
+                                     status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    refs = attend_backward(synth.bits_to_f64(q[0]), synth.bits_to_f64(k), synth.bits_to_f64(v),
+                           synth.bits_to_f64(do[0]), P[0], W, theta)[:3]
+    for got, ref, name in zip((dq, dk, dv), refs, ("dq", "dk", "dv")):
+        g = got[0].double().cpu().numpy()
+        for h in range(ref.shape[1]):
+            scale = float(np.abs(ref[:, h]).max())
+            assert np.abs(g[:, h] - ref[:, h]).max() <= 2e-2 * scale, f"{name} head {h}"

@@ -139,7 +139,9 @@ def test_backward_host_validation(ps):
     # rotated Q (1 x 300 x 4 x 128 bf16), rotated K, {LSE, D} pairs over 384 padded rows
     assert need >= 300 * 4 * 128 * 2 + 300 * 2 * 128 * 2 + 4 * 384 * 8
     assert lib.ps_prefill_backward_workspace_size(1, 300, 4, 3, 128, ctypes.byref(b)) == 1  # Hq % Hkv
-    assert lib.ps_prefill_backward_workspace_size(1, 300, 4, 2, 64, ctypes.byref(b)) == 2   # head_dim
+    assert lib.ps_prefill_backward_workspace_size(1, 300, 4, 2, 96, ctypes.byref(b)) == 2   # head_dim
+    assert lib.ps_prefill_backward_workspace_size(1, 300, 4, 2, 64, ctypes.byref(b)) == 0
+    assert lib.ps_prefill_backward_workspace_size(1, 300, 4, 2, 128, ctypes.byref(b)) == 0
     assert lib.ps_prefill_backward_workspace_size(0, 300, 4, 2, 128, ctypes.byref(b)) == 1
     fake = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: validation fails first
     odd = ctypes.c_void_p((1 << 20) + 2)
@@ -154,7 +156,7 @@ def test_backward_host_validation(ps):
     assert call(q=None) == 1          # null pointer
     assert call(W=0) == 1             # window < 1
     assert call(scale=0.0) == 1       # scale must be positive
-    assert call(hd=64) == 2           # head_dim 128 only
+    assert call(hd=96) == 2           # head_dim 64 or 128 only
     assert call(q=odd) == 3           # 16-byte alignment
     assert call(ws=None) == 4         # no workspace
     assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == 4  # workspace not 256-byte aligned
@@ -186,3 +188,11 @@ def test_prefill_position_encoding_validation(ps):
     ring.pe_mode = 1
     assert call(0, ring) == 1                            # ring is Reset PE
     assert call(1, ring) == 4                            # consistent: fails later, on the workspace
+
+
+def test_prefill_head_dims(ps):
+    b = ctypes.c_size_t()
+    assert ps.lib.ps_prefill_workspace_size(1, 300, 4, 2, 64, 0, 0, ctypes.byref(b)) == 0
+    assert b.value >= 300 * 4 * 64 * 2 + 300 * 2 * 64 * 2
+    assert ps.lib.ps_prefill_workspace_size(1, 300, 4, 2, 96, 0, 0, ctypes.byref(b)) == 2
+    assert ps.lib.ps_prefill_workspace_size(1, 300, 4, 2, 256, 0, 0, ctypes.byref(b)) == 2
