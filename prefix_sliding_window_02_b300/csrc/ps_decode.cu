@@ -8,8 +8,11 @@
 // decode).  The step is a memory-bound GEMV, so it runs on CUDA cores.
 //
 // Work split ("stream-K" over tiles): the (sequence, kv head) segments are laid
-// end to end as 16-slot tiles, N tiles in all; warp w of NW owns tiles
-// [w*N/NW, (w+1)*N/NW), whatever the sequence lengths.  Each warp streams its
+// end to end as 16-slot tiles, N tiles in all; warp w of the first NWe warps
+// owns tiles [w*N/NWe, (w+1)*N/NWe), whatever the sequence lengths, where
+// NWe = min(NW, ceil(N / kMinTilesPerWarp)): a short batch uses fewer warps, each
+// with a few tiles in flight, rather than one tile on every warp of the grid and
+// as many partial records to merge.  Each warp streams its
 // tiles through a private STAGES-deep TMA ring in shared memory and writes
 // one partial (unnormalised O, running max, running sum) per segment piece
 // it touches.  Piece (warp w, segment sg) goes to record w + sg, which is
@@ -29,6 +32,13 @@
 namespace ps {
 
 constexpr int kDecTile = 16;  // slots per tile
+constexpr int kMinTilesPerWarp = 4;
+
+// Warps that take tiles: all NW of the grid, or fewer for a short tile line.
+__host__ __device__ __forceinline__ int64_t working_warps(int64_t N, int64_t NW) {
+  const int64_t need = (N + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
+  return need < NW ? need : NW;
+}
 
 struct DecodeParams {
   CUtensorMap tmk;  // 3D {D, Hkv, total_slots}, box {D, 1, kDecTile}
@@ -172,10 +182,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     for (int i = threadIdx.x; i <= p.nseq; i += blockDim.x) p.seg_tiles[i] = pfx[i];
 
   const int64_t N = (int64_t)pfx[p.nseq] * p.hkv;
-  const int64_t NW = p.nwarps_total;
+  const int64_t NWe = working_warps(N, p.nwarps_total);
   const int w = blockIdx.x * WARPS + warp;
-  const int64_t lo = N * w / NW, hi = N * (w + 1) / NW;
-  if (lo >= hi) return;  // no block-wide barrier follows
+  if (w >= NWe) return;  // no block-wide barrier follows
+  const int64_t lo = N * w / NWe, hi = N * (w + 1) / NWe;  // never empty: N >= NWe
 
   uint8_t* my_tiles = tiles + warp * STAGES * S::STAGE_BYTES;
   uint64_t* my_bars = bars + warp * STAGES;
@@ -418,68 +428,90 @@ struct CombineParams {
   int32_t nseq, hq, hkv, nwarps_total;
 };
 
-// One warp per (sequence, query head): merge the partial softmax records of the
-// warps that covered its segment, first to last, in one pass with a running
-// maximum.  The cost is one record per warp that touched the segment, never a
-// scan over the warps that did not.
+// One CTA of eight warps per (sequence, query head): merge the partial softmax
+// records of the warps that covered its segment, its first through last warp
+// as the partial kernel recorded them (every working warp owns at least one
+// tile, so each of them wrote a record).  The warps take an eighth of the
+// records each, read them eight at a time (loads first, then the
+// running-maximum merges), and merge their results through shared memory, so a
+// segment spread over many warps (a short batch) costs a few load latencies,
+// not one per record.
+constexpr int kCombineWarps = 8;
+
 template <int D, int G>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ CombineParams p) {
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    decode_combine_kernel(const __grid_constant__ CombineParams p) {
   using S = DecShape<D, G>;
-  constexpr int EPL = S::EPL;
-  const int lane = threadIdx.x & 31;
+  constexpr int EPL = S::EPL, NWARP = kCombineWarps, U = 8;
+  __shared__ float sm_m[NWARP], sm_l[NWARP];
+  __shared__ float sm_a[NWARP][D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dependency_wait();  // the partial records come from the previous kernel
   allow_dependents();
-  const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int64_t gw = blockIdx.x;  // (sequence, query head)
   if (gw >= (int64_t)p.nseq * p.hq) return;
   const int s = (int)(gw / p.hq), hq = (int)(gw % p.hq);
   const int h = hq / G, gg = hq % G;
   const int32_t nt = p.seg_tiles[s + 1] - p.seg_tiles[s];
   __nv_bfloat16* o = p.out + gw * D + lane * EPL;
   if (nt == 0) {  // sequence rejected by the device checks
+    if (warp == 0) {
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] = __float2bfloat16_rn(0.f);
-    if (lane == 0) p.lse[gw] = -INFINITY;
+      for (int e = 0; e < EPL; ++e) o[e] = __float2bfloat16_rn(0.f);
+      if (lane == 0) p.lse[gw] = -INFINITY;
+    }
     return;
   }
   const int64_t sg = (int64_t)s * p.hkv + h;
-  const int64_t N = (int64_t)p.seg_tiles[p.nseq] * p.hkv;
-  const int64_t NW = p.nwarps_total;
+  const int w0 = p.seg_warps[2 * sg];
+  const int R = p.seg_warps[2 * sg + 1] - w0 + 1;
+  const int k_lo = R * warp / NWARP, k_hi = R * (warp + 1) / NWARP;
   float M = -INFINITY, l = 0.f, a[EPL] = {};
-  auto merge = [&](int w) {
-    const float* r = p.rec + (size_t)(w + sg) * S::REC;
-    const float mw = r[G * D + gg], lw = r[G * D + G + gg];
-    float aw[EPL];
+  for (int k0 = k_lo; k0 < k_hi; k0 += U) {
+    float mw[U], lw[U], aw[U][EPL];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) aw[e] = r[gg * D + lane * EPL + e];
-    const float mn = fmaxf(M, mw);
-    const float f_old = fast_exp2(M - mn), f_new = fast_exp2(mw - mn);
-    l = l * f_old + lw * f_new;
+    for (int u = 0; u < U; ++u) {
+      const float* r = p.rec + (size_t)(w0 + min(k0 + u, k_hi - 1) + sg) * S::REC;
+      mw[u] = r[G * D + gg];
+      lw[u] = r[G * D + G + gg];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) a[e] = a[e] * f_old + aw[e] * f_new;
-    M = mn;
-  };
-  if (N >= NW) {
-    // every warp owns at least one tile: the segment's records are those of
-    // its first through last warp
-    const int w0 = p.seg_warps[2 * sg], w1 = p.seg_warps[2 * sg + 1];
-    for (int w = w0; w <= w1; ++w) merge(w);
-  } else {
-    // fewer tiles than warps: each warp owns at most one tile, so the records
-    // are one per tile.  Warp w owns tiles [floor(N w / NW), floor(N (w+1) / NW)),
-    // so tile g belongs to w(g) = floor(((g + 1) NW - 1) / N); the lanes find the
-    // owners of 32 tiles at a time.
-    const int64_t g0 = (int64_t)p.seg_tiles[s] * p.hkv + (int64_t)h * nt;
-    for (int t0 = 0; t0 < nt; t0 += 32) {
-      int wl = 0;
-      if (t0 + lane < nt) wl = (int)(((g0 + t0 + lane + 1) * NW - 1) / N);
-      const int cnt = min(32, nt - t0);
-      for (int i = 0; i < cnt; ++i) merge(__shfl_sync(0xffffffffu, wl, i));
+      for (int e = 0; e < EPL; ++e) aw[u][e] = r[gg * D + lane * EPL + e];
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (k0 + u >= k_hi) break;
+      const float mn = fmaxf(M, mw[u]);
+      const float f_old = fast_exp2(M - mn), f_new = fast_exp2(mw[u] - mn);
+      l = l * f_old + lw[u] * f_new;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) a[e] = a[e] * f_old + aw[u][e] * f_new;
+      M = mn;
     }
   }
-  const float inv = 1.f / l;
+  if (lane == 0) {
+    sm_m[warp] = M;
+    sm_l[warp] = l;
+  }
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) o[e] = __float2bfloat16_rn(a[e] * inv);
-  if (lane == 0) p.lse[gw] = (M + log2f(l)) * 0.69314718055994530942f;
+  for (int e = 0; e < EPL; ++e) sm_a[warp][lane * EPL + e] = a[e];
+  __syncthreads();
+  if (warp != 0) return;
+  float Mt = sm_m[0];
+#pragma unroll
+  for (int x = 1; x < NWARP; ++x) Mt = fmaxf(Mt, sm_m[x]);
+  float lt = 0.f, at[EPL] = {};
+#pragma unroll
+  for (int x = 0; x < NWARP; ++x) {
+    if (sm_m[x] == -INFINITY) continue;  // a warp with no records
+    const float f = fast_exp2(sm_m[x] - Mt);
+    lt += sm_l[x] * f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) at[e] += sm_a[x][lane * EPL + e] * f;
+  }
+  const float inv = 1.f / lt;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) o[e] = __float2bfloat16_rn(at[e] * inv);
+  if (lane == 0) p.lse[gw] = (Mt + log2f(lt)) * 0.69314718055994530942f;
 }
 
 // ----------------------------------------------------------------- host ----
@@ -661,7 +693,7 @@ extern "C" ps_status_t ps_decode_combine(const ps_cache_desc* cache, int32_t n_q
   c.hkv = cache->n_kv_heads;
   c.nwarps_total = pl.nwarps;
   const int64_t warps = (int64_t)nseq * n_q_heads;
-  if (launch_dependent(pl.combine, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0,
+  if (launch_dependent(pl.combine, dim3((unsigned)warps), dim3(kCombineWarps * 32), 0,
                        (cudaStream_t)stream, c) != cudaSuccess)
     return PS_ERR_CUDA;
   return launch_status();
