@@ -279,6 +279,10 @@ ps_status_t ps_prefill_backward_workspace_size(int32_t batch, int32_t seqlen, in
  *     to ps_prefill (without a ring; q_start within [0, 2^31 - 1 - seqlen], not
  *     checked here); out (bf16 [batch, seqlen, n_q_heads, head_dim]) and lse
  *     (fp32 [batch, n_q_heads, seqlen]) are its results; d_out: bf16 like out.
+ *   fwd_workspace : NULL, or the workspace of that ps_prefill call (Continue
+ *     PE, no ring, same arguments), still holding the rotated Q and K it wrote
+ *     at its start; the backward then reads them from there instead of
+ *     rotating Q and K again (256-byte aligned; only read).
  *   dq : device fp32 [batch, seqlen, n_q_heads, head_dim], gradient of raw q;
  *   dk, dv : device fp32 [batch, seqlen, n_kv_heads, head_dim] (summed over the
  *     query heads of each group).  The rotation is differentiated exactly; the
@@ -299,9 +303,10 @@ ps_status_t ps_prefill_backward(const void* q, const void* k, const void* v, con
                                 const float* lse, const void* d_out, int32_t batch,
                                 int32_t seqlen, const int32_t* q_start, const int32_t* prefix_len,
                                 int32_t window, int32_t n_q_heads, int32_t n_kv_heads,
-                                int32_t head_dim, float scale, double rope_theta, float* dq,
-                                float* dk, float* dv, void* workspace, size_t workspace_bytes,
-                                int32_t* status, void* stream);
+                                int32_t head_dim, float scale, double rope_theta,
+                                const void* fwd_workspace, float* dq, float* dk, float* dv,
+                                void* workspace, size_t workspace_bytes, int32_t* status,
+                                void* stream);
 
 /*
  * Tile geometry used by ps_prefill for one batch row: nq x nk tiles of

@@ -293,8 +293,10 @@ def prefill_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: tor
                      lse: torch.Tensor, d_out: torch.Tensor, q_start: torch.Tensor,
                      prefix_len: torch.Tensor, window: int, scale: Optional[float] = None,
                      rope_theta: float = 10000.0, status: Optional[torch.Tensor] = None,
-                     stream=None):
-    """ps_prefill_backward: returns fp32 (dq [B,S,Hq,D], dk, dv [B,S,Hkv,D])."""
+                     stream=None, fwd_workspace: Optional[torch.Tensor] = None):
+    """ps_prefill_backward: returns fp32 (dq [B,S,Hq,D], dk, dv [B,S,Hkv,D]).
+    ``fwd_workspace``: the workspace the forward ps_prefill call (no ring, Continue PE,
+    same arguments) used, to reuse its rotated Q and K."""
     B, S, hq, D, hkv = _check_prefill_shapes(q, k, v, q_start, prefix_len)
     _shape(out, q.shape, "out")
     _shape(d_out, q.shape, "d_out")
@@ -302,6 +304,11 @@ def prefill_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: tor
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (d_out, "d_out")):
         _need(t, BF16, n)
     _need(lse, torch.float32, "lse")
+    if fwd_workspace is not None:
+        need = prefill_workspace_size(B, S, hq, hkv, D)
+        if fwd_workspace.numel() < need or not fwd_workspace.is_cuda:
+            raise ValueError(f"fwd_workspace: expected a CUDA buffer of at least {need} bytes "
+                             "from the forward call")
     _need(q_start, torch.int32, "q_start")
     _need(prefix_len, torch.int32, "prefix_len")
     if scale is None:
@@ -315,9 +322,9 @@ def prefill_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: tor
     ws = torch.empty(b.value, dtype=torch.uint8, device=q.device)
     check(lib.ps_prefill_backward(_vp(q), _vp(k), _vp(v), _vp(out), _vp(lse), _vp(d_out), B, S,
                                   _vp(q_start), _vp(prefix_len), window, hq, hkv, D,
-                                  ctypes.c_float(scale), ctypes.c_double(rope_theta), _vp(dq),
-                                  _vp(dk), _vp(dv), _vp(ws), ws.numel(), _vp(status),
-                                  _stream(stream)), "ps_prefill_backward")
+                                  ctypes.c_float(scale), ctypes.c_double(rope_theta),
+                                  _vp(fwd_workspace), _vp(dq), _vp(dk), _vp(dv), _vp(ws), ws.numel(),
+                                  _vp(status), _stream(stream)), "ps_prefill_backward")
     return dq, dk, dv
 
 

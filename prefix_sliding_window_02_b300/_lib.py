@@ -82,7 +82,8 @@ def _load():
         "ps_prefill_backward_workspace_size": (ctypes.c_int, [i32, i32, i32, i32, i32,
                                                               ctypes.POINTER(sz)]),
         "ps_prefill_backward": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32,
-                                               i32, i32, f32, f64, vp, vp, vp, vp, sz, vp, vp]),
+                                               i32, i32, f32, f64, vp, vp, vp, vp, vp, sz, vp,
+                                               vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

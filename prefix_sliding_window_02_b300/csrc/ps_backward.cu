@@ -187,6 +187,7 @@ struct PrepParams {
   float2* ld;       // [B, Hq, s_pad]
   const int32_t* q_start;
   int32_t B, S, s_pad, hq, hkv;
+  int32_t rotate;  // 0: the forward's rotated Q and K are reused, only D is computed
   RopeTurns turns;
 };
 
@@ -202,10 +203,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ P
   grid_dependency_wait();
   allow_dependents();
   const int64_t n_rows = (int64_t)p.B * p.S;
-  const int heads = p.hq + p.hkv;
+  const int heads = p.rotate ? p.hq + p.hkv : 0;
   for (int64_t r0 = (int64_t)blockIdx.x * kPrepRows; r0 < n_rows;
        r0 += (int64_t)gridDim.x * kPrepRows) {
-    for (int t = threadIdx.x; t < kPrepRows * NPAIR; t += blockDim.x) {
+    for (int t = threadIdx.x; t < (p.rotate ? kPrepRows * NPAIR : 0); t += blockDim.x) {
       const int rr = t / NPAIR, i = t % NPAIR;
       const int64_t r = r0 + rr;
       if (r < n_rows) {
@@ -870,8 +871,9 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
                                            const int32_t* prefix_len, int32_t window,
                                            int32_t n_q_heads, int32_t n_kv_heads,
                                            int32_t head_dim, float scale, double rope_theta,
-                                           float* dq, float* dk, float* dv, void* workspace,
-                                           size_t workspace_bytes, int32_t* status, void* stream) {
+                                           const void* fwd_workspace, float* dq, float* dk,
+                                           float* dv, void* workspace, size_t workspace_bytes,
+                                           int32_t* status, void* stream) {
   if (!q || !k || !v || !out || !lse || !d_out || !q_start || !prefix_len || !dq || !dk || !dv)
     return PS_ERR_INVALID_ARGUMENT;
   if (batch < 1 || seqlen < 1 || window < 1 || n_q_heads < 1 || n_kv_heads < 1 ||
@@ -884,6 +886,7 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
   const bwd::Layout L = bwd::layout(batch, seqlen, n_q_heads, n_kv_heads, head_dim);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PS_ERR_WORKSPACE;
   if (workspace_bytes < L.total) return PS_ERR_WORKSPACE;
+  if (fwd_workspace && (reinterpret_cast<uintptr_t>(fwd_workspace) & 255u)) return PS_ERR_WORKSPACE;
   const int32_t nq = (seqlen + bwd::kT - 1) / bwd::kT;
   const int64_t n_dkdv = (int64_t)nq * n_kv_heads * batch;
   const int64_t n_dq = (int64_t)nq * n_q_heads * batch;
@@ -897,8 +900,12 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
   g.o = static_cast<const uint4*>(out);
   g.dout = static_cast<const uint4*>(d_out);
   g.lse = lse;
+  // rotated Q and K: the forward's (same layout at the start of its workspace),
+  // or rotated here into this workspace
+  const uint8_t* qk = fwd_workspace ? static_cast<const uint8_t*>(fwd_workspace) : ws;
   g.qh = reinterpret_cast<uint4*>(ws + L.q_off);
   g.kh = reinterpret_cast<uint4*>(ws + L.k_off);
+  g.rotate = fwd_workspace ? 0 : 1;
   g.ld = reinterpret_cast<float2*>(ws + L.ld_off);
   g.q_start = q_start;
   g.B = batch;
@@ -927,9 +934,9 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
   const uint32_t box[4] = {64u, 1u, (uint32_t)bwd::kT, 1u};
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const bool okm = encode_tmap(&p.tmq, bf, 4, ws + L.q_off, qd, qs, box, sw) &&
+  const bool okm = encode_tmap(&p.tmq, bf, 4, qk + L.q_off, qd, qs, box, sw) &&
                    encode_tmap(&p.tmdo, bf, 4, d_out, qd, qs, box, sw) &&
-                   encode_tmap(&p.tmk, bf, 4, ws + L.k_off, kd, ks, box, sw) &&
+                   encode_tmap(&p.tmk, bf, 4, qk + L.k_off, kd, ks, box, sw) &&
                    encode_tmap(&p.tmv, bf, 4, v, kd, ks, box, sw);
   if (!okm) return PS_ERR_CUDA;
   p.ld = reinterpret_cast<const float2*>(ws + L.ld_off);

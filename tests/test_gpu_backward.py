@@ -141,3 +141,31 @@ def test_training_backward_full_size_sampled():
         if kr:
             _close(dk[b, kr].double().cpu().numpy(), rk, f"dk b={b}")
             _close(dv[b, kr].double().cpu().numpy(), rv, f"dv b={b}")
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_backward_reuses_forward_rotations_bit_exactly(D):
+    """Given the forward's workspace, the backward reads the rotated Q and K the
+    forward left there instead of rotating again: the gradients are the same bits."""
+    import prefix_sliding_window_02_b300 as ps
+    seed, B, S, hq, hkv, P, W, theta = 44, 2, 700, 4, 2, [37, 300], 128, 10000.0
+    pos = np.arange(S)
+    q = np.stack([synth.query_bits(seed, b, pos, hq, D) for b in range(B)])
+    kv = [synth.History(seed, b, hkv, D).rows_bits(pos) for b in range(B)]
+    k = np.stack([x[0] for x in kv])
+    v = np.stack([x[1] for x in kv])
+    do = np.stack([synth.normal_bf16(seed, STREAM_DO, b, pos, hq, D) for b in range(B)])
+    i32 = dict(dtype=torch.int32, device="cuda")
+    tq, tk, tv, tdo = (bits_to_bf16_tensor(x) for x in (q, k, v, do))
+    qs = torch.tensor([0, 50], **i32)
+    pl = torch.tensor(P, **i32)
+    status = torch.zeros(1, **i32)
+    ws = torch.empty(ps.prefill_workspace_size(B, S, hq, hkv, D), dtype=torch.uint8, device="cuda")
+    out, lse = ps.prefill(tq, tk, tv, qs, pl, W, rope_theta=theta, workspace=ws, status=status)
+    a = ps.prefill_backward(tq, tk, tv, out, lse, tdo, qs, pl, W, rope_theta=theta, status=status)
+    b = ps.prefill_backward(tq, tk, tv, out, lse, tdo, qs, pl, W, rope_theta=theta, status=status,
+                            fwd_workspace=ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)

@@ -288,3 +288,37 @@ def test_prefill_head_dim_64_extend_from_ring(ps):
     out, lse = _run(ps, q, k, v, [c0] * B, [P] * B, W, theta, ring=cache)
     _check_rows(seed, out, lse, q, [c0] * B, [P] * B, W, theta, [range(S)] * B, hkv, "D=64 extend")
     assert cache.check_status() == 0
+
+
+def test_prefill_extend_ragged_chunks_through_ring_seq(ps):
+    """Three batch rows extend three of four cached sequences, chosen through
+    ring_seq (not in order), each at its own chunk start and with its own prefix:
+    inside the prefix, just past P + W, and long after (with eviction)."""
+    seed, hq, hkv, D, W, theta, S = 45, 4, 2, 128, 64, 10000.0, 160
+    P_seq = [20, 5, 40, 0]            # prefix of each cached sequence
+    c0_seq = [900, 30, 110, 400]      # positions already cached per sequence
+    cache = ps.RingCache(4, hkv, D, W, P_seq, rope_theta=theta)
+    append_runs(cache, {s: [(0, c0_seq[s])] for s in range(4)}, synth_source(seed, hkv, D))
+    rows = [2, 0, 1]                  # batch row b extends sequence rows[b]
+    c0 = [c0_seq[s] for s in rows]
+    P = [P_seq[s] for s in rows]
+    B = len(rows)
+    q = np.stack([synth.query_bits(seed, s, np.arange(c0[b], c0[b] + S), hq, D)
+                  for b, s in enumerate(rows)])
+    kv = [synth.History(seed, s, hkv, D).rows_bits(np.arange(c0[b], c0[b] + S))
+          for b, s in enumerate(rows)]
+    k = np.stack([x[0] for x in kv])
+    v = np.stack([x[1] for x in kv])
+    i32 = dict(dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, **i32)
+    out, lse = ps.prefill(bits_to_bf16_tensor(q), bits_to_bf16_tensor(k), bits_to_bf16_tensor(v),
+                          torch.tensor(c0, **i32), torch.tensor(P, **i32), W, rope_theta=theta,
+                          ring=cache, ring_seq=torch.tensor(rows, **i32), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and cache.check_status() == 0
+    for b, s in enumerate(rows):
+        hist = synth.History(seed, s, hkv, D)
+        for r in range(S):
+            o_ref, l_ref = attend(synth.bits_to_f64(q[b, r]), c0[b] + r, P[b], W, hist.rows, theta)
+            assert_attention_close(bf16_tensor_to_f64(out[b, r]), lse[b, :, r].cpu().numpy(), o_ref,
+                                   l_ref, f"b={b} (sequence {s}) row={r}")

@@ -148,10 +148,10 @@ def test_backward_host_validation(ps):
     i32 = ctypes.c_void_p(1 << 21)
     f = ctypes.c_void_p(1 << 22)
 
-    def call(q=fake, W=64, hd=128, ws=fake, ws_bytes=need, dq=f, scale=0.088):
+    def call(q=fake, W=64, hd=128, ws=fake, ws_bytes=need, dq=f, scale=0.088, fwd=None):
         return lib.ps_prefill_backward(q, fake, fake, fake, f, fake, 1, 300, i32, i32, W, 4, 2, hd,
-                                       ctypes.c_float(scale), ctypes.c_double(1e4), dq, f, f, ws,
-                                       ws_bytes, None, None)
+                                       ctypes.c_float(scale), ctypes.c_double(1e4), fwd, dq, f, f,
+                                       ws, ws_bytes, None, None)
 
     assert call(q=None) == 1          # null pointer
     assert call(W=0) == 1             # window < 1
@@ -161,6 +161,7 @@ def test_backward_host_validation(ps):
     assert call(ws=None) == 4         # no workspace
     assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == 4  # workspace not 256-byte aligned
     assert call(ws_bytes=need - 1) == 4  # workspace too small
+    assert call(fwd=ctypes.c_void_p((1 << 20) + 16)) == 4  # forward workspace not 256-byte aligned
 
 
 def test_prefill_position_encoding_validation(ps):
