@@ -234,12 +234,14 @@ def run_decode(ps, torch, cache, q, k, v, pos, steps, warmup, dist=None, per_ker
     stream = torch.cuda.current_stream()
 
     def step(i, evs=None):
+        if evs is None:  # the step: ps_decode_append (fused append, partial, combine)
+            cache.decode_append(q[i], k[i], v[i], pos[i], out=out, lse=lse, workspace=ws)
+            return
+        # the same step as three calls, with events around the partial kernel alone
         cache.append_tokens(pos[i], k[i], v[i])
-        if evs is not None:
-            evs[0].record(stream)
+        evs[0].record(stream)
         cache.decode_partial(q[i], pos[i], workspace=ws)
-        if evs is not None:
-            evs[1].record(stream)
+        evs[1].record(stream)
         cache.decode_combine(out, lse, workspace=ws)
 
     for i in range(warmup):
@@ -774,7 +776,7 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "breakdown_median": parts,
                "how": "per step: one pinned host -> device copy of the packed q, k, v, pos; "
-                      "DecodeGraph replay (ps_kv_append + ps_decode captured in a CUDA graph); "
+                      "DecodeGraph replay (ps_decode_append captured in a CUDA graph); "
                       "one device -> host copy of the packed O and LSE; stream sync; host wall clock"}
     del cache, q, k, v
     torch.cuda.empty_cache()
@@ -833,7 +835,8 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (N(0,1) bf16 K/V/Q, random-init)",
         "config": {"workload": "steady decode: 64 sequences at position 131072+step, P uniform "
                                "64..512, W 4096, Hq 16 / Hkv 8, D 128, one layer per step "
-                               "(append + split-KV partial + combine)",
+                               "(ps_decode_append: the new token's append inside the split-KV "
+                               "partial kernel, then the combine)",
                    "layers_for_model_rate": LAYERS, "l2": "inputs larger than L2 "
                    f"({kv_bytes / 1e9:.2f} GB of K/V read per step vs 126 MB L2)",
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
@@ -851,7 +854,7 @@ def main():
         "small_batch_decode": small,
         "comparators": comparators,
         "full_causal": full, "e2e": e2e,
-        "gpu_launches": 3 * args.steps, "clocks": clk, "cpu_baseline": cpu,
+        "gpu_launches": 2 * args.steps, "clocks": clk, "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

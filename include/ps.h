@@ -187,6 +187,25 @@ ps_status_t ps_decode_combine(const ps_cache_desc* cache, int32_t n_q_heads, voi
                               const void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * ps_decode_append: one whole decode step in one call, the equivalent of
+ * ps_kv_append of one token per sequence (run s: sequence s, position pos[s])
+ * followed by ps_decode with the same positions, without the separate append
+ * launch.  The warp whose tile holds a sequence's new slot finds the slot's
+ * previous occupant there; it puts the new token's K, rotated at pos[s] with
+ * the same arithmetic as ps_kv_append, and its V in its place, in the tile it
+ * reads and in the pool, so the cache afterwards holds the same bits as after
+ * the two separate calls, and out / lse are the same bits too.
+ *   k, v : device bf16 [nseq, n_kv_heads, head_dim], raw (un-rotated) K and V of
+ *          the new tokens, 16-byte aligned.
+ *   Other arguments, workspace and errors: as ps_decode.  A sequence the device
+ *   checks refuse is neither appended nor attended (out 0, lse -inf).
+ */
+ps_status_t ps_decode_append(const ps_cache_desc* cache, const void* q, const void* k,
+                             const void* v, const int32_t* pos, int32_t n_q_heads, float scale,
+                             void* out, float* lse, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/*
  * ps_decode_noalloc: ps_decode without a caller-supplied workspace, for
  * callers that cannot allocate device memory when they decode -- a host that
  * has no allocator of its own (plain C linking this library), code that runs

@@ -181,6 +181,34 @@ class RingCache:
                             _vp(out), _vp(lse), _vp(ws), ws.numel(), _stream(stream)), "ps_decode")
         return out, lse
 
+    def decode_append(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, pos: torch.Tensor,
+                      scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                      stream=None):
+        """ps_decode_append: append one token per sequence (k, v [nseq, Hkv, D] raw at
+        pos) and decode q [nseq, Hq, D] at the same positions, in one call."""
+        hq = self._check_q(q, pos)
+        _shape(k, (self.nseq, self.n_kv_heads, self.head_dim), "k")
+        _shape(v, (self.nseq, self.n_kv_heads, self.head_dim), "v")
+        if out is not None:
+            _shape(out, q.shape, "out")
+        if lse is not None:
+            _shape(lse, (self.nseq, hq), "lse")
+        for t, n in ((q, "q"), (k, "k"), (v, "v")):
+            _need(t, BF16, n)
+        _need(pos, torch.int32, "pos")
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.head_dim)
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty(q.shape[0], hq, dtype=torch.float32, device=q.device)
+        ws = self.workspace(hq) if workspace is None else workspace
+        check(lib.ps_decode_append(ctypes.byref(self.desc), _vp(q), _vp(k), _vp(v), _vp(pos), hq,
+                                   ctypes.c_float(scale), _vp(out), _vp(lse), _vp(ws), ws.numel(),
+                                   _stream(stream)), "ps_decode_append")
+        return out, lse
+
     def decode_partial(self, q: torch.Tensor, pos: torch.Tensor, scale: Optional[float] = None,
                        workspace: Optional[torch.Tensor] = None, stream=None) -> None:
         """ps_decode_partial: the K/V-streaming launch of ps_decode."""
@@ -329,14 +357,15 @@ def prefill_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: tor
 
 
 class DecodeGraph:
-    """One decode step of a RingCache (ps_kv_append of one token per sequence, then
-    ps_decode) captured once in a CUDA graph over fixed device buffers.
+    """One decode step of a RingCache (ps_decode_append: one new token per sequence
+    appended and attended in one call) captured once in a CUDA graph over fixed
+    device buffers.
 
     The step's inputs live in one packed device buffer ``inp`` (views ``q`` [nseq, Hq,
     D], ``k``, ``v`` [nseq, Hkv, D] bf16 raw, ``pos`` [nseq] int32) and its results in
     one packed buffer ``res`` (views ``out`` [nseq, Hq, D] bf16, ``lse`` [nseq, Hq]
     fp32), so a caller moves a step's data with one copy each way; ``replay()``
-    launches the three kernels of the step from the graph.  ``in_layout`` /
+    launches the two kernels of the step from the graph.  ``in_layout`` /
     ``res_layout`` give (offset, nbytes) of each view, for packing host buffers the
     same way.  The graph keeps the cache, its workspace and these buffers alive.
     """
@@ -378,9 +407,8 @@ class DecodeGraph:
         self.graph = torch.cuda.CUDAGraph()
         # relaxed: the decode call queries occupancy and sets kernel attributes on the host
         with torch.cuda.graph(self.graph, capture_error_mode="relaxed"):
-            cache.append(self._seq, self.pos, self._cu, self.k, self.v)
-            cache.decode(self.q, self.pos, scale=scale, out=self.out, lse=self.lse,
-                         workspace=self._ws)
+            cache.decode_append(self.q, self.k, self.v, self.pos, scale=scale, out=self.out,
+                                lse=self.lse, workspace=self._ws)
 
     def replay(self) -> None:
         """Append the step's tokens and decode them (asynchronous, current stream)."""

@@ -23,7 +23,7 @@ PS_DEV_BAD_SEQ = 0x20
 
 EXPORTS = (
     "ps_status_string", "ps_ring_slots", "ps_kv_append", "ps_decode_workspace_size",
-    "ps_decode", "ps_decode_partial", "ps_decode_combine", "ps_decode_noalloc",
+    "ps_decode", "ps_decode_partial", "ps_decode_combine", "ps_decode_noalloc", "ps_decode_append",
     "ps_prefill_workspace_size", "ps_prefill", "ps_prefill_tile_grid", "ps_prefill_tile_classes",
     "ps_prefill_backward_workspace_size", "ps_prefill_backward",
     "ps_check_device_status", "ps_device_code_version", "ps_test_force_wait_timeout",
@@ -69,6 +69,7 @@ def _load():
         "ps_decode_partial": (ctypes.c_int, [pdesc, vp, vp, i32, f32, vp, sz, vp]),
         "ps_decode_combine": (ctypes.c_int, [pdesc, i32, vp, vp, vp, sz, vp]),
         "ps_decode_noalloc": (ctypes.c_int, [pdesc, vp, vp, i32, f32, vp, vp, vp]),
+        "ps_decode_append": (ctypes.c_int, [pdesc, vp, vp, vp, vp, i32, f32, vp, vp, vp, sz, vp]),
         "ps_prefill_workspace_size": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, i32,
                                                      ctypes.POINTER(sz)]),
         "ps_prefill": (ctypes.c_int, [vp, vp, vp, i32, i32, vp, vp, i32, i32, i32, i32, f32, f64,

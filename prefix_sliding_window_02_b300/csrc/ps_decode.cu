@@ -28,6 +28,7 @@
 // per scheduler) keep the scheduler busy while one warp waits on shared
 // memory or shuffles.
 #include "ps_internal.h"
+#include "ps_rope.cuh"
 
 namespace ps {
 
@@ -44,6 +45,10 @@ struct DecodeParams {
   CUtensorMap tmk;  // 3D {D, Hkv, total_slots}, box {D, 1, kDecTile}
   CUtensorMap tmv;
   const __nv_bfloat16* q;  // [nseq, Hq, D]
+  const __nv_bfloat16* k_new;  // [nseq, Hkv, D] raw K of the new tokens (fused append), or null
+  const __nv_bfloat16* v_new;  // [nseq, Hkv, D]
+  __nv_bfloat16* k_pool;       // the pools, written by the fused append
+  __nv_bfloat16* v_pool;
   const int32_t* pos;
   const int32_t* prefix_len;
   int32_t* status;
@@ -220,6 +225,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
   uint32_t parity = 0;  // bit st = parity expected next on stage st
   float qf[G][EPL], qr[G][EPL], acc[G][EPL], m[NPASS], lsum[NPASS];
   int cur_L = 0;
+  int cur_slot = -1;      // fused append: the new token's slot in the current sequence
+  float kc[EPL], ksn[EPL];  // fused append: (cos, sin) of this lane's pairs at pos[s]
   int32_t seg_P = 0;      // prefix length of the current sequence
   bool seg_reset = false; // Reset PE changes this sequence's prefix scores
   bool ok = true;
@@ -253,6 +260,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
           const int i = (lane & 15) * EPL + e;
           float c, sn;
           rope_cos_sin(ppos, p.turns.f[i], c, sn);
+          kc[e] = c;
+          ksn[e] = sn;
           const float y = (lane < 16) ? (x[e] * c - partner * sn) : (x[e] * c + partner * sn);
           // rotated Q is rounded to bf16, as the cache stores rotated K
           qf[gg][e] = __bfloat162float(__float2bfloat16_rn(y)) * p.scale_log2;
@@ -270,6 +279,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         m[ps_] = -INFINITY;
         lsum[ps_] = 0.f;
       }
+      cur_slot = p.k_new ? ring_slot(ppos, seg_P, p.window) : -1;
     }
 
     // the lanes decide together: shuffles and the drain below need the whole warp
@@ -279,6 +289,46 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     }
     parity ^= 1u << st;
     consumed = cur.g + 1;
+
+    // Fused append (ps_decode_append): the tile holding the new token's slot
+    // came with the slot's previous occupant.  Put the new token's K (rotated
+    // at pos[s] exactly as ps_kv_append does) and V in its place, in the tile
+    // and in the pool; this warp is the only reader of this head's part of
+    // that row in this launch.
+    if (cur_slot >= 0 && t == cur_slot / TS) {
+      const int64_t src = ((int64_t)s * p.hkv + h) * D + lane * EPL;
+      float x[EPL];
+      load_row_f32<EPL>(reinterpret_cast<const uint8_t*>(p.k_new + src), x);
+      float rk[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const float partner = __shfl_xor_sync(0xffffffffu, x[e], 16);
+        rk[e] = lane < 16 ? rope_first(x[e], partner, kc[e], ksn[e])
+                          : rope_second(partner, x[e], kc[e], ksn[e]);
+      }
+      uint32_t kw[EPL / 2], vw[EPL / 2];
+#pragma unroll
+      for (int e = 0; e < EPL / 2; ++e) {
+        kw[e] = pack_bf16(rk[2 * e], rk[2 * e + 1]);
+        vw[e] = reinterpret_cast<const uint32_t*>(p.v_new + src)[e];
+      }
+      uint8_t* ks = my_tiles + st * S::STAGE_BYTES + (cur_slot % TS) * (D * 2) + lane * (EPL * 2);
+      const int64_t row = p.map.row(s, cur_slot);
+#pragma unroll
+      for (int e = 0; e < EPL / 2; ++e) {
+        reinterpret_cast<uint32_t*>(ks)[e] = kw[e];
+        reinterpret_cast<uint32_t*>(ks + S::TILE_BYTES)[e] = vw[e];
+      }
+      if (row >= 0) {
+        const int64_t dst = (row * p.hkv + h) * D + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL / 2; ++e) {
+          reinterpret_cast<uint32_t*>(p.k_pool + dst)[e] = kw[e];
+          reinterpret_cast<uint32_t*>(p.v_pool + dst)[e] = vw[e];
+        }
+      }
+      __syncwarp();
+    }
 
     const uint8_t* kt = my_tiles + st * S::STAGE_BYTES;
     const uint8_t* vt = kt + S::TILE_BYTES;
@@ -630,14 +680,18 @@ static float* records_of(void* ws, int nseq, int hkv) {
                                   align256((size_t)nseq * hkv * 2 * 4));
 }
 
-extern "C" ps_status_t ps_decode_partial(const ps_cache_desc* cache, const void* q,
-                                         const int32_t* pos, int32_t n_q_heads, float scale,
-                                         void* workspace, size_t workspace_bytes, void* stream) {
+// The partial launch, with (k_new, v_new) the fused append's new tokens or null.
+static ps_status_t decode_partial(const ps_cache_desc* cache, const void* q, const void* k_new,
+                                  const void* v_new, const int32_t* pos, int32_t n_q_heads,
+                                  float scale, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
   if (!q || !pos || !(scale > 0.f)) return PS_ERR_INVALID_ARGUMENT;
   DecPlan pl;
   ps_status_t st = prepare_decode(cache, n_q_heads, workspace, workspace_bytes, &pl);
   if (st != PS_OK) return st;
   if (!aligned16(q)) return PS_ERR_ALIGNMENT;
+  if ((k_new || v_new) && (!k_new || !v_new)) return PS_ERR_INVALID_ARGUMENT;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PS_ERR_ALIGNMENT;
   const int D = cache->head_dim, hkv = cache->n_kv_heads, nseq = cache->nseq;
   DecodeParams p;
   const uint64_t dims[3] = {(uint64_t)D, (uint64_t)hkv, (uint64_t)cache->total_slots};
@@ -649,6 +703,10 @@ extern "C" ps_status_t ps_decode_partial(const ps_cache_desc* cache, const void*
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return PS_ERR_CUDA;
   p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  p.k_pool = static_cast<__nv_bfloat16*>(cache->k_pool);
+  p.v_pool = static_cast<__nv_bfloat16*>(cache->v_pool);
   p.pos = pos;
   p.prefix_len = cache->prefix_len;
   p.status = cache->status;
@@ -671,6 +729,13 @@ extern "C" ps_status_t ps_decode_partial(const ps_cache_desc* cache, const void*
                        (cudaStream_t)stream, p) != cudaSuccess)
     return PS_ERR_CUDA;
   return launch_status();
+}
+
+extern "C" ps_status_t ps_decode_partial(const ps_cache_desc* cache, const void* q,
+                                         const int32_t* pos, int32_t n_q_heads, float scale,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_partial(cache, q, nullptr, nullptr, pos, n_q_heads, scale, workspace,
+                        workspace_bytes, stream);
 }
 
 extern "C" ps_status_t ps_decode_combine(const ps_cache_desc* cache, int32_t n_q_heads, void* out,
@@ -705,6 +770,17 @@ extern "C" ps_status_t ps_decode(const ps_cache_desc* cache, const void* q, cons
   if (!out || !lse) return PS_ERR_INVALID_ARGUMENT;
   ps_status_t st = ps_decode_partial(cache, q, pos, n_q_heads, scale, workspace, workspace_bytes,
                                      stream);
+  if (st != PS_OK) return st;
+  return ps_decode_combine(cache, n_q_heads, out, lse, workspace, workspace_bytes, stream);
+}
+
+extern "C" ps_status_t ps_decode_append(const ps_cache_desc* cache, const void* q, const void* k,
+                                        const void* v, const int32_t* pos, int32_t n_q_heads,
+                                        float scale, void* out, float* lse, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (!out || !lse || !k || !v) return PS_ERR_INVALID_ARGUMENT;
+  ps_status_t st = decode_partial(cache, q, k, v, pos, n_q_heads, scale, workspace,
+                                  workspace_bytes, stream);
   if (st != PS_OK) return st;
   return ps_decode_combine(cache, n_q_heads, out, lse, workspace, workspace_bytes, stream);
 }

@@ -7,6 +7,7 @@
 // they are appended, and never again (Continue PE, agihunt.info paragraph on
 // position encodings).
 #include "ps_internal.h"
+#include "ps_rope.cuh"
 
 namespace ps {
 
@@ -132,8 +133,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_con
         const float2 t0 = ang[2 * e], t1 = ang[2 * e + 1];
         const float x0 = bf16lo(aw[e]), x1 = bf16hi(aw[e]);  // first-half elements
         const float y0 = bf16lo(bw[e]), y1 = bf16hi(bw[e]);  // their partners
-        raw[e] = pack_bf16(x0 * t0.x - y0 * t0.y, x1 * t1.x - y1 * t1.y);
-        rbw[e] = pack_bf16(y0 * t0.x + x0 * t0.y, y1 * t1.x + x1 * t1.y);
+        raw[e] = pack_bf16(rope_first(x0, y0, t0.x, t0.y), rope_first(x1, y1, t1.x, t1.y));
+        rbw[e] = pack_bf16(rope_second(x0, y0, t0.x, t0.y), rope_second(x1, y1, t1.x, t1.y));
       }
       p.kp[dst + g] = ra;
       p.kp[dst + half_vec + g] = rb;

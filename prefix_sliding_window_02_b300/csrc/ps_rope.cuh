@@ -8,6 +8,16 @@
 
 namespace ps {
 
+// One rotation pair (x: element i of the first half, y: its partner i + D/2)
+// by the angle with cosine c and sine s; explicit roundings, shared by every
+// kernel that rotates keys so that they all store the same bf16 values.
+__device__ __forceinline__ float rope_first(float x, float y, float c, float s) {
+  return __fmaf_rn(x, c, -__fmul_rn(y, s));
+}
+__device__ __forceinline__ float rope_second(float x, float y, float c, float s) {
+  return __fmaf_rn(y, c, __fmul_rn(x, s));
+}
+
 // Rotates 8 rotation pairs: elements 8g..8g+7 of the first half (a) with their
 // partners 8g+64.. of the second half (b); cs holds (cos, sin) of each pair.
 __device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, const float2* cs,
@@ -23,10 +33,8 @@ __device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, const fl
     const float2 t0 = cs[2 * e], t1 = cs[2 * e + 1];
     const float x0 = bf16lo(aw[e]), x1 = bf16hi(aw[e]);
     const float y0 = bf16lo(bw[e]), y1 = bf16hi(bw[e]);
-    raw[e] = pack_bf16(__fmaf_rn(x0, t0.x, -__fmul_rn(y0, t0.y)),
-                       __fmaf_rn(x1, t1.x, -__fmul_rn(y1, t1.y)));
-    rbw[e] = pack_bf16(__fmaf_rn(y0, t0.x, __fmul_rn(x0, t0.y)),
-                       __fmaf_rn(y1, t1.x, __fmul_rn(x1, t1.y)));
+    raw[e] = pack_bf16(rope_first(x0, y0, t0.x, t0.y), rope_first(x1, y1, t1.x, t1.y));
+    rbw[e] = pack_bf16(rope_second(x0, y0, t0.x, t0.y), rope_second(x1, y1, t1.x, t1.y));
   }
 }
 

@@ -267,3 +267,50 @@ def test_decode_graph_replays_the_eager_step(ps):
     for s in range(nseq):
         assert_attention_close(g.out[s].float().cpu().numpy(), g.lse[s].cpu().numpy(), *ref[s])
     assert eager.check_status() == 0 and graphed.check_status() == 0
+
+
+# ------------------------------------------------------------- fused append --
+@pytest.mark.parametrize("nseq,hq,hkv,D,P,W,pos0,pe,bs", [
+    (3, 16, 8, 128, [100, 0, 7], 64, [50, 1000, 170], 0, None),     # causal / evicting mixes
+    (2, 8, 2, 64, [0, 33], 16, [0, 5000], 0, None),                 # D 64, first token, W 16
+    (4, 16, 8, 128, [512, 64, 300, 1], 4096, [131072, 4159, 4395, 262143], 1, None),  # Reset PE
+    (3, 16, 8, 128, [100, 0, 7], 64, [50, 1000, 170], 0, 16),       # paged
+])
+def test_decode_append_equals_append_then_decode(ps, nseq, hq, hkv, D, P, W, pos0, pe, bs):
+    """ps_decode_append over 40 steps (each evicting) leaves the same cache bits and
+    returns the same out / lse bits as ps_kv_append followed by ps_decode, and
+    matches the oracle."""
+    seed, theta = 18, 10000.0
+    pos0 = np.array(pos0)
+    caches = []
+    for _ in range(2):
+        kw = dict(rope_theta=theta, pe_mode=pe)
+        if bs:
+            probe = ps.RingCache(nseq, hkv, D, W, P, block_size=bs, device="cpu", **kw)
+            kw.update(block_size=bs,
+                      block_order=np.random.default_rng(7).permutation(nseq * probe.blocks_per_seq))
+        c = ps.RingCache(nseq, hkv, D, W, P, **kw)
+        append_runs(c, {s: live_runs(int(pos0[s]) - 1, P[s], W) for s in range(nseq)
+                        if pos0[s] > 0}, synth_source(seed, hkv, D))
+        caches.append(c)
+    sep, fused = caches
+    for step in range(40):
+        pos = pos0 + step
+        kv = [synth.History(seed, s, hkv, D).rows_bits([int(pos[s])]) for s in range(nseq)]
+        k = bits_to_bf16_tensor(np.concatenate([x[0] for x in kv]))
+        v = bits_to_bf16_tensor(np.concatenate([x[1] for x in kv]))
+        q = _queries(seed, nseq, pos, hq, D)
+        tpos = torch.tensor(pos, dtype=torch.int32, device="cuda")
+        sep.append_tokens(tpos, k, v)
+        o_a, l_a = sep.decode(q, tpos)
+        o_b, l_b = fused.decode_append(q, k, v, tpos)
+        torch.cuda.synchronize()
+        assert torch.equal(o_a, o_b) and torch.equal(l_a, l_b), step
+    assert torch.equal(sep.k_pool, fused.k_pool) and torch.equal(sep.v_pool, fused.v_pool)
+    assert sep.check_status() == 0 and fused.check_status() == 0
+    ref = attend_reset_pe if pe else attend
+    for s in range(nseq):
+        qs = synth.bits_to_f64(synth.query_bits(seed, s, int(pos[s]), hq, D))[0]
+        o_ref, l_ref = ref(qs, int(pos[s]), P[s], W, synth.History(seed, s, hkv, D).rows, theta)
+        assert_attention_close(bf16_tensor_to_f64(o_b[s]), l_b[s].cpu().numpy(), o_ref, l_ref,
+                               f"seq {s}")

@@ -42,6 +42,16 @@ def test_build_targets_sm_103a_only():
     assert mod.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
+def test_decode_append_host_validation(ps):
+    desc = ps.CacheDesc()
+    f = ctypes.c_void_p(1 << 20)
+    # k / v missing, then an invalid descriptor: refused before any CUDA call
+    assert ps.lib.ps_decode_append(ctypes.byref(desc), f, None, f, f, 16, ctypes.c_float(0.1), f, f,
+                                   f, 0, None) == 1
+    assert ps.lib.ps_decode_append(ctypes.byref(desc), f, f, f, f, 16, ctypes.c_float(0.1), f, f,
+                                   f, 0, None) == 1
+
+
 def test_code_version_query_needs_a_device(ps):
     v = ctypes.c_int32(0)
     assert ps.lib.ps_device_code_version(None) == 1
