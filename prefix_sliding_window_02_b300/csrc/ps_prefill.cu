@@ -865,20 +865,26 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       const uint64_t dq = tc::sdesc_sw128(aq, 16, 1024);
       const uint64_t dk = tc::sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dv = tc::sdesc_sw128(smem_u32(sV), kHalf, 1024);
+      // descriptors as 32-bit halves: only the low word (start address) moves,
+      // and it never carries into the high word
+      const uint32_t q_lo = (uint32_t)dq, q_hi = (uint32_t)(dq >> 32);
+      const uint32_t k_lo = (uint32_t)dk, k_hi = (uint32_t)(dk >> 32);
+      const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
+      auto mk = [](uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; };
       auto qk = [&](int i, int sk) {
-        const uint64_t a = dq + (uint64_t)((i * kTile) >> 4), b = dk + (uint64_t)((sk * kTile) >> 4);
+        const uint32_t a = q_lo + (uint32_t)((i * kTile) >> 4), b = k_lo + (uint32_t)((sk * kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-          tc::mma_bf16(tmem + i * 128, a + off, b + off, kIdescQK, kk > 0);
+          tc::mma_bf16(tmem + i * 128, mk(a + off, q_hi), mk(b + off, k_hi), kIdescQK, kk > 0);
         }
         tc::commit(smem_u32(&bar->s_full[i]));
       };
       auto pv = [&](int i, int sv, bool acc) {
-        const uint64_t b = dv + (uint64_t)((sv * kTile) >> 4);
+        const uint32_t b = v_lo + (uint32_t)((sv * kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          tc::mma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, b + ((kk * 2048) >> 4),
+          tc::mma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, mk(b + ((kk * 2048) >> 4), v_hi),
                           kIdescPV, acc || kk > 0);
       };
       // P_i V of tile gt (the item's jt-th) from step stage st; the item's first
