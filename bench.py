@@ -435,9 +435,10 @@ def comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak):
 
 def run_decode_e2e(ps, torch, cache, steps, warmup, seed):
     """Same decode step through host buffers, with the package's DecodeGraph: per
-    step one pinned host -> device copy of the step's packed q, k, v, pos, one
-    graph replay (append + decode), one device -> host copy of the packed O and
-    LSE, and a stream synchronisation."""
+    step one native call (ps_decode_graph_step) that issues the pinned host ->
+    device copy of the step's packed q, k, v, pos, the graph launch (append +
+    decode) and the device -> host copy of the packed O and LSE, then waits for
+    the stream.  Each timed step reads its own host input row."""
     d = DEC
     nseq, hq, hkv, D = d["nseq"], d["hq"], d["hkv"], d["D"]
     g = ps.DecodeGraph(cache, hq)
@@ -455,42 +456,41 @@ def run_decode_e2e(ps, torch, cache, steps, warmup, seed):
     hres = torch.empty(g.res.numel(), dtype=torch.uint8).pin_memory()
     stream = torch.cuda.current_stream()
 
-    def step(i):
-        g.inp.copy_(hin[i], non_blocking=True)
-        g.replay()
-        hres.copy_(g.res, non_blocking=True)
-        stream.synchronize()
-
     for i in range(warmup):
-        step(i)
+        g.step(hin[i], hres)
     t0 = time.perf_counter()
     for i in range(steps):
-        step(warmup + i)
+        g.step(hin[warmup + i], hres)
     dt = time.perf_counter() - t0
 
-    # where an end-to-end step goes: the same steps again, with events between
-    # the copy in, the replay and the copy out, and the host clock around each
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
-    host = []
-    for i in range(steps):
-        h0 = time.perf_counter()
-        e = ev[i]
-        e[0].record(stream)
-        g.inp.copy_(hin[warmup + i], non_blocking=True)
-        e[1].record(stream)
+    # where a step goes: the host wall clock of the same native call with the
+    # copies left out one at a time (re-appending the last rows' positions), and
+    # the graph's device time between events
+    def wall(fn):
+        ts = []
+        for i in range(steps):
+            h0 = time.perf_counter()
+            fn(warmup + i)
+            ts.append(1e3 * (time.perf_counter() - h0))
+        return statistics.median(ts)
+
+    parts = {"step_ms": wall(lambda i: g.step(hin[i], hres)),
+             "without_d2h_ms": wall(lambda i: g.step(hin[i], None)),
+             "without_h2d_ms": wall(lambda i: g.step(None, hres)),
+             "graph_only_ms": wall(lambda i: g.step(None, None))}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dev = []
+    for _ in range(steps):
+        e0.record(stream)
         g.replay()
-        e[2].record(stream)
-        hres.copy_(g.res, non_blocking=True)
-        e[3].record(stream)
+        e1.record(stream)
         stream.synchronize()
-        host.append(1e3 * (time.perf_counter() - h0))
-    med = statistics.median
-    parts = {"h2d_ms": med(e[0].elapsed_time(e[1]) for e in ev),
-             "replay_ms": med(e[1].elapsed_time(e[2]) for e in ev),
-             "d2h_ms": med(e[2].elapsed_time(e[3]) for e in ev),
-             "device_ms": med(e[0].elapsed_time(e[3]) for e in ev),
-             "host_step_ms": med(host)}
-    parts["host_only_ms"] = parts["host_step_ms"] - parts["device_ms"]
+        dev.append(e0.elapsed_time(e1))
+    parts["graph_device_ms"] = statistics.median(dev)
+    parts["h2d_cost_ms"] = parts["step_ms"] - parts["without_h2d_ms"]
+    parts["d2h_cost_ms"] = parts["step_ms"] - parts["without_d2h_ms"]
+    parts["launch_and_sync_ms"] = parts["graph_only_ms"] - parts["graph_device_ms"]
+    g.close()
     return dt, g.inp.numel(), g.res.numel(), parts
 
 
@@ -771,13 +771,17 @@ def main():
     full = None
     pre = None
     if rank == 0 or world == 1:
-        dt, h2d, d2h, parts = run_decode_e2e(ps, torch, cache, min(args.steps, 200), 5, seed + 7)
-        e2e = {"value": d["nseq"] * min(args.steps, 200) / dt, "unit": "tok/s",
+        e2e_steps = 200
+        dt, h2d, d2h, parts = run_decode_e2e(ps, torch, cache, e2e_steps, 10, seed + 7)
+        e2e = {"value": d["nseq"] * e2e_steps / dt, "unit": "tok/s", "steps": e2e_steps,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "breakdown_median": parts,
-               "how": "per step: one pinned host -> device copy of the packed q, k, v, pos; "
-                      "DecodeGraph replay (ps_decode_append captured in a CUDA graph); "
-                      "one device -> host copy of the packed O and LSE; stream sync; host wall clock"}
+               "how": "per step one native call (DecodeGraph.step -> ps_decode_graph_step): "
+                      "pinned host -> device copy of the packed q, k, v, pos; launch of "
+                      "ps_decode_append captured in a CUDA graph; device -> host copy of the "
+                      "packed O and LSE; stream sync; host wall clock over 200 steps. "
+                      "breakdown_median: host wall clock of one such call, and with either "
+                      "copy left out; graph_device_ms: the graph between CUDA events"}
     del cache, q, k, v
     torch.cuda.empty_cache()
 

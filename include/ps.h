@@ -15,13 +15,17 @@
  *
  * Conventions for every call
  *   - Pointers marked "device" are CUDA device pointers owned by the caller
- *     (e.g. torch tensors).  The library never allocates, frees or keeps them.
+ *     (e.g. torch tensors).  The library never allocates or frees them; only
+ *     a decode-graph handle (ps_decode_graph_create) keeps them, until its
+ *     destroy call.
  *   - "bf16" is IEEE bfloat16 (__nv_bfloat16), stored row-major as documented.
  *   - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL is
- *     the legacy default stream) and never synchronises.  The library keeps no
- *     state between calls and is thread-safe, with one exception:
- *     ps_decode_noalloc uses a scratch array inside the library that all its
- *     calls share (see its comment).
+ *     the legacy default stream) and never synchronises, except
+ *     ps_decode_graph_step when asked to.  The library keeps no state between
+ *     calls and is thread-safe, with two exceptions: ps_decode_noalloc uses a
+ *     scratch array inside the library that all its calls share, and a
+ *     decode-graph handle is caller-owned state that one caller steps at a
+ *     time (see their comments).
  *   - Host-side checks run before any launch and return a ps_status_t.
  *     Checks that need device data (per-sequence prefix lengths, positions,
  *     pool bases) run inside the kernels: a failing sequence is skipped and
@@ -231,6 +235,81 @@ ps_status_t ps_decode_append(const ps_cache_desc* cache, const void* q, const vo
 ps_status_t ps_decode_noalloc(const ps_cache_desc* cache, const void* q, const int32_t* pos,
                               int32_t n_q_heads, float scale, void* out, float* lse,
                               void* stream);
+
+/*
+ * Decode-step executor: the generation loop of the "伪代码" section (one step
+ * per new token: append its K/V, attend, hand the output on) for a caller whose
+ * new tokens arrive from and whose outputs go back to host memory.  A step's
+ * inputs travel as one packed input block and its results as one packed result
+ * block, and ps_decode_graph_step moves the block in, runs ps_decode_append
+ * from a CUDA graph built once, and moves the results out, in one call.  The
+ * pages have no counterpart; it is a packaging of ps_decode_append.
+ *
+ * ps_decode_step_layout_get: byte offsets of the views in the two blocks for
+ * nseq sequences; each view starts on a 256-byte boundary:
+ *   input block  = q [nseq, n_q_heads, D] bf16 raw | k [nseq, Hkv, D] bf16 raw
+ *                | v [nseq, Hkv, D] bf16 | pos [nseq] int32
+ *   result block = out [nseq, n_q_heads, D] bf16 | lse [nseq, n_q_heads] fp32
+ * in_bytes / res_bytes: the blocks' sizes (each view's size rounded up to 256).
+ * Errors: null layout, nseq or heads < 1, Hq % Hkv != 0 -> PS_ERR_INVALID_ARGUMENT;
+ * head_dim not 64 or 128 -> PS_ERR_UNSUPPORTED.
+ */
+typedef struct ps_decode_step_layout {
+  size_t q_off, k_off, v_off, pos_off, in_bytes;
+  size_t out_off, lse_off, res_bytes;
+} ps_decode_step_layout;
+
+ps_status_t ps_decode_step_layout_get(int32_t nseq, int32_t n_q_heads, int32_t n_kv_heads,
+                                      int32_t head_dim, ps_decode_step_layout* layout);
+
+/* Opaque handle of one captured decode step. */
+typedef struct ps_decode_graph ps_decode_graph;
+
+/*
+ * ps_decode_graph_create: capture one ps_decode_append on `cache` into a CUDA
+ * graph and instantiate it, on the current device.
+ *   cache : the ring the step appends to and reads; the descriptor's values
+ *     (pools, tables, prefix lengths pointer, W, P bound, pe_mode ...) are
+ *     copied at capture, so later steps use them as they were here.
+ *   inp, res : device blocks laid out by ps_decode_step_layout_get for
+ *     (cache->nseq, n_q_heads, cache->n_kv_heads, cache->head_dim), 256-byte
+ *     aligned, owned by the caller and kept alive (with cache's buffers and
+ *     the workspace) until ps_decode_graph_destroy.
+ *   workspace : as for ps_decode_append (ps_decode_workspace_size bytes).
+ *   graph : receives the handle.
+ * The capture runs on a private stream and launches nothing: the cache is not
+ * touched until the first step.  The handle owns the graph and its
+ * instantiation (driver resources, no caller memory).  Errors: as
+ * ps_decode_append's host checks, a null or misaligned block or a null
+ * `graph` -> PS_ERR_INVALID_ARGUMENT / PS_ERR_ALIGNMENT, a failed capture or
+ * instantiation -> PS_ERR_CUDA; on error *graph is NULL.
+ */
+ps_status_t ps_decode_graph_create(const ps_cache_desc* cache, int32_t n_q_heads, float scale,
+                                   void* inp, void* res, void* workspace, size_t workspace_bytes,
+                                   ps_decode_graph** graph);
+
+/*
+ * ps_decode_graph_step: one decode step, in order on `stream` (which must
+ * belong to the graph's device; NULL = that device's legacy default stream):
+ *   1. host_in != NULL: copy in_bytes from host_in into the input block;
+ *      NULL: the caller has filled the input block on the device;
+ *   2. launch the graph (ps_decode_append);
+ *   3. host_res != NULL: copy res_bytes of the result block into host_res.
+ * sync != 0: wait for the stream before returning, so host_res holds the
+ * step's results.  Host buffers should be page-locked (pinned) for the copies
+ * to run asynchronously; with pageable memory they still complete, staged by
+ * the driver.  A handle is stepped by one caller at a time (steps on
+ * different streams would race on the blocks).  Errors: null graph or
+ * another device current -> PS_ERR_INVALID_ARGUMENT; a failed copy, launch or
+ * synchronisation -> PS_ERR_CUDA.  Device-side refusals are reported through
+ * the cache's status word, as for ps_decode_append.
+ */
+ps_status_t ps_decode_graph_step(ps_decode_graph* graph, const void* host_in, void* host_res,
+                                 int32_t sync, void* stream);
+
+/* ps_decode_graph_destroy: release the handle (NULL is a no-op).  Steps in
+ * flight must have completed. */
+ps_status_t ps_decode_graph_destroy(ps_decode_graph* graph);
 
 /*
  * ps_prefill_workspace_size: device workspace for ps_prefill (rotated Q and K,

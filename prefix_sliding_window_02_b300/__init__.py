@@ -11,13 +11,13 @@ from typing import Optional, Sequence
 
 import torch
 
-from ._lib import (CacheDesc, PsError, check, lib, PS_DEV_BAD_POS, PS_DEV_BAD_PREFIX,  # noqa: F401
-                   PS_DEV_BAD_RUN, PS_DEV_BAD_SEQ, PS_DEV_BAD_SLOT, PS_DEV_TIMEOUT, PS_PE_CONTINUE,
-                   PS_PE_RESET)
+from ._lib import (CacheDesc, PsError, StepLayout, check, lib,  # noqa: F401
+                   PS_DEV_BAD_POS, PS_DEV_BAD_PREFIX, PS_DEV_BAD_RUN, PS_DEV_BAD_SEQ,
+                   PS_DEV_BAD_SLOT, PS_DEV_TIMEOUT, PS_PE_CONTINUE, PS_PE_RESET)
 
-__all__ = ["RingCache", "DecodeGraph", "ring_slots", "decode_workspace_size", "prefill_workspace_size",
-           "prefill", "prefill_backward", "prefill_tile_grid", "prefill_tile_classes", "PsError",
-           "lib"]
+__all__ = ["RingCache", "DecodeGraph", "decode_step_layout", "ring_slots", "decode_workspace_size",
+           "prefill_workspace_size", "prefill", "prefill_backward", "prefill_tile_grid",
+           "prefill_tile_classes", "PsError", "lib"]
 
 BF16 = torch.bfloat16
 
@@ -356,35 +356,39 @@ def prefill_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: tor
     return dq, dk, dv
 
 
+def decode_step_layout(nseq: int, n_q_heads: int, n_kv_heads: int, head_dim: int):
+    """ps_decode_step_layout_get: {name: (offset, nbytes)} of the packed input block
+    (q, k, v, pos) and of the result block (out, lse), and the blocks' sizes."""
+    L = StepLayout()
+    check(lib.ps_decode_step_layout_get(nseq, n_q_heads, n_kv_heads, head_dim, ctypes.byref(L)),
+          "ps_decode_step_layout_get")
+    q_b, kv_b = nseq * n_q_heads * head_dim * 2, nseq * n_kv_heads * head_dim * 2
+    inp = {"q": (L.q_off, q_b), "k": (L.k_off, kv_b), "v": (L.v_off, kv_b),
+           "pos": (L.pos_off, nseq * 4)}
+    res = {"out": (L.out_off, q_b), "lse": (L.lse_off, nseq * n_q_heads * 4)}
+    return inp, L.in_bytes, res, L.res_bytes
+
+
 class DecodeGraph:
     """One decode step of a RingCache (ps_decode_append: one new token per sequence
-    appended and attended in one call) captured once in a CUDA graph over fixed
-    device buffers.
+    appended and attended in one call) captured once in a CUDA graph by the
+    library (ps_decode_graph_create) over fixed device buffers.
 
     The step's inputs live in one packed device buffer ``inp`` (views ``q`` [nseq, Hq,
     D], ``k``, ``v`` [nseq, Hkv, D] bf16 raw, ``pos`` [nseq] int32) and its results in
     one packed buffer ``res`` (views ``out`` [nseq, Hq, D] bf16, ``lse`` [nseq, Hq]
-    fp32), so a caller moves a step's data with one copy each way; ``replay()``
-    launches the two kernels of the step from the graph.  ``in_layout`` /
-    ``res_layout`` give (offset, nbytes) of each view, for packing host buffers the
-    same way.  The graph keeps the cache, its workspace and these buffers alive.
+    fp32); ``in_layout`` / ``res_layout`` give (offset, nbytes) of each view, for
+    packing host buffers the same way.  ``step(host_in, host_res)`` is one native
+    call that copies a packed host input block in, launches the graph, copies the
+    results out and waits; ``replay()`` launches the graph alone on inputs already
+    in ``inp``.  The object keeps the cache, its workspace and these buffers alive.
     """
 
     def __init__(self, cache: "RingCache", n_q_heads: int, scale: Optional[float] = None):
         nseq, hkv, D = cache.nseq, cache.n_kv_heads, cache.head_dim
         dev = cache.k_pool.device
-
-        def layout(parts):
-            out, off = {}, 0
-            for name, nbytes in parts:
-                out[name] = (off, nbytes)
-                off += (nbytes + 255) // 256 * 256
-            return out, off
-
-        self.in_layout, n_in = layout([("q", nseq * n_q_heads * D * 2), ("k", nseq * hkv * D * 2),
-                                       ("v", nseq * hkv * D * 2), ("pos", nseq * 4)])
-        self.res_layout, n_res = layout([("out", nseq * n_q_heads * D * 2),
-                                         ("lse", nseq * n_q_heads * 4)])
+        self.in_layout, n_in, self.res_layout, n_res = decode_step_layout(nseq, n_q_heads, hkv, D)
+        # 256-byte aligned: torch's caching allocator hands out 512-byte aligned blocks
         self.inp = torch.zeros(n_in, dtype=torch.uint8, device=dev)
         self.res = torch.zeros(n_res, dtype=torch.uint8, device=dev)
 
@@ -398,21 +402,52 @@ class DecodeGraph:
         self.pos = view(self.inp, self.in_layout, "pos", torch.int32, (nseq,))
         self.out = view(self.res, self.res_layout, "out", BF16, (nseq, n_q_heads, D))
         self.lse = view(self.res, self.res_layout, "lse", torch.float32, (nseq, n_q_heads))
-        self._seq = torch.arange(nseq, dtype=torch.int32, device=dev)
-        self._cu = torch.arange(nseq + 1, dtype=torch.int32, device=dev)
         self._ws = torch.empty(decode_workspace_size(nseq, n_q_heads, hkv, D), dtype=torch.uint8,
                                device=dev)
         self.cache = cache
-        torch.cuda.synchronize(dev)
-        self.graph = torch.cuda.CUDAGraph()
-        # relaxed: the decode call queries occupancy and sets kernel attributes on the host
-        with torch.cuda.graph(self.graph, capture_error_mode="relaxed"):
-            cache.decode_append(self.q, self.k, self.v, self.pos, scale=scale, out=self.out,
-                                lse=self.lse, workspace=self._ws)
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        self._h = ctypes.c_void_p()
+        with torch.cuda.device(dev):
+            check(lib.ps_decode_graph_create(ctypes.byref(cache.desc), n_q_heads,
+                                             ctypes.c_float(scale), _vp(self.inp), _vp(self.res),
+                                             _vp(self._ws), self._ws.numel(),
+                                             ctypes.byref(self._h)), "ps_decode_graph_create")
 
-    def replay(self) -> None:
-        """Append the step's tokens and decode them (asynchronous, current stream)."""
-        self.graph.replay()
+    @staticmethod
+    def _host(t: Optional[torch.Tensor], nbytes: int, what: str):
+        if t is None:
+            return None
+        if t.device.type != "cpu" or t.dtype != torch.uint8 or not t.is_contiguous() \
+                or t.numel() != nbytes:
+            raise ValueError(f"{what}: contiguous uint8 CPU tensor of {nbytes} bytes expected")
+        return ctypes.c_void_p(t.data_ptr())
+
+    def step(self, host_in: Optional[torch.Tensor], host_res: Optional[torch.Tensor],
+             sync: bool = True, stream=None) -> None:
+        """ps_decode_graph_step: copy ``host_in`` (packed like ``inp``; None: ``inp`` is
+        already filled) in, run the step, copy the results into ``host_res`` (packed
+        like ``res``; None: leave them on the device) and, with ``sync``, wait.  Pinned
+        host tensors keep the copies asynchronous."""
+        check(lib.ps_decode_graph_step(self._h, self._host(host_in, self.inp.numel(), "host_in"),
+                                       self._host(host_res, self.res.numel(), "host_res"),
+                                       int(bool(sync)), _stream(stream)), "ps_decode_graph_step")
+
+    def replay(self, stream=None) -> None:
+        """Append the step's tokens and decode them (asynchronous; current stream)."""
+        self.step(None, None, sync=False, stream=stream)
+
+    def close(self) -> None:
+        """Release the graph (steps in flight must have completed)."""
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            check(lib.ps_decode_graph_destroy(h), "ps_decode_graph_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown: the library may be gone
+            pass
 
 
 def prefill_tile_grid(seqlen: int, q_start: int, prefix_len: int, window: int,

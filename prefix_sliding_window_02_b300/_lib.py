@@ -27,6 +27,8 @@ EXPORTS = (
     "ps_prefill_workspace_size", "ps_prefill", "ps_prefill_tile_grid", "ps_prefill_tile_classes",
     "ps_prefill_backward_workspace_size", "ps_prefill_backward",
     "ps_check_device_status", "ps_device_code_version", "ps_test_force_wait_timeout",
+    "ps_decode_step_layout_get", "ps_decode_graph_create", "ps_decode_graph_step",
+    "ps_decode_graph_destroy",
 )
 
 
@@ -51,6 +53,13 @@ class CacheDesc(ctypes.Structure):
         ("blocks_per_seq", ctypes.c_int32),
         ("pe_mode", ctypes.c_int32),
     ]
+
+
+class StepLayout(ctypes.Structure):
+    """Mirror of ``ps_decode_step_layout``."""
+    _fields_ = [(name, ctypes.c_size_t) for name in
+                ("q_off", "k_off", "v_off", "pos_off", "in_bytes", "out_off", "lse_off",
+                 "res_bytes")]
 
 
 def _load():
@@ -80,6 +89,12 @@ def _load():
         "ps_check_device_status": (ctypes.c_int, [vp, ctypes.POINTER(i32)]),
         "ps_device_code_version": (ctypes.c_int, [ctypes.POINTER(i32)]),
         "ps_test_force_wait_timeout": (ctypes.c_int, [i32, i64]),
+        "ps_decode_step_layout_get": (ctypes.c_int, [i32, i32, i32, i32,
+                                                     ctypes.POINTER(StepLayout)]),
+        "ps_decode_graph_create": (ctypes.c_int, [pdesc, i32, f32, vp, vp, vp, sz,
+                                                  ctypes.POINTER(vp)]),
+        "ps_decode_graph_step": (ctypes.c_int, [vp, vp, vp, i32, vp]),
+        "ps_decode_graph_destroy": (ctypes.c_int, [vp]),
         "ps_prefill_backward_workspace_size": (ctypes.c_int, [i32, i32, i32, i32, i32,
                                                               ctypes.POINTER(sz)]),
         "ps_prefill_backward": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32,

@@ -589,14 +589,17 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
 //   warps 0-3  softmax, rescale and epilogue of head 0 (one thread per row)
 //   warps 4-7  the same for head 1
 //   warp 8     TMA producer (Q per item, then K / V tiles through two rings)
-//   warp 9     tcgen05 issuer
+//   warps 9-10 tcgen05 issuers, one per head, taking turns
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each.  Each softmax
 // thread writes its row of probabilities as bf16 over the first 64 columns of
 // its S, and P V reads them from there (tensor-memory A operand), so P never
-// touches shared memory.  The issuer interleaves the heads: P_0 V, S_0 = Q_0 K,
-// P_1 V, S_1 = Q_1 K, so one head's softmax overlaps the other head's MMAs.
-// Tensor-core instructions of one thread run in issue order, which is what
-// lets S_i(j+1) overwrite the columns P_i(j) V has just read.  Across items,
+// touches shared memory.  The products reach the tensor pipe with the heads
+// interleaved: P_0 V, S_0 = Q_0 K, P_1 V, S_1 = Q_1 K, so one head's softmax
+// overlaps the other head's MMAs.  Each head's products come from its own
+// issuing thread, and the two threads pass a token after each group of
+// products, so each one's barrier waits run while the other's products
+// execute.  Tensor-core instructions of one thread run in issue order, which is
+// what lets S_i(j+1) overwrite the columns P_i(j) V has just read.  Across items,
 // the next Q is loaded once the last Q K of the current item completes
 // (q_empty), and the next item's first P V waits until the epilogue has read
 // O out of tensor memory (o_free), so the next item's loads and first Q K
@@ -604,20 +607,21 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
 // ---------------------------------------------------------------------------
 namespace ws {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSt = 2;  // steps in flight: each holds a K tile and a V tile
 constexpr int kStK = kSt, kStV = kSt;
 template <int D>
 constexpr int smem_bytes() {
   return (2 + kStK + kStV) * Geom<D>::kTile + 1024 /*barriers*/ + 1024 /*alignment*/;
 }
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;  // issuers: warps kMmaWarp + head
 
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t step_full[kSt], step_empty[kSt];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
-  uint64_t drain;  // after an abort: the issuer's products have completed
+  uint64_t turn[2];  // turn[i]: issuer i may issue its next group
+  uint64_t drain;    // after an abort: the issuers' products have completed
   uint32_t tmem_slot;
   int32_t abort;
 };
@@ -765,18 +769,19 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
   }
   if (tid == 32) {
     mbar_init(&bar->q_full, 1);
-    mbar_init(&bar->q_empty, 1);
+    mbar_init(&bar->q_empty, 2);  // a commit from each issuer
     for (int s = 0; s < kSt; ++s) {
       mbar_init(&bar->step_full[s], 1);
-      mbar_init(&bar->step_empty[s], 1);
+      mbar_init(&bar->step_empty[s], 2);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->p_full[i], 4);  // one arrival per softmax warp
       mbar_init(&bar->o_done[i], 1);
       mbar_init(&bar->o_free[i], 4);
+      mbar_init(&bar->turn[i], 1);
     }
-    mbar_init(&bar->drain, 1);
+    mbar_init(&bar->drain, 2);
     bar->abort = 0;
     fence_mbar_init();
   }
@@ -854,15 +859,23 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // -------------------------------------------------------------- issuer
+  } else if (warp >= kMmaWarp) {
+    // ------------------------------------------------------------- issuers
+    // Issuer i issues head i's products.  Every mbarrier operation of an issuing
+    // thread stalls it for hundreds of cycles while the tensor-core queue is only
+    // a few products deep, so one thread alone leaves the pipe idle during its
+    // waits.  Here each step is one group of products per head, and the groups
+    // are issued strictly in turn (head 0's group t, head 1's group t, head 0's
+    // group t + 1, ...): an issuer hands the turn on as soon as its group is
+    // issued, and has done its own waits for the next group (operand tiles, its
+    // head's P, O free) while the other's products were being issued.
     if (lane == 0) {
-      const uint32_t aq = smem_u32(sQ);
+      const int i = warp - kMmaWarp;  // head of the pair
       // Descriptors are built once: moving a descriptor by `off` bytes adds
       // off / 16 to its start-address field (shared addresses stay below 256 KB,
       // so the 14-bit field never carries), which keeps the issue of the 16
       // products of a step off the critical path.
-      const uint64_t dq = tc::sdesc_sw128(aq, 16, 1024);
+      const uint64_t dq = tc::sdesc_sw128(smem_u32(sQ + i * kTile), 16, 1024);
       const uint64_t dk = tc::sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dv = tc::sdesc_sw128(smem_u32(sV), kHalf, 1024);
       // descriptors as 32-bit halves: only the low word (start address) moves,
@@ -871,36 +884,28 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       const uint32_t k_lo = (uint32_t)dk, k_hi = (uint32_t)(dk >> 32);
       const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
       auto mk = [](uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; };
-      auto qk = [&](int i, int sk) {
-        const uint32_t a = q_lo + (uint32_t)((i * kTile) >> 4), b = k_lo + (uint32_t)((sk * kTile) >> 4);
+      const uint32_t tS = tmem + i * 128, tO = tmem + 256 + i * 128;
+      auto qk = [&](int sk) {
+        const uint32_t b = k_lo + (uint32_t)((sk * kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-          tc::mma_bf16(tmem + i * 128, mk(a + off, q_hi), mk(b + off, k_hi), kIdescQK, kk > 0);
+          tc::mma_bf16(tS, mk(q_lo + off, q_hi), mk(b + off, k_hi), kIdescQK, kk > 0);
         }
         tc::commit(smem_u32(&bar->s_full[i]));
       };
-      auto pv = [&](int i, int sv, bool acc) {
+      auto pv = [&](int sv, bool acc) {
         const uint32_t b = v_lo + (uint32_t)((sv * kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          tc::mma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, mk(b + ((kk * 2048) >> 4), v_hi),
-                          kIdescPV, acc || kk > 0);
+          tc::mma_bf16_ts(tO, tS + kk * 8, mk(b + ((kk * 2048) >> 4), v_hi), kIdescPV,
+                          acc || kk > 0);
       };
-      // P_i V of tile gt (the item's jt-th) from step stage st; the item's first
-      // one overwrites O_i, which must wait until the previous item's epilogue
-      // has read O_i out.  Every mbarrier operation of this thread stalls it for
-      // hundreds of cycles while the tensor-core queue is only a few products
-      // deep, so each step waits on one barrier for both operand tiles and
-      // releases them with one commit.
-      auto pv_step = [&](int i, int gt, int jt, int st, int k) -> bool {
-        if (!wait(&bar->p_full[i], gt & 1, abort, p.wait_ns)) return false;
-        if (jt == 0 && !wait(&bar->o_free[i], (k & 1) ^ 1, abort, p.wait_ns)) return false;
-        tc::fence_after();
-        pv(i, st, jt > 0);
-        return true;
-      };
-      int g = 0, k = 0, kq = 0;  // kq: Q loads consumed
+      // t counts the groups this issuer has issued.  turn[0] completes a phase
+      // each time issuer 1 hands over, turn[1] each time issuer 0 does; neither
+      // can run two phases ahead of its waiter, since each hand-over needs the
+      // other issuer's previous one.
+      int g = 0, k = 0, kq = 0, t = 0;  // kq: Q loads consumed
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_items; u += gridDim.x) {
         const Item it = make_item(p, u);
@@ -908,26 +913,31 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         if (n <= 0) continue;
         if (!(ok = wait(&bar->q_full, kq & 1, abort, p.wait_ns))) break;
         ++kq;
-        for (int j = 0; ok && j <= n; ++j) {
+        for (int j = 0; j <= n; ++j, ++t) {
           const int gs = g + k + j, st = gs % kSt;  // step index: n + 1 steps per item
+          // step gs brings K(j) for Q K of tile j and V(j-1) for P V of tile j-1
           if (!(ok = wait(&bar->step_full[st], (gs / kSt) & 1, abort, p.wait_ns))) break;
-          for (int i = 0; i < 2 && ok; ++i) {
-            if (j > 0 && !(ok = pv_step(i, g + j - 1, j - 1, st, k))) break;
-            if (j < n) {
-              if (i == 0 && j == n0 && j > 0) {  // Reset PE: the second query has landed
-                if (!(ok = wait(&bar->q_full, kq & 1, abort, p.wait_ns))) break;
-                ++kq;
-                tc::fence_after();
-              }
-              qk(i, st);
-            } else {
-              tc::commit(smem_u32(&bar->o_done[i]));
-            }
+          // P_i(j-1) is written; the item's first P V overwrites O_i, which the
+          // previous item's epilogue must have read out
+          if (j > 0 && !(ok = wait(&bar->p_full[i], (g + j - 1) & 1, abort, p.wait_ns))) break;
+          if (j == 1 && !(ok = wait(&bar->o_free[i], (k & 1) ^ 1, abort, p.wait_ns))) break;
+          if (j < n && j == n0 && j > 0) {  // Reset PE: the second query has landed
+            if (!(ok = wait(&bar->q_full, kq & 1, abort, p.wait_ns))) break;
+            ++kq;
           }
-          if (!ok) break;
+          const bool turn = i == 0 ? (t == 0 || wait(&bar->turn[0], (t - 1) & 1, abort, p.wait_ns))
+                                   : wait(&bar->turn[1], t & 1, abort, p.wait_ns);
+          if (!(ok = turn)) break;
+          tc::fence_after();
+          if (j > 0) pv(st, j > 1);
+          if (j < n)
+            qk(st);
+          else
+            tc::commit(smem_u32(&bar->o_done[i]));
           tc::commit(smem_u32(&bar->step_empty[st]));
           // every Q K reading the current Q is issued: it may be replaced
           if (j == n - 1 || (j == n0 - 1 && n0 > 0)) tc::commit(smem_u32(&bar->q_empty));
+          mbar_arrive(&bar->turn[i ^ 1]);
         }
         g += n;
         ++k;
@@ -1052,7 +1062,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       for (int s = 0; s < kSt; ++s)
         if (last_step[s] >= 0)
           mbar_wait(&bar->step_full[s], (uint32_t)((last_step[s] / kSt) & 1), p.wait_ns);
-    } else if (warp == kMmaWarp && lane == 0) {
+    } else if (warp >= kMmaWarp && lane == 0) {
       tc::commit(smem_u32(&bar->drain));
       mbar_wait(&bar->drain, 0, p.wait_ns);
     }

@@ -232,9 +232,11 @@ def test_decode_reset_pe_shapes(ps, nseq, hq, hkv, D, P, W, pos):
 
 
 def test_decode_graph_replays_the_eager_step(ps):
-    """DecodeGraph (append + decode captured once, replayed per step) gives the same
-    bits as the eager calls on an identical cache, and stays within the oracle's
-    tolerance, across steps that evict."""
+    """DecodeGraph (append + decode captured once by the library, then launched per
+    step, alternately on inputs filled on the device and through one native call
+    that copies packed host blocks in and out) gives the same bits as the eager
+    calls on an identical cache, and stays within the oracle's tolerance, across
+    steps that evict."""
     seed, nseq, hq, hkv, D, W, theta = 17, 3, 4, 2, 128, 64, 10000.0
     P = np.array([5, 40, 0])
     pos0 = np.array([100, 70, 300])
@@ -256,17 +258,34 @@ def test_decode_graph_replays_the_eager_step(ps):
         tpos = torch.tensor(pos, dtype=torch.int32, device="cuda")
         eager.append_tokens(tpos, k, v)
         o_e, l_e = eager.decode(q, tpos)
-        g.q.copy_(q)
-        g.k.copy_(k)
-        g.v.copy_(v)
-        g.pos.copy_(tpos)
-        g.replay()
-        torch.cuda.synchronize()
-        assert torch.equal(g.out, o_e) and torch.equal(g.lse, l_e), step
+        if step % 2 == 0:  # inputs filled on the device, graph launched alone
+            g.q.copy_(q)
+            g.k.copy_(k)
+            g.v.copy_(v)
+            g.pos.copy_(tpos)
+            g.replay()
+            torch.cuda.synchronize()
+            o_g, l_g = g.out, g.lse
+        else:  # one native call: packed host block in, step, packed results out
+            hin = torch.zeros(g.inp.numel(), dtype=torch.uint8)
+            hres = torch.zeros(g.res.numel(), dtype=torch.uint8)
+            if step % 4 == 1:  # page-locked, the serving case; else pageable
+                hin, hres = hin.pin_memory(), hres.pin_memory()
+            for name, t in (("q", q), ("k", k), ("v", v), ("pos", tpos)):
+                o, nb = g.in_layout[name]
+                hin[o:o + nb].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+            g.step(hin, hres)
+            o, nb = g.res_layout["out"]
+            o_g = hres[o:o + nb].view(torch.bfloat16).view(o_e.shape).cuda()
+            o, nb = g.res_layout["lse"]
+            l_g = hres[o:o + nb].view(torch.float32).view(l_e.shape).cuda()
+        assert torch.equal(o_g, o_e) and torch.equal(l_g, l_e), step
     ref = _oracle_rows(seed, range(nseq), pos, P, W, hq, hkv, D, theta)
     for s in range(nseq):
         assert_attention_close(g.out[s].float().cpu().numpy(), g.lse[s].cpu().numpy(), *ref[s])
     assert eager.check_status() == 0 and graphed.check_status() == 0
+    g.close()
+    g.close()  # a second close is a no-op
 
 
 # ------------------------------------------------------------- fused append --

@@ -207,3 +207,51 @@ def test_prefill_head_dims(ps):
     assert b.value >= 300 * 4 * 64 * 2 + 300 * 2 * 64 * 2
     assert ps.lib.ps_prefill_workspace_size(1, 300, 4, 2, 96, 0, 0, ctypes.byref(b)) == 2
     assert ps.lib.ps_prefill_workspace_size(1, 300, 4, 2, 256, 0, 0, ctypes.byref(b)) == 2
+
+
+def test_decode_step_layout(ps):
+    """Packed step blocks: each view 256-byte aligned, in the documented order, no
+    overlap, block sizes rounded up to 256; invalid shapes refused."""
+    L = ps.StepLayout()
+    for nseq, hq, hkv, D in ((1, 1, 1, 64), (3, 16, 8, 128), (64, 16, 8, 128), (257, 8, 1, 64)):
+        assert ps.lib.ps_decode_step_layout_get(nseq, hq, hkv, D, ctypes.byref(L)) == 0
+        sizes = [("q_off", nseq * hq * D * 2), ("k_off", nseq * hkv * D * 2),
+                 ("v_off", nseq * hkv * D * 2), ("pos_off", nseq * 4)]
+        end = 0
+        for name, nb in sizes:
+            off = getattr(L, name)
+            assert off % 256 == 0 and off == end
+            end = off + (nb + 255) // 256 * 256
+        assert L.in_bytes == end
+        assert L.out_off == 0 and L.lse_off == (nseq * hq * D * 2 + 255) // 256 * 256
+        assert L.res_bytes == L.lse_off + (nseq * hq * 4 + 255) // 256 * 256
+        inp, n_in, res, n_res = ps.decode_step_layout(nseq, hq, hkv, D)
+        assert n_in == L.in_bytes and n_res == L.res_bytes and inp["v"] == (L.v_off, nseq * hkv * D * 2)
+    for args, code in (((0, 16, 8, 128), 1), ((4, 16, 6, 128), 1), ((4, 0, 8, 128), 1),
+                       ((4, 16, 8, 96), 2)):
+        assert ps.lib.ps_decode_step_layout_get(*args, ctypes.byref(L)) == code
+    assert ps.lib.ps_decode_step_layout_get(4, 16, 8, 128, None) == 1
+
+
+def test_decode_graph_host_validation(ps):
+    """The executor refuses bad arguments before any CUDA call; a null handle is
+    refused by step and ignored by destroy."""
+    lib, f = ps.lib, ctypes.c_void_p(1 << 20)
+    h = ctypes.c_void_p(123)
+    desc = _bad_desc(ps, nseq=4, n_kv_heads=8, capacity=10)
+    one = ctypes.c_float(0.1)
+    assert lib.ps_decode_graph_create(ctypes.byref(desc), 16, one, f, f, f, 1 << 20, None) == 1
+    assert lib.ps_decode_graph_create(None, 16, one, f, f, f, 1 << 20, ctypes.byref(h)) == 1
+    assert h.value is None  # cleared on every refusal
+    assert lib.ps_decode_graph_create(ctypes.byref(desc), 16, one, None, f, f, 1 << 20,
+                                      ctypes.byref(h)) == 1
+    assert lib.ps_decode_graph_create(ctypes.byref(desc), 16, one, ctypes.c_void_p((1 << 20) + 16),
+                                      f, f, 1 << 20, ctypes.byref(h)) == 3
+    assert lib.ps_decode_graph_create(ctypes.byref(desc), 12, one, f, f, f, 1 << 20,
+                                      ctypes.byref(h)) == 1  # Hq % Hkv
+    bad_d = _bad_desc(ps, nseq=4, n_kv_heads=8, head_dim=96)
+    assert lib.ps_decode_graph_create(ctypes.byref(bad_d), 16, one, f, f, f, 1 << 20,
+                                      ctypes.byref(h)) == 2
+    assert h.value is None
+    assert lib.ps_decode_graph_step(None, f, f, 1, None) == 1
+    assert lib.ps_decode_graph_destroy(None) == 0
