@@ -273,11 +273,11 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ P
 // ---------------------------------------------------------------------------
 
 // dQ side, first half: this thread's query row against kNC keys (key indices
-// base..).  P = exp2(S * scale_log2 - lse2), zero unless key x (relative to
-// base) has x < A1 or B0 <= x < B1; kept in registers.
+// base..).  P = exp2(S * scale_log2 - lse2), zero unless bit x of km is set
+// (key x, relative to base, admitted); kept in registers.
 template <bool MASK>
-__device__ __forceinline__ void p_row(uint32_t tS, float scale_log2, float lse2, int32_t A1,
-                                      int32_t B0, int32_t B1, float (&pr)[kNC]) {
+__device__ __forceinline__ void p_row(uint32_t tS, float scale_log2, float lse2,
+                                      const uint32_t (&km)[kNC / 32], float (&pr)[kNC]) {
 #pragma unroll
   for (int c = 0; c < kNC / 32; ++c) {
     uint32_t sv[32];
@@ -292,8 +292,8 @@ __device__ __forceinline__ void p_row(uint32_t tS, float scale_log2, float lse2,
       x0 = ex2(x0);
       x1 = ex2(x1);
       if (MASK) {
-        x0 = ((x < A1) || (x >= B0 && x < B1)) ? x0 : 0.f;
-        x1 = ((x + 1 < A1) || (x + 1 >= B0 && x + 1 < B1)) ? x1 : 0.f;
+        x0 = (km[x >> 5] & (1u << (x & 31))) ? x0 : 0.f;
+        x1 = (km[(x + 1) >> 5] & (1u << ((x + 1) & 31))) ? x1 : 0.f;
       }
       pr[x] = x0;
       pr[x + 1] = x1;
@@ -323,11 +323,11 @@ __device__ __forceinline__ void ds_row(uint32_t tP, float drow, const float (&pr
 
 // dK/dV side, first half: this thread's key row against kNC queries whose
 // {LSE*log2e, D} pairs are ld[0..kNC) (as float4: two queries each).  P^T is
-// zero unless query e has LO <= e <= HI; kept in registers and written as bf16
-// pairs over the first kNC / 2 columns for dV += P^T dO.
+// zero unless bit e of km is set (query e admits the key); kept in registers
+// and written as bf16 pairs over the first kNC / 2 columns for dV += P^T dO.
 template <bool MASK>
-__device__ __forceinline__ void p_col(uint32_t tS, float scale_log2, const float4* ld, int32_t LO,
-                                      int32_t HI, float (&pr)[kNC]) {
+__device__ __forceinline__ void p_col(uint32_t tS, float scale_log2, const float4* ld,
+                                      const uint32_t (&km)[kNC / 32], float (&pr)[kNC]) {
 #pragma unroll
   for (int c = 0; c < kNC / 32; ++c) {
     uint32_t sv[32];  // the bf16 pairs are packed into its first half as it is consumed
@@ -343,8 +343,8 @@ __device__ __forceinline__ void p_col(uint32_t tS, float scale_log2, const float
       x0 = ex2(x0);
       x1 = ex2(x1);
       if (MASK) {
-        x0 = (x >= LO && x <= HI) ? x0 : 0.f;
-        x1 = (x + 1 >= LO && x + 1 <= HI) ? x1 : 0.f;
+        x0 = (km[x >> 5] & (1u << (x & 31))) ? x0 : 0.f;
+        x1 = (km[(x + 1) >> 5] & (1u << ((x + 1) & 31))) ? x1 : 0.f;
       }
       pr[x] = x0;
       pr[x + 1] = x1;
@@ -541,6 +541,11 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
       const int32_t hi = (int32_t)(hi64 < -1 ? -1 : (hi64 > kNC - 1 ? kNC - 1 : hi64));
       const uint32_t tS = tmem + bf * 128 + part * kNC + lane_off;
       const float4* ld = reinterpret_cast<const float4*>(sLd + sa * kT + part * kNC);
+      uint32_t kmask[kNC / 32];
+      if (masked) {
+#pragma unroll
+        for (int w = 0; w < kNC / 32; ++w) kmask[w] = keep_bits(32 * w, 0, lo, hi + 1);
+      }
       ok = mbar_wait_abort(&bar->s_full[bf], ph, abort, p.wait_ns) &&
            mbar_wait_abort(&bar->a_full[sa], (t / kSa) & 1, abort, p.wait_ns);  // the LSE / D pairs
       if (!__all_sync(0xffffffffu, ok)) {
@@ -549,9 +554,9 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
       }
       tc::fence_after();
       if (masked)
-        p_col<true>(tS, p.scale_log2, ld, lo, hi, pr);
+        p_col<true>(tS, p.scale_log2, ld, kmask, pr);
       else
-        p_col<false>(tS, p.scale_log2, ld, 0, kNC - 1, pr);
+        p_col<false>(tS, p.scale_log2, ld, kmask, pr);
       release(&bar->p_ready[bf], lane, true);
       ok = mbar_wait_abort(&bar->dp_full[bf], ph, abort, p.wait_ns);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -716,6 +721,12 @@ __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar
                           tile_class(km, c0, q0r, q1r, ka, kb, P, p.W) != kFull;
       const int32_t base = ka + part * kNC;
       const uint32_t tS = tmem + bf * 128 + part * kNC + lane_off;
+      uint32_t kmask[kNC / 32];
+      if (masked) {
+#pragma unroll
+        for (int w = 0; w < kNC / 32; ++w)
+          kmask[w] = keep_bits(32 * w, a1 - base, b0 - base, b1 - base);
+      }
       ok = mbar_wait_abort(&bar->s_full[bf], ph, abort, p.wait_ns);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -723,9 +734,9 @@ __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar
       }
       tc::fence_after();
       if (masked)
-        p_row<true>(tS, p.scale_log2, ldr.x, a1 - base, b0 - base, b1 - base, pr);
+        p_row<true>(tS, p.scale_log2, ldr.x, kmask, pr);
       else
-        p_row<false>(tS, p.scale_log2, ldr.x, 0, 0, 0, pr);
+        p_row<false>(tS, p.scale_log2, ldr.x, kmask, pr);
       release(&bar->p_ready[bf], lane, false);
       ok = mbar_wait_abort(&bar->dp_full[bf], ph, abort, p.wait_ns);
       if (!__all_sync(0xffffffffu, ok)) {

@@ -34,6 +34,19 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// Bits [lo, hi) of a 32-bit word (0 <= lo, hi <= 32; none when hi <= lo).
+__device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
+  return (uint32_t)((1ull << hi) - 1) & ~(uint32_t)((1ull << lo) - 1);
+}
+
+// One bit per column c0 .. c0 + 31: set iff the column lies in [0, a1) or in
+// [b0, b1).  A row's keep-mask is built once per tile, so the element mask of
+// a partial tile costs a bit test and a select per element.
+__device__ __forceinline__ uint32_t keep_bits(int c0, int32_t a1, int32_t b0, int32_t b1) {
+  auto clamp32 = [](int32_t x) { return x < 0 ? 0 : (x > 32 ? 32 : x); };
+  return bit_range(0, clamp32(a1 - c0)) | bit_range(clamp32(b0 - c0), clamp32(b1 - c0));
+}
+
 // d = a * b on two lanes at once.
 __device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"

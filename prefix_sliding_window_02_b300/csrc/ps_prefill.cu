@@ -392,6 +392,10 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
 
   const int row = tid;
   const int64_t qpos = q0 + row;
+  // admitted key indices of this row: [0, a1) and [b0, b1)
+  const int32_t a1 = keys_below(km, min((int64_t)P, qpos + 1));
+  const int32_t b0 = keys_below(km, max((int64_t)0, qpos - p.W + 1));
+  const int32_t b1 = keys_below(km, qpos + 1);
   float m_ref = -INFINITY, l = 0.f;
   bool ok = true;
   int committed_pv = 0;
@@ -446,14 +450,17 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
       for (int j = 0; j < 32; ++j) s[c * 32 + j] = __uint_as_float(r[j]) * p.scale_log2;
     }
     if (masked) {
+      // kept columns: j < A1 (prefix keys) or B0 <= j < B1 (window keys); a
+      // split tile's two visits keep only the keys before / after the prefix
+      const int32_t A1 = mode == kVisitLaterPart ? 0 : a1 - ka;
+      const int32_t B0 =
+          mode == kVisitPrefixPart ? 0 : (mode == kVisitLaterPart ? max(b0, vs.kP) : b0) - ka;
+      const int32_t B1 = mode == kVisitPrefixPart ? 0 : b1 - ka;
+      uint32_t kmask[kBN / 32];
 #pragma unroll
-      for (int j = 0; j < kBN; ++j) {
-        const int32_t kidx = ka + j;
-        const bool keep = kidx < km.n_keys && admitted(qpos, key_pos(km, kidx), P, p.W) &&
-                          (mode != kVisitPrefixPart || kidx < vs.kP) &&
-                          (mode != kVisitLaterPart || kidx >= vs.kP);
-        s[j] = keep ? s[j] : -INFINITY;
-      }
+      for (int w = 0; w < kBN / 32; ++w) kmask[w] = keep_bits(32 * w, A1, B0, B1);
+#pragma unroll
+      for (int j = 0; j < kBN; ++j) s[j] = (kmask[j >> 5] & (1u << (j & 31))) ? s[j] : -INFINITY;
     }
     float mt = s[0];
 #pragma unroll
@@ -668,7 +675,7 @@ __device__ __forceinline__ Item make_item(const PrefillParams& p, int u) {
 }  // namespace ws
 
 // One query row's share of a 128-key tile: S from TMEM, optional element mask
-// (keep column c iff c < A1 or B0 <= c < B1), online-softmax bookkeeping with a
+// (keep column c iff bit c of km is set), online-softmax bookkeeping with a
 // lazy rescale, and P = exp2(S * scale - m) stored back over the first 64
 // columns as bf16 pairs.  The row sum adds the fp32 probabilities: summing
 // the bf16-rounded ones instead moves the LSE of rows with few keys by up to
@@ -678,8 +685,9 @@ __device__ __forceinline__ Item make_item(const PrefillParams& p, int u) {
 // of three-input and packed instructions: this per-row chain, S -> P, is what
 // the other head's MMAs have to cover.
 template <bool MASK>
-__device__ __forceinline__ float softmax_tile(uint32_t tS, int j, float scale_log2, int32_t A1,
-                                              int32_t B0, int32_t B1, float& m_used, float& l) {
+__device__ __forceinline__ float softmax_tile(uint32_t tS, int j, float scale_log2,
+                                              const uint32_t (&km)[kBN / 32], float& m_used,
+                                              float& l) {
   float s[kBN];
   {
     uint32_t r0[32], r1[32], r2[32], r3[32];
@@ -698,10 +706,7 @@ __device__ __forceinline__ float softmax_tile(uint32_t tS, int j, float scale_lo
   }
   if (MASK) {
 #pragma unroll
-    for (int c = 0; c < kBN; ++c) {
-      const bool keep = (c < A1) || (c >= B0 && c < B1);
-      s[c] = keep ? s[c] : -INFINITY;
-    }
+    for (int c = 0; c < kBN; ++c) s[c] = (km[c >> 5] & (1u << (c & 31))) ? s[c] : -INFINITY;
   }
   float mx8[8];
 #pragma unroll
@@ -975,6 +980,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         const int32_t A1 = mode == kVisitLaterPart ? 0 : a1 - ka;
         const int32_t B0 = mode == kVisitPrefixPart ? 0 : (mode == kVisitLaterPart ? max(b0, it.v.kP) : b0) - ka;
         const int32_t B1 = mode == kVisitPrefixPart ? 0 : b1 - ka;
+        uint32_t km[kBN / 32];
         ok = wait(&bar->s_full[i], (g + j) & 1, abort, p.wait_ns);
         // tcgen05.ld / st are warp-collective (.sync.aligned): the warp decides
         // together and reconverges here after the per-thread spin
@@ -984,10 +990,13 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         }
         tc::fence_after();
         float alpha;
-        if (masked)
-          alpha = softmax_tile<true>(tS, j, p.scale_log2, A1, B0, B1, m_used, l);
-        else
-          alpha = softmax_tile<false>(tS, j, p.scale_log2, 0, 0, 0, m_used, l);
+        if (masked) {
+#pragma unroll
+          for (int w = 0; w < kBN / 32; ++w) km[w] = keep_bits(32 * w, A1, B0, B1);
+          alpha = softmax_tile<true>(tS, j, p.scale_log2, km, m_used, l);
+        } else {
+          alpha = softmax_tile<false>(tS, j, p.scale_log2, km, m_used, l);
+        }
         if (__any_sync(0xffffffffu, alpha != 1.f)) {  // alpha is 1 on the other rows
           // O_i already holds every P V issued before S_i(j), which has completed,
           // and P_i(j) V is not issued before this thread arrives below

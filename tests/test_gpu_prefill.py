@@ -106,6 +106,8 @@ def _check_rows(seed, out, lse, q, q_start, P, W, theta, rows_per_b, hkv, what="
     (1, 200, 8, 1, [300], 16, 0),        # P >= S: causal through the prefix
     (1, 260, 4, 2, [4], 1, 0),           # W = 1, StreamingLLM-like sink of 4
     (2, 200, 4, 2, [17, 130], 70, 2),    # q x 4: sharper softmax, stale-max rescaling
+    (2, 300, 3, 3, [37, 200], 100, 0),   # one query head per KV head: split prefix tile, band
+    (1, 333, 6, 2, [150], 90, 0),        # three query heads per KV head (odd group)
 ])
 def test_prefill_all_rows(ps, B, S, hq, hkv, P, W, qs):
     seed, D, theta = 31, 128, 10000.0
