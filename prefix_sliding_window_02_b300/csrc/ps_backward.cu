@@ -90,6 +90,8 @@ struct Geo {
 struct Params {
   CUtensorMap tmq, tmdo;  // rotated Q, dO  {D, Hq, S, B}, 128-row boxes
   CUtensorMap tmk, tmv;   // rotated K, V   {D, Hkv, S, B}
+  // head dim 128: fp32 gradients {D, H, S, B}, 32 x 32 boxes, 128-byte swizzle
+  CUtensorMap tmdq, tmdk, tmdv;
   const float2* ld;       // [B, Hq, s_pad] {LSE * log2(e), D}; rows >= S are zero
   const int32_t* q_start;
   const int32_t* prefix_len;
@@ -170,6 +172,56 @@ __device__ __forceinline__ void store_chunk(uint32_t taddr, float* dst, int c, b
     *reinterpret_cast<uint4*>(dst + c * kPairs + e) = make_uint4(a[e], a[e + 1], a[e + 2], a[e + 3]);
     *reinterpret_cast<uint4*>(dst + kH + c * kPairs + e) =
         make_uint4(b[e], b[e + 1], b[e + 2], b[e + 3]);
+  }
+}
+
+// Head dim 128: the same values as store_chunk for the warp's 32 rows (lanes),
+// written through shared memory and two tensor stores (columns [32 c, 32 c + 32)
+// and their partners 64 further on), so that each store moves whole 128-byte
+// row segments instead of one 16-byte piece per row.  `stage` (8 KB,
+// 1024-byte aligned) holds the two 32 x 32 fp32 boxes in the 128-byte swizzled
+// layout of the tensor map.  Rows past the tensor's end are clipped by the
+// store.  Lane 0 commits the stores; the caller waits for them to have read
+// shared memory before it is reused or released.
+__device__ __forceinline__ void store_chunk_tma(uint32_t taddr, uint8_t* stage,
+                                                const CUtensorMap* map, int c, float mul, bool rot,
+                                                int32_t pos, const RopeTurns& turns, int32_t head,
+                                                int32_t row0, int32_t b, int lane) {
+  constexpr int kPairs = 32, kH = 64;
+  uint32_t a[kPairs], v[kPairs];
+  tld(taddr + c * kPairs, a);
+  tld(taddr + kH + c * kPairs, v);
+  tc::wait_ld();
+#pragma unroll
+  for (int e = 0; e < kPairs; ++e) {
+    const float x = __uint_as_float(a[e]) * mul, y = __uint_as_float(v[e]) * mul;
+    float rx = x, ry = y;
+    if (rot) {
+      float cs, sn;
+      rope_cos_sin(pos, turns.f[c * kPairs + e], cs, sn);
+      rx = x * cs + y * sn;  // rotation by -angle
+      ry = y * cs - x * sn;
+    }
+    a[e] = __float_as_uint(rx);
+    v[e] = __float_as_uint(ry);
+  }
+  const uint32_t s0 = smem_u32(stage);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {  // 16-byte chunk j of this row, swizzled
+    const uint32_t off = lane * 128 + ((j ^ (lane & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s0 + off), "r"(a[4 * j]),
+                 "r"(a[4 * j + 1]), "r"(a[4 * j + 2]), "r"(a[4 * j + 3])
+                 : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s0 + 4096 + off),
+                 "r"(v[4 * j]), "r"(v[4 * j + 1]), "r"(v[4 * j + 2]), "r"(v[4 * j + 3])
+                 : "memory");
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_4d(map, stage, c * kPairs, head, row0, b);
+    tma_store_4d(map, stage + 4096, kH + c * kPairs, head, row0, b);
+    bulk_commit();
   }
 }
 
@@ -575,7 +627,15 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
       tc::fence_after();
       const bool valid = k0r + row <= k1r;
       const int64_t base = (((int64_t)b * p.S + (valid ? k0r + row : 0)) * p.hkv + hk) * D;
-      if (n > 0) {
+      if (n > 0 && D == 128) {
+        // staging in the operand rings, free now that every product has completed
+        const int32_t row0 = k0r + quad * 32;
+        store_chunk_tma(tmem + kTAcc + lane_off, smem + kOffA + warp * 8192, &p.tmdv, part, 1.f,
+                        false, 0, p.turns, hk, row0, b, lane);
+        store_chunk_tma(tmem + kTAcc + 128 + lane_off, smem + kOffB + warp * 8192, &p.tmdk, part,
+                        p.scale, true, (int32_t)kpos, p.turns, hk, row0, b, lane);
+        if (lane == 0) bulk_wait_read_all();
+      } else if (n > 0) {
         store_chunk<D>(tmem + kTAcc + lane_off, p.dv + base, part, valid, 1.f, false, 0, p.turns);
         store_chunk<D>(tmem + kTAcc + 128 + lane_off, p.dk + base, part, valid, p.scale, true,
                        (int32_t)kpos, p.turns);
@@ -755,7 +815,11 @@ __device__ __forceinline__ void dq_cta(const Params& p, uint8_t* smem, Bars* bar
       tc::fence_after();
       const bool valid = q0r + row <= q1r;
       float* dst = p.dq + (((int64_t)b * p.S + (valid ? q0r + row : 0)) * p.hq + h) * D;
-      if (n > 0) {
+      if (n > 0 && D == 128) {
+        store_chunk_tma(tmem + kTAcc + lane_off, smem + kOffA + warp * 8192, &p.tmdq, part,
+                        p.scale, true, (int32_t)qpos, p.turns, h, q0r + quad * 32, b, lane);
+        if (lane == 0) bulk_wait_read_all();
+      } else if (n > 0) {
         store_chunk<D>(tmem + kTAcc + lane_off, dst, part, valid, p.scale, true, (int32_t)qpos,
                        p.turns);
       } else if (valid) {
@@ -950,6 +1014,18 @@ extern "C" ps_status_t ps_prefill_backward(const void* q, const void* k, const v
                    encode_tmap(&p.tmk, bf, 4, qk + L.k_off, kd, ks, box, sw) &&
                    encode_tmap(&p.tmv, bf, 4, v, kd, ks, box, sw);
   if (!okm) return PS_ERR_CUDA;
+  if (head_dim == 128) {
+    const uint64_t fqs[3] = {(uint64_t)head_dim * 4, (uint64_t)n_q_heads * head_dim * 4,
+                             (uint64_t)seqlen * n_q_heads * head_dim * 4};
+    const uint64_t fks[3] = {(uint64_t)head_dim * 4, (uint64_t)n_kv_heads * head_dim * 4,
+                             (uint64_t)seqlen * n_kv_heads * head_dim * 4};
+    const uint32_t fbox[4] = {32u, 1u, 32u, 1u};
+    const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    if (!encode_tmap(&p.tmdq, f32, 4, dq, qd, fqs, fbox, sw) ||
+        !encode_tmap(&p.tmdk, f32, 4, dk, kd, fks, fbox, sw) ||
+        !encode_tmap(&p.tmdv, f32, 4, dv, kd, fks, fbox, sw))
+      return PS_ERR_CUDA;
+  }
   p.ld = reinterpret_cast<const float2*>(ws + L.ld_off);
   p.q_start = q_start;
   p.prefix_len = prefix_len;
