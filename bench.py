@@ -312,6 +312,50 @@ def ragged_leg(ps, torch, steps, seed, hbm_peak):
     return rep
 
 
+def ragged_full_causal_leg(ps, torch, steps, seed):
+    """The ragged decode workload's sequences and positions under full causal
+    attention (nothing evicted, every past position cached and read).  Its 143 GB
+    of K/V run as two halves of 128 sequences, one after the other; each half's
+    cache packs its sequences with per-sequence pool bases (a sequence's rows start
+    after the previous sequence's last position), and one step of the whole batch
+    is the sum of the two halves' median step times."""
+    import synth
+    d = DEC
+    nseq = 256
+    pos0 = synth.uniform_int(seed, 11, nseq, 1024, 262143)  # the ragged leg's draw
+    warm = 3
+    n_steps = steps + warm
+    step_ms, kv_bytes = 0.0, 0.0
+    for half in (slice(0, nseq // 2), slice(nseq // 2, nseq)):
+        p = pos0[half].astype(np.int64)
+        n = len(p)
+        W = int(p.max()) + n_steps + 1  # no position ever leaves the window
+        used = p + n_steps
+        base = np.concatenate([[0], np.cumsum(used)[:-1]])
+        cache = ps.RingCache(n, d["hkv"], d["D"], W, np.zeros(n, dtype=np.int64),
+                             rope_theta=d["theta"], prefix_max=0, zero=False,
+                             slot_base=base.tolist())
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(seed + 17)
+        fill_random(cache, {s: [(0, int(p[s]))] for s in range(n)}, gen, torch)
+        shape = (n_steps, n)
+        q = torch.randn(*shape, d["hq"], d["D"], generator=gen, device="cuda").to(torch.bfloat16)
+        k = torch.randn(*shape, d["hkv"], d["D"], generator=gen, device="cuda").to(torch.bfloat16)
+        v = torch.randn(*shape, d["hkv"], d["D"], generator=gen, device="cuda").to(torch.bfloat16)
+        pos = (torch.from_numpy(p.astype(np.int32)).cuda()[None, :]
+               + torch.arange(n_steps, dtype=torch.int32, device="cuda")[:, None]).contiguous()
+        step_ms += statistics.median(step_times(ps, torch, cache, q, k, v, pos, steps, warm))
+        kv_bytes += float(np.sum(2 * d["hkv"] * (p + 1) * d["D"] * 2))
+        del cache, q, k, v, pos
+        torch.cuda.empty_cache()
+    return {"decode_tok_s": nseq / (step_ms / 1e3), "decode_ms_per_step": step_ms,
+            "kv_gb_per_step": kv_bytes / 1e9,
+            "how": "same library and sequences, W > every position (no eviction), P = 0; two "
+                   "halves of 128 sequences run one after the other (%.0f GB of K/V read per "
+                   "step in all), step time = sum of the halves' medians over %d steps"
+                   % (kv_bytes / 1e9, steps)}
+
+
 def step_times(ps, torch, cache, q, k, v, pos, steps, warmup):
     """Per-step device times (ms) of `steps` decode steps (append + partial +
     combine), each bracketed by events on the launching stream, after `warmup`."""
@@ -790,6 +834,10 @@ def main():
     ragged = flat = comparators = small = None
     if not args.no_extra and (rank == 0 or world == 1):
         ragged = ragged_leg(ps, torch, 100, 4, hbm_peak)
+        if not args.no_baselines:
+            fc = ragged_full_causal_leg(ps, torch, 10, 4)
+            fc["decode_speedup"] = fc["decode_ms_per_step"] / ragged["step_ms"]
+            ragged["full_causal"] = fc
         flat = flatness_leg(ps, torch, seed)
         small = small_batch_leg(ps, torch, seed + 21)
         comparators = comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak)

@@ -61,13 +61,19 @@ class RingCache:
     ``block_table[s, i]`` names the block of the sequence's logical slots
     [i * block_size, (i + 1) * block_size); ``block_order`` (a permutation of the
     block ids, default identity) sets that assignment.
+    ``slot_base`` (contiguous only): the first pool row of each sequence instead of
+    ``s * capacity``; the pools then hold ``max(slot_base) + capacity`` rows.
+    Sequences touch only the rows of the slots they fill, so reservations may
+    overlap where a sequence never fills its whole capacity (e.g. a full-history
+    cache whose sequences stop at different positions).
     """
 
     def __init__(self, nseq: int, n_kv_heads: int, head_dim: int, window: int,
                  prefix_len: Sequence[int] | torch.Tensor, rope_theta: float = 10000.0,
                  prefix_max: Optional[int] = None, capacity: Optional[int] = None,
                  device="cuda", zero: bool = True, block_size: Optional[int] = None,
-                 block_order: Optional[Sequence[int]] = None, pe_mode: int = 0):
+                 block_order: Optional[Sequence[int]] = None, pe_mode: int = 0,
+                 slot_base: Optional[Sequence[int]] = None):
         pl = torch.as_tensor(prefix_len, dtype=torch.int32).reshape(-1)
         if pl.numel() != nseq:
             raise ValueError("prefix_len must have nseq entries")
@@ -76,8 +82,17 @@ class RingCache:
         self.nseq, self.n_kv_heads, self.head_dim, self.window = nseq, n_kv_heads, head_dim, window
         self.rope_theta = float(rope_theta)
         self.block_size = block_size
+        if slot_base is not None and block_size is not None:
+            raise ValueError("slot_base applies to contiguous caches only")
+        if slot_base is not None:
+            base = torch.as_tensor(slot_base, dtype=torch.int64).reshape(-1)
+            if base.numel() != nseq or int(base.min()) < 0:
+                raise ValueError("slot_base must have nseq non-negative entries")
+        else:
+            base = torch.arange(nseq, dtype=torch.int64) * self.capacity
+        self._base = base
         if block_size is None:
-            rows = nseq * self.capacity
+            rows = int(base.max()) + self.capacity
             self.block_table = None
             self.blocks_per_seq = 0
         else:
@@ -92,7 +107,7 @@ class RingCache:
         alloc = torch.zeros if zero else torch.empty
         self.k_pool = alloc(rows, n_kv_heads, head_dim, dtype=BF16, device=device)
         self.v_pool = alloc(rows, n_kv_heads, head_dim, dtype=BF16, device=device)
-        self.slot_base = (torch.arange(nseq, dtype=torch.int64) * self.capacity).to(device)
+        self.slot_base = base.to(device)
         self.prefix_len = pl.to(device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self._ws = None
@@ -110,7 +125,7 @@ class RingCache:
         """Pool rows of the sequence's logical slots 0..capacity-1, in slot order."""
         slots = torch.arange(self.capacity, dtype=torch.int64)
         if self.block_table is None:
-            return seq * self.capacity + slots
+            return int(self._base[seq]) + slots
         bt = self.block_table[seq].cpu().to(torch.int64)
         return bt[slots // self.block_size] * self.block_size + slots % self.block_size
 

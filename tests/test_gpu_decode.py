@@ -333,3 +333,36 @@ def test_decode_append_equals_append_then_decode(ps, nseq, hq, hkv, D, P, W, pos
         o_ref, l_ref = ref(qs, int(pos[s]), P[s], W, synth.History(seed, s, hkv, D).rows, theta)
         assert_attention_close(bf16_tensor_to_f64(o_b[s]), l_b[s].cpu().numpy(), o_ref, l_ref,
                                f"seq {s}")
+
+
+def test_decode_with_per_sequence_slot_bases(ps):
+    """Full-history caches whose sequences stop at different positions, packed with
+    per-sequence pool bases: each sequence's reservation (capacity rows) overlaps the
+    next sequences', but the rows it fills do not.  Decode over a few appended steps
+    matches the oracle, and the rows past each sequence's filled slots are untouched."""
+    seed, hq, hkv, D, theta, steps = 23, 4, 2, 128, 10000.0, 3
+    pos0 = np.array([50, 300, 130])
+    nseq = len(pos0)
+    W = int(pos0.max()) + steps + 1          # no eviction: every position stays
+    P = np.zeros(nseq, dtype=np.int64)
+    used = pos0 + steps                      # slots each sequence fills
+    base = np.concatenate([[0], np.cumsum(used)[:-1]])
+    cache = ps.RingCache(nseq, hkv, D, W, P, rope_theta=theta, slot_base=base.tolist())
+    assert cache.k_pool.shape[0] == int(base.max()) + W
+    append_runs(cache, {s: [(0, int(pos0[s]))] for s in range(nseq)}, synth_source(seed, hkv, D))
+    for step in range(steps):
+        pos = pos0 + step
+        kv = [synth.History(seed, s, hkv, D).rows_bits([int(pos[s])]) for s in range(nseq)]
+        k = bits_to_bf16_tensor(np.concatenate([x[0] for x in kv]))
+        v = bits_to_bf16_tensor(np.concatenate([x[1] for x in kv]))
+        tpos = torch.tensor(pos, dtype=torch.int32, device="cuda")
+        o, lse = cache.decode_append(_queries(seed, nseq, pos, hq, D), k, v, tpos)
+        torch.cuda.synchronize()
+        assert cache.check_status() == 0
+        ref = _oracle_rows(seed, range(nseq), pos, P, W, hq, hkv, D, theta)
+        for s in range(nseq):
+            assert_attention_close(bf16_tensor_to_f64(o[s]), lse[s].cpu().numpy(), *ref[s],
+                                   f"step {step} seq {s}")
+    # the last sequence's tail of its reservation was never written (zero-initialised)
+    last = int(base[-1] + used[-1])
+    assert torch.count_nonzero(cache.k_pool[last:]).item() == 0
