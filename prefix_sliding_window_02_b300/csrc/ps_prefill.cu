@@ -241,6 +241,7 @@ struct PrefillParams {
   CUtensorMap tmv;  // values     {D, Hkv, S or Skv, B}
   __nv_bfloat16* out;
   float* lse;
+  int32_t out32;  // out is 32-byte aligned: rows are stored 32 bytes at a time
   const int32_t* q_start;
   const int32_t* prefix_len;
   int32_t* status;
@@ -308,6 +309,30 @@ __device__ __forceinline__ Visits make_visits(const KeyMap& km, int64_t q0, int6
     }
   }
   return v;
+}
+
+// 32 fp32 columns of one output row (O * inv) as bf16 at dst.  One lane writes
+// one row, so each store instruction touches 32 rows: 32-byte pieces (dst
+// 32-byte aligned, out32) fill whole sectors, with half as many instructions as
+// 16-byte ones.
+__device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, const uint32_t (&o)[32],
+                                                float inv, bool out32) {
+  uint32_t w[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    w[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+  if (out32) {
+#pragma unroll
+    for (int e = 0; e < 16; e += 8)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 2 * e),
+                   "r"(w[e]), "r"(w[e + 1]), "r"(w[e + 2]), "r"(w[e + 3]), "r"(w[e + 4]),
+                   "r"(w[e + 5]), "r"(w[e + 6]), "r"(w[e + 7])
+                   : "memory");
+  } else {
+#pragma unroll
+    for (int e = 0; e < 16; e += 4)
+      *reinterpret_cast<uint4*>(dst + 2 * e) = make_uint4(w[e], w[e + 1], w[e + 2], w[e + 3]);
+  }
 }
 
 template <int D>
@@ -556,17 +581,7 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const __grid_constant__
       uint32_t r[32];
       tc::ld32(tO + lane_off + c * 32, r);
       tc::wait_ld();
-      if (qrow <= q1r) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          uint4 v;
-          v.x = pack_bf16(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv);
-          v.y = pack_bf16(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
-          v.z = pack_bf16(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv);
-          v.w = pack_bf16(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
-          *reinterpret_cast<uint4*>(orow + c * 32 + j) = v;
-        }
-      }
+      if (qrow <= q1r) store_row_chunk(orow + c * 32, r, inv, p.out32 != 0);
     }
     if (qrow <= q1r)
       p.lse[((int64_t)b * p.hq + h) * p.S + qrow] = (m_ref + __log2f(l)) * 0.69314718055994530942f;
@@ -1036,17 +1051,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bar->o_free[i]);
         }
-        if (qrow <= it.q1r) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
-          }
-        }
+        if (qrow <= it.q1r) store_row_chunk(orow + c * 32, o, inv, p.out32 != 0);
       }
       if (qrow <= it.q1r)
         p.lse[((int64_t)it.b * p.hq + it.h0 + i) * p.S + qrow] =
@@ -1278,6 +1283,7 @@ extern "C" ps_status_t ps_prefill(const void* q, const void* k, const void* v, i
                              CU_TENSOR_MAP_SWIZZLE_128B);
   if (!okm) return PS_ERR_CUDA;
   p.out = static_cast<__nv_bfloat16*>(out);
+  p.out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   p.lse = lse;
   p.q_start = q_start;
   p.prefix_len = prefix_len;

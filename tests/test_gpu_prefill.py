@@ -324,3 +324,25 @@ def test_prefill_extend_ragged_chunks_through_ring_seq(ps):
             o_ref, l_ref = attend(synth.bits_to_f64(q[b, r]), c0[b] + r, P[b], W, hist.rows, theta)
             assert_attention_close(bf16_tensor_to_f64(out[b, r]), lse[b, :, r].cpu().numpy(), o_ref,
                                    l_ref, f"b={b} (sequence {s}) row={r}")
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 2), (3, 3)])
+def test_prefill_output_only_16_byte_aligned(ps, hq, hkv):
+    """An output buffer that is 16- but not 32-byte aligned takes the 16-byte store
+    path and gives the same bits as an aligned one (pair and odd-group kernels)."""
+    seed, B, S, D, W, theta = 41, 1, 300, 128, 100, 10000.0
+    P, q_start = [37], [0]
+    q, k, v = _inputs(seed, B, S, q_start, hq, hkv, D)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    args = (bits_to_bf16_tensor(q), bits_to_bf16_tensor(k), bits_to_bf16_tensor(v),
+            torch.tensor(q_start, **i32), torch.tensor(P, **i32), W)
+    ref, ref_lse = ps.prefill(*args, rope_theta=theta)
+    n = B * S * hq * D
+    raw = torch.zeros(n + 64, dtype=torch.bfloat16, device="cuda")
+    off = next(o for o in range(0, 64, 8) if (raw.data_ptr() + 2 * o) % 32 == 16)
+    out = raw[off:off + n].view(B, S, hq, D)
+    assert out.data_ptr() % 32 == 16
+    got, got_lse = ps.prefill(*args, rope_theta=theta, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref) and torch.equal(got_lse, ref_lse)
+    assert torch.count_nonzero(raw[:off]).item() == 0 and torch.count_nonzero(raw[off + n:]).item() == 0
