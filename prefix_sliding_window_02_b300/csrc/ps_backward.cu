@@ -75,6 +75,9 @@ constexpr int kSmem = kOffBars + 256 /*barriers*/ + 1024 /*alignment*/;
 static_assert(kOffLd + kSaKV * kLdBytes <= kOffB, "LSE / D slots fit in the spare slot");
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, 128, false);   // S, dP: both operands K-major
 constexpr uint32_t kTAcc = 256;                                  // accumulator columns
+// dK/dV CTA: P^T(t) is packed into the second half of each softmax warp's column
+// share of the other step buffer (the first half of each share holds dS^T)
+constexpr uint32_t kPOff = kNC / 2;
 
 // Per head dim D (64 or 128): the bytes a 128-row tile fills of its slot, its
 // 64-column halves, the accumulations' instruction descriptor (N = D, B
@@ -376,10 +379,11 @@ __device__ __forceinline__ void ds_row(uint32_t tP, float drow, const float (&pr
 // dK/dV side, first half: this thread's key row against kNC queries whose
 // {LSE*log2e, D} pairs are ld[0..kNC) (as float4: two queries each).  P^T is
 // zero unless bit e of km is set (query e admits the key); kept in registers
-// and written as bf16 pairs over the first kNC / 2 columns for dV += P^T dO.
+// and written as kNC / 2 columns of bf16 pairs at tP for dV += P^T dO.
 template <bool MASK>
-__device__ __forceinline__ void p_col(uint32_t tS, float scale_log2, const float4* ld,
-                                      const uint32_t (&km)[kNC / 32], float (&pr)[kNC]) {
+__device__ __forceinline__ void p_col(uint32_t tS, uint32_t tP, float scale_log2,
+                                      const float4* ld, const uint32_t (&km)[kNC / 32],
+                                      float (&pr)[kNC]) {
 #pragma unroll
   for (int c = 0; c < kNC / 32; ++c) {
     uint32_t sv[32];  // the bf16 pairs are packed into its first half as it is consumed
@@ -402,7 +406,7 @@ __device__ __forceinline__ void p_col(uint32_t tS, float scale_log2, const float
       pr[x + 1] = x1;
       sv[e / 2] = pack_bf16(x0, x1);
     }
-    tc::st16(tS + 16 * c, reinterpret_cast<const uint32_t(&)[16]>(sv));
+    tc::st16(tP + 16 * c, reinterpret_cast<const uint32_t(&)[16]>(sv));
   }
 }
 
@@ -532,8 +536,12 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
       const uint64_t bOm = tc::sdesc_sw128(smem_u32(sB), kHalf, 1024);
       auto soa = [](int t) { return (uint64_t)(((t % kSa) * kTile) >> 4); };
       auto sob = [](int t) { return (uint64_t)(((t % kSb) * kTile) >> 4); };
-      // per step t (buffer t & 1): dV += P^T dO, dP^T = V dO^T, then S^T of
-      // step t+1, then dK += dS^T Q
+      // Per step t (buffer t & 1): dP^T = V dO^T, dV += P^T dO, S^T of step
+      // t+1, then dK += dS^T Q.  The softmax warps write P^T(t) into the other
+      // buffer's unused half -- the columns of dP^T(t-1) they have already
+      // consumed, beside dS^T(t-1) -- so dP^T(t), on the path to dS^T(t), does
+      // not wait for dV(t) to read P^T(t); S^T(t+1) then overwrites that buffer
+      // after dV(t) and dK(t-1) have read it (one thread's products run in order).
       bool ok = mbar_wait_abort(&bar->res_full, 0, abort, p.wait_ns) &&
                 mbar_wait_abort(&bar->a_full[0], 0, abort, p.wait_ns);
       if (ok) {
@@ -549,9 +557,9 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
                    mbar_wait_abort(&bar->b_full[t % kSb], (t / kSb) & 1, abort, p.wait_ns)))
           break;
         tc::fence_after();
-        mma_ts8<D>(tmem + kTAcc, tb, bOm + sob(t), t > 0);  // dV += P^T dO
-        mma_ss8<D>(tb, aV, bO + sob(t), false);              // dP^T = V dO^T
+        mma_ss8<D>(tb, aV, bO + sob(t), false);  // dP^T = V dO^T
         tc::commit(smem_u32(&bar->dp_full[bf]));
+        mma_ts8<D>(tmem + kTAcc, tmem + (bf ^ 1) * 128 + kPOff, bOm + sob(t), t > 0);  // dV
         tc::commit(smem_u32(&bar->b_empty[t % kSb]));
         if (t + 1 < n) {
           if (!(ok = mbar_wait_abort(&bar->a_full[(t + 1) % kSa], ((t + 1) / kSa) & 1, abort, p.wait_ns)))
@@ -605,10 +613,12 @@ __device__ __forceinline__ void dkdv_cta(const Params& p, uint8_t* smem, Bars* b
         break;
       }
       tc::fence_after();
+      // P^T(t) goes to the other buffer, beside dS^T(t-1) (see the issuer)
+      const uint32_t tPo = tmem + (bf ^ 1) * 128 + part * kNC + kPOff + lane_off;
       if (masked)
-        p_col<true>(tS, p.scale_log2, ld, kmask, pr);
+        p_col<true>(tS, tPo, p.scale_log2, ld, kmask, pr);
       else
-        p_col<false>(tS, p.scale_log2, ld, kmask, pr);
+        p_col<false>(tS, tPo, p.scale_log2, ld, kmask, pr);
       release(&bar->p_ready[bf], lane, true);
       ok = mbar_wait_abort(&bar->dp_full[bf], ph, abort, p.wait_ns);
       if (!__all_sync(0xffffffffu, ok)) {
