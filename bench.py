@@ -546,6 +546,25 @@ def prefill_flops(S, P, W, hq, D, bm=128, bn=128):
     return 4.0 * D * hq * float(pairs)
 
 
+def timed_rounds(torch, fn, steps, rounds=5):
+    """Device time per call of fn(): `rounds` rounds of about steps / rounds calls,
+    each round between CUDA events with a synchronisation on both sides; returns
+    the median over rounds of the per-call mean, and the per-round means (a
+    transient clock drop from the power cap moves one round, not the median)."""
+    per = max(1, -(-steps // rounds))
+    means = []
+    for _ in range(rounds):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(per):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        means.append(e0.elapsed_time(e1) / per)
+    return statistics.median(means), means
+
+
 def run_prefill(ps, torch, S, P, W, steps, warmup, seed, full_causal=False, B=None):
     """Times whole ps_prefill calls (RoPE pre-pass + tile kernel) on one layer's
     resident q, k, v; returns ms per call and the tile classes of one row."""
@@ -568,17 +587,11 @@ def run_prefill(ps, torch, S, P, W, steps, warmup, seed, full_causal=False, B=No
     for _ in range(warmup):
         ps.prefill(q, k, v, qs, pl, W, rope_theta=d["theta"], out=out, lse=lse, workspace=ws,
                    status=status)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        ps.prefill(q, k, v, qs, pl, W, rope_theta=d["theta"], out=out, lse=lse, workspace=ws,
-                   status=status)
-    e1.record()
-    torch.cuda.synchronize()
+    ms, _ = timed_rounds(torch, lambda: ps.prefill(q, k, v, qs, pl, W, rope_theta=d["theta"],
+                                                   out=out, lse=lse, workspace=ws, status=status),
+                         steps)
     assert int(status.item()) == 0, f"prefill device status {int(status.item())}"
     assert torch.isfinite(lse).all()
-    ms = e0.elapsed_time(e1) / steps
     cls = ps.prefill_tile_classes(S, 0, P, W).cpu().numpy()
     n_skip, n_part, n_full = [(cls == c).sum() for c in (0, 1, 2)]
     return ms, dict(skip=int(n_skip), partial=int(n_part), full=int(n_full))
@@ -595,7 +608,8 @@ def prefill_report(ps, torch, name, B, S, P, W, steps, seed, bf16_peak, full_cau
     rep = {"workload": name, "ms": ms, "tflops_algorithmic": flops / ms / 1e9,
            "tflops_on_nonskipped_tiles": tile_flops / ms / 1e9,
            "frac_of_measured_bf16_burst": tile_flops / ms / 1e9 / bf16_peak,
-           "timed": "whole ps_prefill call: RoPE pre-pass + tile kernel",
+           "timed": "whole ps_prefill call: RoPE pre-pass + tile kernel; median over 5 rounds "
+                    "of the per-call mean",
            "tiles_per_row_and_head": cls,
            "skip_fraction_of_causal_tiles": 1 - (cls["partial"] + cls["full"]) / causal_tiles}
     if full_causal_steps:
@@ -625,16 +639,10 @@ def backward_report(ps, torch, B, S, P, W, steps, seed, bf16_peak):
     for _ in range(2):
         ps.prefill_backward(q, k, v, out, lse, do, qs, pl, W, rope_theta=d["theta"], status=status,
                             fwd_workspace=fws)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        ps.prefill_backward(q, k, v, out, lse, do, qs, pl, W, rope_theta=d["theta"], status=status,
-                            fwd_workspace=fws)
-    e1.record()
-    torch.cuda.synchronize()
+    ms, _ = timed_rounds(torch, lambda: ps.prefill_backward(
+        q, k, v, out, lse, do, qs, pl, W, rope_theta=d["theta"], status=status,
+        fwd_workspace=fws), steps)
     assert int(status.item()) == 0
-    ms = e0.elapsed_time(e1) / steps
     fwd_alg = B * prefill_flops(S, P, W, hq, D)
     exe = B * backward_executed_flops(S, P, W, hq, hkv, D)
     torch.cuda.empty_cache()
@@ -642,7 +650,8 @@ def backward_report(ps, torch, B, S, P, W, steps, seed, bf16_peak):
             "ms": ms, "tflops_algorithmic": 2.5 * fwd_alg / ms / 1e9,
             "tflops_executed": exe / ms / 1e9,
             "frac_of_measured_bf16_burst": 2.5 * fwd_alg / ms / 1e9 / bf16_peak,
-            "timed": "whole ps_prefill_backward call reusing the forward's rotated Q and K: "
+            "timed": "median over 5 rounds of the per-call mean of whole ps_prefill_backward "
+                     "calls reusing the forward's rotated Q and K: "
                      "pre-pass (D = rowsum(dO * O)) + the dQ / dK,dV kernel; "
                      "algorithmic = 2.5 x forward FLOPs (dV, dP, dQ, dK over the admitted pairs), "
                      "executed = the tensor-core products the kernels issue"}
@@ -834,13 +843,14 @@ def main():
     ragged = flat = comparators = small = None
     if not args.no_extra and (rank == 0 or world == 1):
         ragged = ragged_leg(ps, torch, 100, 4, hbm_peak)
+        flat = flatness_leg(ps, torch, seed)
+        small = small_batch_leg(ps, torch, seed + 21)
+        comparators = comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak)
+        # last of the decode legs: its 135 GB-per-step run draws the most power
         if not args.no_baselines:
             fc = ragged_full_causal_leg(ps, torch, 10, 4)
             fc["decode_speedup"] = fc["decode_ms_per_step"] / ragged["step_ms"]
             ragged["full_causal"] = fc
-        flat = flatness_leg(ps, torch, seed)
-        small = small_batch_leg(ps, torch, seed + 21)
-        comparators = comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak)
 
     # prefill (one layer) and the truncated-backprop training forward
     try:
