@@ -29,14 +29,17 @@
 // narrower products would halve the rate.  TMEM (512 columns) holds two step
 // buffers of 128 columns and the fp32 accumulators (dV | dK, or dQ).  A step
 // (one streamed tile) runs in its buffer: S is computed there, the softmax
-// warps turn it into P (kept in registers; in a dK/dV CTA also written back
-// as bf16 for dV += P^T dO), dP then overwrites the buffer, and the softmax
-// warps turn it into dS, written back as bf16 over its first columns, the
-// tensor-memory A operand of dQ += dS K or dK += dS^T Q.  The issuer orders
-// the products as dP(t), S(t+1), dQ / dK(t), so S(t+1) runs while the softmax
-// warps compute dS(t), and dS(t)'s product runs while they compute P(t+1).
-// Tensor-core instructions of one thread execute in issue order, which lets
-// a product overwrite a buffer that an earlier product has just read.
+// warps turn it into P (kept in registers), dP then overwrites the buffer, and
+// the softmax warps turn it into dS, written back as bf16 pairs over the first
+// half of each warp's columns, the tensor-memory A operand of dQ += dS K or
+// dK += dS^T Q.  In a dK/dV CTA P^T also goes back as bf16 for dV += P^T dO,
+// into the other buffer's second halves (columns of the previous step's dP^T
+// already consumed), so that dP^T(t) need not wait for dV(t).  The issuer
+// orders the products dP(t), S(t+1), dQ(t) in a dQ CTA and dP^T(t), dV(t),
+// S^T(t+1), dK(t) in a dK/dV CTA: S(t+1) runs while the softmax warps compute
+// dS(t), and dS(t)'s product while they compute P(t+1).  Tensor-core
+// instructions of one thread execute in issue order, which lets a product
+// overwrite a buffer that an earlier product has just read.
 //
 // CTA roles (320 threads): warps 0-7 are the softmax warps (two per TMEM lane
 // quadrant, each on 64 of a step's 128 columns), warp 8 issues the TMA copies,
