@@ -170,7 +170,8 @@ def fill_random(cache, runs_per_seq, gen, torch, chunk_tokens=1 << 21):
 
 
 # ---- decode ---------------------------------------------------------------
-def decode_setup(ps, torch, seed, W, P, pos0, n_steps, full_causal=False, pe_mode=0):
+def decode_setup(ps, torch, seed, W, P, pos0, n_steps, full_causal=False, pe_mode=0,
+                 block_size=None):
     """Ring cache holding, per sequence, the live K/V of positions < pos0[s]
     (random values), plus every step's q, k, v and positions resident in HBM.
     pos0 is one position for all sequences or one per sequence."""
@@ -180,9 +181,14 @@ def decode_setup(ps, torch, seed, W, P, pos0, n_steps, full_causal=False, pe_mod
     if full_causal:
         W = int(pos0.max()) + n_steps + 1
         P = np.zeros(nseq, dtype=np.int64)
+    prefix_max = int(max(P.max(), d["Pmax"] if not full_causal else 0))
+    order = None
+    if block_size:  # paged: the sequences' blocks in a shuffled order over the pool
+        nblocks = nseq * -(-(prefix_max + W) // block_size)
+        order = np.random.default_rng(seed).permutation(nblocks).tolist()
     cache = ps.RingCache(nseq, d["hkv"], d["D"], W, P, rope_theta=d["theta"],
-                         prefix_max=int(max(P.max(), d["Pmax"] if not full_causal else 0)), zero=False,
-                         pe_mode=pe_mode)
+                         prefix_max=prefix_max, zero=False, pe_mode=pe_mode,
+                         block_size=block_size, block_order=order)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(seed)
     runs = {s: live_runs(int(pos0[s]) - 1, int(P[s]), W) for s in range(nseq)}
@@ -277,11 +283,12 @@ def run_decode(ps, torch, cache, q, k, v, pos, steps, warmup, dist=None, per_ker
     return total_ms, kern_ms, out, lse
 
 
-def decode_leg(ps, torch, name, P, W, pos0, steps, warmup, seed, hbm_peak, pe_mode=0):
+def decode_leg(ps, torch, name, P, W, pos0, steps, warmup, seed, hbm_peak, pe_mode=0,
+               block_size=None):
     """One decode workload: append + partial + combine per step, one layer."""
     d = DEC
     cache, q, k, v, pos, L = decode_setup(ps, torch, seed, W, P, pos0, steps + warmup,
-                                          pe_mode=pe_mode)
+                                          pe_mode=pe_mode, block_size=block_size)
     total_ms, kern_ms, out, _ = run_decode(ps, torch, cache, q, k, v, pos, steps, warmup)
     assert cache.check_status() == 0 and torch.isfinite(out.float()).all()
     nseq = len(P)
@@ -451,8 +458,8 @@ def small_batch_leg(ps, torch, seed, steps=200):
 def comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak):
     """The same library on the same shapes with a plain sliding window (P = 0)
     and a StreamingLLM-style 4-token sink (P = 4): decode at the steady-decode
-    shapes, prefill at the 32K prefill shape; and Reset PE decode at the
-    steady-decode shapes."""
+    shapes, prefill at the 32K prefill shape; Reset PE decode and prefill at
+    those shapes; and decode through a paged ring (shuffled 64-slot blocks)."""
     d = DEC
     out = {}
     for name, pval in (("sliding_window_P0", 0), ("streaming_sink_P4", 4)):
@@ -474,6 +481,27 @@ def comparator_legs(ps, torch, args, seed, hbm_peak, bf16_peak):
     out["reset_pe"] = {"decode_tok_s_per_layer": r["tok_s_per_layer"], "decode_step_ms": r["step_ms"],
                        "decode_partial_ms": r["partial_kernel_ms"], "decode_partial_gbs": r["partial_gbs"],
                        "decode_partial_frac_of_measured_hbm": r["partial_frac_of_measured_hbm"]}
+    # Reset PE prefill at the 32K shape (prefix tiles visited with the renumbered query)
+    if not args.no_prefill:
+        try:
+            ms, _ = run_prefill(ps, torch, PRE["S"], PRE["P"], PRE["W"], args.prefill_steps, 3,
+                                seed + 14, pe_mode=ps.PS_PE_RESET)
+            flops = prefill_flops(PRE["S"], PRE["P"], PRE["W"], PRE["hq"], PRE["D"])
+            out["reset_pe"].update({"prefill_ms": ms, "prefill_tflops_algorithmic": flops / ms / 1e9})
+        except Exception as e:  # a comparator must not take the bench line down
+            out["reset_pe"]["prefill_error"] = str(e)[:200]
+    # paged ring (64-slot blocks in a shuffled order) at the steady-decode shapes
+    try:
+        r = decode_leg(ps, torch, "decode, 64 x 131072, W 4096, paged (64-slot blocks, shuffled)",
+                       decode_prefix_lens(seed, d["nseq"]), d["W"], d["pos0"], 100, 5, seed + 15,
+                       hbm_peak, block_size=64)
+        out["paged_block64"] = {"decode_tok_s_per_layer": r["tok_s_per_layer"],
+                                "decode_step_ms": r["step_ms"],
+                                "decode_partial_ms": r["partial_kernel_ms"],
+                                "decode_partial_gbs": r["partial_gbs"],
+                                "decode_partial_frac_of_measured_hbm": r["partial_frac_of_measured_hbm"]}
+    except Exception as e:
+        out["paged_block64"] = {"error": str(e)[:200]}
     return out
 
 
@@ -565,7 +593,7 @@ def timed_rounds(torch, fn, steps, rounds=5):
     return statistics.median(means), means
 
 
-def run_prefill(ps, torch, S, P, W, steps, warmup, seed, full_causal=False, B=None):
+def run_prefill(ps, torch, S, P, W, steps, warmup, seed, full_causal=False, B=None, pe_mode=0):
     """Times whole ps_prefill calls (RoPE pre-pass + tile kernel) on one layer's
     resident q, k, v; returns ms per call and the tile classes of one row."""
     d = PRE
@@ -582,13 +610,15 @@ def run_prefill(ps, torch, S, P, W, steps, warmup, seed, full_causal=False, B=No
     pl = torch.full((B,), P, dtype=torch.int32, device="cuda")
     out = torch.empty_like(q)
     lse = torch.empty(B, hq, S, dtype=torch.float32, device="cuda")
-    ws = torch.empty(ps.prefill_workspace_size(B, S, hq, hkv, D), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(ps.prefill_workspace_size(B, S, hq, hkv, D, pe_mode=pe_mode),
+                     dtype=torch.uint8, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for _ in range(warmup):
         ps.prefill(q, k, v, qs, pl, W, rope_theta=d["theta"], out=out, lse=lse, workspace=ws,
-                   status=status)
+                   status=status, pe_mode=pe_mode)
     ms, _ = timed_rounds(torch, lambda: ps.prefill(q, k, v, qs, pl, W, rope_theta=d["theta"],
-                                                   out=out, lse=lse, workspace=ws, status=status),
+                                                   out=out, lse=lse, workspace=ws, status=status,
+                                                   pe_mode=pe_mode),
                          steps)
     assert int(status.item()) == 0, f"prefill device status {int(status.item())}"
     assert torch.isfinite(lse).all()
