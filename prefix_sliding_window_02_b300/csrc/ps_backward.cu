@@ -54,9 +54,8 @@ namespace ps {
 namespace bwd {
 
 constexpr int kT = 128;                  // rows of every tile (resident and streamed)
-constexpr int kHD = 128;                 // largest head dim: shared-memory slots are sized for it
 constexpr int kHalf = kT * 128;          // one 64-column swizzled half of a tile: 16 KB
-constexpr int kTile = 2 * kHalf;         // one slot: 32 KB
+constexpr int kTile = 2 * kHalf;         // one slot: 32 KB, sized for head dim 128
 constexpr int kLdBytes = kT * 8;         // {LSE*log2e, D} pairs of one query tile
 constexpr int kSoftWarps = 8;
 constexpr int kParts = kSoftWarps / 4;   // softmax warps per TMEM lane quadrant
