@@ -57,3 +57,32 @@ def test_consistent_shapes_reach_the_device_check(ps):
     q, k, v, qs, pl = _inputs()
     with pytest.raises(ValueError, match="CUDA"):
         ps.prefill(q, k, v, qs, pl, 16)
+
+
+def test_ring_cache_slot_bases(ps):
+    """Per-sequence pool bases: the pools end a capacity past the last base,
+    rows_of follows the bases, and malformed bases are refused."""
+    c = ps.RingCache(3, 2, 64, 8, [0, 0, 0], slot_base=[0, 5, 20], device="cpu")
+    assert c.k_pool.shape[0] == 20 + c.capacity
+    assert c.desc.total_slots == 20 + c.capacity
+    assert c.slot_base.tolist() == [0, 5, 20]
+    assert c.rows_of(1).tolist() == list(range(5, 5 + c.capacity))
+    d = ps.RingCache(2, 2, 64, 8, [3, 1], device="cpu")  # default: s * capacity
+    assert d.slot_base.tolist() == [0, d.capacity] and d.k_pool.shape[0] == 2 * d.capacity
+    with pytest.raises(ValueError, match="slot_base"):
+        ps.RingCache(3, 2, 64, 8, [0, 0, 0], slot_base=[0, 5], device="cpu")
+    with pytest.raises(ValueError, match="slot_base"):
+        ps.RingCache(2, 2, 64, 8, [0, 0], slot_base=[0, -1], device="cpu")
+    with pytest.raises(ValueError, match="slot_base"):
+        ps.RingCache(2, 2, 64, 8, [0, 0], slot_base=[0, 16], block_size=16, device="cpu")
+
+
+def test_decode_graph_host_buffers_checked(ps):
+    """DecodeGraph.step refuses host blocks of the wrong size, type or device
+    before any call into the library."""
+    with pytest.raises(ValueError, match="host_in"):
+        ps.DecodeGraph._host(torch.zeros(10, dtype=torch.uint8), 11, "host_in")
+    with pytest.raises(ValueError, match="host_res"):
+        ps.DecodeGraph._host(torch.zeros(11, dtype=torch.int32), 11, "host_res")
+    assert ps.DecodeGraph._host(None, 11, "host_in") is None
+    assert ps.DecodeGraph._host(torch.zeros(11, dtype=torch.uint8), 11, "host_in").value
