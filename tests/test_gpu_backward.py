@@ -42,6 +42,8 @@ def _close(g, ref, what):
     (1, 384, 8, 2, [0], 128, 128),         # G = 4; plain sliding window
     (1, 200, 4, 2, [300], 16, 128),        # P >= S: causal through the prefix
     (2, 1024, 16, 8, [64, 64], 256, 128),  # training-shaped, reduced: 4W tokens, loss on all
+    (1, 300, 8, 1, [37], 100, 128),        # G = 8: one dK/dV CTA sums eight query heads
+    (1, 300, 6, 2, [37], 100, 128),        # G = 3 (odd group)
 ])
 def test_backward_matches_oracle(ps, B, S, hq, hkv, P, W, D):
     seed, theta = 41, 10000.0

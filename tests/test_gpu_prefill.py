@@ -108,6 +108,7 @@ def _check_rows(seed, out, lse, q, q_start, P, W, theta, rows_per_b, hkv, what="
     (2, 200, 4, 2, [17, 130], 70, 2),    # q x 4: sharper softmax, stale-max rescaling
     (2, 300, 3, 3, [37, 200], 100, 0),   # one query head per KV head: split prefix tile, band
     (1, 333, 6, 2, [150], 90, 0),        # three query heads per KV head (odd group)
+    (1, 300, 8, 2, [50], 100, 0),        # four query heads per KV head: two pairs per KV head
 ])
 def test_prefill_all_rows(ps, B, S, hq, hkv, P, W, qs):
     seed, D, theta = 31, 128, 10000.0
