@@ -255,3 +255,38 @@ def test_decode_graph_host_validation(ps):
     assert h.value is None
     assert lib.ps_decode_graph_step(None, f, f, 1, None) == 1
     assert lib.ps_decode_graph_destroy(None) == 0
+
+
+def test_boundary_usable_from_plain_c(ps, tmp_path):
+    """A C99 program that includes ps.h and links libps.so (no Python, no torch)
+    calls host-side entry points and gets the same answers as the binding."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.dirname(ps.lib._name)
+    src = tmp_path / "boundary.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "ps.h"
+int main(void) {
+  ps_decode_step_layout L;
+  if (ps_decode_step_layout_get(64, 16, 8, 128, &L) != PS_OK) return 1;
+  if (ps_decode_step_layout_get(0, 16, 8, 128, &L) != PS_ERR_INVALID_ARGUMENT) return 2;
+  if (ps_decode_graph_destroy(NULL) != PS_OK) return 3;
+  if (strcmp(ps_status_string(PS_ERR_ALIGNMENT), "PS_ERR_ALIGNMENT") != 0) return 4;
+  printf("%zu %zu %zu\n", L.v_off, L.in_bytes, L.res_bytes);
+  return 0;
+}
+''')
+    exe = tmp_path / "boundary"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(root, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-lps",
+                    "-Wl,-rpath," + libdir], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    inp, n_in, _, n_res = ps.decode_step_layout(64, 16, 8, 128)
+    assert r.stdout.split() == [str(inp["v"][0]), str(n_in), str(n_res)]
